@@ -1,0 +1,407 @@
+#!/usr/bin/env python3
+"""Benchmark of tree-verify MLA-absorb attention on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch: packed visibility bits
+from the parent array (kdt_build_visibility), then kdt_verify_attn (scores, mask,
+online softmax, P.V, split merge, epilogue). Inputs are resident in HBM; L2 is
+flushed (256 MiB write) between steps outside the timed events.
+
+Workload: the H=64, 8K-prefix, 64-node-tree configuration -- B=8, H=64, every
+prefix 8192, T=64 geometric-bias tree, bf16 q/c_kv/k_pe, fp32 out + lse -- seeded
+synthetic data (``workloads``). ``--config`` selects another configuration.
+
+Multi-GPU: each rank runs its own copy of the workload (weak scaling, no
+collective on the data path); rank 0 reports the work of all ranks over the
+slowest rank's time.
+
+``--impl reference`` times the CPU oracle as it stands on the host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "verify-attn µs/call, TFLOP/s and KV GB/s at H=64; fraction of roofline"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    except Exception:
+        d = dict(FALLBACK)
+        d["source"] = "fallback"
+        return d
+
+
+def depths(parent_row):
+    d = np.zeros(len(parent_row), dtype=np.int64)
+    for i, p in enumerate(parent_row):
+        d[i] = 1 if p < 0 else d[p] + 1
+    return d
+
+
+def workload_counts(case):
+    """Algorithmic FLOPs and bytes of one call (visible keys only; exps not counted)."""
+    vis_keys = 0
+    for b in range(case.B):
+        vis_keys += int(case.prefix_len[b]) * case.T + int(depths(case.parent[b]).sum())
+    flops = 2.0 * (wl.D_C + wl.D_C + wl.D_R) * case.H * vis_keys
+    elt = 2 if case.dtype == "bf16" else 4
+    kv_bytes = float(sum(int(k) for k in case.kv_len) * (wl.D_C + wl.D_R) * elt)
+    rows = case.B * case.T * case.H
+    q_bytes = rows * (wl.D_C + wl.D_R) * elt
+    out_bytes = rows * wl.D_C * 4 + rows * 4
+    meta = case.B * 4 + case.B * case.T * 4 + case.B * case.T * case.W * 4
+    return dict(flops=flops, kv_bytes=kv_bytes, bytes=kv_bytes + q_bytes + out_bytes + meta, visible_keys=vis_keys)
+
+
+class ClockSampler:
+    """nvidia-smi clocks during the timed region (the query fields of the profiling recipe)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def make_workload(name):
+    case = wl.make_config(name)
+    return case
+
+
+def run_reference(args, case, counts):
+    """Time the CPU oracle on a bounded sample of the workload (rows of sequence 0)."""
+    import oracle
+    oracle.build()
+    nthreads = oracle.num_threads()
+    per_row_flops = counts["flops"] / case.rows
+    # calibrate: a few rows, then size a sample for about --ref-seconds of CPU work
+    rows = np.arange(min(16, case.rows))
+    t0 = time.perf_counter()
+    oracle.verify_attn_rows(case, rows)
+    t_cal = time.perf_counter() - t0
+    n = int(min(case.rows, max(len(rows), len(rows) * args.ref_seconds / max(t_cal, 1e-6) / max(1, args.steps))))
+    n = max(1, n)
+    sample = np.arange(n)
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle.verify_attn_rows(case, sample[: min(n, 8)])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.verify_attn_rows(case, sample)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    flops = per_row_flops * n
+    tflops = flops / sec / 1e12
+    desc = f"first {n} rows (b=0, queries 0..{(n - 1) // case.H}, all heads) of the workload per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(args.config), "sample_rows": n},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def workload_name(name):
+    d = wl.CONFIGS[name]
+    pre = d["prefix"]
+    pre_s = f"U[{pre[1]},{pre[2]}]" if isinstance(pre, tuple) else str(pre)
+    return (f"{name}: B={d['B']} H={d['H']} prefix={pre_s} T={d['T']} {d['dtype']} "
+            f"tree={d['tree']} latent=512 rope=64 scale=1/sqrt(192)")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kdt", choices=["kdt", "reference"])
+    ap.add_argument("--config", default="target", choices=list(wl.CONFIGS))
+    ap.add_argument("--kernel-impl", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--ref-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        case = make_workload(args.config)
+        counts = workload_counts(case)
+        print(json.dumps(run_reference(args, case, counts)), flush=True)
+        return 0
+
+    import torch
+    import speculative_decoding_tree_absorb_gb300 as kdt
+    from speculative_decoding_tree_absorb_gb300 import build_lib
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0:
+        build_lib.build()
+    if dist is not None:
+        dist.barrier()
+    kdt.lib()
+
+    case = make_workload(args.config)
+    counts = workload_counts(case)
+    dev = torch.device("cuda", local_rank)
+
+    def conv(x):
+        if case.dtype == "bf16":
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(x)
+
+    host = dict(q_nope=conv(case.q_nope), q_pe=conv(case.q_pe), c_kv=conv(case.c_kv), k_pe=conv(case.k_pe),
+                prefix_len=torch.from_numpy(case.prefix_len.astype(np.int32)),
+                parent=torch.from_numpy(case.parent.astype(np.int32)))
+    d = {k: v.to(dev) for k, v in host.items()}
+    B, T, H = case.B, case.T, case.H
+    W = case.W
+    out = torch.empty((B, T, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    vis = torch.empty((B, T, W), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], vis=vis,
+                      max_kv_len=case.max_kv_len, scale=case.scale, out=out, lse=lse, err=err,
+                      impl=args.kernel_impl, num_splits=args.num_splits)
+    pl = kdt.plan(a)
+    ws = torch.empty(max(1, pl["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    lib = kdt.lib()
+    import ctypes
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    parent_ptr = ctypes.c_void_p(d["parent"].data_ptr())
+    vis_ptr = ctypes.c_void_p(vis.data_ptr())
+    err_ptr = ctypes.c_void_p(err.data_ptr())
+    ws_ptr = ctypes.c_void_p(ws.data_ptr())
+    ws_n = ws.numel()
+    launches_per_step = 1 + pl["num_launches"]
+
+    def step():
+        st = lib.kdt_build_visibility(parent_ptr, B, T, vis_ptr, err_ptr, sptr)
+        if st != 0:
+            raise kdt.KdtError(st, "kdt_build_visibility")
+        st = lib.kdt_verify_attn(ctypes.byref(a), ws_ptr, ws_n, sptr)
+        if st != 0:
+            raise kdt.KdtError(st, "kdt_verify_attn")
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0, "malformed tree reported"
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            e0, e1, e2 = ev[k]
+            e0.record(stream)
+            st = lib.kdt_build_visibility(parent_ptr, B, T, vis_ptr, err_ptr, sptr)
+            e1.record(stream)
+            st2 = lib.kdt_verify_attn(ctypes.byref(a), ws_ptr, ws_n, sptr)
+            e2.record(stream)
+            if st or st2:
+                raise kdt.KdtError(st or st2, "timed step")
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        t_wall = time.perf_counter() - t_wall
+    clocks = clk.summary()
+    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
+    attn_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    ms = statistics.mean(step_ms)
+    ms_attn = statistics.mean(attn_ms)
+    ms_attn_median = statistics.median(attn_ms)
+    if dist is not None:
+        t = torch.tensor([ms, ms_attn], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_attn = float(t[0]), float(t[1])
+
+    # ---- end to end through the public API with host buffers ----------------------
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+
+    def e2e_step():
+        for k_, v in pinned.items():
+            d[k_].copy_(v, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.fill_(1)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_mean = statistics.mean(e2e_ms)
+
+    # ---- parity spot check of this very run against the oracle (a few rows) --------
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    flops = counts["flops"]
+    peaks = load_peaks()
+    tflops = flops / (ms * 1e-3) / 1e12 * world
+    attn_tflops = flops / (ms_attn * 1e-3) / 1e12
+    if pl["impl"] == "tcgen05":
+        peak = peaks["bf16_tflops"]
+        bound, peak_note = "tensor", f"bf16 dense, cuBLAS burst ({peaks['source']})"
+    else:
+        peak = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        bound, peak_note = "alu", "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock"
+    tensor_roof_us = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+    hbm_roof_us = counts["bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e6
+    roof_us = max(tensor_roof_us, hbm_roof_us)
+
+    cpu_baseline = None
+    if not args.no_cpu_baseline and world >= 1:
+        ref_args = argparse.Namespace(steps=1, warmup=0, ref_seconds=args.ref_seconds, config=args.config,
+                                      gpus=1)
+        r = run_reference(ref_args, case, counts)
+        cpu_baseline = dict(r["cpu_baseline"])
+
+    line = {
+        "metric": METRIC,
+        "value": tflops,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if case.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": workload_name(args.config), "B": B, "H": H, "T": T,
+                   "prefix": [int(x) for x in case.prefix_len[:4]] + (["..."] if B > 4 else []),
+                   "kernel_impl": pl["impl"], "num_splits": pl["num_splits"],
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world} (weak scaling, no collective)"},
+        "us_per_call": ms * 1e3,
+        "us_per_call_attention": ms_attn * 1e3,
+        "us_per_call_attention_median": ms_attn_median * 1e3,
+        "tflops_attention": attn_tflops,
+        "kv_gbs": counts["kv_bytes"] / (ms_attn * 1e-3) / 1e9,
+        "workload_roofline": {"roofline_us": roof_us, "tensor_us": tensor_roof_us, "hbm_us": hbm_roof_us,
+                              "frac": roof_us / (ms * 1e3), "basis": f"max(FLOPs/bf16 peak, bytes/HBM) of "
+                                                                    f"{peaks['source']} peaks"},
+        "roofline": {"bound": bound, "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": attn_tflops / peak, "traffic": None, "peak_basis": peak_note,
+                     "kernel": f"verify_{pl['impl']} (+ split merge when num_splits > 1)"},
+        "algorithmic": {"flops": flops, "bytes": counts["bytes"], "kv_bytes": counts["kv_bytes"]},
+        "clocks": clocks,
+        "e2e": {"value": flops * world / (e2e_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_mean, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cpu_baseline,
+        "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

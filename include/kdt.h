@@ -1,0 +1,172 @@
+/*
+ * kdt.h -- C ABI of libkdt.so: DDTree tree-verify MLA-absorb attention with
+ * visibility masking, for NVIDIA GB300 (sm_103a).
+ *
+ * The method (page "The Verify-Attn Kernel: A Single File Write That Completed a
+ * Critical Piece of the DDTree Engine", section "The Design Journey: From Concept
+ * to CUDA"; page "The Moment of Truth: Validating a Custom CUDA Attention Kernel
+ * for Speculative Decoding", sections "Context" and "The Design Journey: From
+ * Theory to Silicon"): for every sequence b, draft-tree query i and head h,
+ *
+ *   s_j = scale * ( q_nope[b,i,h,:512] . c_kv[b,j,:512] + q_pe[b,i,h,:64] . k_pe[b,j,:64] )
+ *
+ * over the visible keys j -- the shared prefix j < prefix_len[b], plus tree node i
+ * itself and its ancestors (node t at cache row prefix_len[b] + t) -- then
+ *
+ *   out[b,i,h,:] = sum_j softmax(s)_j * c_kv[b,j,:]      (the latent; the w_vc
+ *                                                          up-projection stays outside)
+ *   lse[b,i,h]   = ln sum_j exp(s_j)                      (natural log, scaled scores)
+ *
+ * The per-row lse is what merges this result with attention computed elsewhere
+ * over other keys (section "Design Decisions and Trade-Offs" of the first page:
+ * long prefix by another kernel, tree tail by this one, combined by log-sum-exp).
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are caller-owned DEVICE pointers, row-major and
+ *    contiguous, 16-byte aligned, with no aliasing between inputs and outputs.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream). Argument
+ *    checks run on the host before any launch and never synchronise. A launch
+ *    failure is returned as KDT_ERR_CUDA; faults inside a kernel surface at the
+ *    caller's next synchronisation.
+ *  - The library allocates no memory: scratch space is the caller's `workspace`.
+ *    It keeps no global state except a per-device cache of the SM count and
+ *    kernel attributes. Concurrent calls are safe given distinct workspaces.
+ *  - Errors found in the DATA on the device (a malformed tree) are reported
+ *    through a caller-provided device word `err` (0 = ok, else 1 + the flat index
+ *    b*T + i of the first offending parent entry), never by a trap.
+ */
+#ifndef KDT_H
+#define KDT_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDT_OK = 0,
+    KDT_ERR_NULL_ARG = 1,     /* a required pointer is NULL, or both/neither of parent and vis */
+    KDT_ERR_BAD_SHAPE = 2,    /* sizes out of range or inconsistent (B, T, H, strides, kv bounds) */
+    KDT_ERR_UNSUPPORTED = 3,  /* valid but not implemented here (D_c != 512, D_r != 64, impl) */
+    KDT_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than kdt_verify_attn_workspace_size() */
+    KDT_ERR_CUDA = 5          /* a CUDA runtime call or kernel launch failed */
+} kdt_status;
+
+/* Static, never-NULL English name of a status. */
+const char *kdt_status_str(kdt_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int kdt_version(void);
+
+typedef enum { KDT_F32 = 0, KDT_BF16 = 1 } kdt_dtype;
+
+/* Kernel family. AUTO picks by dtype and shape: bf16 inputs use the tcgen05
+ * tensor-core kernel, fp32 inputs the SIMT kernel (which computes in fp32; the
+ * tensor path would round inputs). SIMT is valid for both dtypes. */
+typedef enum { KDT_IMPL_AUTO = 0, KDT_IMPL_SIMT = 1, KDT_IMPL_TCGEN05 = 2 } kdt_impl;
+
+/*
+ * kdt_build_visibility -- draft-tree parent array -> packed ancestor bits.
+ *
+ * The mask comes from the tree (page "The Moment of Truth ...", section
+ * "Context"): tree key t is visible to query i iff t == i or t is an ancestor of i
+ * ("The Verify-Attn Kernel ...", sections "The Design Journey" and "Assumptions
+ * and the Path Forward").
+ *
+ *   parent  device int32 [B,T]; parent[b,0] is normally -1 (the root). Requires
+ *           -1 <= parent[b,i] < i (topological order; several roots allowed).
+ *   vis     device uint32 [B,T,W], W = ceil(T/32): bit (t % 32) of word t / 32 of
+ *           vis[b,i] is set iff t == i or t is an ancestor of i. Bits >= T are 0.
+ *   err     device int32, may be NULL. Zeroed, then set to 1 + (b*T + i) of the
+ *           first parent entry outside [-1, i); rows reached through such an entry
+ *           stop at it. If NULL, malformed entries are silently cut the same way.
+ * Errors: KDT_ERR_NULL_ARG (parent or vis NULL), KDT_ERR_BAD_SHAPE (B < 0, T < 1,
+ * T > 4096), KDT_ERR_CUDA.
+ */
+kdt_status kdt_build_visibility(const int32_t *parent, int B, int T, uint32_t *vis, int32_t *err,
+                                cudaStream_t stream);
+
+/* Arguments of kdt_verify_attn. Sizes: B >= 0 sequences, 1 <= T <= 4096 tree
+ * queries per sequence, 1 <= H <= 1024 heads. */
+typedef struct {
+    int B, T, H;
+    int D_c;                /* latent width, must be 512 */
+    int D_r;                /* rope width, must be 64 */
+    kdt_dtype dtype;        /* element type of q_nope, q_pe, c_kv, k_pe (all the same) */
+    const void *q_nope;     /* [B,T,H,512] absorbed query (q_nope . w_kc done by the caller) */
+    const void *q_pe;       /* [B,T,H,64] rotated rope query */
+    const void *c_kv;       /* [B,L,512] latent cache; row j of sequence b at c_kv + (b*L + j)*512 */
+    const void *k_pe;       /* [B,L,64]  rope keys, same row indexing */
+    int64_t kv_row_stride;  /* L: rows per sequence in c_kv/k_pe, >= max_kv_len */
+    const int32_t *prefix_len; /* device [B]: shared-prefix length; tree node t at row prefix_len[b]+t */
+    int max_kv_len;         /* host bound: >= max_b prefix_len[b] + T (sizes the grid, no sync) */
+    const int32_t *parent;  /* device [B,T] parent array, or NULL */
+    const uint32_t *vis;    /* device [B,T,ceil(T/32)] packed visibility bits, or NULL */
+    float scale;            /* score scale, e.g. 1/sqrt(192) */
+    float *out;             /* device fp32 [B,T,H,512] */
+    float *lse;             /* device fp32 [B,T,H], or NULL */
+    int32_t *err;           /* device int32 error word for the parent path, or NULL */
+    int impl;               /* kdt_impl */
+    int num_splits;         /* KV splits per row tile; 0 = choose automatically */
+} kdt_verify_args;
+
+/*
+ * kdt_verify_attn -- tree-verify MLA-absorb attention (the definition at the top).
+ *
+ * Exactly one of `parent` and `vis` must be non-NULL. With `parent`, the bits are
+ * first built into the workspace as by kdt_build_visibility (and `err` reports a
+ * malformed tree). With `vis`, the caller's bits are used as given: they need not
+ * come from a tree, and a row whose visible set is empty (no prefix, no bit set)
+ * gets out = 0 and lse = -inf.
+ * Rows of c_kv/k_pe at or beyond prefix_len[b] + T are never read, whatever they
+ * hold. Inputs are all fp32 or all bf16; out and lse are fp32.
+ * `workspace` must hold kdt_verify_attn_workspace_size(a) bytes (256-byte aligned;
+ * may be NULL when that size is 0). Its contents need no initialisation.
+ * Errors: KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE (including prefix bound violations
+ * detectable on the host: max_kv_len > kv_row_stride, max_kv_len < T),
+ * KDT_ERR_UNSUPPORTED (D_c != 512, D_r != 64, unknown impl, TCGEN05 with fp32),
+ * KDT_ERR_WORKSPACE, KDT_ERR_CUDA. prefix_len values are device data: the caller
+ * guarantees prefix_len[b] + T <= max_kv_len.
+ */
+kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* Bytes of workspace kdt_verify_attn needs for these arguments (0 possible).
+ * Depends only on host-side fields (sizes, dtype, impl, num_splits, which of
+ * parent/vis is given). Returns 0 for arguments kdt_verify_attn would reject. */
+size_t kdt_verify_attn_workspace_size(const kdt_verify_args *a);
+
+/* What kdt_verify_attn will launch for these arguments. */
+typedef struct {
+    int impl;               /* KDT_IMPL_SIMT or KDT_IMPL_TCGEN05 */
+    int num_splits;         /* KV splits actually used */
+    int num_launches;       /* kernels launched per call */
+    int ctas;               /* CTAs of the main attention kernel */
+    size_t workspace_bytes;
+} kdt_plan;
+
+kdt_status kdt_verify_attn_plan(const kdt_verify_args *a, kdt_plan *plan);
+
+/*
+ * kdt_merge_attn_states -- combine two attention results over DISJOINT key sets
+ * (e.g. a long prefix done elsewhere and the tree tail done here; section "Design
+ * Decisions and Trade-Offs" of "The Verify-Attn Kernel ..."):
+ *   M = max(lse_a, lse_b), w = exp(lse - M),
+ *   o = (w_a o_a + w_b o_b) / (w_a + w_b),  lse = M + ln(w_a + w_b);
+ * both -inf gives o = 0, lse = -inf.
+ *   o_a, o_b, o    device fp32 [rows, D]; lse_a, lse_b, lse  device fp32 [rows].
+ *   D a multiple of 4, 4 <= D <= 4096. `o`/`lse` may alias o_a/lse_a (in place).
+ * Errors: KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE, KDT_ERR_CUDA.
+ */
+kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const float *o_b,
+                                 const float *lse_b, int64_t rows, int D, float *o, float *lse,
+                                 cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDT_H */

@@ -1,0 +1,11 @@
+"""GB300-native (sm_103a) DDTree tree-verify MLA-absorb attention.
+
+The compute path is libkdt.so (C ABI in include/kdt.h, CUDA kernels in csrc/);
+this package holds the build script and a thin ctypes binding with the same names.
+"""
+from .kdt import (  # noqa: F401
+    DEFAULT_SCALE, EXPORTS, IMPLS, KdtError, VerifyArgs, build_visibility, lib, make_args,
+    merge_attn_states, plan, status_str, verify_attn, workspace_size,
+)
+
+__version__ = "0.1.0"

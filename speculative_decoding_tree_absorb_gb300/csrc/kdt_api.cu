@@ -1,0 +1,217 @@
+// C ABI of libkdt.so: argument checks, planning (kernel family, KV splits,
+// workspace layout) and launches. See include/kdt.h for the contract.
+#include "kdt_internal.cuh"
+
+#include <atomic>
+#include <math.h>
+
+namespace kdt {
+
+int sm_count() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+    const int slot = dev & 63;
+    int v = cached[slot].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        cached[slot].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Plan {
+    int impl = KDT_IMPL_SIMT;
+    int splits = 1;
+    int blocks_per_split = 1;
+    int ctas = 0;
+    int launches = 0;
+    size_t vis_off = 0, vis_bytes = 0;
+    size_t po_off = 0, po_bytes = 0;
+    size_t pl_off = 0, pl_bytes = 0;
+    size_t ws_bytes = 0;
+};
+
+kdt_status check_args(const kdt_verify_args *a) {
+    if (!a) return KDT_ERR_NULL_ARG;
+    if (a->B < 0 || a->B > 65535 || a->T < 1 || a->T > kMaxT || a->H < 1 || a->H > 1024)
+        return KDT_ERR_BAD_SHAPE;
+    if (a->D_c != kDc || a->D_r != kDr) return KDT_ERR_UNSUPPORTED;
+    if (a->dtype != KDT_F32 && a->dtype != KDT_BF16) return KDT_ERR_UNSUPPORTED;
+    if (a->impl != KDT_IMPL_AUTO && a->impl != KDT_IMPL_SIMT && a->impl != KDT_IMPL_TCGEN05)
+        return KDT_ERR_UNSUPPORTED;
+    if (a->num_splits < 0) return KDT_ERR_BAD_SHAPE;
+    if (a->B == 0) return KDT_OK;
+    if (!a->q_nope || !a->q_pe || !a->c_kv || !a->k_pe || !a->prefix_len || !a->out) return KDT_ERR_NULL_ARG;
+    if ((a->parent == nullptr) == (a->vis == nullptr)) return KDT_ERR_NULL_ARG;
+    if (a->max_kv_len < a->T || (int64_t)a->max_kv_len > a->kv_row_stride) return KDT_ERR_BAD_SHAPE;
+    if (!aligned16(a->q_nope) || !aligned16(a->q_pe) || !aligned16(a->c_kv) || !aligned16(a->k_pe) ||
+        !aligned16(a->out) || (reinterpret_cast<uintptr_t>(a->lse) & 3u))
+        return KDT_ERR_BAD_SHAPE;
+    if (!(a->scale == a->scale) || isinf(a->scale)) return KDT_ERR_BAD_SHAPE;
+    return KDT_OK;
+}
+
+// Pure function of host-side fields: kernel family, splits, workspace layout.
+kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
+    kdt_status st = check_args(a);
+    if (st != KDT_OK) return st;
+    Plan p;
+    if (a->B == 0) {
+        *pl = p;
+        return KDT_OK;
+    }
+    if (a->impl == KDT_IMPL_TCGEN05) return KDT_ERR_UNSUPPORTED;   // tensor path not built yet
+    p.impl = KDT_IMPL_SIMT;
+    const int64_t rows_seq = (int64_t)a->T * a->H;
+    const int64_t rows_total = rows_seq * a->B;
+    const int row_tiles = (int)((rows_seq + kSimtRows - 1) / kSimtRows);
+    const int nblk = (a->max_kv_len + kSimtKeys - 1) / kSimtKeys;
+    const int64_t base = (int64_t)row_tiles * a->B;
+    int splits;
+    if (a->num_splits > 0) {
+        splits = a->num_splits;
+    } else {
+        // fill about two waves of one-CTA-per-SM, with at least 4 key blocks per split
+        const int64_t want = (2LL * sm_count() + base - 1) / base;
+        splits = (int)(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
+        const int cap = nblk / 4 > 1 ? nblk / 4 : 1;
+        if (splits > cap) splits = cap;
+    }
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    if (splits > nblk) splits = nblk;
+    p.blocks_per_split = (nblk + splits - 1) / splits;
+    p.splits = (nblk + p.blocks_per_split - 1) / p.blocks_per_split;
+    p.ctas = (int)(base * p.splits);
+    size_t off = 0;
+    if (a->parent) {
+        const int W = (a->T + 31) / 32;
+        p.vis_off = off;
+        p.vis_bytes = (size_t)a->B * a->T * W * sizeof(uint32_t);
+        off = align_up(off + p.vis_bytes);
+    }
+    if (p.splits > 1) {
+        p.po_off = off;
+        p.po_bytes = (size_t)p.splits * rows_total * kDc * sizeof(float);
+        off = align_up(off + p.po_bytes);
+        p.pl_off = off;
+        p.pl_bytes = (size_t)p.splits * rows_total * sizeof(float);
+        off = align_up(off + p.pl_bytes);
+    }
+    p.ws_bytes = off;
+    p.launches = (a->parent ? 1 : 0) + 1 + (p.splits > 1 ? 1 : 0);
+    *pl = p;
+    return KDT_OK;
+}
+
+}  // namespace
+}  // namespace kdt
+
+using namespace kdt;
+
+extern "C" {
+
+const char *kdt_status_str(kdt_status s) {
+    switch (s) {
+        case KDT_OK: return "ok";
+        case KDT_ERR_NULL_ARG: return "null argument";
+        case KDT_ERR_BAD_SHAPE: return "bad shape or layout";
+        case KDT_ERR_UNSUPPORTED: return "unsupported configuration";
+        case KDT_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDT_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int kdt_version(void) { return 100; }
+
+kdt_status kdt_build_visibility(const int32_t *parent, int B, int T, uint32_t *vis, int32_t *err,
+                                cudaStream_t stream) {
+    if (B < 0 || B > 65535 || T < 1 || T > kMaxT) return KDT_ERR_BAD_SHAPE;
+    if (B > 0 && (!parent || !vis)) return KDT_ERR_NULL_ARG;
+    return launch_build_visibility(parent, B, T, vis, err, stream) == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
+}
+
+size_t kdt_verify_attn_workspace_size(const kdt_verify_args *a) {
+    Plan p;
+    if (make_plan(a, &p) != KDT_OK) return 0;
+    return p.ws_bytes;
+}
+
+kdt_status kdt_verify_attn_plan(const kdt_verify_args *a, kdt_plan *out) {
+    if (!out) return KDT_ERR_NULL_ARG;
+    Plan p;
+    kdt_status st = make_plan(a, &p);
+    if (st != KDT_OK) return st;
+    out->impl = p.impl;
+    out->num_splits = p.splits;
+    out->num_launches = p.launches;
+    out->ctas = p.ctas;
+    out->workspace_bytes = p.ws_bytes;
+    return KDT_OK;
+}
+
+kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    Plan p;
+    kdt_status st = make_plan(a, &p);
+    if (st != KDT_OK) return st;
+    if (a->B == 0) return KDT_OK;
+    if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return KDT_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+
+    VerifyParams vp;
+    vp.B = a->B;
+    vp.T = a->T;
+    vp.H = a->H;
+    vp.W = (a->T + 31) / 32;
+    vp.L = a->kv_row_stride;
+    vp.q_nope = a->q_nope;
+    vp.q_pe = a->q_pe;
+    vp.c_kv = a->c_kv;
+    vp.k_pe = a->k_pe;
+    vp.prefix_len = a->prefix_len;
+    vp.scale_log2 = a->scale * 1.4426950408889634f;
+    vp.out = a->out;
+    vp.lse = a->lse;
+    vp.num_splits = p.splits;
+    vp.blocks_per_split = p.blocks_per_split;
+    vp.rows_total = (int64_t)a->B * a->T * a->H;
+    vp.part_o = p.splits > 1 ? reinterpret_cast<float *>(ws + p.po_off) : nullptr;
+    vp.part_lse = p.splits > 1 ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
+
+    if (a->parent) {
+        uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);
+        if (launch_build_visibility(a->parent, a->B, a->T, vis, a->err, stream) != cudaSuccess) return KDT_ERR_CUDA;
+        vp.vis = vis;
+    } else {
+        vp.vis = a->vis;
+    }
+    if (launch_verify_simt(vp, a->dtype, stream) != cudaSuccess) return KDT_ERR_CUDA;
+    if (p.splits > 1) {
+        if (launch_merge_splits(vp.part_o, vp.part_lse, p.splits, vp.rows_total, a->out, a->lse, stream) !=
+            cudaSuccess)
+            return KDT_ERR_CUDA;
+    }
+    return KDT_OK;
+}
+
+kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                                 int64_t rows, int D, float *o, float *lse, cudaStream_t stream) {
+    if (rows < 0 || D < 4 || D > 4096 || (D & 3)) return KDT_ERR_BAD_SHAPE;
+    if (rows == 0) return KDT_OK;
+    if (!o_a || !lse_a || !o_b || !lse_b || !o || !lse) return KDT_ERR_NULL_ARG;
+    if (!aligned16(o_a) || !aligned16(o_b) || !aligned16(o)) return KDT_ERR_BAD_SHAPE;
+    if (rows > (int64_t)1 << 34) return KDT_ERR_BAD_SHAPE;
+    return launch_merge_two(o_a, lse_a, o_b, lse_b, rows, D, o, lse, stream) == cudaSuccess ? KDT_OK
+                                                                                               : KDT_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Internal declarations shared by the translation units of libkdt.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kdt.h"
+
+namespace kdt {
+
+constexpr int kDc = 512;   // latent width of the MLA cache
+constexpr int kDr = 64;    // rope width
+constexpr int kDqk = kDc + kDr;
+constexpr int kMaxSplits = 32;
+constexpr int kMaxT = 4096;
+
+// Everything an attention kernel needs, already validated on the host.
+struct VerifyParams {
+    int B, T, H, W;            // W = ceil(T/32) visibility words per query
+    int64_t L;                 // cache rows per sequence
+    const void *q_nope, *q_pe, *c_kv, *k_pe;
+    const int32_t *prefix_len;
+    const uint32_t *vis;       // [B,T,W]
+    float scale_log2;          // scale * log2(e): scores are kept in base-2 units
+    float *out, *lse;          // final outputs (used when num_splits == 1)
+    float *part_o, *part_lse;  // [num_splits, rows_total, 512] / [num_splits, rows_total]
+    int num_splits;
+    int blocks_per_split;      // key blocks (of the kernel's block size) per split
+    int64_t rows_total;        // B*T*H
+};
+
+// K0: parent -> packed ancestor bits.
+cudaError_t launch_build_visibility(const int32_t *parent, int B, int T, uint32_t *vis, int32_t *err,
+                                    cudaStream_t s);
+
+// K3: SIMT verify (fp32 arithmetic, fp32 or bf16 inputs).
+constexpr int kSimtRows = 64;
+constexpr int kSimtKeys = 64;
+cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, cudaStream_t s);
+
+// K2: merge the split partials into out/lse.
+cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int num_splits, int64_t rows,
+                                float *out, float *lse, cudaStream_t s);
+
+// Public two-state merge.
+cudaError_t launch_merge_two(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                             int64_t rows, int D, float *o, float *lse, cudaStream_t s);
+
+// Per-device SM count (cached).
+int sm_count();
+
+}  // namespace kdt

@@ -1,0 +1,198 @@
+"""Thin Python binding of libkdt.so (ctypes). Argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; this module passes device
+pointers (``tensor.data_ptr()``) and the current CUDA stream, and allocates
+output and workspace tensors with torch when the caller does not pass them.
+There is no CPU fallback: if libkdt.so is missing, importing the library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libkdt.so")
+
+KDT_OK, KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE, KDT_ERR_UNSUPPORTED, KDT_ERR_WORKSPACE, KDT_ERR_CUDA = range(6)
+KDT_F32, KDT_BF16 = 0, 1
+IMPLS = {"auto": 0, "simt": 1, "tcgen05": 2}
+IMPL_NAMES = {v: k for k, v in IMPLS.items()}
+DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
+
+# Names the header declares (checked by the CPU test suite against include/kdt.h).
+EXPORTS = ("kdt_status_str", "kdt_version", "kdt_build_visibility", "kdt_verify_attn",
+           "kdt_verify_attn_workspace_size", "kdt_verify_attn_plan", "kdt_merge_attn_states")
+
+
+class KdtError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+
+
+class VerifyArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+        ("D_c", ctypes.c_int), ("D_r", ctypes.c_int), ("dtype", ctypes.c_int),
+        ("q_nope", ctypes.c_void_p), ("q_pe", ctypes.c_void_p),
+        ("c_kv", ctypes.c_void_p), ("k_pe", ctypes.c_void_p),
+        ("kv_row_stride", ctypes.c_int64),
+        ("prefix_len", ctypes.c_void_p),
+        ("max_kv_len", ctypes.c_int),
+        ("parent", ctypes.c_void_p), ("vis", ctypes.c_void_p),
+        ("scale", ctypes.c_float),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("err", ctypes.c_void_p),
+        ("impl", ctypes.c_int), ("num_splits", ctypes.c_int),
+    ]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("impl", ctypes.c_int), ("num_splits", ctypes.c_int), ("num_launches", ctypes.c_int),
+                ("ctas", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libkdt.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libkdt.so not found at {LIB_PATH}: build it with "
+                              "`python -m speculative_decoding_tree_absorb_gb300.build_lib` "
+                              "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp = ctypes.c_void_p
+        L.kdt_status_str.argtypes = [ctypes.c_int]
+        L.kdt_status_str.restype = ctypes.c_char_p
+        L.kdt_version.argtypes = []
+        L.kdt_version.restype = ctypes.c_int
+        L.kdt_build_visibility.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+        L.kdt_build_visibility.restype = ctypes.c_int
+        L.kdt_verify_attn.argtypes = [ctypes.POINTER(VerifyArgs), vp, ctypes.c_size_t, vp]
+        L.kdt_verify_attn.restype = ctypes.c_int
+        L.kdt_verify_attn_workspace_size.argtypes = [ctypes.POINTER(VerifyArgs)]
+        L.kdt_verify_attn_workspace_size.restype = ctypes.c_size_t
+        L.kdt_verify_attn_plan.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(Plan)]
+        L.kdt_verify_attn_plan.restype = ctypes.c_int
+        L.kdt_merge_attn_states.argtypes = [vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int, vp, vp, vp]
+        L.kdt_merge_attn_states.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().kdt_status_str(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != KDT_OK:
+        raise KdtError(status, where)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return KDT_F32
+    if t.dtype == torch.bfloat16:
+        return KDT_BF16
+    raise TypeError(f"inputs must be float32 or bfloat16, got {t.dtype}")
+
+
+def make_args(q_nope, q_pe, c_kv, k_pe, prefix_len, *, parent=None, vis=None, max_kv_len=None,
+              scale=DEFAULT_SCALE, out=None, lse=None, err=None, impl="auto", num_splits=0) -> VerifyArgs:
+    """Fill the C argument struct from tensors (no checks beyond what the library does)."""
+    B, T, H = q_nope.shape[0], q_nope.shape[1], q_nope.shape[2]
+    L = c_kv.shape[1]
+    a = VerifyArgs()
+    a.B, a.T, a.H = B, T, H
+    a.D_c, a.D_r = q_nope.shape[3], q_pe.shape[3]
+    a.dtype = _dtype_code(q_nope)
+    a.q_nope, a.q_pe, a.c_kv, a.k_pe = (t.data_ptr() for t in (q_nope, q_pe, c_kv, k_pe))
+    a.kv_row_stride = L
+    a.prefix_len = prefix_len.data_ptr()
+    a.max_kv_len = int(L if max_kv_len is None else max_kv_len)
+    a.parent = None if parent is None else parent.data_ptr()
+    a.vis = None if vis is None else vis.data_ptr()
+    a.scale = float(scale)
+    a.out = None if out is None else out.data_ptr()
+    a.lse = None if lse is None else lse.data_ptr()
+    a.err = None if err is None else err.data_ptr()
+    a.impl = IMPLS[impl] if isinstance(impl, str) else int(impl)
+    a.num_splits = int(num_splits)
+    return a
+
+
+def plan(args: VerifyArgs) -> dict:
+    p = Plan()
+    _check(lib().kdt_verify_attn_plan(ctypes.byref(args), ctypes.byref(p)), "kdt_verify_attn_plan")
+    return dict(impl=IMPL_NAMES.get(p.impl, p.impl), num_splits=p.num_splits, num_launches=p.num_launches,
+                ctas=p.ctas, workspace_bytes=int(p.workspace_bytes))
+
+
+def workspace_size(args: VerifyArgs) -> int:
+    return int(lib().kdt_verify_attn_workspace_size(ctypes.byref(args)))
+
+
+def build_visibility(parent, err=None, stream=None):
+    """parent int32 [B,T] (cuda) -> packed bits uint32-as-int32 tensor [B,T,ceil(T/32)]."""
+    import torch
+    B, T = parent.shape
+    vis = torch.empty((B, T, (T + 31) // 32), dtype=torch.int32, device=parent.device)
+    _check(lib().kdt_build_visibility(_ptr(parent), B, T, _ptr(vis), _ptr(err), _stream_ptr(stream)),
+           "kdt_build_visibility")
+    return vis
+
+
+def verify_attn(q_nope, q_pe, c_kv, k_pe, prefix_len, *, parent=None, vis=None, max_kv_len=None,
+                scale=DEFAULT_SCALE, out=None, lse=None, err=None, impl="auto", num_splits=0,
+                workspace=None, stream=None, want_lse=True):
+    """Tree-verify MLA-absorb attention. Returns (out [B,T,H,512] fp32, lse [B,T,H] fp32 or None).
+
+    ``max_kv_len`` defaults to the cache row stride (c_kv.shape[1]), a valid host
+    bound that needs no device->host read of prefix_len.
+    """
+    import torch
+    B, T, H = q_nope.shape[:3]
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((B, T, H, q_nope.shape[3]), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    a = make_args(q_nope, q_pe, c_kv, k_pe, prefix_len, parent=parent, vis=vis, max_kv_len=max_kv_len,
+                  scale=scale, out=out, lse=lse, err=err, impl=impl, num_splits=num_splits)
+    need = workspace_size(a)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kdt_verify_attn(ctypes.byref(a), _ptr(workspace), ws_bytes, _stream_ptr(stream)),
+           "kdt_verify_attn")
+    return out, lse
+
+
+def merge_attn_states(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
+    """Log-sum-exp merge of two attention states over disjoint key sets."""
+    import torch
+    D = o_a.shape[-1]
+    rows = lse_a.numel()
+    if out is None:
+        out = torch.empty_like(o_a)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    _check(lib().kdt_merge_attn_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, D, _ptr(out),
+                                       _ptr(lse), _stream_ptr(stream)), "kdt_merge_attn_states")
+    return out, lse

@@ -1,0 +1,128 @@
+"""CPU checks of the C ABI: the library loads, exports every function include/kdt.h
+declares, the ctypes struct matches the C layout, and host-side argument checks
+reject bad calls before any launch (none of these calls touch a GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kdt.h")
+
+
+@pytest.fixture(scope="module")
+def kdt():
+    from speculative_decoding_tree_absorb_gb300 import build_lib
+    build_lib.build()
+    import speculative_decoding_tree_absorb_gb300 as k
+    return k
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    names = set(re.findall(r"\b(kdt_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declarations_are_exported(kdt):
+    names = _declared_functions()
+    assert len(names) >= 7
+    lib = kdt.lib()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in kdt.h but not exported by libkdt.so"
+    assert set(kdt.EXPORTS) <= set(names)
+    nm = subprocess.run(["nm", "-D", "--defined-only", kdt.kdt.LIB_PATH], capture_output=True, text=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}$", nm, flags=re.M), n
+
+
+def test_struct_layout_matches_header(kdt, tmp_path):
+    prog = tmp_path / "layout.c"
+    fields = [f[0] for f in kdt.VerifyArgs._fields_]
+    body = "\n".join(f'printf("{f} %zu\\n", offsetof(kdt_verify_args, {f}));' for f in fields)
+    prog.write_text(f"""
+#include <stdio.h>
+#include <stddef.h>
+#include "kdt.h"
+int main(void) {{
+  printf("size %zu\\n", sizeof(kdt_verify_args));
+  printf("plan %zu\\n", sizeof(kdt_plan));
+  {body}
+  return 0;
+}}
+""")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", str(prog),
+                    "-o", str(exe)], check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    assert int(out["size"]) == ctypes.sizeof(kdt.VerifyArgs)
+    assert int(out["plan"]) == ctypes.sizeof(kdt.kdt.Plan)
+    for f in fields:
+        assert int(out[f]) == getattr(kdt.VerifyArgs, f).offset, f
+
+
+def _args(kdt, **kw):
+    a = kdt.VerifyArgs()
+    a.B, a.T, a.H, a.D_c, a.D_r, a.dtype = 2, 9, 8, 512, 64, 0
+    # fake, 256-aligned non-null addresses: only host-side checks run in these tests
+    a.q_nope, a.q_pe, a.c_kv, a.k_pe = 0x10000, 0x20000, 0x30000, 0x40000
+    a.kv_row_stride, a.prefix_len, a.max_kv_len = 46, 0x50000, 46
+    a.parent, a.vis = 0x60000, None
+    a.scale, a.out, a.lse, a.err, a.impl, a.num_splits = 0.07, 0x70000, 0x80000, None, 1, 2
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _status(kdt, a):
+    return kdt.lib().kdt_verify_attn(ctypes.byref(a), None, 0, None)
+
+
+def test_host_checks_reject_bad_arguments(kdt):
+    K = kdt.kdt
+    assert _status(kdt, _args(kdt, D_c=256)) == K.KDT_ERR_UNSUPPORTED
+    assert _status(kdt, _args(kdt, D_r=32)) == K.KDT_ERR_UNSUPPORTED
+    assert _status(kdt, _args(kdt, dtype=7)) == K.KDT_ERR_UNSUPPORTED
+    assert _status(kdt, _args(kdt, impl=9)) == K.KDT_ERR_UNSUPPORTED
+    assert _status(kdt, _args(kdt, q_nope=None)) == K.KDT_ERR_NULL_ARG
+    assert _status(kdt, _args(kdt, out=None)) == K.KDT_ERR_NULL_ARG
+    assert _status(kdt, _args(kdt, parent=None)) == K.KDT_ERR_NULL_ARG           # neither mask input
+    assert _status(kdt, _args(kdt, vis=0x90000)) == K.KDT_ERR_NULL_ARG           # both mask inputs
+    assert _status(kdt, _args(kdt, T=0)) == K.KDT_ERR_BAD_SHAPE
+    assert _status(kdt, _args(kdt, H=0)) == K.KDT_ERR_BAD_SHAPE
+    assert _status(kdt, _args(kdt, B=-1)) == K.KDT_ERR_BAD_SHAPE
+    assert _status(kdt, _args(kdt, max_kv_len=47)) == K.KDT_ERR_BAD_SHAPE        # beyond the row stride
+    assert _status(kdt, _args(kdt, max_kv_len=8)) == K.KDT_ERR_BAD_SHAPE         # below T
+    assert _status(kdt, _args(kdt, c_kv=0x30004)) == K.KDT_ERR_BAD_SHAPE         # misaligned
+    assert _status(kdt, _args(kdt, num_splits=-1)) == K.KDT_ERR_BAD_SHAPE
+    assert _status(kdt, _args(kdt, scale=float("nan"))) == K.KDT_ERR_BAD_SHAPE
+    # a valid call without the workspace it needs is refused before launching
+    assert _status(kdt, _args(kdt)) == K.KDT_ERR_WORKSPACE
+    assert _status(kdt, _args(kdt, B=0)) == K.KDT_OK                             # nothing to do
+    lib = kdt.lib()
+    assert lib.kdt_build_visibility(None, 2, 0, None, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_build_visibility(None, 2, 5, None, None, None) == K.KDT_ERR_NULL_ARG
+    assert lib.kdt_merge_attn_states(None, None, None, None, 4, 6, None, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_merge_attn_states(None, None, None, None, 4, 512, None, None, None) == K.KDT_ERR_NULL_ARG
+    assert kdt.status_str(K.KDT_ERR_WORKSPACE) == "workspace missing or too small"
+    assert lib.kdt_version() >= 100
+
+
+def test_plan_and_workspace_are_host_only(kdt):
+    a = _args(kdt, num_splits=3)
+    p = kdt.plan(a)
+    assert p["impl"] == "simt" and p["num_splits"] == 1            # 46 keys = one 64-key block
+    assert p["num_launches"] == 2                                  # visibility + attention
+    assert kdt.workspace_size(a) == p["workspace_bytes"] >= 2 * 9 * 4
+    b = _args(kdt, kv_row_stride=4096 + 32, max_kv_len=4096 + 32, T=32, H=64, B=1, num_splits=8, vis=0x90000,
+              parent=None)
+    p = kdt.plan(b)
+    assert p["num_splits"] == 8 and p["num_launches"] == 2        # attention + merge
+    rows = 1 * 32 * 64
+    assert p["workspace_bytes"] >= 8 * rows * 512 * 4 + 8 * rows * 4
+    assert kdt.workspace_size(_args(kdt, D_c=3)) == 0

@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same
+seeded inputs. Visibility bits must match bit for bit; attention must satisfy
+|gpu - oracle| <= atol + rtol*|oracle| elementwise on out and lse with
+(atol, rtol) = (1e-4, 1e-4) for fp32 inputs and (2e-2, 2e-2) for bf16 inputs."""
+import zlib
+
+import numpy as np
+import pytest
+
+import workloads as wl
+from tests import gpu_util as G
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+IMPLS_BY_DTYPE = {"f32": ["simt"], "bf16": ["simt", "auto"]}
+
+
+@pytest.fixture(scope="module")
+def kdt():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_tree_absorb_gb300 import build_lib
+    build_lib.build()
+    import speculative_decoding_tree_absorb_gb300 as k
+    return k
+
+
+def _compare(case, out, lse, ref_out, ref_lse, what):
+    atol, rtol = H.TOL[case.dtype]
+    H.assert_close(out, ref_out, atol, rtol, what + " out")
+    H.assert_close(lse, ref_lse, atol, rtol, what + " lse")
+
+
+# ---------------------------------------------------------------- visibility --
+
+def test_visibility_bit_exact_on_every_small_tree(kdt, oracle_mod):
+    import torch
+    for T in range(1, 7):
+        parents = np.stack(list(H.all_parent_arrays(T)))
+        got = kdt.build_visibility(torch.from_numpy(parents).cuda()).cpu().numpy().view(np.uint32)
+        np.testing.assert_array_equal(got, oracle_mod.build_visibility(parents))
+
+
+@pytest.mark.parametrize("T", [1, 9, 31, 32, 33, 64, 100, 128, 129, 200, 1000])
+@pytest.mark.parametrize("kind", ["uniform", "geometric", "depth16", "window8", "chain", "star"])
+def test_visibility_bit_exact_on_config_trees(kdt, oracle_mod, T, kind):
+    import torch
+    parents = np.stack([wl.TREE_KINDS[kind](77, f"v/{b}", T) for b in range(5)])
+    got = kdt.build_visibility(torch.from_numpy(parents).cuda()).cpu().numpy().view(np.uint32)
+    np.testing.assert_array_equal(got, oracle_mod.build_visibility(parents))
+
+
+def test_visibility_error_word_matches_oracle(kdt, oracle_mod):
+    import torch
+    p = np.stack([wl.tree_geometric(5, f"e/{b}", 40) for b in range(3)])
+    p[2, 7] = 9            # >= i
+    p[1, 30] = -3          # < -1
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kdt.build_visibility(torch.from_numpy(p).cuda(), err=err)
+    with pytest.raises(oracle_mod.OracleError) as e:
+        oracle_mod.build_visibility(p)
+    assert int(err.item()) == 1 * 40 + 30 + 1
+    assert f"flat index {1 * 40 + 30}" in str(e.value)
+    # a well-formed tree clears the word
+    kdt.build_visibility(torch.from_numpy(p[:1].copy()).cuda(), err=err)
+    assert int(err.item()) == 0
+
+
+# ------------------------------------------------------------------- attention --
+
+EDGE_CASES = [
+    # name, B, T, H, prefix, tree
+    ("pages_p0_b8", 2, 9, 8, 0, "uniform"),
+    ("pages_p1_b4", 3, 5, 8, 1, "uniform"),
+    ("pages_p37_b8", 2, 9, 8, 37, "uniform"),
+    ("single_query", 2, 1, 8, 70, "uniform"),
+    ("t31", 1, 31, 4, 19, "geometric"),
+    ("t32", 2, 32, 2, 64, "uniform"),
+    ("t33", 2, 33, 2, 63, "depth16"),
+    ("ragged_tail", 3, 17, 4, (3, 130, 64), "geometric"),
+    ("one_head", 2, 12, 1, (5, 200), "window8"),
+    ("h16_multi_tile", 1, 20, 16, 150, "uniform"),
+    ("chain", 2, 24, 8, 90, "chain"),
+    ("star", 2, 24, 8, 90, "star"),
+    ("h128", 1, 3, 128, 300, "uniform"),
+    ("wide_tree", 1, 130, 2, 10, "geometric"),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("name,B,T,Hh,prefix,tree", EDGE_CASES)
+def test_edge_cases_match_oracle(kdt, oracle_mod, dtype, name, B, T, Hh, prefix, tree):
+    case = wl.make_case(name, B=B, T=T, H=Hh, prefix=prefix, dtype=dtype, tree=tree, seed=zlib.crc32(name.encode()) % 1000)
+    ref_out, ref_lse = oracle_mod.verify_attn(case)
+    for impl in IMPLS_BY_DTYPE[dtype]:
+        for use_bits in (False, True):
+            out, lse, err = G.run(case, impl=impl, use_bits=use_bits)
+            assert err == 0
+            assert np.isfinite(out).all() and np.isfinite(lse).all()
+            _compare(case, out, lse, ref_out, ref_lse, f"{name}/{impl}/bits={use_bits}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiny_config_full(kdt, oracle_mod, dtype):
+    case = wl.make_config("tiny", dtype=dtype)
+    ref_out, ref_lse = oracle_mod.verify_attn(case)
+    for impl in IMPLS_BY_DTYPE[dtype]:
+        out, lse, err = G.run(case, impl=impl)
+        assert err == 0
+        _compare(case, out, lse, ref_out, ref_lse, f"tiny/{impl}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_result_independent_of_split_count(kdt, oracle_mod, dtype):
+    case = wl.make_case("splits", B=3, T=16, H=8, prefix=(700, 33, 1000), dtype=dtype, tree="geometric", seed=5)
+    ref_out, ref_lse = oracle_mod.verify_attn(case)
+    for impl in IMPLS_BY_DTYPE[dtype]:
+        base = None
+        for s in (1, 2, 3, 5, 8, 17, 32):
+            out, lse, _ = G.run(case, impl=impl, num_splits=s)
+            _compare(case, out, lse, ref_out, ref_lse, f"splits={s}/{impl}")
+            if base is None:
+                base = (out, lse)
+            else:
+                H.assert_close(out, base[0], 1e-5, 1e-5, "split vs unsplit")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_caller_bits_including_empty_rows(kdt, oracle_mod, dtype):
+    case = wl.make_case("bits", B=2, T=40, H=4, prefix=(0, 65), dtype=dtype, tree="uniform", seed=8)
+    vis = wl.random_vis_bits(8, "bits", case.B, case.T, density=0.3, force_self=False)
+    vis[0, 3] = 0            # prefix 0 and no bit: empty visible set
+    vis[0, 39] = 0
+    ref_out, ref_lse = oracle_mod.verify_attn(case, vis=vis)
+    for impl in IMPLS_BY_DTYPE[dtype]:
+        out, lse, _ = G.run(case, impl=impl, vis=vis)
+        assert np.isneginf(lse[0, 3]).all() and (out[0, 3] == 0).all()
+        _compare(case, out, lse, ref_out, ref_lse, f"bits/{impl}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_single_visible_key_is_exact(kdt, dtype):
+    case = wl.make_case("one", B=2, T=6, H=64, prefix=0, dtype=dtype, tree="uniform", seed=13)
+    for impl in IMPLS_BY_DTYPE[dtype]:
+        out, lse, _ = G.run(case, impl=impl)
+        want = H.widen(case.c_kv[:, 0], dtype)
+        for h in range(case.H):
+            np.testing.assert_array_equal(out[:, 0, h].astype(np.float64), want)
+
+
+def test_golden_zero_query_closed_form(kdt):
+    for dtype in ("f32", "bf16"):
+        for g in H.read_golden_cases("q_zero_uniform.txt"):
+            T = len(g["parent"])
+            case = wl.make_case(g["name"], B=1, T=T, H=8, prefix=g["prefix"], dtype=dtype, tree=g["parent"], seed=5)
+            case.q_nope[:] = 0
+            case.q_pe[:] = 0
+            for impl in IMPLS_BY_DTYPE[dtype]:
+                out, lse, _ = G.run(case, impl=impl)
+                np.testing.assert_allclose(lse[0], np.log(np.array(g["count"], dtype=np.float64))[:, None]
+                                           * np.ones((1, 8)), rtol=1e-5, atol=1e-5)
+                ck = H.widen(case.c_kv[0], dtype)
+                for i, path in g["paths"].items():
+                    rows = list(range(g["prefix"])) + [g["prefix"] + t for t in path]
+                    np.testing.assert_allclose(out[0, i], np.broadcast_to(ck[rows].mean(0), (8, 512)),
+                                               rtol=1e-4, atol=1e-5)
+
+
+def test_merge_attn_states_matches_oracle(kdt, oracle_mod):
+    import torch
+    rng = np.random.default_rng(3)
+    n, D = 1000, 512
+    o_a = rng.standard_normal((n, D)).astype(np.float32)
+    o_b = rng.standard_normal((n, D)).astype(np.float32)
+    la = (rng.standard_normal(n) * 5).astype(np.float32)
+    lb = (rng.standard_normal(n) * 5).astype(np.float32)
+    la[::7] = -np.inf
+    lb[::11] = -np.inf
+    ref_o, ref_l = oracle_mod.merge_states(o_a, la, o_b, lb)
+    t = [torch.from_numpy(x).cuda() for x in (o_a, la, o_b, lb)]
+    o, l = kdt.merge_attn_states(*t)
+    H.assert_close(o.cpu().numpy(), ref_o, 1e-5, 1e-5, "merge o")
+    H.assert_close(l.cpu().numpy(), ref_l, 1e-5, 1e-5, "merge lse")
+    # in place into the first state
+    kdt.merge_attn_states(*t, out=t[0], lse=t[1])
+    H.assert_close(t[0].cpu().numpy(), ref_o, 1e-5, 1e-5, "merge in place")
+
+
+# ------------------------------------------------------- full-size configurations --
+
+def _sample_rows(case, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(case.rows, size=min(n, case.rows), replace=False)
+    # always include the first and last row of every sequence (tile edges)
+    edge = np.concatenate([[b * case.T * case.H, (b + 1) * case.T * case.H - 1] for b in range(case.B)])
+    return np.unique(np.concatenate([rows, edge]))
+
+
+@pytest.mark.parametrize("name", ["kimi", "ragged", "target", "long", "dsv3"])
+def test_full_size_config_sampled(kdt, oracle_mod, name):
+    case = wl.make_config(name)
+    out, lse, err = G.run(case, impl="auto")
+    assert err == 0
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    rows = _sample_rows(case, 192, seed=len(name))
+    ref_out, ref_lse = oracle_mod.verify_attn_rows(case, rows)
+    _compare(case, out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, name)
