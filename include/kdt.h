@@ -28,9 +28,10 @@
  *    checks run on the host before any launch and never synchronise. A launch
  *    failure is returned as KDT_ERR_CUDA; faults inside a kernel surface at the
  *    caller's next synchronisation.
- *  - The library allocates no memory: scratch space is the caller's `workspace`.
- *    It keeps no global state except a per-device cache of the SM count and
- *    kernel attributes. Concurrent calls are safe given distinct workspaces.
+ *  - The library allocates no memory: scratch space is the caller's `workspace`
+ *    (kdt_verify_attn_noalloc, at the end, uses a fixed array inside the library
+ *    instead). It keeps no other global state than a per-device cache of the SM
+ *    count. Concurrent calls are safe given distinct workspaces.
  *  - Errors found in the DATA on the device (a malformed tree) are reported
  *    through a caller-provided device word `err` (0 = ok, else 1 + the flat index
  *    b*T + i of the first offending parent entry), never by a trap.
@@ -164,6 +165,38 @@ kdt_status kdt_verify_attn_plan(const kdt_verify_args *a, kdt_plan *plan);
 kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const float *o_b,
                                  const float *lse_b, int64_t rows, int D, float *o, float *lse,
                                  cudaStream_t stream);
+
+/*
+ * kdt_verify_attn_noalloc -- kdt_verify_attn without a caller workspace.
+ *
+ * The method's pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory when they call the library: a
+ * serving engine that reserved nearly all HBM for its KV-cache pool at start-up
+ * (a later cudaMalloc fails, or would fragment the pool), a plugin inside a host
+ * framework whose allocator it may not call, or a latency-critical loop that cannot
+ * afford the implicit device synchronisation of cudaMalloc/cudaFree.
+ *
+ * Same arguments, results and errors as kdt_verify_attn, but the scratch space
+ * (packed visibility bits built from `parent`, split-KV partials) lives in a fixed
+ * device array of KDT_NOALLOC_SCRATCH_BYTES inside libkdt.so, present on every GPU
+ * that loads the library until the process exits. Nothing is allocated: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *  - Size limit: if the call needs more scratch than KDT_NOALLOC_SCRATCH_BYTES, an
+ *    automatic split count (num_splits == 0) is lowered until the partials fit;
+ *    if the call still does not fit, or an explicit num_splits does not fit, it
+ *    returns KDT_ERR_WORKSPACE and launches nothing.
+ *  - Set-up: the first call made on a device (with that device current) looks up
+ *    the array's device address with cudaGetSymbolAddress; make that first call
+ *    before any stream capture on that device.
+ *  - Sharing: every call on a device uses the same array and it keeps the last
+ *    call's contents. The kernels overwrite every scratch byte they read, so no
+ *    clearing is needed, but calls whose work overlaps on the GPU (other streams,
+ *    other host threads) race on the array: order them on one stream or serialise
+ *    them.
+ */
+#define KDT_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+kdt_status kdt_verify_attn_noalloc(const kdt_verify_args *a, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

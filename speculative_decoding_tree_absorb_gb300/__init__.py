@@ -5,7 +5,7 @@ this package holds the build script and a thin ctypes binding with the same name
 """
 from .kdt import (  # noqa: F401
     DEFAULT_SCALE, EXPORTS, IMPLS, KdtError, VerifyArgs, build_visibility, lib, make_args,
-    merge_attn_states, plan, status_str, verify_attn, workspace_size,
+    merge_attn_states, plan, status_str, verify_attn, verify_attn_noalloc, workspace_size,
 )
 
 __version__ = "0.1.0"

@@ -23,7 +23,8 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 
 # Names the header declares (checked by the CPU test suite against include/kdt.h).
 EXPORTS = ("kdt_status_str", "kdt_version", "kdt_build_visibility", "kdt_verify_attn",
-           "kdt_verify_attn_workspace_size", "kdt_verify_attn_plan", "kdt_merge_attn_states")
+           "kdt_verify_attn_workspace_size", "kdt_verify_attn_plan", "kdt_merge_attn_states",
+           "kdt_verify_attn_noalloc")
 
 
 class KdtError(RuntimeError):
@@ -80,6 +81,8 @@ def lib():
         L.kdt_verify_attn_plan.restype = ctypes.c_int
         L.kdt_merge_attn_states.argtypes = [vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int, vp, vp, vp]
         L.kdt_merge_attn_states.restype = ctypes.c_int
+        L.kdt_verify_attn_noalloc.argtypes = [ctypes.POINTER(VerifyArgs), vp]
+        L.kdt_verify_attn_noalloc.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -195,4 +198,19 @@ def merge_attn_states(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
         lse = torch.empty_like(lse_a)
     _check(lib().kdt_merge_attn_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, D, _ptr(out),
                                        _ptr(lse), _stream_ptr(stream)), "kdt_merge_attn_states")
+    return out, lse
+
+
+def verify_attn_noalloc(q_nope, q_pe, c_kv, k_pe, prefix_len, *, out, lse=None, parent=None, vis=None,
+                        max_kv_len=None, scale=DEFAULT_SCALE, err=None, impl="auto", num_splits=0, stream=None):
+    """kdt_verify_attn_noalloc: the same attention with the library's fixed scratch array.
+
+    For callers that must not allocate device memory at call time: the caller passes
+    every input and output (``out`` is required); the library neither allocates nor
+    asks for a workspace. Calls on one device share the scratch array, so calls
+    that overlap on the GPU race; see include/kdt.h.
+    """
+    a = make_args(q_nope, q_pe, c_kv, k_pe, prefix_len, parent=parent, vis=vis, max_kv_len=max_kv_len,
+                  scale=scale, out=out, lse=lse, err=err, impl=impl, num_splits=num_splits)
+    _check(lib().kdt_verify_attn_noalloc(ctypes.byref(a), _stream_ptr(stream)), "kdt_verify_attn_noalloc")
     return out, lse
