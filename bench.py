@@ -42,6 +42,33 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 SMS = 152
 FP32_LANES_PER_SM = 128
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# dominant kernel from an ncu capture, with the hash of the kernel source it was
+# taken on; reported only while the source is unchanged (see profiles/).
+TRAFFIC = {
+    ("tcgen05", "target"): {"src_hash": "d93285aeebdb0232", "bytes": 151.02e6,
+                            "profile": "profiles/verify_tc_target.md"},
+    ("simt", "target"): {"src_hash": None, "bytes": 155.52e6, "profile": "profiles/verify_simt_target.md"},
+}
+
+
+def kernel_src_hash(impl):
+    import hashlib
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_absorb_gb300", "csrc")
+    files = ["verify_tc.cu", "tc_ptx.cuh"] if impl == "tcgen05" else ["verify_simt.cu"]
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(impl, config):
+    t = TRAFFIC.get((impl, config))
+    if not t or t["src_hash"] != kernel_src_hash(impl):
+        return None
+    return t["bytes"]
+
 
 def load_peaks():
     try:
@@ -386,7 +413,8 @@ def main():
                               "frac": roof_us / (ms * 1e3), "basis": f"max(FLOPs/bf16 peak, bytes/HBM) of "
                                                                     f"{peaks['source']} peaks"},
         "roofline": {"bound": bound, "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": attn_tflops / peak, "traffic": None, "peak_basis": peak_note,
+                     "frac": attn_tflops / peak, "traffic": measured_traffic(pl["impl"], args.config),
+                     "peak_basis": peak_note,
                      "kernel": f"verify_{pl['impl']} (+ split merge when num_splits > 1)"},
         "algorithmic": {"flops": flops, "bytes": counts["bytes"], "kv_bytes": counts["kv_bytes"]},
         "clocks": clocks,

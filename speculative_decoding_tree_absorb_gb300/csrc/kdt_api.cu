@@ -68,19 +68,28 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         *pl = p;
         return KDT_OK;
     }
-    if (a->impl == KDT_IMPL_TCGEN05) return KDT_ERR_UNSUPPORTED;   // tensor path not built yet
-    p.impl = KDT_IMPL_SIMT;
     const int64_t rows_seq = (int64_t)a->T * a->H;
     const int64_t rows_total = rows_seq * a->B;
-    const int row_tiles = (int)((rows_seq + kSimtRows - 1) / kSimtRows);
-    const int nblk = (a->max_kv_len + kSimtKeys - 1) / kSimtKeys;
+    // Kernel family: bf16 inputs go to the tensor-core kernel; fp32 inputs stay on the
+    // SIMT kernel (the tensor path would round them).
+    const bool tc = a->impl == KDT_IMPL_TCGEN05 || (a->impl == KDT_IMPL_AUTO && a->dtype == KDT_BF16);
+    if (tc && a->dtype != KDT_BF16) return KDT_ERR_UNSUPPORTED;
+    if (tc && (rows_total >= ((int64_t)1 << 31) || a->kv_row_stride >= ((int64_t)1 << 31)))
+        return KDT_ERR_BAD_SHAPE;
+    p.impl = tc ? KDT_IMPL_TCGEN05 : KDT_IMPL_SIMT;
+    const int unit_rows = tc ? tc_rows_per_unit() : kSimtRows;
+    const int unit_keys = tc ? tc_keys_per_block() : kSimtKeys;
+    const int row_tiles = (int)((rows_seq + unit_rows - 1) / unit_rows);
+    const int nblk = (a->max_kv_len + unit_keys - 1) / unit_keys;
     const int64_t base = (int64_t)row_tiles * a->B;
+    // concurrent units: one CTA per SM for SIMT, one 2-CTA cluster per SM pair for tcgen05
+    const int64_t slots = tc ? sm_count() / 2 : sm_count();
     int splits;
     if (a->num_splits > 0) {
         splits = a->num_splits;
     } else {
-        // fill about two waves of one-CTA-per-SM, with at least 4 key blocks per split
-        const int64_t want = (2LL * sm_count() + base - 1) / base;
+        // fill about two waves, with at least 4 key blocks per split
+        const int64_t want = (2LL * slots + base - 1) / base;
         splits = (int)(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
         const int cap = nblk / 4 > 1 ? nblk / 4 : 1;
         if (splits > cap) splits = cap;
@@ -89,7 +98,7 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     if (splits > nblk) splits = nblk;
     p.blocks_per_split = (nblk + splits - 1) / splits;
     p.splits = (nblk + p.blocks_per_split - 1) / p.blocks_per_split;
-    p.ctas = (int)(base * p.splits);
+    p.ctas = (int)(base * p.splits * (tc ? 2 : 1));
     size_t off = 0;
     if (a->parent) {
         const int W = (a->T + 31) / 32;
@@ -186,6 +195,7 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     vp.rows_total = (int64_t)a->B * a->T * a->H;
     vp.part_o = p.splits > 1 ? reinterpret_cast<float *>(ws + p.po_off) : nullptr;
     vp.part_lse = p.splits > 1 ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
+    vp.err = a->err;
 
     if (a->parent) {
         uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);
@@ -193,8 +203,11 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
         vp.vis = vis;
     } else {
         vp.vis = a->vis;
+        if (a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t), stream) != cudaSuccess) return KDT_ERR_CUDA;
     }
-    if (launch_verify_simt(vp, a->dtype, stream) != cudaSuccess) return KDT_ERR_CUDA;
+    const cudaError_t e = p.impl == KDT_IMPL_TCGEN05 ? launch_verify_tc(vp, stream)
+                                                     : launch_verify_simt(vp, a->dtype, stream);
+    if (e != cudaSuccess) return KDT_ERR_CUDA;
     if (p.splits > 1) {
         if (launch_merge_splits(vp.part_o, vp.part_lse, p.splits, vp.rows_total, a->out, a->lse, stream) !=
             cudaSuccess)

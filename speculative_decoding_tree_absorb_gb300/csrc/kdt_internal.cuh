@@ -28,6 +28,7 @@ struct VerifyParams {
     int num_splits;
     int blocks_per_split;      // key blocks (of the kernel's block size) per split
     int64_t rows_total;        // B*T*H
+    int32_t *err;              // caller error word (tensor-core path: negative = pipeline timeout)
 };
 
 // K0: parent -> packed ancestor bits.
@@ -38,6 +39,11 @@ cudaError_t launch_build_visibility(const int32_t *parent, int B, int T, uint32_
 constexpr int kSimtRows = 64;
 constexpr int kSimtKeys = 64;
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, cudaStream_t s);
+
+// K1: tcgen05 verify (bf16 inputs), 2-CTA clusters of 128 query rows x 128-key blocks.
+int tc_rows_per_unit();
+int tc_keys_per_block();
+cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t s);
 
 // K2: merge the split partials into out/lse.
 cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int num_splits, int64_t rows,
