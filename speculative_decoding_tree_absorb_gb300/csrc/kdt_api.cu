@@ -30,6 +30,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Plan {
     int impl = KDT_IMPL_SIMT;
     int splits = 1;
+    int tail_tiles = 0, tail_splits = 0;   // tensor path: split only the last partial wave
     int blocks_per_split = 1;
     int ctas = 0;
     int launches = 0;
@@ -87,6 +88,21 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     int splits;
     if (a->num_splits > 0) {
         splits = a->num_splits;
+    } else if (tc && base >= slots) {
+        // Enough tiles for full waves: keep whole tiles, and cut only the tiles of the
+        // last partial wave into key ranges so that wave occupies every cluster.
+        splits = 1;
+        const int64_t rem = base % slots;
+        if (rem > 0) {
+            int ts = (int)(slots / rem);
+            if (ts > kMaxSplits) ts = kMaxSplits;
+            const int cap = nblk / 2 > 1 ? nblk / 2 : 1;
+            if (ts > cap) ts = cap;
+            if (ts >= 2) {
+                p.tail_tiles = (int)rem;
+                p.tail_splits = ts;
+            }
+        }
     } else {
         // fill about two waves, with at least 4 key blocks per split
         const int64_t want = (2LL * slots + base - 1) / base;
@@ -98,7 +114,8 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     if (splits > nblk) splits = nblk;
     p.blocks_per_split = (nblk + splits - 1) / splits;
     p.splits = (nblk + p.blocks_per_split - 1) / p.blocks_per_split;
-    p.ctas = (int)(base * p.splits * (tc ? 2 : 1));
+    p.ctas = (int)((p.tail_splits > 0 ? base - p.tail_tiles + (int64_t)p.tail_tiles * p.tail_splits
+                                      : base * p.splits) * (tc ? 2 : 1));
     size_t off = 0;
     if (a->parent) {
         const int W = (a->T + 31) / 32;
@@ -106,16 +123,18 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         p.vis_bytes = (size_t)a->B * a->T * W * sizeof(uint32_t);
         off = align_up(off + p.vis_bytes);
     }
-    if (p.splits > 1) {
+    if (p.splits > 1 || p.tail_splits > 0) {
+        const int64_t prow = p.tail_splits > 0 ? (int64_t)p.tail_tiles * unit_rows : rows_total;
+        const int ns = p.tail_splits > 0 ? p.tail_splits : p.splits;
         p.po_off = off;
-        p.po_bytes = (size_t)p.splits * rows_total * kDc * sizeof(float);
+        p.po_bytes = (size_t)ns * prow * kDc * sizeof(float);
         off = align_up(off + p.po_bytes);
         p.pl_off = off;
-        p.pl_bytes = (size_t)p.splits * rows_total * sizeof(float);
+        p.pl_bytes = (size_t)ns * prow * sizeof(float);
         off = align_up(off + p.pl_bytes);
     }
     p.ws_bytes = off;
-    p.launches = (a->parent ? 1 : 0) + 1 + (p.splits > 1 ? 1 : 0);
+    p.launches = (a->parent ? 1 : 0) + 1 + ((p.splits > 1 || p.tail_splits > 0) ? 1 : 0);
     *pl = p;
     return KDT_OK;
 }
@@ -193,9 +212,12 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     vp.num_splits = p.splits;
     vp.blocks_per_split = p.blocks_per_split;
     vp.rows_total = (int64_t)a->B * a->T * a->H;
-    vp.part_o = p.splits > 1 ? reinterpret_cast<float *>(ws + p.po_off) : nullptr;
-    vp.part_lse = p.splits > 1 ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
+    const bool partials = p.splits > 1 || p.tail_splits > 0;
+    vp.part_o = partials ? reinterpret_cast<float *>(ws + p.po_off) : nullptr;
+    vp.part_lse = partials ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
     vp.err = a->err;
+    vp.tail_tiles = p.tail_tiles;
+    vp.tail_splits = p.tail_splits;
 
     if (a->parent) {
         uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);
@@ -208,7 +230,13 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     const cudaError_t e = p.impl == KDT_IMPL_TCGEN05 ? launch_verify_tc(vp, stream)
                                                      : launch_verify_simt(vp, a->dtype, stream);
     if (e != cudaSuccess) return KDT_ERR_CUDA;
-    if (p.splits > 1) {
+    if (p.tail_splits > 0) {
+        const int rows_seq = a->T * a->H;
+        const int row_tiles = (rows_seq + tc_rows_per_unit() - 1) / tc_rows_per_unit();
+        if (launch_merge_tail(vp.part_o, vp.part_lse, p.tail_splits, p.tail_tiles, a->B * row_tiles - p.tail_tiles,
+                              row_tiles, tc_rows_per_unit(), rows_seq, a->out, a->lse, stream) != cudaSuccess)
+            return KDT_ERR_CUDA;
+    } else if (p.splits > 1) {
         if (launch_merge_splits(vp.part_o, vp.part_lse, p.splits, vp.rows_total, a->out, a->lse, stream) !=
             cudaSuccess)
             return KDT_ERR_CUDA;

@@ -29,6 +29,11 @@ struct VerifyParams {
     int blocks_per_split;      // key blocks (of the kernel's block size) per split
     int64_t rows_total;        // B*T*H
     int32_t *err;              // caller error word (tensor-core path: negative = pipeline timeout)
+    // Tail splitting (tensor-core path, num_splits == 1): the last `tail_tiles` row
+    // tiles are each cut into `tail_splits` key ranges whose partial states land in
+    // part_o/part_lse compactly ([tail_splits][tail_tiles*128][512]) and are merged
+    // by launch_merge_tail. tail_splits == 0: off.
+    int tail_tiles, tail_splits;
 };
 
 // K0: parent -> packed ancestor bits.
@@ -48,6 +53,11 @@ cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t s);
 // K2: merge the split partials into out/lse.
 cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int num_splits, int64_t rows,
                                 float *out, float *lse, cudaStream_t s);
+
+// K2 for tail splitting: merge compact partials of the last `tail_tiles` row tiles.
+cudaError_t launch_merge_tail(const float *part_o, const float *part_lse, int splits, int tail_tiles,
+                              int first_tile, int row_tiles, int rows_per_tile, int rows_seq, float *out, float *lse,
+                              cudaStream_t s);
 
 // Public two-state merge.
 cudaError_t launch_merge_two(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,

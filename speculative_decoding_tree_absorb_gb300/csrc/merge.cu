@@ -33,15 +33,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__global__ void __launch_bounds__(kWarpsPerCta * 32) merge_splits_kernel(const float *__restrict__ part_o,
-                                                                         const float *__restrict__ part_lse,
-                                                                         int S, int64_t rows,
-                                                                         float *__restrict__ out,
-                                                                         float *__restrict__ lse) {
+// Merge the S partial states of one row (partial s at part_o[(s*stride + k)*512],
+// part_lse[s*stride + k]) into out_row / lse_out. One warp.
+__device__ __forceinline__ void merge_row(const float *__restrict__ part_o, const float *__restrict__ part_lse, int S,
+                                          int64_t stride, int64_t k, float *__restrict__ out_row, float *lse_out) {
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    if (row >= rows) return;
-    const float ls = lane < S ? part_lse[(int64_t)lane * rows + row] : -INFINITY;
+    const float ls = lane < S ? part_lse[(int64_t)lane * stride + k] : -INFINITY;
     const float M = warp_max(ls);
     const float w = (M == -INFINITY || ls == -INFINITY) ? 0.f : expf(ls - M);
     const float wsum = warp_sum(w);
@@ -51,7 +48,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_splits_kernel(const f
     for (int s = 0; s < S; ++s) {
         const float ws = __shfl_sync(0xffffffffu, w, s);
         if (ws == 0.f) continue;
-        const float4 *src = reinterpret_cast<const float4 *>(part_o + ((int64_t)s * rows + row) * kDc);
+        const float4 *src = reinterpret_cast<const float4 *>(part_o + ((int64_t)s * stride + k) * kDc);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const float4 v = __ldg(src + lane + 32 * c);
@@ -62,11 +59,40 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_splits_kernel(const f
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    float4 *dst = reinterpret_cast<float4 *>(out + row * kDc);
+    float4 *dst = reinterpret_cast<float4 *>(out_row);
 #pragma unroll
     for (int c = 0; c < 4; ++c)
         dst[lane + 32 * c] = make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv);
-    if (lane == 0 && lse) lse[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+    if (lane == 0 && lse_out) *lse_out = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32) merge_splits_kernel(const float *__restrict__ part_o,
+                                                                         const float *__restrict__ part_lse,
+                                                                         int S, int64_t rows,
+                                                                         float *__restrict__ out,
+                                                                         float *__restrict__ lse) {
+    const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    merge_row(part_o, part_lse, S, rows, row, out + row * kDc, lse ? lse + row : nullptr);
+}
+
+// Same merge for compact tail partials: compact row k belongs to row tile
+// first_tile + k / rows_per_tile, i.e. sequence b = tile / row_tiles and local row
+// (tile % row_tiles) * rows_per_tile + k % rows_per_tile; rows past the sequence end
+// are skipped.
+__global__ void __launch_bounds__(kWarpsPerCta * 32) merge_tail_kernel(const float *__restrict__ part_o,
+                                                                       const float *__restrict__ part_lse, int S,
+                                                                       int64_t nrows, int first_tile, int row_tiles,
+                                                                       int rows_per_tile, int rows_seq,
+                                                                       float *__restrict__ out,
+                                                                       float *__restrict__ lse) {
+    const int64_t k = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (k >= nrows) return;
+    const int tile = first_tile + (int)(k / rows_per_tile);
+    const int local = (tile % row_tiles) * rows_per_tile + (int)(k % rows_per_tile);
+    if (local >= rows_seq) return;
+    const int64_t row = (int64_t)(tile / row_tiles) * rows_seq + local;
+    merge_row(part_o, part_lse, S, nrows, k, out + row * kDc, lse ? lse + row : nullptr);
 }
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_two_kernel(const float *o_a, const float *lse_a,
@@ -102,6 +128,17 @@ cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int 
     if (rows == 0) return cudaSuccess;
     const int64_t ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
     merge_splits_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, s>>>(part_o, part_lse, num_splits, rows, out, lse);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_tail(const float *part_o, const float *part_lse, int splits, int tail_tiles,
+                              int first_tile, int row_tiles, int rows_per_tile, int rows_seq, float *out, float *lse,
+                              cudaStream_t s) {
+    const int64_t nrows = (int64_t)tail_tiles * rows_per_tile;
+    if (nrows == 0) return cudaSuccess;
+    const int64_t ctas = (nrows + kWarpsPerCta - 1) / kWarpsPerCta;
+    merge_tail_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, s>>>(part_o, part_lse, splits, nrows, first_tile, row_tiles,
+                                                                  rows_per_tile, rows_seq, out, lse);
     return cudaGetLastError();
 }
 

@@ -69,8 +69,12 @@ constexpr int kRows = 128;             // query rows per unit (MMA M)
 constexpr int kKeys = 128;             // keys per block (S MMA N, P.V K)
 constexpr int kThreads = 384;          // 12 warps
 constexpr int kChunkBytes = kKeys * 128;          // [128 keys x 64 dims] bf16, 128B-swizzled: 16 KB
-constexpr int kChunksPerBlock = 9;                // 8 latent chunks + 1 rope chunk
-constexpr int kNK = 8;                            // S-CTA key-chunk ring slots
+// TMA throughput per SM grows with the bytes of one request (fixed cost per box),
+// so key tiles travel as 32 KB requests (two 64-dim sub-tiles) and value halves as
+// 64 KB requests (four sub-tiles), from a 4-D view of the cache.
+constexpr int kSlotBytes = 2 * kChunkBytes;       // S-CTA ring slot: 128 keys x 128 dims
+constexpr int kSlotsPerBlock = 5;                 // 4 latent slots + 1 rope slot (half used)
+constexpr int kNK = 4;                            // S-CTA key ring slots (128 KB)
 constexpr int kPBytes = kRows * kKeys * 2;        // P tile: 32 KB (two 128B-swizzled halves)
 constexpr int kNP = 2;                            // P slots in the O-CTA
 constexpr int kVHalfBytes = 4 * kChunkBytes;      // V for 256 latent columns: 64 KB
@@ -81,8 +85,8 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 // Shared-memory layout (same offsets in both CTAs of the cluster; roles use
 // different parts). All tiles 1024-byte aligned for the 128B swizzle.
 constexpr int kOffQpe = 0;                                  // S: Q_pe tile 16 KB
-constexpr int kOffKRing = kOffQpe + kChunkBytes;            // S: 8 x 16 KB
-constexpr int kOffPStage = kOffKRing + kNK * kChunkBytes;   // S: 2 x 32 KB staging of P
+constexpr int kOffKRing = kOffQpe + kChunkBytes;            // S: 4 x 32 KB
+constexpr int kOffPStage = kOffKRing + kNK * kSlotBytes;    // S: 2 x 32 KB staging of P
 constexpr int kOffAStage = kOffPStage + kNP * kPBytes;      // S: [kNP][128] alpha staging
 constexpr int kOffRowMax = kOffAStage + kNP * kRows * 4;    // S: [2 blocks][2 halves][128] partial maxima
 constexpr int kOffLSum = kOffRowMax + 2 * 2 * kRows * 4;    // S: [128] partial row sums
@@ -131,6 +135,7 @@ struct TcParams {
     float scale_log2;
     float *out, *lse, *part_o, *part_lse;
     int32_t *err;
+    int tail_tiles, tail_splits;   // tail splitting (see VerifyParams); 0 = off
 };
 
 __device__ __forceinline__ bool aborted(const Barriers &bar) {
@@ -228,8 +233,9 @@ __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, uint
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    verify_tc_kernel(const __grid_constant__ CUtensorMap map_ckv, const __grid_constant__ CUtensorMap map_kpe,
-                     const __grid_constant__ CUtensorMap map_qpe, const TcParams p) {
+    verify_tc_kernel(const __grid_constant__ CUtensorMap map_ckv2, const __grid_constant__ CUtensorMap map_ckv4,
+                     const __grid_constant__ CUtensorMap map_kpe, const __grid_constant__ CUtensorMap map_qpe,
+                     const TcParams p) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ Barriers bar;
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -238,16 +244,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- unit -> (b, row tile, split) --------------------------------------------
+    // ---- unit -> (b, row tile, key range) ------------------------------------------
+    // Uniform mode: unit = (tile, split) with num_splits key ranges per tile. Tail mode
+    // (tail_splits > 0, num_splits == 1): tiles before the last tail_tiles are whole
+    // units; each of the last tail_tiles tiles is cut into tail_splits key ranges so the
+    // final wave of clusters is as full as the others.
     const int unit = blockIdx.x >> 1;
-    const int split = unit % p.num_splits;
-    const int rt = (unit / p.num_splits) % p.row_tiles;
-    const int b = unit / (p.num_splits * p.row_tiles);
+    const int tiles = p.B * p.row_tiles;
+    const int first_tail = tiles - p.tail_tiles;
+    int tile, split, nsplit;
+    if (p.tail_splits > 0) {
+        if (unit < first_tail) {
+            tile = unit;
+            split = 0;
+            nsplit = 1;
+        } else {
+            tile = first_tail + (unit - first_tail) / p.tail_splits;
+            split = (unit - first_tail) % p.tail_splits;
+            nsplit = p.tail_splits;
+        }
+    } else {
+        tile = unit / p.num_splits;
+        split = unit % p.num_splits;
+        nsplit = p.num_splits;
+    }
+    const int rt = tile % p.row_tiles;
+    const int b = tile / p.row_tiles;
     const int P = p.prefix_len[b];
     const int kv_len = P + p.T;
     const int nblk = (kv_len + kKeys - 1) / kKeys;
-    const int kb0 = split * p.blocks_per_split;
-    const int kb1 = min(nblk, kb0 + p.blocks_per_split);
+    const int bps = p.tail_splits > 0 ? (nblk + nsplit - 1) / nsplit : p.blocks_per_split;
+    const int kb0 = split * bps;
+    const int kb1 = min(nblk, kb0 + bps);
     const int nb = kb1 > kb0 ? kb1 - kb0 : 0;       // blocks of this unit (0: empty split)
     const int key_base = kv_len - nblk * kKeys;     // first key of block 0 (<= 0)
     const int r0 = rt * kRows;
@@ -290,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             // ---------------- TMA producer: Q_pe once, then key chunks ----------------
             if (elect_one() && nb > 0) {
-                tma_prefetch_desc(&map_ckv);
+                tma_prefetch_desc(&map_ckv2);
                 tma_prefetch_desc(&map_kpe);
                 mbar_arrive_expect_tx(&bar.qpe_full, kChunkBytes);
                 tma_load_2d(qpe_tile, &map_qpe, &bar.qpe_full, 0, (int)((int64_t)b * p.rows_seq + r0));
@@ -299,11 +327,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int issued = 0;
                 for (int j = 0; j < nb && !aborted(bar); ++j) {
                     const int key0 = key_base + (kb0 + j) * kKeys;
-                    for (int c = 0; c < kChunksPerBlock; ++c) {
+                    for (int c = 0; c < kSlotsPerBlock; ++c) {
                         if (issued >= kNK && !wait_or_abort(bar, &bar.kempty[slot], phase ^ 1, p.err, -2)) break;
-                        mbar_arrive_expect_tx(&bar.kfull[slot], kChunkBytes);
-                        if (c < 8) tma_load_3d(kring + slot * kChunkBytes, &map_ckv, &bar.kfull[slot], c * 64, key0, b);
-                        else tma_load_3d(kring + slot * kChunkBytes, &map_kpe, &bar.kfull[slot], 0, key0, b);
+                        if (c < 4) {      // latent dims [128c, 128c + 128): two sub-tiles in one request
+                            mbar_arrive_expect_tx(&bar.kfull[slot], kSlotBytes);
+                            tma_load_4d(kring + slot * kSlotBytes, &map_ckv2, &bar.kfull[slot], 0, key0, 2 * c, b);
+                        } else {          // rope dims
+                            mbar_arrive_expect_tx(&bar.kfull[slot], kChunkBytes);
+                            tma_load_3d(kring + slot * kSlotBytes, &map_kpe, &bar.kfull[slot], 0, key0, b);
+                        }
                         ++issued;
                         if (++slot == kNK) { slot = 0; phase ^= 1; }
                     }
@@ -332,15 +364,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     KDT_TC_TRACE(kEvSMmaStart, j);
                     const uint32_t d = tmem_s0 + buf * kKeys;
-                    for (int c = 0; c < kChunksPerBlock; ++c) {
+                    for (int c = 0; c < kSlotsPerBlock; ++c) {
                         if (!(ok = wait_or_abort(bar, &bar.kfull[slot], phase, p.err, -5))) break;
                         tc_fence_after();
-                        const uint32_t kaddr = smem_u32(kring + slot * kChunkBytes);
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t bdesc = sdesc_sw128(kaddr + kk * 32, 16, 1024);
-                            const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-                            if (c < 8) mma_ts(d, tmem_q + c * 32 + kk * 8, bdesc, idesc, acc);
-                            else mma_ss(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024), bdesc, idesc, acc);
+                        const uint32_t kaddr = smem_u32(kring + slot * kSlotBytes);
+                        if (c < 4) {
+                            for (int t = 0; t < 2; ++t)            // sub-tile t: dims 128c + 64t .. +64
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t bdesc = sdesc_sw128(kaddr + t * kChunkBytes + kk * 32, 16, 1024);
+                                    mma_ts(d, tmem_q + 64 * c + 32 * t + 8 * kk, bdesc, idesc,
+                                           (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
+                                }
+                        } else {
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
+                                       sdesc_sw128(kaddr + kk * 32, 16, 1024), idesc, 1u);
                         }
                         mma_commit(&bar.kempty[slot]);
                         if (++slot == kNK) { slot = 0; phase ^= 1; }
@@ -436,10 +474,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     m_run = mx;
                     l_run *= alpha;
                 }
-                // staging slot (and the peer's P slot) free once P.V of block j - kNP is done
+                // the peer's P slot and this CTA's staging slot ps are free once P.V of
+                // block j - kNP is done
                 ok = j < kNP || warp_wait_cluster(bar, &bar.pempty[ps], ((j / kNP) - 1) & 1, p.err, -7);
                 if (!ok) continue;                                 // caught at the next barrier
                 if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxSlot, j);
+                // staging slot ps: its previous copy (block j - kNP) landed before P.V of that
+                // block could run, which the pempty wait above has seen
                 unsigned char *stage = smem + kOffPStage + ps * kPBytes + half * (kPBytes / 2);
                 float lsum = 0.f;
                 const bool live = m_run > -INFINITY;
@@ -503,7 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             // ---------------- TMA producer: V halves -----------------------------------------
             if (elect_one() && nb > 0) {
-                tma_prefetch_desc(&map_ckv);
+                tma_prefetch_desc(&map_ckv4);
                 int slot = 0;
                 uint32_t phase = 0;
                 int issued = 0;
@@ -512,9 +553,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < 2; ++h) {
                         if (issued >= kNV && !wait_or_abort(bar, &bar.vempty[slot], phase ^ 1, p.err, -8)) break;
                         mbar_arrive_expect_tx(&bar.vfull[slot], kVHalfBytes);
-                        unsigned char *dst = vbase + slot * kVHalfBytes;
-                        for (int q = 0; q < 4; ++q)
-                            tma_load_3d(dst + q * kChunkBytes, &map_ckv, &bar.vfull[slot], 256 * h + 64 * q, key0, b);
+                        // latent dims [256h, 256h + 256): four sub-tiles in one request
+                        tma_load_4d(vbase + slot * kVHalfBytes, &map_ckv4, &bar.vfull[slot], 0, key0, 4 * h, b);
                         ++issued;
                         if (++slot == kNV) { slot = 0; phase ^= 1; }
                     }
@@ -655,10 +695,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // epilogue
             const int R = r0 + row;
-            const bool partial = p.num_splits > 1;
             const int64_t grow = (int64_t)b * p.rows_seq + R;
-            float *orow = partial ? p.part_o + ((int64_t)split * p.rows_total + grow) * kDc : p.out + grow * kDc;
-            float *lrow = partial ? p.part_lse + (int64_t)split * p.rows_total + grow : (p.lse ? p.lse + grow : nullptr);
+            float *orow, *lrow;
+            if (nsplit == 1) {
+                orow = p.out + grow * kDc;
+                lrow = p.lse ? p.lse + grow : nullptr;
+            } else if (p.tail_splits > 0) {                  // compact tail partials
+                const int64_t nrows = (int64_t)p.tail_tiles * kRows;
+                const int64_t k = (int64_t)(tile - first_tail) * kRows + row;
+                orow = p.part_o + ((int64_t)split * nrows + k) * kDc;
+                lrow = p.part_lse + (int64_t)split * nrows + k;
+            } else {
+                orow = p.part_o + ((int64_t)split * p.rows_total + grow) * kDc;
+                lrow = p.part_lse + (int64_t)split * p.rows_total + grow;
+            }
             if (nb == 0) {
                 if (R < p.rows_seq) {
                     for (int c = 0; c < kDc; c += 4) *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -726,7 +776,7 @@ bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims
               const cuuint32_t *box) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint32_t es[3] = {1, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
     memset(m, 0, sizeof(*m));
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -739,13 +789,17 @@ int tc_rows_per_unit() { return kRows; }
 int tc_keys_per_block() { return kKeys; }
 
 cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
-    CUtensorMap map_ckv, map_kpe, map_qpe;
+    CUtensorMap map_ckv2, map_ckv4, map_kpe, map_qpe;
     const cuuint64_t L = (cuuint64_t)vp.L;
     {
-        cuuint64_t dims[3] = {(cuuint64_t)kDc, L, (cuuint64_t)vp.B};
-        cuuint64_t strides[2] = {(cuuint64_t)kDc * 2, L * kDc * 2};
-        cuuint32_t box[3] = {64, kKeys, 1};
-        if (!make_map(&map_ckv, vp.c_kv, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        // c_kv viewed as [B][8 dim-blocks][L keys][64]: a box of (64, 128 keys, n blocks)
+        // lands as n consecutive [128 x 64] 128B-swizzled sub-tiles.
+        cuuint64_t dims[4] = {64, L, (cuuint64_t)(kDc / 64), (cuuint64_t)vp.B};
+        cuuint64_t strides[3] = {(cuuint64_t)kDc * 2, 128, L * kDc * 2};
+        cuuint32_t box2[4] = {64, kKeys, 2, 1};
+        cuuint32_t box4[4] = {64, kKeys, 4, 1};
+        if (!make_map(&map_ckv2, vp.c_kv, 4, dims, strides, box2)) return cudaErrorInvalidValue;
+        if (!make_map(&map_ckv4, vp.c_kv, 4, dims, strides, box4)) return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[3] = {(cuuint64_t)kDr, L, (cuuint64_t)vp.B};
@@ -778,10 +832,14 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     p.part_o = vp.part_o;
     p.part_lse = vp.part_lse;
     p.err = vp.err;
-    const int64_t units = (int64_t)p.B * p.row_tiles * p.num_splits;
+    p.tail_tiles = vp.tail_tiles;
+    p.tail_splits = vp.tail_splits;
+    const int64_t tiles = (int64_t)p.B * p.row_tiles;
+    const int64_t units = p.tail_splits > 0 ? tiles - p.tail_tiles + (int64_t)p.tail_tiles * p.tail_splits
+                                            : tiles * p.num_splits;
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    verify_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, s>>>(map_ckv, map_kpe, map_qpe, p);
+    verify_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, s>>>(map_ckv2, map_ckv4, map_kpe, map_qpe, p);
     return cudaGetLastError();
 }
 

@@ -205,15 +205,36 @@ def test_running_max_jumps_force_output_rescale(kdt, oracle_mod, dtype):
         else:
             case.c_kv[b, n // 2:n] *= 6.0
     ref_out, ref_lse = oracle_mod.verify_attn(case)
-    # fp32 rounding of the 576-term score dots grows with |q||c_kv| and the output error
-    # with |c_kv|: both are 6x here, so the fp32 bound is scaled by 6 (bf16 keeps its own).
-    atol, rtol = (6e-4, 6e-4) if dtype == "f32" else H.TOL["bf16"]
+    # The absolute error of the output grows with the magnitude of the values it averages
+    # (fp32: rounding of the 576-term score dots and the sums; bf16: rounding of P), and
+    # the cache here is 6x larger than in the N(0,1) configurations, so the absolute
+    # term of each bound is scaled by 6; the relative term is unchanged.
+    atol, rtol = (6e-4, 1e-4) if dtype == "f32" else (6 * 2e-2, 2e-2)
     for impl in IMPLS_BY_DTYPE[dtype]:
         for s in (0, 1, 4):
             out, lse, err = G.run(case, impl=impl, num_splits=s)
             assert err == 0
             H.assert_close(out, ref_out, atol, rtol, f"jump/{impl}/splits={s} out")
             H.assert_close(lse, ref_lse, atol, rtol, f"jump/{impl}/splits={s} lse")
+
+
+def test_tail_tiles_split_to_fill_the_last_wave(kdt, oracle_mod):
+    # 2 sequences x 40 row tiles = 80 tiles: more than one wave of 2-CTA clusters, with
+    # a partial last wave whose tiles are cut into key ranges and merged afterwards.
+    import torch
+    case = wl.make_case("tail", B=2, T=40, H=128, prefix=(700, 650), dtype="bf16", tree="geometric", seed=17)
+    d = G.to_device(case)
+    out = torch.empty((case.B, case.T, case.H, 512), device="cuda")
+    a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
+                      max_kv_len=case.max_kv_len, out=out)
+    pl = kdt.plan(a)
+    assert pl["impl"] == "tcgen05" and pl["num_launches"] == 3          # visibility, attention, tail merge
+    out_g, lse_g, err = G.run(case, impl="auto", dev_tensors=d)
+    assert err == 0
+    rows_tail = np.arange(case.rows - 4 * 128 - 256, case.rows)         # the last tiles, both sides of a cut
+    rows = np.unique(np.concatenate([rows_tail, _sample_rows(case, 128, seed=4)]))
+    ref_out, ref_lse = oracle_mod.verify_attn_rows(case, rows)
+    _compare(case, out_g.reshape(-1, 512)[rows], lse_g.reshape(-1)[rows], ref_out, ref_lse, "tail")
 
 
 def test_auto_picks_tensor_cores_for_bf16(kdt):
