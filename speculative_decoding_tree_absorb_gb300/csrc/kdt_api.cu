@@ -30,7 +30,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Plan {
     int impl = KDT_IMPL_SIMT;
     int splits = 1;
-    int tail_tiles = 0, tail_splits = 0;   // tensor path: split only the last partial wave
+    int tail_units = 0, tail_splits = 0;   // tensor path: split only the last partial wave
     int blocks_per_split = 1;
     int ctas = 0;
     int launches = 0;
@@ -80,16 +80,16 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     p.impl = tc ? KDT_IMPL_TCGEN05 : KDT_IMPL_SIMT;
     const int unit_rows = tc ? tc_rows_per_unit() : kSimtRows;
     const int unit_keys = tc ? tc_keys_per_block() : kSimtKeys;
-    const int row_tiles = (int)((rows_seq + unit_rows - 1) / unit_rows);
+    const int unit_tiles = (int)((rows_seq + unit_rows - 1) / unit_rows);   // work units per sequence
     const int nblk = (a->max_kv_len + unit_keys - 1) / unit_keys;
-    const int64_t base = (int64_t)row_tiles * a->B;
-    // concurrent units: one CTA per SM for SIMT, one 2-CTA cluster per SM pair for tcgen05
-    const int64_t slots = tc ? sm_count() / 2 : sm_count();
+    const int64_t base = (int64_t)unit_tiles * a->B;
+    // concurrent units: one CTA per SM for SIMT, the resident 4-CTA clusters for tcgen05
+    const int64_t slots = tc ? tc_max_clusters() : sm_count();
     int splits;
     if (a->num_splits > 0) {
         splits = a->num_splits;
     } else if (tc && base >= slots) {
-        // Enough tiles for full waves: keep whole tiles, and cut only the tiles of the
+        // Enough units for full waves: keep whole units, and cut only the units of the
         // last partial wave into key ranges so that wave occupies every cluster.
         splits = 1;
         const int64_t rem = base % slots;
@@ -99,7 +99,7 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
             const int cap = nblk / 2 > 1 ? nblk / 2 : 1;
             if (ts > cap) ts = cap;
             if (ts >= 2) {
-                p.tail_tiles = (int)rem;
+                p.tail_units = (int)rem;
                 p.tail_splits = ts;
             }
         }
@@ -114,8 +114,8 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     if (splits > nblk) splits = nblk;
     p.blocks_per_split = (nblk + splits - 1) / splits;
     p.splits = (nblk + p.blocks_per_split - 1) / p.blocks_per_split;
-    p.ctas = (int)((p.tail_splits > 0 ? base - p.tail_tiles + (int64_t)p.tail_tiles * p.tail_splits
-                                      : base * p.splits) * (tc ? 2 : 1));
+    p.ctas = (int)((p.tail_splits > 0 ? base - p.tail_units + (int64_t)p.tail_units * p.tail_splits
+                                      : base * p.splits) * (tc ? 4 : 1));
     size_t off = 0;
     if (a->parent) {
         const int W = (a->T + 31) / 32;
@@ -124,7 +124,7 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         off = align_up(off + p.vis_bytes);
     }
     if (p.splits > 1 || p.tail_splits > 0) {
-        const int64_t prow = p.tail_splits > 0 ? (int64_t)p.tail_tiles * unit_rows : rows_total;
+        const int64_t prow = p.tail_splits > 0 ? (int64_t)p.tail_units * unit_rows : rows_total;
         const int ns = p.tail_splits > 0 ? p.tail_splits : p.splits;
         p.po_off = off;
         p.po_bytes = (size_t)ns * prow * kDc * sizeof(float);
@@ -216,7 +216,7 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     vp.part_o = partials ? reinterpret_cast<float *>(ws + p.po_off) : nullptr;
     vp.part_lse = partials ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
     vp.err = a->err;
-    vp.tail_tiles = p.tail_tiles;
+    vp.tail_units = p.tail_units;
     vp.tail_splits = p.tail_splits;
 
     if (a->parent) {
@@ -232,9 +232,9 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     if (e != cudaSuccess) return KDT_ERR_CUDA;
     if (p.tail_splits > 0) {
         const int rows_seq = a->T * a->H;
-        const int row_tiles = (rows_seq + tc_rows_per_unit() - 1) / tc_rows_per_unit();
-        if (launch_merge_tail(vp.part_o, vp.part_lse, p.tail_splits, p.tail_tiles, a->B * row_tiles - p.tail_tiles,
-                              row_tiles, tc_rows_per_unit(), rows_seq, a->out, a->lse, stream) != cudaSuccess)
+        const int unit_tiles = (rows_seq + tc_rows_per_unit() - 1) / tc_rows_per_unit();
+        if (launch_merge_tail(vp.part_o, vp.part_lse, p.tail_splits, p.tail_units, a->B * unit_tiles - p.tail_units,
+                              unit_tiles, tc_rows_per_unit(), rows_seq, a->out, a->lse, stream) != cudaSuccess)
             return KDT_ERR_CUDA;
     } else if (p.splits > 1) {
         if (launch_merge_splits(vp.part_o, vp.part_lse, p.splits, vp.rows_total, a->out, a->lse, stream) !=

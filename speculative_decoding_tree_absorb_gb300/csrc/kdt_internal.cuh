@@ -29,11 +29,12 @@ struct VerifyParams {
     int blocks_per_split;      // key blocks (of the kernel's block size) per split
     int64_t rows_total;        // B*T*H
     int32_t *err;              // caller error word (tensor-core path: negative = pipeline timeout)
-    // Tail splitting (tensor-core path, num_splits == 1): the last `tail_tiles` row
-    // tiles are each cut into `tail_splits` key ranges whose partial states land in
-    // part_o/part_lse compactly ([tail_splits][tail_tiles*128][512]) and are merged
-    // by launch_merge_tail. tail_splits == 0: off.
-    int tail_tiles, tail_splits;
+    // Tail splitting (tensor-core path, num_splits == 1): the last `tail_units` work
+    // units (tc_rows_per_unit() rows each) are each cut into `tail_splits` key ranges
+    // whose partial states land in part_o/part_lse compactly
+    // ([tail_splits][tail_units * rows per unit][512]) and are merged by
+    // launch_merge_tail. tail_splits == 0: off.
+    int tail_units, tail_splits;
 };
 
 // K0: parent -> packed ancestor bits.
@@ -45,8 +46,10 @@ constexpr int kSimtRows = 64;
 constexpr int kSimtKeys = 64;
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, cudaStream_t s);
 
-// K1: tcgen05 verify (bf16 inputs), 2-CTA clusters of 128 query rows x 128-key blocks.
-int tc_rows_per_unit();
+// K1: tcgen05 verify (bf16 inputs), 4-CTA clusters (two CTA pairs) of two 128-row
+// tiles x 128-key blocks.
+int tc_rows_per_unit();   // query rows of one work unit (256)
+int tc_max_clusters();    // 4-CTA clusters resident at once on the current device
 int tc_keys_per_block();
 cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t s);
 
@@ -54,7 +57,8 @@ cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t s);
 cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int num_splits, int64_t rows,
                                 float *out, float *lse, cudaStream_t s);
 
-// K2 for tail splitting: merge compact partials of the last `tail_tiles` row tiles.
+// K2 for tail splitting: merge compact partials of the last `tail_tiles` units of
+// `rows_per_tile` rows (unit index = b * row_tiles + unit within the sequence).
 cudaError_t launch_merge_tail(const float *part_o, const float *part_lse, int splits, int tail_tiles,
                               int first_tile, int row_tiles, int rows_per_tile, int rows_seq, float *out, float *lse,
                               cudaStream_t s);

@@ -10,20 +10,28 @@
 //
 // GB300 design (differs from the pages' SIMT block-per-(b,h,i) kernel):
 //  * All heads x tree queries of one sequence form the M dimension: a work unit is
-//    128 consecutive query rows of one sequence and a range of 128-key blocks.
-//    Every head shares the latent cache, so S = Q K^T and O = P V are dense
-//    contractions on the 5th-generation tensor cores.
-//  * A unit runs on a 2-CTA cluster split by role, because one SM cannot hold
-//    Q (128 x 576 bf16), the 128 x 512 fp32 output accumulator and the scores:
-//      - rank 0, the S-CTA: Q_nope lives in tensor memory as the MMA A operand
-//        (256 columns), Q_pe in shared memory; per key block it computes
-//        S[128 x 128] into one of two TMEM score buffers (256 columns), runs the
-//        online softmax (one thread per row), and writes P (bf16) straight into
-//        the O-CTA's shared memory over DSMEM;
-//      - rank 1, the O-CTA: the whole fp32 O[128 x 512] accumulator occupies its
-//        512 TMEM columns; per block it issues O += P V (N = 256, two halves) with
-//        V = c_kv tiles fetched by TMA, and rescales rows of O in TMEM on the rare
-//        occasions the running maximum grows past the threshold below.
+//    256 consecutive query rows (two 128-row tiles) of one sequence and a range of
+//    128-key blocks. Every head shares the latent cache, so S = Q K^T and O = P V are
+//    dense contractions on the 5th-generation tensor cores.
+//  * A unit runs on a 4-CTA cluster of two CTA pairs, each pair one M = 256 MMA
+//    (tcgen05 .cta_group::2): the S pair (ranks 0, 1) computes scores and the
+//    softmax, the O pair (ranks 2, 3) accumulates the output; S-CTA k hands its
+//    128 rows of P to O-CTA 2 + k. In a pair each CTA loads only HALF of the B
+//    operand (S pair: 64 of a block's 128 keys; O pair: 128 of 256 latent columns),
+//    and the MMA reads both halves, so every SM fetches and stores half the cache
+//    bytes a single-CTA MMA of the same rows would. Roles are split because one SM
+//    cannot hold Q (128 x 576 bf16), the 128 x 512 fp32 output accumulator and the
+//    scores:
+//      - an S-CTA: its Q_nope rows live in tensor memory as the MMA A operand
+//        (256 columns), Q_pe in shared memory; per key block the pair computes
+//        S[256 x 128] into one of two TMEM score buffers (256 columns), each CTA
+//        runs the online softmax of its rows (one thread per row) and copies P
+//        (bf16) and the block's rescale factors into its O-CTA's shared memory with
+//        ONE bulk copy (the copy engine's cost is per request, not per byte);
+//      - an O-CTA: the fp32 O[128 x 512] accumulator of its rows occupies its 512
+//        TMEM columns; per block the pair issues O += P V (N = 256, two halves) and
+//        rescales rows of O in TMEM on the rare occasions the running maximum
+//        grows past the threshold below.
 //  * Key blocks are aligned to END at kv_len, so no row at or beyond
 //    prefix_len + T is ever fetched; the leading block may start before row 0,
 //    where TMA fills zeros and the mask removes the keys. Only blocks holding tree
@@ -37,6 +45,7 @@
 #include "kdt_internal.cuh"
 #include "tc_ptx.cuh"
 
+#include <atomic>
 #include <math.h>
 #include <string.h>
 
@@ -51,74 +60,95 @@ namespace {
 
 using namespace tc;
 
-// Trace events (rank 0 = S-CTA, rank 1 = O-CTA).
+// Trace events (ranks 0-1 = S-CTAs, ranks 2-3 = O-CTAs).
 enum TraceEvent {
     kEvSMmaStart = 0,    // S MMA thread: score buffer free, starts issuing block
     kEvSMmaIssued,       // S MMA thread: all chunks of the block issued
     kEvSoftmaxIn,        // softmax warp 4: scores of the block in TMEM
     kEvSoftmaxLoaded,    // softmax warp 4: scores loaded, buffer released
     kEvSoftmaxSlot,      // softmax warp 4: P slot free in the O-CTA
-    kEvSoftmaxSent,      // softmax warp 4: P written and published
+    kEvSoftmaxSent,      // softmax: P of the block staged and its copy issued
     kEvCorrIn,           // correction warp 4: P of the block arrived
     kEvOMmaStart,        // O MMA thread: block checked, starts issuing P.V
     kEvOMmaIssued,       // O MMA thread: P.V of the block issued
+    kEvKIssue,           // S producer: key chunk u requested (index = chunk use)
+    kEvKFull,            // S MMA thread: key chunk u landed in both CTAs
+    kEvSoftmaxLd,        // softmax warp 4: scores in registers
+    kEvVIssue,           // O producer: value chunk u requested
+    kEvVFull,            // O MMA thread: value chunk u landed in both CTAs
+    kEvKEmpty,           // S producer: the pair's MMAs finished reading key chunk u
     kNumTraceEvents
 };
 
-constexpr int kRows = 128;             // query rows per unit (MMA M)
+constexpr int kRows = 128;             // query rows per CTA (the pair's MMA has M = 256)
 constexpr int kKeys = 128;             // keys per block (S MMA N, P.V K)
+constexpr int kHalfKeys = kKeys / 2;   // keys of a block held by one S-CTA
 constexpr int kThreads = 384;          // 12 warps
-constexpr int kChunkBytes = kKeys * 128;          // [128 keys x 64 dims] bf16, 128B-swizzled: 16 KB
-// TMA throughput per SM grows with the bytes of one request (fixed cost per box),
-// so key tiles travel as 32 KB requests (two 64-dim sub-tiles) and value halves as
-// 64 KB requests (four sub-tiles), from a 4-D view of the cache.
-constexpr int kSlotBytes = 2 * kChunkBytes;       // S-CTA ring slot: 128 keys x 128 dims
-constexpr int kSlotsPerBlock = 5;                 // 4 latent slots + 1 rope slot (half used)
+// Operand tiles are [rows x 64 bf16] with 128-byte rows, 128B-swizzled.
+constexpr int kKSub = kHalfKeys * 128;            // S-CTA key sub-tile [64 keys x 64 dims]: 8 KB
+constexpr int kVSub = kKeys * 128;                // O-CTA value sub-tile [128 keys x 64 dims]: 16 KB
+// Tiles travel as 32 KB requests from 4-D views of the cache (few, large requests:
+// the copy engine's cost is per request).
+constexpr int kKSlotBytes = 4 * kKSub;            // S ring slot: 64 keys x 256 latent dims
+constexpr int kKUsesPerBlock = 3;                 // two latent slots + one rope slot (8 KB used)
 constexpr int kNK = 4;                            // S-CTA key ring slots (128 KB)
-constexpr int kPBytes = kRows * kKeys * 2;        // P tile: 32 KB (two 128B-swizzled halves)
-constexpr int kNP = 2;                            // P slots in the O-CTA
-constexpr int kVHalfBytes = 4 * kChunkBytes;      // V for 256 latent columns: 64 KB
-constexpr int kNV = 2;                            // V half slots in the O-CTA
+constexpr int kQpeBytes = kRows * 128;            // Q_pe tile of one S-CTA: 16 KB
+constexpr int kPBytes = kRows * kKeys * 2;        // P tile of one CTA: 32 KB (two 128B-swizzled halves)
+// A P slot holds the tile followed by the block's rescale factors, so one bulk copy
+// per block carries both.
+constexpr int kPSlotBytes = kPBytes + 1024;       // 32 KB P + alpha[128] (+ pad to 1 KB alignment)
+constexpr uint32_t kPTx = kPBytes + kRows * 4;    // bytes copied into a P slot per block
+constexpr int kNS = 2;                            // S-CTA staging slots (free once the copy landed)
+constexpr int kNP = 3;                            // O-CTA P slots (free once P.V of the block ran)
+constexpr int kVSlotBytes = 2 * kVSub;            // O ring slot: 128 keys x 128 latent dims
+constexpr int kNV = 3;                            // O-CTA value ring slots (96 KB)
+constexpr uint32_t kCmdDone = 0xffffffffu;        // correction command: no more rescales
 constexpr uint64_t kWaitLimit = 200000000ull;     // ns a wait may poll before giving up
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
-// Shared-memory layout (same offsets in both CTAs of the cluster; roles use
+// Shared-memory layout (same offsets in every CTA of the cluster; roles use
 // different parts). All tiles 1024-byte aligned for the 128B swizzle.
 constexpr int kOffQpe = 0;                                  // S: Q_pe tile 16 KB
-constexpr int kOffKRing = kOffQpe + kChunkBytes;            // S: 4 x 32 KB
-constexpr int kOffPStage = kOffKRing + kNK * kSlotBytes;    // S: 2 x 32 KB staging of P
-constexpr int kOffAStage = kOffPStage + kNP * kPBytes;      // S: [kNP][128] alpha staging
-constexpr int kOffRowMax = kOffAStage + kNP * kRows * 4;    // S: [2 blocks][2 halves][128] partial maxima
+constexpr int kOffKRing = kOffQpe + kQpeBytes;              // S: 4 x 32 KB
+constexpr int kOffPStage = kOffKRing + kNK * kKSlotBytes;   // S: 2 x 33 KB staging of P + alpha
+constexpr int kOffRowMax = kOffPStage + kNS * kPSlotBytes;  // S: [2 blocks][2 halves][128] partial maxima
 constexpr int kOffLSum = kOffRowMax + 2 * 2 * kRows * 4;    // S: [128] partial row sums
-constexpr int kOffP = 0;                                    // O: 2 x 32 KB
-constexpr int kOffV = kOffP + kNP * kPBytes;                // O: 2 x 64 KB
-constexpr int kOffAlpha = kOffV + kNV * kVHalfBytes;        // O: [kNP][128] floats
-constexpr int kOffStats = kOffAlpha + kNP * kRows * 4;      // O: [128] x (m, l)
+constexpr int kOffP = 0;                                    // O: 3 x 33 KB P + alpha
+constexpr int kOffV = kOffP + kNP * kPSlotBytes;            // O: 3 x 32 KB
+constexpr int kOffStats = kOffV + kNV * kVSlotBytes;        // O: [128] x (m, l)
 constexpr int kSEnd = kOffLSum + kRows * 4;
 constexpr int kOEnd = kOffStats + kRows * 8;
-constexpr uint32_t kPTx = kPBytes + kRows * 4;              // bytes landing in a P slot per block
 constexpr int kTileBytes = kSEnd > kOEnd ? kSEnd : kOEnd;
 constexpr int kSmemBytes = kTileBytes + 1024;               // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
+// Barriers (same layout in every CTA). "leader" = the even CTA of a pair, which
+// issues the pair's MMAs; barriers the MMA thread waits on live in the leader.
 struct Barriers {
-    // S-CTA
-    uint64_t kfull[kNK], kempty[kNK];
-    uint64_t sfull[2], sempty[2];
-    uint64_t qpe_full, q_ready;
-    uint64_t pempty[kNP];          // arrived by the O-CTA's MMA commits (multicast)
-    // O-CTA
-    uint64_t pfull[kNP];           // arrived remotely by the S-CTA softmax warps
-    uint64_t vfull[kNV], vempty[kNV];
-    // Per-block handshake between the correction warps and the MMA thread. Each pair
-    // strictly alternates (request -> response), so every parity wait is exact.
-    uint64_t corr_done;            // correction warps -> MMA: block j checked (need_rescale set)
-    uint64_t ack;                  // MMA -> correction warps: flag of block j read
-    uint64_t o_ready;              // MMA -> correction warps: all P.V before block j complete
-    uint64_t rescaled;             // correction warps -> MMA: rows of O rescaled
-    uint64_t stats_full;
-    uint64_t sync_bar;             // MMA thread's own completion probe (mid-stream)
-    uint64_t drain;                // completion probe for this CTA's own MMAs before TMEM is freed
-    int need_rescale;
+    // S pair
+    uint64_t kfull[kNK];           // leader: both halves of a key chunk landed (tx of both CTAs)
+    uint64_t kempty[kNK];          // each S-CTA: its half of the chunk was read (MMA commit)
+    uint64_t sfull[2];             // each S-CTA: scores of a block are in its TMEM
+    uint64_t sempty[2];            // leader: both CTAs' softmax warps have read the buffer (16 arrivals)
+    uint64_t qpe_full;             // leader: both Q_pe tiles landed
+    uint64_t q_ready;              // leader: both CTAs' Q_nope stored in TMEM (16 arrivals)
+    uint64_t pempty[kNP];          // each S-CTA: O-CTA P slot free again (O pair's MMA commit)
+    uint64_t sfree[kNS];           // each S-CTA: the copy out of a staging slot has landed
+    // O pair
+    uint64_t pfull[kNP];           // each O-CTA: P + alpha of a block landed from its S-CTA
+    uint64_t pready[2][kNP];       // leader: P slot filled in O-CTA k, its rescale flag written
+    uint64_t vfull[kNV];           // leader: both halves of a value chunk landed
+    uint64_t vempty[kNV];          // each O-CTA: its half of the chunk was read
+    // Rare rescale hand-over: the MMA thread lets its P.V drain, then sends `go` with a
+    // command (P slot whose alphas to apply, or kCmdDone at the end) to each O-CTA whose
+    // rows need it, and waits for `rescaled` (one arrival per O-CTA).
+    uint64_t go;                   // each O-CTA: a command is in `cmd`
+    uint64_t rescaled;             // leader: rows of O rescaled (or no rescale needed) per O-CTA
+    uint64_t stats_full;           // each O-CTA: final (m, l) of its rows from its S-CTA
+    uint64_t sync_bar;             // leader: MMA thread's own completion probe (mid-stream)
+    uint64_t drain;                // completion of all MMAs of the pair before TMEM is read or freed
+    uint32_t need[2][kNP];         // leader: per-CTA "some row of O needs a rescale" per P slot
+    uint32_t cmd;                  // each O-CTA: correction command
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -135,17 +165,19 @@ struct TcParams {
     float scale_log2;
     float *out, *lse, *part_o, *part_lse;
     int32_t *err;
-    int tail_tiles, tail_splits;   // tail splitting (see VerifyParams); 0 = off
+    int tail_units, tail_splits;   // tail splitting (see VerifyParams); 0 = off
+    int pairs_per_seq;             // work units (two row tiles each) per sequence
 };
 
 __device__ __forceinline__ bool aborted(const Barriers &bar) {
     return *reinterpret_cast<const volatile int *>(&bar.abort_flag) != 0;
 }
 
-// Wait until every tcgen05 operation this thread issued has completed.
-__device__ __forceinline__ void drain_mmas(Barriers &bar) {
-    mma_commit(&bar.drain);
-    mbar_wait(&bar.drain, 0, kWaitLimit);
+// Wait until every tcgen05 operation this (MMA-issuing) thread issued has completed;
+// the completion also arrives on the drain barrier of the other CTAs in `mask`.
+__device__ __forceinline__ void drain_mmas(Barriers &bar, uint16_t mask) {
+    mma_commit_pair(&bar.drain, mask);
+    mbar_wait_cluster(&bar.drain, 0, kWaitLimit);
 }
 
 // Order this thread's DSMEM stores (generic proxy) before a later release-arrive
@@ -160,14 +192,6 @@ __device__ __forceinline__ void set_abort(Barriers &bar, int32_t *err, int code)
     if (err) atomicCAS(err, 0, code);
 }
 
-__device__ __forceinline__ bool wait_or_abort(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err,
-                                              int code) {
-    if (*reinterpret_cast<volatile int *>(&bar.abort_flag)) return false;
-    if (mbar_wait(b, parity, kWaitLimit)) return true;
-    set_abort(bar, err, code);
-    return false;
-}
-
 __device__ __forceinline__ bool wait_cluster_or_abort(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err,
                                                       int code) {
     if (*reinterpret_cast<volatile int *>(&bar.abort_flag)) return false;
@@ -179,10 +203,6 @@ __device__ __forceinline__ bool wait_cluster_or_abort(Barriers &bar, uint64_t *b
 // Warp-uniform waits: every lane polls, and the warp proceeds only if all lanes saw
 // the phase complete, so warp-collective tcgen05 loads/stores after a wait are never
 // reached by part of a warp.
-__device__ __forceinline__ bool warp_wait(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err, int code) {
-    return __all_sync(0xffffffffu, wait_or_abort(bar, b, parity, err, code));
-}
-
 __device__ __forceinline__ bool warp_wait_cluster(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err,
                                                   int code) {
     return __all_sync(0xffffffffu, wait_cluster_or_abort(bar, b, parity, err, code));
@@ -232,8 +252,8 @@ __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, uint
     return base + ((uint32_t)(32 * (warp & 3)) << 16) + col;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    verify_tc_kernel(const __grid_constant__ CUtensorMap map_ckv2, const __grid_constant__ CUtensorMap map_ckv4,
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
+    verify_tc_kernel(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_vs,
                      const __grid_constant__ CUtensorMap map_kpe, const __grid_constant__ CUtensorMap map_qpe,
                      const TcParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -244,32 +264,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- unit -> (b, row tile, key range) ------------------------------------------
-    // Uniform mode: unit = (tile, split) with num_splits key ranges per tile. Tail mode
-    // (tail_splits > 0, num_splits == 1): tiles before the last tail_tiles are whole
-    // units; each of the last tail_tiles tiles is cut into tail_splits key ranges so the
-    // final wave of clusters is as full as the others.
-    const int unit = blockIdx.x >> 1;
-    const int tiles = p.B * p.row_tiles;
-    const int first_tail = tiles - p.tail_tiles;
-    int tile, split, nsplit;
+    // ---- roles ------------------------------------------------------------------------
+    const bool s_role = rank < 2;                  // ranks 0, 1: S pair; 2, 3: O pair
+    const int kpair = (int)(rank & 1);            // row tile of the unit = position in the pair
+    const bool leader = kpair == 0;               // issues the pair's MMAs
+    const uint32_t lead_rank = rank & ~1u;
+    const uint32_t o_rank = 2u + (uint32_t)kpair;  // the O-CTA an S-CTA feeds
+    constexpr uint16_t kMaskS = 0x3, kMaskO = 0xC;
+
+    // ---- unit -> (b, two row tiles, key range) -------------------------------------
+    // Uniform mode: unit = (pair of row tiles, split) with num_splits key ranges. Tail
+    // mode (tail_splits > 0, num_splits == 1): units before the last tail_units are
+    // whole; each of the last tail_units is cut into tail_splits key ranges so the final
+    // wave of clusters is as full as the others.
+    const int unit = blockIdx.x >> 2;
+    const int units = p.B * p.pairs_per_seq;
+    const int first_tail = units - p.tail_units;
+    int pair, split, nsplit;
     if (p.tail_splits > 0) {
         if (unit < first_tail) {
-            tile = unit;
+            pair = unit;
             split = 0;
             nsplit = 1;
         } else {
-            tile = first_tail + (unit - first_tail) / p.tail_splits;
+            pair = first_tail + (unit - first_tail) / p.tail_splits;
             split = (unit - first_tail) % p.tail_splits;
             nsplit = p.tail_splits;
         }
     } else {
-        tile = unit / p.num_splits;
+        pair = unit / p.num_splits;
         split = unit % p.num_splits;
         nsplit = p.num_splits;
     }
-    const int rt = tile % p.row_tiles;
-    const int b = tile / p.row_tiles;
+    const int b = pair / p.pairs_per_seq;
+    const int rt = 2 * (pair % p.pairs_per_seq) + kpair;   // past the sequence when row_tiles is odd
     const int P = p.prefix_len[b];
     const int kv_len = P + p.T;
     const int nblk = (kv_len + kKeys - 1) / kKeys;
@@ -283,111 +311,125 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---- set-up: barriers, TMEM ------------------------------------------------------
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNK; ++i) { mbar_init(&bar.kfull[i], 1); mbar_init(&bar.kempty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&bar.sfull[i], 1); mbar_init(&bar.sempty[i], 8); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&bar.sfull[i], 1); mbar_init(&bar.sempty[i], 16); }
         mbar_init(&bar.qpe_full, 1);
-        mbar_init(&bar.q_ready, 8);
-        for (int i = 0; i < kNP; ++i) { mbar_init(&bar.pempty[i], 1); mbar_init(&bar.pfull[i], 1); }
+        mbar_init(&bar.q_ready, 16);
+        for (int i = 0; i < kNP; ++i) {
+            mbar_init(&bar.pempty[i], 1);
+            mbar_init(&bar.pfull[i], 1);
+            mbar_init(&bar.pready[0][i], 1);
+            mbar_init(&bar.pready[1][i], 1);
+            bar.need[0][i] = bar.need[1][i] = 0;
+        }
+        for (int i = 0; i < kNS; ++i) mbar_init(&bar.sfree[i], 1);
         for (int i = 0; i < kNV; ++i) { mbar_init(&bar.vfull[i], 1); mbar_init(&bar.vempty[i], 1); }
-        mbar_init(&bar.corr_done, 1);
-        mbar_init(&bar.ack, 1);
-        mbar_init(&bar.o_ready, 1);
-        mbar_init(&bar.rescaled, 1);
-        mbar_init(&bar.sync_bar, 1);
-        bar.need_rescale = 0;
+        mbar_init(&bar.go, 1);
+        mbar_init(&bar.rescaled, 2);
         mbar_init(&bar.stats_full, 4);
+        mbar_init(&bar.sync_bar, 1);
         mbar_init(&bar.drain, 1);
+        bar.cmd = 0;
         bar.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {
-        tmem_alloc(&bar.tmem_base, 512);
-        tmem_relinquish();
+    if (warp == 0) {           // collective over the pair: both CTAs get the same columns
+        tmem_alloc_pair(&bar.tmem_base, 512);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();            // peer barriers initialised before any remote arrive
+    cluster_sync();            // every barrier of the cluster initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem = bar.tmem_base;
 
-    if (rank == 0) {
+    if (s_role) {
         // =============================== S-CTA ===============================
         unsigned char *qpe_tile = smem + kOffQpe;
         unsigned char *kring = smem + kOffKRing;
         const uint32_t tmem_q = tmem;                 // Q_nope: columns [0, 256)
         const uint32_t tmem_s0 = tmem + 256;          // score buffers at 256 and 384
         if (warp == 0) {
-            // ---------------- TMA producer: Q_pe once, then key chunks ----------------
+            // ------- TMA producer: Q_pe once, then this CTA's half of each key chunk -------
             if (elect_one() && nb > 0) {
-                tma_prefetch_desc(&map_ckv2);
+                tma_prefetch_desc(&map_ks);
                 tma_prefetch_desc(&map_kpe);
-                mbar_arrive_expect_tx(&bar.qpe_full, kChunkBytes);
-                tma_load_2d(qpe_tile, &map_qpe, &bar.qpe_full, 0, (int)((int64_t)b * p.rows_seq + r0));
+                if (leader) mbar_arrive_expect_tx(&bar.qpe_full, 2 * kQpeBytes);
+                tma_load_2d_pair(qpe_tile, &map_qpe, map_to_rank(&bar.qpe_full, lead_rank), 0,
+                                 (int)((int64_t)b * p.rows_seq + r0));
                 int slot = 0;
                 uint32_t phase = 0;
                 int issued = 0;
                 for (int j = 0; j < nb && !aborted(bar); ++j) {
-                    const int key0 = key_base + (kb0 + j) * kKeys;
-                    for (int c = 0; c < kSlotsPerBlock; ++c) {
-                        if (issued >= kNK && !wait_or_abort(bar, &bar.kempty[slot], phase ^ 1, p.err, -2)) break;
-                        if (c < 4) {      // latent dims [128c, 128c + 128): two sub-tiles in one request
-                            mbar_arrive_expect_tx(&bar.kfull[slot], kSlotBytes);
-                            tma_load_4d(kring + slot * kSlotBytes, &map_ckv2, &bar.kfull[slot], 0, key0, 2 * c, b);
+                    const int key0 = key_base + (kb0 + j) * kKeys + kpair * kHalfKeys;   // this CTA's 64 keys
+                    for (int c = 0; c < kKUsesPerBlock; ++c) {
+                        // the pair's MMAs have read the slot's previous contents
+                        if (issued >= kNK && !wait_cluster_or_abort(bar, &bar.kempty[slot], phase ^ 1, p.err, -2))
+                            break;
+                        if (issued >= kNK) KDT_TC_TRACE(kEvKEmpty, issued - kNK);
+                        const uint32_t kb = map_to_rank(&bar.kfull[slot], lead_rank);
+                        if (c < 2) {      // latent dims [256c, 256c + 256): four sub-tiles in one request
+                            if (leader) mbar_arrive_expect_tx(&bar.kfull[slot], 2 * kKSlotBytes);
+                            tma_load_4d_pair(kring + slot * kKSlotBytes, &map_ks, kb, 0, key0, 4 * c, b);
                         } else {          // rope dims
-                            mbar_arrive_expect_tx(&bar.kfull[slot], kChunkBytes);
-                            tma_load_3d(kring + slot * kSlotBytes, &map_kpe, &bar.kfull[slot], 0, key0, b);
+                            if (leader) mbar_arrive_expect_tx(&bar.kfull[slot], 2 * kKSub);
+                            tma_load_3d_pair(kring + slot * kKSlotBytes, &map_kpe, kb, 0, key0, b);
                         }
+                        KDT_TC_TRACE(kEvKIssue, issued);
                         ++issued;
                         if (++slot == kNK) { slot = 0; phase ^= 1; }
                     }
                 }
-                // drain: every issued chunk must land before this CTA may exit
+                // drain: the MMA commits for the last uses of every slot mean this CTA's
+                // copies have landed and been read; none may be in flight at exit
                 const int outstanding = issued < kNK ? issued : kNK;
                 int s = slot;
                 uint32_t ph = phase;
                 for (int k = 0; k < outstanding; ++k) {
                     if (--s < 0) { s = kNK - 1; ph ^= 1; }
-                    mbar_wait(&bar.kfull[s], ph, kWaitLimit);
+                    mbar_wait_cluster(&bar.kempty[s], ph, kWaitLimit);
                 }
             }
         } else if (warp == 1) {
-            // ---------------- MMA issuer: S = Q K^T ---------------------------------------
-            if (elect_one() && nb > 0) {
-                const uint32_t idesc = idesc_bf16_f32(kRows, kKeys, 0, 0);
-                bool ok = wait_or_abort(bar, &bar.q_ready, 0, p.err, -3) &&
-                          wait_or_abort(bar, &bar.qpe_full, 0, p.err, -3);
+            // ---------------- MMA issuer (leader): S = Q K^T for 256 rows -----------------
+            if (leader && elect_one() && nb > 0) {
+                const uint32_t idesc = idesc_bf16_f32(2 * kRows, kKeys, 0, 0);
+                bool ok = wait_cluster_or_abort(bar, &bar.q_ready, 0, p.err, -3) &&
+                          wait_cluster_or_abort(bar, &bar.qpe_full, 0, p.err, -3);
                 tc_fence_after();
                 int slot = 0;
                 uint32_t phase = 0;
                 for (int j = 0; j < nb && ok; ++j) {
                     const int buf = j & 1;
-                    if (j >= 2 && !(ok = wait_or_abort(bar, &bar.sempty[buf], ((j >> 1) - 1) & 1, p.err, -4))) break;
+                    if (j >= 2 && !(ok = wait_cluster_or_abort(bar, &bar.sempty[buf], ((j >> 1) - 1) & 1, p.err, -4)))
+                        break;
                     tc_fence_after();
                     KDT_TC_TRACE(kEvSMmaStart, j);
                     const uint32_t d = tmem_s0 + buf * kKeys;
-                    for (int c = 0; c < kSlotsPerBlock; ++c) {
-                        if (!(ok = wait_or_abort(bar, &bar.kfull[slot], phase, p.err, -5))) break;
+                    for (int c = 0; c < kKUsesPerBlock; ++c) {
+                        if (!(ok = wait_cluster_or_abort(bar, &bar.kfull[slot], phase, p.err, -5))) break;
                         tc_fence_after();
-                        const uint32_t kaddr = smem_u32(kring + slot * kSlotBytes);
-                        if (c < 4) {
-                            for (int t = 0; t < 2; ++t)            // sub-tile t: dims 128c + 64t .. +64
+                        KDT_TC_TRACE(kEvKFull, j * kKUsesPerBlock + c);
+                        const uint32_t kaddr = smem_u32(kring + slot * kKSlotBytes);
+                        if (c < 2) {
+                            for (int t = 0; t < 4; ++t)            // sub-tile t: dims 256c + 64t .. +64
                                 for (int kk = 0; kk < 4; ++kk) {
-                                    const uint64_t bdesc = sdesc_sw128(kaddr + t * kChunkBytes + kk * 32, 16, 1024);
-                                    mma_ts(d, tmem_q + 64 * c + 32 * t + 8 * kk, bdesc, idesc,
-                                           (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
+                                    const uint64_t bdesc = sdesc_sw128(kaddr + t * kKSub + kk * 32, 16, 1024);
+                                    mma_ts_pair(d, tmem_q + 128 * c + 32 * t + 8 * kk, bdesc, idesc,
+                                                (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
                                 }
                         } else {
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
-                                       sdesc_sw128(kaddr + kk * 32, 16, 1024), idesc, 1u);
+                                mma_ss_pair(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
+                                            sdesc_sw128(kaddr + kk * 32, 16, 1024), idesc, 1u);
                         }
-                        mma_commit(&bar.kempty[slot]);
+                        mma_commit_pair(&bar.kempty[slot], kMaskS);   // slot free in both S-CTAs
                         if (++slot == kNK) { slot = 0; phase ^= 1; }
                     }
                     if (!ok) break;
-                    mma_commit(&bar.sfull[buf]);
+                    mma_commit_pair(&bar.sfull[buf], kMaskS);
                     KDT_TC_TRACE(kEvSMmaIssued, j);
                 }
-                drain_mmas(bar);
+                drain_mmas(bar, 0x1);
             }
         } else if (warp >= 4) {
             // ---------------- Q_nope -> TMEM, then softmax ---------------------------------
@@ -411,7 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.q_ready);
+                if (lane == 0) mbar_arrive_remote_cta(&bar.q_ready, lead_rank);
             }
             const int qi = min(R, p.rows_seq - 1) / p.H;
             const uint32_t *visrow = p.vis + ((int64_t)b * p.T + qi) * p.W;
@@ -423,10 +465,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool fail = false;
             for (int j = 0; j < nb; ++j) {
                 // No warp leaves this loop on its own: every iteration meets the other seven
-                // at the named barrier, which ORs their failures.
+                // at the named barriers, which OR their failures.
                 const int buf = j & 1;
-                const int ps = j % kNP;
-                ok = ok && warp_wait(bar, &bar.sfull[buf], (j >> 1) & 1, p.err, -6);
+                const int ss = j % kNS;                            // staging slot here
+                const int ps = j % kNP;                            // P slot in the O-CTA
+                ok = ok && warp_wait_cluster(bar, &bar.sfull[buf], (j >> 1) & 1, p.err, -6);
                 float x[64];
                 float mx = -INFINITY;
                 if (ok) {
@@ -437,6 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_ld32(tmem_lane_addr(sbase, warp, 0), r0v);
                     tmem_ld32(tmem_lane_addr(sbase, warp, 32), r1v);
                     tmem_wait_ld();
+                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxLd, j);
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         x[q] = __uint_as_float(r0v[q]) * p.scale_log2;
@@ -444,7 +488,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.sempty[buf]);  // score buffer may be overwritten
+                    if (lane == 0) mbar_arrive_remote_cta(&bar.sempty[buf], lead_rank);   // buffer may be overwritten
                     if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxLoaded, j);
                     const int key0 = key_base + (kb0 + j) * kKeys + 64 * half;
                     if (key0 < 0 || key0 + 64 > P) {               // leading pad or tree keys: mask
@@ -474,87 +518,92 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     m_run = mx;
                     l_run *= alpha;
                 }
-                // the peer's P slot and this CTA's staging slot ps are free once P.V of
-                // block j - kNP is done
-                ok = j < kNP || warp_wait_cluster(bar, &bar.pempty[ps], ((j / kNP) - 1) & 1, p.err, -7);
-                if (!ok) continue;                                 // caught at the next barrier
-                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxSlot, j);
-                // staging slot ps: its previous copy (block j - kNP) landed before P.V of that
-                // block could run, which the pempty wait above has seen
-                unsigned char *stage = smem + kOffPStage + ps * kPBytes + half * (kPBytes / 2);
-                float lsum = 0.f;
-                const bool live = m_run > -INFINITY;
+                // the O-CTA's P slot is free once P.V of block j - kNP has run; this CTA's
+                // staging slot once the copy of block j - kNS has landed
+                ok = (j < kNP || warp_wait_cluster(bar, &bar.pempty[ps], ((j / kNP) - 1) & 1, p.err, -7)) &&
+                     (j < kNS || warp_wait_cluster(bar, &bar.sfree[ss], ((j / kNS) - 1) & 1, p.err, -19));
+                if (ok) {
+                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxSlot, j);
+                    unsigned char *slot_base = smem + kOffPStage + ss * kPSlotBytes;
+                    unsigned char *stage = slot_base + half * (kPBytes / 2);
+                    float lsum = 0.f;
+                    const bool live = m_run > -INFINITY;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {                      // 8 chunks of 8 keys
-                    uint32_t w[4];
+                    for (int u = 0; u < 8; ++u) {                  // 8 chunks of 8 keys
+                        uint32_t w[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float e0 = live ? fast_exp2(x[u * 8 + 2 * q] - m_run) : 0.f;
-                        const float e1 = live ? fast_exp2(x[u * 8 + 2 * q + 1] - m_run) : 0.f;
-                        lsum += e0 + e1;
-                        w[q] = pack_bf16x2(e0, e1);
+                        for (int q = 0; q < 4; ++q) {
+                            const float e0 = live ? fast_exp2(x[u * 8 + 2 * q] - m_run) : 0.f;
+                            const float e1 = live ? fast_exp2(x[u * 8 + 2 * q + 1] - m_run) : 0.f;
+                            lsum += e0 + e1;
+                            w[q] = pack_bf16x2(e0, e1);
+                        }
+                        *reinterpret_cast<uint4 *>(stage + row * 128 + ((u ^ (row & 7)) << 4)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    *reinterpret_cast<uint4 *>(stage + row * 128 + ((u ^ (row & 7)) << 4)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                    l_run += lsum;
+                    if (half == 0) reinterpret_cast<float *>(slot_base + kPBytes)[row] = alpha;
+                    fence_proxy_async_smem();                      // staging visible to the copy engine
                 }
-                l_run += lsum;
-                float *astage = reinterpret_cast<float *>(smem + kOffAStage + ps * kRows * 4);
-                if (half == 0) astage[row] = alpha;
-                fence_proxy_async_smem();                          // staging visible to the copy engine
-                __syncwarp();
-                if (lane == 0) {
-                    const uint32_t rows_off = (uint32_t)(32 * (warp & 3)) * 128;
-                    bulk_copy_to_peer(smem_u32(smem + kOffP + ps * kPBytes + half * (kPBytes / 2) + rows_off),
-                                      stage + rows_off, 32 * 128, &bar.pfull[ps], 1);
-                    if (half == 0) {
-                        const uint32_t a_off = (uint32_t)(32 * (warp & 3)) * 4;
-                        bulk_copy_to_peer(smem_u32(smem + kOffAlpha + ps * kRows * 4 + a_off),
-                                          reinterpret_cast<unsigned char *>(astage) + a_off, 32 * 4, &bar.pfull[ps], 1);
-                    }
+                // every warp reaches this barrier each block; one copy then carries the
+                // whole tile and its rescale factors to the O-CTA
+                if (barrier_or<3, 256>(!ok)) {
+                    fail = true;
+                    break;
                 }
-                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxSent, j);
+                if (threadIdx.x == 128) {
+                    bulk_copy_to_peer(smem_u32(smem + kOffP + ps * kPSlotBytes), smem + kOffPStage + ss * kPSlotBytes,
+                                      kPTx, &bar.pfull[ps], o_rank);
+                    KDT_TC_TRACE(kEvSoftmaxSent, j);
+                }
             }
-            // The peer's MMA commits free a P slot by arriving on pempty here; the arrivals
-            // for the last kNP blocks are consumed before this CTA may leave, so none can
-            // land in the shared memory of a CTA that later runs on this SM.
+            // The O pair's MMA commits (pempty) and the O-CTA's watcher (sfree) arrive
+            // here; the arrivals for the last blocks are consumed before this CTA may
+            // leave, so none can land in the shared memory of a CTA that later runs here.
             if (!fail && ok && warp == 4) {
                 for (int ps = 0; ps < kNP && ps < nb; ++ps) {
                     const int j_last = ps + ((nb - 1 - ps) / kNP) * kNP;
                     ok = warp_wait_cluster(bar, &bar.pempty[ps], (j_last / kNP) & 1, p.err, -18) && ok;
+                }
+                for (int ss = 0; ss < kNS && ss < nb; ++ss) {
+                    const int j_last = ss + ((nb - 1 - ss) / kNS) * kNS;
+                    ok = warp_wait_cluster(bar, &bar.sfree[ss], (j_last / kNS) & 1, p.err, -20) && ok;
                 }
             }
             // final statistics for the O-CTA epilogue: (m, l) with l summed over both halves
             if (half == 1) lsum_s[row] = l_run;
             fail = barrier_or<2, 256>(fail || !ok) || fail;
             if (!fail && half == 0 && nb > 0) {
-                const uint32_t dst = map_to_rank(smem + kOffStats + row * 8, 1);
+                const uint32_t dst = map_to_rank(smem + kOffStats + row * 8, o_rank);
                 st_cluster_f32(dst, m_run);
                 st_cluster_f32(dst + 4, l_run + lsum_s[row]);
                 publish_remote_stores();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(&bar.stats_full, 1);
+                if (lane == 0) mbar_arrive_remote(&bar.stats_full, o_rank);
             }
         }
     } else {
         // =============================== O-CTA ===============================
         unsigned char *pbase = smem + kOffP;
         unsigned char *vbase = smem + kOffV;
-        const float *alpha_s = reinterpret_cast<const float *>(smem + kOffAlpha);
         const float2 *stats_s = reinterpret_cast<const float2 *>(smem + kOffStats);
         if (warp == 0) {
-            // ---------------- TMA producer: V halves -----------------------------------------
+            // ------- TMA producer: this CTA's 128 of each 256 latent columns of V -------
             if (elect_one() && nb > 0) {
-                tma_prefetch_desc(&map_ckv4);
+                tma_prefetch_desc(&map_vs);
                 int slot = 0;
                 uint32_t phase = 0;
                 int issued = 0;
                 for (int j = 0; j < nb && !aborted(bar); ++j) {
                     const int key0 = key_base + (kb0 + j) * kKeys;
                     for (int h = 0; h < 2; ++h) {
-                        if (issued >= kNV && !wait_or_abort(bar, &bar.vempty[slot], phase ^ 1, p.err, -8)) break;
-                        mbar_arrive_expect_tx(&bar.vfull[slot], kVHalfBytes);
-                        // latent dims [256h, 256h + 256): four sub-tiles in one request
-                        tma_load_4d(vbase + slot * kVHalfBytes, &map_ckv4, &bar.vfull[slot], 0, key0, 4 * h, b);
+                        if (issued >= kNV && !wait_cluster_or_abort(bar, &bar.vempty[slot], phase ^ 1, p.err, -8))
+                            break;
+                        if (leader) mbar_arrive_expect_tx(&bar.vfull[slot], 2 * kVSlotBytes);
+                        // latent dims [256h + 128k, +128): two sub-tiles in one request
+                        tma_load_4d_pair(vbase + slot * kVSlotBytes, &map_vs, map_to_rank(&bar.vfull[slot], lead_rank),
+                                         0, key0, 4 * h + 2 * kpair, b);
+                        KDT_TC_TRACE(kEvVIssue, issued);
                         ++issued;
                         if (++slot == kNV) { slot = 0; phase ^= 1; }
                     }
@@ -564,134 +613,118 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint32_t ph = phase;
                 for (int k = 0; k < outstanding; ++k) {
                     if (--s < 0) { s = kNV - 1; ph ^= 1; }
-                    mbar_wait(&bar.vfull[s], ph, kWaitLimit);
+                    mbar_wait_cluster(&bar.vempty[s], ph, kWaitLimit);
                 }
             }
         } else if (warp == 1) {
-            // ---------------- MMA issuer: O += P V --------------------------------------------
-            if (elect_one() && nb > 0) {
-                const uint32_t idesc = idesc_bf16_f32(kRows, 256, 0, 1);
+            // ---------------- MMA issuer (leader): O += P V for 256 rows --------------------
+            if (leader && elect_one() && nb > 0) {
+                const uint32_t idesc = idesc_bf16_f32(2 * kRows, 256, 0, 1);
                 int slot = 0;
                 uint32_t phase = 0;
                 uint32_t rs_phase = 0, sync_phase = 0;
                 bool ok = true;
                 for (int j = 0; j < nb && ok; ++j) {
                     const int ps = j % kNP;
-                    if (!(ok = wait_or_abort(bar, &bar.corr_done, j & 1, p.err, -9))) break;
+                    const uint32_t par = (uint32_t)(j / kNP) & 1;
+                    if (!(ok = wait_cluster_or_abort(bar, &bar.pready[0][ps], par, p.err, -9) &&
+                               wait_cluster_or_abort(bar, &bar.pready[1][ps], par, p.err, -9)))
+                        break;
                     KDT_TC_TRACE(kEvOMmaStart, j);
-                    const int need = *reinterpret_cast<volatile int *>(&bar.need_rescale);
-                    mbar_arrive(&bar.ack);
-                    if (need) {
-                        // let every P.V issued so far finish, hand O to the correction warps,
-                        // and wait until they have rescaled it
-                        mma_commit(&bar.sync_bar);
-                        if (!(ok = wait_or_abort(bar, &bar.sync_bar, sync_phase, p.err, -15))) break;
+                    const uint32_t n0 = *reinterpret_cast<volatile uint32_t *>(&bar.need[0][ps]);
+                    const uint32_t n1 = *reinterpret_cast<volatile uint32_t *>(&bar.need[1][ps]);
+                    if (n0 | n1) {
+                        // let every P.V issued so far finish, then hand O to the CTAs whose
+                        // rows need the rescale (the others count as done at once)
+                        mma_commit_pair(&bar.sync_bar, 0x4);
+                        if (!(ok = wait_cluster_or_abort(bar, &bar.sync_bar, sync_phase, p.err, -15))) break;
                         sync_phase ^= 1;
                         tc_fence_before();
-                        mbar_arrive(&bar.o_ready);
-                        if (!(ok = wait_or_abort(bar, &bar.rescaled, rs_phase, p.err, -16))) break;
+                        for (uint32_t k = 0; k < 2; ++k) {
+                            if (k == 0 ? n0 : n1) {
+                                st_cluster_u32(map_to_rank(&bar.cmd, 2 + k), (uint32_t)ps);
+                                mbar_arrive_remote(&bar.go, 2 + k);      // release: command first
+                            } else {
+                                mbar_arrive(&bar.rescaled);
+                            }
+                        }
+                        if (!(ok = wait_cluster_or_abort(bar, &bar.rescaled, rs_phase, p.err, -16))) break;
                         rs_phase ^= 1;
                     }
                     tc_fence_after();
-                    const uint32_t paddr = smem_u32(pbase + ps * kPBytes);
+                    const uint32_t paddr = smem_u32(pbase + ps * kPSlotBytes);
                     for (int h = 0; h < 2; ++h) {
-                        if (!(ok = wait_or_abort(bar, &bar.vfull[slot], phase, p.err, -10))) break;
+                        if (!(ok = wait_cluster_or_abort(bar, &bar.vfull[slot], phase, p.err, -10))) break;
                         tc_fence_after();
-                        const uint32_t vaddr = smem_u32(vbase + slot * kVHalfBytes);
+                        KDT_TC_TRACE(kEvVFull, 2 * j + h);
+                        const uint32_t vaddr = smem_u32(vbase + slot * kVSlotBytes);
                         for (int kk = 0; kk < kKeys / 16; ++kk) {
                             const uint64_t adesc = sdesc_sw128(paddr + (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bdesc = sdesc_sw128(vaddr + kk * 2048, kChunkBytes, 1024);
-                            mma_ss(tmem + 256 * h, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                            const uint64_t bdesc = sdesc_sw128(vaddr + kk * 2048, kVSub, 1024);
+                            mma_ss_pair(tmem + 256 * h, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
                         }
-                        mma_commit(&bar.vempty[slot]);
+                        mma_commit_pair(&bar.vempty[slot], kMaskO);   // slot free in both O-CTAs
                         if (++slot == kNV) { slot = 0; phase ^= 1; }
                     }
                     if (!ok) break;
                     KDT_TC_TRACE(kEvOMmaIssued, j);
-                    // release the P slot in the S-CTA once this block's P.V has read it
-                    asm volatile(
-                        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], "
-                        "%1;" ::"r"(smem_u32(&bar.pempty[ps])),
-                        "h"((uint16_t)1)
-                        : "memory");
+                    // P slot ps of both O-CTAs is free again: tell both S-CTAs
+                    mma_commit_pair(&bar.pempty[ps], kMaskS);
                 }
-                drain_mmas(bar);
+                for (uint32_t k = 0; k < 2; ++k) {       // release the correction warps
+                    st_cluster_u32(map_to_rank(&bar.cmd, 2 + k), kCmdDone);
+                    mbar_arrive_remote(&bar.go, 2 + k);
+                }
+                drain_mmas(bar, kMaskO);
+            }
+        } else if (warp == 2) {
+            // ---------------- P watcher: P of each block landed, and does O need a rescale? --
+            for (int j = 0; j < nb; ++j) {
+                const int ps = j % kNP;
+                if (lane == 0) mbar_arrive_expect_tx(&bar.pfull[ps], kPTx);   // P + alpha of block j
+                if (!warp_wait_cluster(bar, &bar.pfull[ps], (j / kNP) & 1, p.err, -11)) break;
+                if (lane == 0) KDT_TC_TRACE(kEvCorrIn, j);
+                const float4 a4 = reinterpret_cast<const float4 *>(pbase + ps * kPSlotBytes + kPBytes)[lane];
+                const bool need =
+                    j > 0 && __any_sync(0xffffffffu, a4.x != 1.f || a4.y != 1.f || a4.z != 1.f || a4.w != 1.f);
+                if (lane == 0) {
+                    mbar_arrive_remote_cta(&bar.sfree[j % kNS], (uint32_t)kpair);   // its staging slot is reusable
+                    st_cluster_u32(map_to_rank(&bar.need[kpair][ps], lead_rank), need ? 1u : 0u);
+                    mbar_arrive_remote(&bar.pready[kpair][ps], lead_rank);          // release: flag first
+                }
+                __syncwarp();
             }
         } else if (warp >= 4 && warp < 8) {
             // ---------------- correction (rare rescale) and epilogue -------------------------
             // Warps 4-7 only (one per TMEM lane quadrant): named barrier 1 counts 128 threads.
+            // They sleep on `go` until the MMA thread hands O over for a rescale or ends.
             const int row = 32 * (warp & 3) + lane;
             bool ok = true;
-            uint32_t rs_phase = 0;
-            for (int j = 0; j < nb; ++j) {
-                // Every correction warp reaches the named barriers below each block, whatever
-                // happened, so a timeout in one warp cannot strand the others there; the
-                // decision to stop is the barrier's OR-reduction of the warps' failures.
-                const int ps = j % kNP;
-                if (threadIdx.x == 128) mbar_arrive_expect_tx(&bar.pfull[ps], kPTx);   // P + alpha of block j
-                ok = ok && warp_wait_cluster(bar, &bar.pfull[ps], (j / kNP) & 1, p.err, -11);
-                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvCorrIn, j);
-                const float a = ok ? alpha_s[ps * kRows + row] : 1.f;
-                const bool mine = ok && j > 0 && __any_sync(0xffffffffu, a != 1.f);
-                uint32_t fail_any, need_any;
-                asm volatile(
-                    "{\n\t.reg .pred pin, pout;\n\t"
-                    "setp.ne.u32 pin, %1, 0;\n\t"
-                    "bar.red.or.pred pout, 1, 128, pin;\n\t"
-                    "selp.u32 %0, 1, 0, pout;\n\t}"
-                    : "=r"(fail_any)
-                    : "r"(ok ? 0u : 1u)
-                    : "memory");
-                asm volatile(
-                    "{\n\t.reg .pred pin, pout;\n\t"
-                    "setp.ne.u32 pin, %1, 0;\n\t"
-                    "bar.red.or.pred pout, 1, 128, pin;\n\t"
-                    "selp.u32 %0, 1, 0, pout;\n\t}"
-                    : "=r"(need_any)
-                    : "r"(mine ? 1u : 0u)
-                    : "memory");
-                if (fail_any) {
+            for (uint32_t e = 0; nb > 0; ++e) {
+                ok = warp_wait_cluster(bar, &bar.go, e & 1, p.err, -12);
+                if (barrier_or<1, 128>(!ok)) {
                     ok = false;
                     break;
                 }
-                if (threadIdx.x == 128) {
-                    bar.need_rescale = need_any ? 1 : 0;
-                    mbar_arrive(&bar.corr_done);          // release: need_rescale visible to the MMA thread
-                }
-                if (need_any) {
-                    // O is handed over once every P.V before block j has completed
-                    ok = warp_wait(bar, &bar.o_ready, rs_phase, p.err, -12);
-                    tc_fence_after();
-                    if (ok) {               // whole warp; rows that need no rescale multiply by 1
-                        for (int c = 0; c < 512 / 32; ++c) {
-                            uint32_t r[32];
-                            const uint32_t addr = tmem_lane_addr(tmem, warp, c * 32);
-                            tmem_ld32(addr, r);
-                            tmem_wait_ld();
+                const uint32_t cmd = *reinterpret_cast<volatile uint32_t *>(&bar.cmd);
+                if (cmd == kCmdDone) break;
+                // every P.V before the block in P slot `cmd` has completed: rescale this CTA's
+                // rows of O by that block's factors (rows that need none multiply by 1)
+                const float a = reinterpret_cast<const float *>(pbase + (cmd % kNP) * kPSlotBytes + kPBytes)[row];
+                tc_fence_after();
+                for (int c = 0; c < 512 / 32; ++c) {
+                    uint32_t r[32];
+                    const uint32_t addr = tmem_lane_addr(tmem, warp, c * 32);
+                    tmem_ld32(addr, r);
+                    tmem_wait_ld();
 #pragma unroll
-                            for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * a);
-                            tmem_st32(addr, r);
-                        }
-                        tmem_wait_st();
-                    }
-                    tc_fence_before();
-                    asm volatile(
-                        "{\n\t.reg .pred pin, pout;\n\t"
-                        "setp.ne.u32 pin, %1, 0;\n\t"
-                        "bar.red.or.pred pout, 1, 128, pin;\n\t"
-                        "selp.u32 %0, 1, 0, pout;\n\t}"
-                        : "=r"(fail_any)
-                        : "r"(ok ? 0u : 1u)
-                        : "memory");
-                    if (fail_any) {
-                        ok = false;
-                        break;
-                    }
-                    if (threadIdx.x == 128) mbar_arrive(&bar.rescaled);
-                    rs_phase ^= 1;
+                    for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * a);
+                    tmem_st32(addr, r);
                 }
-                // the MMA thread has read this block's flag before the next one is written
-                ok = warp_wait(bar, &bar.ack, j & 1, p.err, -17);
+                tmem_wait_st();
+                tc_fence_before();
+                barrier_or<1, 128>(false);                 // all four warps' stores done
+                if (threadIdx.x == 128) mbar_arrive_remote(&bar.rescaled, lead_rank);
             }
             // epilogue
             const int R = r0 + row;
@@ -701,8 +734,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 orow = p.out + grow * kDc;
                 lrow = p.lse ? p.lse + grow : nullptr;
             } else if (p.tail_splits > 0) {                  // compact tail partials
-                const int64_t nrows = (int64_t)p.tail_tiles * kRows;
-                const int64_t k = (int64_t)(tile - first_tail) * kRows + row;
+                const int64_t nrows = (int64_t)p.tail_units * 2 * kRows;
+                const int64_t k = ((int64_t)(pair - first_tail) * 2 + kpair) * kRows + row;
                 orow = p.part_o + ((int64_t)split * nrows + k) * kDc;
                 lrow = p.part_lse + (int64_t)split * nrows + k;
             } else {
@@ -714,7 +747,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < kDc; c += 4) *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (lrow) *lrow = -INFINITY;
                 }
-            } else if (ok && warp_wait(bar, &bar.drain, 0, p.err, -13) &&
+            } else if (ok && warp_wait_cluster(bar, &bar.drain, 0, p.err, -13) &&
                        warp_wait_cluster(bar, &bar.stats_full, 0, p.err, -14)) {
                 tc_fence_after();
                 const float2 st = stats_s[row];
@@ -740,18 +773,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (aborted(bar)) {
-        // Error path only: copies the peer issued before it noticed may still be in
-        // flight; give them time to land (they take microseconds) before either CTA
-        // of the cluster can leave.
+        // Error path only: copies another CTA issued before it noticed may still be in
+        // flight; give them time to land (they take microseconds) before any CTA of the
+        // cluster can leave.
         const uint64_t t0 = global_ns();
         do {
             __nanosleep(1000);
         } while (global_ns() - t0 < 200000ull);
     }
-    cluster_sync();            // no CTA leaves while its peer may still touch its shared memory
+    cluster_sync();            // no CTA leaves while another may still touch its shared memory
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc_pair(tmem, 512);
 }
+
+}  // namespace
+
+int tc_rows_per_unit() { return 2 * kRows; }
+int tc_keys_per_block() { return kKeys; }
+
+int tc_max_clusters() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return sm_count() / 4 > 0 ? sm_count() / 4 : 1;
+    const int slot = dev & 63;
+    int n = cached[slot].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(4);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 4;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();    // clear the query's error; plan with the SM count instead
+        return sm_count() / 4 > 0 ? sm_count() / 4 : 1;
+    }
+    cached[slot].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+namespace {
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -785,26 +852,24 @@ bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims
 
 }  // namespace
 
-int tc_rows_per_unit() { return kRows; }
-int tc_keys_per_block() { return kKeys; }
 
 cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
-    CUtensorMap map_ckv2, map_ckv4, map_kpe, map_qpe;
+    CUtensorMap map_ks, map_vs, map_kpe, map_qpe;
     const cuuint64_t L = (cuuint64_t)vp.L;
     {
-        // c_kv viewed as [B][8 dim-blocks][L keys][64]: a box of (64, 128 keys, n blocks)
-        // lands as n consecutive [128 x 64] 128B-swizzled sub-tiles.
+        // c_kv viewed as [B][8 dim-blocks][L keys][64]: a box of (64, n keys, m blocks)
+        // lands as m consecutive [n x 64] 128B-swizzled sub-tiles.
         cuuint64_t dims[4] = {64, L, (cuuint64_t)(kDc / 64), (cuuint64_t)vp.B};
         cuuint64_t strides[3] = {(cuuint64_t)kDc * 2, 128, L * kDc * 2};
-        cuuint32_t box2[4] = {64, kKeys, 2, 1};
-        cuuint32_t box4[4] = {64, kKeys, 4, 1};
-        if (!make_map(&map_ckv2, vp.c_kv, 4, dims, strides, box2)) return cudaErrorInvalidValue;
-        if (!make_map(&map_ckv4, vp.c_kv, 4, dims, strides, box4)) return cudaErrorInvalidValue;
+        cuuint32_t box_k[4] = {64, kHalfKeys, 4, 1};    // S-CTA: its 64 keys x 256 dims
+        cuuint32_t box_v[4] = {64, kKeys, 2, 1};        // O-CTA: 128 keys x its 128 dims
+        if (!make_map(&map_ks, vp.c_kv, 4, dims, strides, box_k)) return cudaErrorInvalidValue;
+        if (!make_map(&map_vs, vp.c_kv, 4, dims, strides, box_v)) return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[3] = {(cuuint64_t)kDr, L, (cuuint64_t)vp.B};
         cuuint64_t strides[2] = {(cuuint64_t)kDr * 2, L * kDr * 2};
-        cuuint32_t box[3] = {64, kKeys, 1};
+        cuuint32_t box[3] = {64, kHalfKeys, 1};
         if (!make_map(&map_kpe, vp.k_pe, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
@@ -832,14 +897,15 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     p.part_o = vp.part_o;
     p.part_lse = vp.part_lse;
     p.err = vp.err;
-    p.tail_tiles = vp.tail_tiles;
+    p.tail_units = vp.tail_units;
     p.tail_splits = vp.tail_splits;
-    const int64_t tiles = (int64_t)p.B * p.row_tiles;
-    const int64_t units = p.tail_splits > 0 ? tiles - p.tail_tiles + (int64_t)p.tail_tiles * p.tail_splits
-                                            : tiles * p.num_splits;
+    p.pairs_per_seq = (p.row_tiles + 1) / 2;
+    const int64_t base = (int64_t)p.B * p.pairs_per_seq;
+    const int64_t units = p.tail_splits > 0 ? base - p.tail_units + (int64_t)p.tail_units * p.tail_splits
+                                            : base * p.num_splits;
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    verify_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, s>>>(map_ckv2, map_ckv4, map_kpe, map_qpe, p);
+    verify_tc_kernel<<<(unsigned)(4 * units), kThreads, kSmemBytes, s>>>(map_ks, map_vs, map_kpe, map_qpe, p);
     return cudaGetLastError();
 }
 

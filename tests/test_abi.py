@@ -126,8 +126,8 @@ def test_plan_and_workspace_are_host_only(kdt):
     rows = 1 * 32 * 64
     assert p["workspace_bytes"] >= 8 * rows * 512 * 4 + 8 * rows * 4
     assert kdt.workspace_size(_args(kdt, D_c=3)) == 0
-    # bf16 inputs plan onto the tensor-core kernel: 2-CTA clusters of 128 rows x 128-key blocks
+    # bf16 inputs plan onto the tensor-core kernel: 4-CTA clusters, each two 128-row tiles
     c = _args(kdt, dtype=1, impl=0, B=8, T=64, H=64, kv_row_stride=8256, max_kv_len=8256, num_splits=1)
     p = kdt.plan(c)
-    assert p["impl"] == "tcgen05" and p["ctas"] == 2 * 8 * 32 and p["num_splits"] == 1
+    assert p["impl"] == "tcgen05" and p["ctas"] == 4 * 8 * 16 and p["num_splits"] == 1
     assert _status(kdt, _args(kdt, dtype=0, impl=2)) == kdt.kdt.KDT_ERR_UNSUPPORTED   # fp32 on tensor cores
