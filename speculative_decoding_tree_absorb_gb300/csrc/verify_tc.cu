@@ -89,16 +89,16 @@ constexpr int kKSub = kHalfKeys * 128;            // S-CTA key sub-tile [64 keys
 constexpr int kVSub = kKeys * 128;                // O-CTA value sub-tile [128 keys x 64 dims]: 16 KB
 // Tiles travel as 32 KB requests from 4-D views of the cache (few, large requests:
 // the copy engine's cost is per request).
-constexpr int kKSlotBytes = 4 * kKSub;            // S ring slot: 64 keys x 256 latent dims
-constexpr int kKUsesPerBlock = 3;                 // two latent slots + one rope slot (8 KB used)
-constexpr int kNK = 4;                            // S-CTA key ring slots (128 KB)
+constexpr int kKSlotBytes = 4 * kKSub;            // S latent ring slot: 64 keys x 256 latent dims
+constexpr int kNK = 4;                            // S-CTA latent key ring slots (128 KB, two blocks)
+constexpr int kNR = 4;                            // S-CTA rope key ring slots of kKSub (32 KB, four blocks)
 constexpr int kQpeBytes = kRows * 128;            // Q_pe tile of one S-CTA: 16 KB
 constexpr int kPBytes = kRows * kKeys * 2;        // P tile of one CTA: 32 KB (two 128B-swizzled halves)
 // A P slot holds the tile followed by the block's rescale factors, so one bulk copy
 // per block carries both.
 constexpr int kPSlotBytes = kPBytes + 1024;       // 32 KB P + alpha[128] (+ pad to 1 KB alignment)
 constexpr uint32_t kPTx = kPBytes + kRows * 4;    // bytes copied into a P slot per block
-constexpr int kNS = 2;                            // S-CTA staging slots (free once the copy landed)
+constexpr int kNS = 1;                            // S-CTA staging slots (free once the copy landed)
 constexpr int kNP = 3;                            // O-CTA P slots (free once P.V of the block ran)
 constexpr int kVSlotBytes = 2 * kVSub;            // O ring slot: 128 keys x 128 latent dims
 constexpr int kNV = 3;                            // O-CTA value ring slots (96 KB)
@@ -110,7 +110,8 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 // different parts). All tiles 1024-byte aligned for the 128B swizzle.
 constexpr int kOffQpe = 0;                                  // S: Q_pe tile 16 KB
 constexpr int kOffKRing = kOffQpe + kQpeBytes;              // S: 4 x 32 KB
-constexpr int kOffPStage = kOffKRing + kNK * kKSlotBytes;   // S: 2 x 33 KB staging of P + alpha
+constexpr int kOffRRing = kOffKRing + kNK * kKSlotBytes;   // S: 4 x 8 KB rope keys
+constexpr int kOffPStage = kOffRRing + kNR * kKSub;         // S: 33 KB staging of P + alpha
 constexpr int kOffRowMax = kOffPStage + kNS * kPSlotBytes;  // S: [2 blocks][2 halves][128] partial maxima
 constexpr int kOffLSum = kOffRowMax + 2 * 2 * kRows * 4;    // S: [128] partial row sums
 constexpr int kOffP = 0;                                    // O: 3 x 33 KB P + alpha
@@ -126,8 +127,10 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 // issues the pair's MMAs; barriers the MMA thread waits on live in the leader.
 struct Barriers {
     // S pair
-    uint64_t kfull[kNK];           // leader: both halves of a key chunk landed (tx of both CTAs)
+    uint64_t kfull[kNK];           // leader: both halves of a latent key chunk landed (tx of both CTAs)
     uint64_t kempty[kNK];          // each S-CTA: its half of the chunk was read (MMA commit)
+    uint64_t rfull[kNR];           // leader: both halves of a rope key chunk landed
+    uint64_t rempty[kNR];          // each S-CTA: its rope chunk was read
     uint64_t sfull[2];             // each S-CTA: scores of a block are in its TMEM
     uint64_t sempty[2];            // leader: both CTAs' softmax warps have read the buffer (16 arrivals)
     uint64_t qpe_full;             // leader: both Q_pe tiles landed
@@ -218,6 +221,38 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_local, const void
     asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
                  : "memory");
+}
+
+// Position in a ring of `kSlots` buffers: slot, its phase parity, uses so far.
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;
+    int n = 0;
+};
+
+template <int kSlots>
+__device__ __forceinline__ void ring_advance(RingPos &r) {
+    ++r.n;
+    if (++r.slot == kSlots) {
+        r.slot = 0;
+        r.phase ^= 1;
+    }
+}
+
+// Wait until the releases of the last (up to kSlots) uses of a ring have arrived: the
+// copies into those slots have landed and been read, and no arrival is still in flight.
+template <int kSlots>
+__device__ __forceinline__ void ring_drain(uint64_t *empty, const RingPos &r) {
+    const int outstanding = r.n < kSlots ? r.n : kSlots;
+    int s = r.slot;
+    uint32_t ph = r.phase;
+    for (int k = 0; k < outstanding; ++k) {
+        if (--s < 0) {
+            s = kSlots - 1;
+            ph ^= 1;
+        }
+        mbar_wait_cluster(&empty[s], ph, kWaitLimit);
+    }
 }
 
 // Named barrier over `count` threads that also ORs a per-thread flag across them.
@@ -311,6 +346,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // ---- set-up: barriers, TMEM ------------------------------------------------------
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNK; ++i) { mbar_init(&bar.kfull[i], 1); mbar_init(&bar.kempty[i], 1); }
+        for (int i = 0; i < kNR; ++i) { mbar_init(&bar.rfull[i], 1); mbar_init(&bar.rempty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&bar.sfull[i], 1); mbar_init(&bar.sempty[i], 16); }
         mbar_init(&bar.qpe_full, 1);
         mbar_init(&bar.q_ready, 16);
@@ -346,6 +382,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         // =============================== S-CTA ===============================
         unsigned char *qpe_tile = smem + kOffQpe;
         unsigned char *kring = smem + kOffKRing;
+        unsigned char *rring = smem + kOffRRing;
         const uint32_t tmem_q = tmem;                 // Q_nope: columns [0, 256)
         const uint32_t tmem_s0 = tmem + 256;          // score buffers at 256 and 384
         if (warp == 0) {
@@ -356,38 +393,35 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 if (leader) mbar_arrive_expect_tx(&bar.qpe_full, 2 * kQpeBytes);
                 tma_load_2d_pair(qpe_tile, &map_qpe, map_to_rank(&bar.qpe_full, lead_rank), 0,
                                  (int)((int64_t)b * p.rows_seq + r0));
-                int slot = 0;
-                uint32_t phase = 0;
-                int issued = 0;
-                for (int j = 0; j < nb && !aborted(bar); ++j) {
+                RingPos kr, rr;
+                bool going = true;
+                for (int j = 0; j < nb && going && !aborted(bar); ++j) {
                     const int key0 = key_base + (kb0 + j) * kKeys + kpair * kHalfKeys;   // this CTA's 64 keys
-                    for (int c = 0; c < kKUsesPerBlock; ++c) {
+                    for (int c = 0; c < 2 && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
                         // the pair's MMAs have read the slot's previous contents
-                        if (issued >= kNK && !wait_cluster_or_abort(bar, &bar.kempty[slot], phase ^ 1, p.err, -2))
+                        if (kr.n >= kNK &&
+                            !(going = wait_cluster_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -2)))
                             break;
-                        if (issued >= kNK) KDT_TC_TRACE(kEvKEmpty, issued - kNK);
-                        const uint32_t kb = map_to_rank(&bar.kfull[slot], lead_rank);
-                        if (c < 2) {      // latent dims [256c, 256c + 256): four sub-tiles in one request
-                            if (leader) mbar_arrive_expect_tx(&bar.kfull[slot], 2 * kKSlotBytes);
-                            tma_load_4d_pair(kring + slot * kKSlotBytes, &map_ks, kb, 0, key0, 4 * c, b);
-                        } else {          // rope dims
-                            if (leader) mbar_arrive_expect_tx(&bar.kfull[slot], 2 * kKSub);
-                            tma_load_3d_pair(kring + slot * kKSlotBytes, &map_kpe, kb, 0, key0, b);
-                        }
-                        KDT_TC_TRACE(kEvKIssue, issued);
-                        ++issued;
-                        if (++slot == kNK) { slot = 0; phase ^= 1; }
+                        if (kr.n >= kNK) KDT_TC_TRACE(kEvKEmpty, kr.n - kNK);
+                        if (leader) mbar_arrive_expect_tx(&bar.kfull[kr.slot], 2 * kKSlotBytes);
+                        tma_load_4d_pair(kring + kr.slot * kKSlotBytes, &map_ks, map_to_rank(&bar.kfull[kr.slot], lead_rank),
+                                         0, key0, 4 * c, b);
+                        KDT_TC_TRACE(kEvKIssue, kr.n);
+                        ring_advance<kNK>(kr);
                     }
+                    if (!going) break;
+                    if (rr.n >= kNR &&
+                        !(going = wait_cluster_or_abort(bar, &bar.rempty[rr.slot], rr.phase ^ 1, p.err, -2)))
+                        break;
+                    if (leader) mbar_arrive_expect_tx(&bar.rfull[rr.slot], 2 * kKSub);
+                    tma_load_3d_pair(rring + rr.slot * kKSub, &map_kpe, map_to_rank(&bar.rfull[rr.slot], lead_rank), 0,
+                                     key0, b);
+                    ring_advance<kNR>(rr);
                 }
                 // drain: the MMA commits for the last uses of every slot mean this CTA's
                 // copies have landed and been read; none may be in flight at exit
-                const int outstanding = issued < kNK ? issued : kNK;
-                int s = slot;
-                uint32_t ph = phase;
-                for (int k = 0; k < outstanding; ++k) {
-                    if (--s < 0) { s = kNK - 1; ph ^= 1; }
-                    mbar_wait_cluster(&bar.kempty[s], ph, kWaitLimit);
-                }
+                ring_drain<kNK>(bar.kempty, kr);
+                ring_drain<kNR>(bar.rempty, rr);
             }
         } else if (warp == 1) {
             // ---------------- MMA issuer (leader): S = Q K^T for 256 rows -----------------
@@ -396,8 +430,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 bool ok = wait_cluster_or_abort(bar, &bar.q_ready, 0, p.err, -3) &&
                           wait_cluster_or_abort(bar, &bar.qpe_full, 0, p.err, -3);
                 tc_fence_after();
-                int slot = 0;
-                uint32_t phase = 0;
+                RingPos kr, rr;
                 for (int j = 0; j < nb && ok; ++j) {
                     const int buf = j & 1;
                     if (j >= 2 && !(ok = wait_cluster_or_abort(bar, &bar.sempty[buf], ((j >> 1) - 1) & 1, p.err, -4)))
@@ -405,25 +438,30 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     KDT_TC_TRACE(kEvSMmaStart, j);
                     const uint32_t d = tmem_s0 + buf * kKeys;
-                    for (int c = 0; c < kKUsesPerBlock; ++c) {
-                        if (!(ok = wait_cluster_or_abort(bar, &bar.kfull[slot], phase, p.err, -5))) break;
+                    for (int c = 0; c < 2; ++c) {
+                        if (!(ok = wait_cluster_or_abort(bar, &bar.kfull[kr.slot], kr.phase, p.err, -5))) break;
                         tc_fence_after();
-                        KDT_TC_TRACE(kEvKFull, j * kKUsesPerBlock + c);
-                        const uint32_t kaddr = smem_u32(kring + slot * kKSlotBytes);
-                        if (c < 2) {
-                            for (int t = 0; t < 4; ++t)            // sub-tile t: dims 256c + 64t .. +64
-                                for (int kk = 0; kk < 4; ++kk) {
-                                    const uint64_t bdesc = sdesc_sw128(kaddr + t * kKSub + kk * 32, 16, 1024);
-                                    mma_ts_pair(d, tmem_q + 128 * c + 32 * t + 8 * kk, bdesc, idesc,
-                                                (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
-                                }
-                        } else {
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ss_pair(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
-                                            sdesc_sw128(kaddr + kk * 32, 16, 1024), idesc, 1u);
-                        }
-                        mma_commit_pair(&bar.kempty[slot], kMaskS);   // slot free in both S-CTAs
-                        if (++slot == kNK) { slot = 0; phase ^= 1; }
+                        KDT_TC_TRACE(kEvKFull, kr.n);
+                        const uint32_t kaddr = smem_u32(kring + kr.slot * kKSlotBytes);
+                        for (int t = 0; t < 4; ++t)                // sub-tile t: dims 256c + 64t .. +64
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t bdesc = sdesc_sw128(kaddr + t * kKSub + kk * 32, 16, 1024);
+                                mma_ts_pair(d, tmem_q + 128 * c + 32 * t + 8 * kk, bdesc, idesc,
+                                            (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        mma_commit_pair(&bar.kempty[kr.slot], kMaskS);   // slot free in both S-CTAs
+                        ring_advance<kNK>(kr);
+                    }
+                    if (!ok) break;
+                    if (!(ok = wait_cluster_or_abort(bar, &bar.rfull[rr.slot], rr.phase, p.err, -5))) break;
+                    tc_fence_after();
+                    {
+                        const uint32_t raddr = smem_u32(rring + rr.slot * kKSub);
+                        for (int kk = 0; kk < 4; ++kk)             // rope dims
+                            mma_ss_pair(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
+                                        sdesc_sw128(raddr + kk * 32, 16, 1024), idesc, 1u);
+                        mma_commit_pair(&bar.rempty[rr.slot], kMaskS);
+                        ring_advance<kNR>(rr);
                     }
                     if (!ok) break;
                     mma_commit_pair(&bar.sfull[buf], kMaskS);
@@ -542,19 +580,21 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                             make_uint4(w[0], w[1], w[2], w[3]);
                     }
                     l_run += lsum;
-                    if (half == 0) reinterpret_cast<float *>(slot_base + kPBytes)[row] = alpha;
+                    // the rescale factors follow the second half of P, which carries them
+                    if (half == 1) reinterpret_cast<float *>(slot_base + kPBytes)[row] = alpha;
                     fence_proxy_async_smem();                      // staging visible to the copy engine
                 }
-                // every warp reaches this barrier each block; one copy then carries the
-                // whole tile and its rescale factors to the O-CTA
-                if (barrier_or<3, 256>(!ok)) {
-                    fail = true;
-                    break;
-                }
-                if (threadIdx.x == 128) {
-                    bulk_copy_to_peer(smem_u32(smem + kOffP + ps * kPSlotBytes), smem + kOffPStage + ss * kPSlotBytes,
-                                      kPTx, &bar.pfull[ps], o_rank);
-                    KDT_TC_TRACE(kEvSoftmaxSent, j);
+                // Each half of P goes to the O-CTA in its own copy once its four warps are
+                // done. A failure here is carried in `ok` to the next all-warp barrier, so
+                // the two halves never part ways.
+                const bool half_fail = half == 0 ? barrier_or<3, 128>(!ok) : barrier_or<4, 128>(!ok);
+                if (half_fail) {
+                    ok = false;
+                } else if (lane == 0 && (warp & 3) == 0) {
+                    const uint32_t off = (uint32_t)half * (kPBytes / 2);
+                    bulk_copy_to_peer(smem_u32(smem + kOffP + ps * kPSlotBytes + off), smem + kOffPStage + ss * kPSlotBytes + off,
+                                      half == 0 ? kPBytes / 2 : kPBytes / 2 + kRows * 4, &bar.pfull[ps], o_rank);
+                    if (half == 0) KDT_TC_TRACE(kEvSoftmaxSent, j);
                 }
             }
             // The O pair's MMA commits (pempty) and the O-CTA's watcher (sfree) arrive
