@@ -201,6 +201,27 @@ __device__ __forceinline__ void tma_load_4d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// Pair loads into OTHER CTAs: the tile lands at this CTA-relative offset in every CTA
+// of `mask` (cluster ranks), and the bytes complete on the barrier at shared::cluster
+// address `bar_cl` (map it to the destination pair's even CTA).
+__device__ __forceinline__ void tma_load_3d_pair_mc(void *dst, const CUtensorMap *map, uint32_t bar_cl, int32_t x,
+                                                    int32_t y, int32_t z, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cl), "r"(x), "r"(y), "r"(z), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair_mc(void *dst, const CUtensorMap *map, uint32_t bar_cl, int32_t x,
+                                                    int32_t y, int32_t z, int32_t w, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cl), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask)
+        : "memory");
+}
+
 // ----------------------------------------------------------------------- DSMEM --
 
 __device__ __forceinline__ uint32_t map_to_rank(const void *local, uint32_t rank) {

@@ -77,6 +77,8 @@ enum TraceEvent {
     kEvVIssue,           // O producer: value chunk u requested
     kEvVFull,            // O MMA thread: value chunk u landed in both CTAs
     kEvKEmpty,           // S producer: the pair's MMAs finished reading key chunk u
+    kEvKIssued,          // S MMA thread: the MMAs of key chunk u are issued
+    kEvRFull,            // S MMA thread: rope chunk of block j landed
     kNumTraceEvents
 };
 
@@ -90,7 +92,7 @@ constexpr int kVSub = kKeys * 128;                // O-CTA value sub-tile [128 k
 // Tiles travel as 32 KB requests from 4-D views of the cache (few, large requests:
 // the copy engine's cost is per request).
 constexpr int kKSlotBytes = 4 * kKSub;            // S latent ring slot: 64 keys x 256 latent dims
-constexpr int kNK = 4;                            // S-CTA latent key ring slots (128 KB, two blocks)
+constexpr int kNK = 3;                            // S-CTA latent key ring slots (96 KB, 1.5 blocks)
 constexpr int kNR = 4;                            // S-CTA rope key ring slots of kKSub (32 KB, four blocks)
 constexpr int kQpeBytes = kRows * 128;            // Q_pe tile of one S-CTA: 16 KB
 constexpr int kPBytes = kRows * kKeys * 2;        // P tile of one CTA: 32 KB (two 128B-swizzled halves)
@@ -98,7 +100,7 @@ constexpr int kPBytes = kRows * kKeys * 2;        // P tile of one CTA: 32 KB (t
 // per block carries both.
 constexpr int kPSlotBytes = kPBytes + 1024;       // 32 KB P + alpha[128] (+ pad to 1 KB alignment)
 constexpr uint32_t kPTx = kPBytes + kRows * 4;    // bytes copied into a P slot per block
-constexpr int kNS = 1;                            // S-CTA staging slots (free once the copy landed)
+constexpr int kNS = 2;                            // S-CTA staging slots (free once the copy landed)
 constexpr int kNP = 3;                            // O-CTA P slots (free once P.V of the block ran)
 constexpr int kVSlotBytes = 2 * kVSub;            // O ring slot: 128 keys x 128 latent dims
 constexpr int kNV = 3;                            // O-CTA value ring slots (96 KB)
@@ -111,7 +113,7 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr int kOffQpe = 0;                                  // S: Q_pe tile 16 KB
 constexpr int kOffKRing = kOffQpe + kQpeBytes;              // S: 4 x 32 KB
 constexpr int kOffRRing = kOffKRing + kNK * kKSlotBytes;   // S: 4 x 8 KB rope keys
-constexpr int kOffPStage = kOffRRing + kNR * kKSub;         // S: 33 KB staging of P + alpha
+constexpr int kOffPStage = kOffRRing + kNR * kKSub;         // S: 2 x 33 KB staging of P + alpha
 constexpr int kOffRowMax = kOffPStage + kNS * kPSlotBytes;  // S: [2 blocks][2 halves][128] partial maxima
 constexpr int kOffLSum = kOffRowMax + 2 * 2 * kRows * 4;    // S: [128] partial row sums
 constexpr int kOffP = 0;                                    // O: 3 x 33 KB P + alpha
@@ -180,7 +182,7 @@ __device__ __forceinline__ bool aborted(const Barriers &bar) {
 // the completion also arrives on the drain barrier of the other CTAs in `mask`.
 __device__ __forceinline__ void drain_mmas(Barriers &bar, uint16_t mask) {
     mma_commit_pair(&bar.drain, mask);
-    mbar_wait_cluster(&bar.drain, 0, kWaitLimit);
+    mbar_wait(&bar.drain, 0, kWaitLimit);
 }
 
 // Order this thread's DSMEM stores (generic proxy) before a later release-arrive
@@ -195,6 +197,17 @@ __device__ __forceinline__ void set_abort(Barriers &bar, int32_t *err, int code)
     if (err) atomicCAS(err, 0, code);
 }
 
+// Waits come in two scopes. Hand-offs that publish no memory of their own (TMA and MMA
+// completions, "done reading" signals) wait with the default CTA-scope acquire, which
+// is much cheaper on the MMA threads' critical path; hand-offs that publish a remote
+// store (flags, commands, statistics) wait with cluster-scope acquire.
+__device__ __forceinline__ bool wait_or_abort(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err, int code) {
+    if (*reinterpret_cast<volatile int *>(&bar.abort_flag)) return false;
+    if (mbar_wait(b, parity, kWaitLimit)) return true;
+    set_abort(bar, err, code);
+    return false;
+}
+
 __device__ __forceinline__ bool wait_cluster_or_abort(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err,
                                                       int code) {
     if (*reinterpret_cast<volatile int *>(&bar.abort_flag)) return false;
@@ -206,6 +219,10 @@ __device__ __forceinline__ bool wait_cluster_or_abort(Barriers &bar, uint64_t *b
 // Warp-uniform waits: every lane polls, and the warp proceeds only if all lanes saw
 // the phase complete, so warp-collective tcgen05 loads/stores after a wait are never
 // reached by part of a warp.
+__device__ __forceinline__ bool warp_wait(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err, int code) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, b, parity, err, code));
+}
+
 __device__ __forceinline__ bool warp_wait_cluster(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err,
                                                   int code) {
     return __all_sync(0xffffffffu, wait_cluster_or_abort(bar, b, parity, err, code));
@@ -251,7 +268,7 @@ __device__ __forceinline__ void ring_drain(uint64_t *empty, const RingPos &r) {
             s = kSlots - 1;
             ph ^= 1;
         }
-        mbar_wait_cluster(&empty[s], ph, kWaitLimit);
+        mbar_wait(&empty[s], ph, kWaitLimit);
     }
 }
 
@@ -305,7 +322,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     const bool leader = kpair == 0;               // issues the pair's MMAs
     const uint32_t lead_rank = rank & ~1u;
     const uint32_t o_rank = 2u + (uint32_t)kpair;  // the O-CTA an S-CTA feeds
-    constexpr uint16_t kMaskS = 0x3, kMaskO = 0xC;
+    constexpr uint16_t kMaskS = 0x3, kMaskO = 0xC, kMaskAll = 0xF;
 
     // ---- unit -> (b, two row tiles, key range) -------------------------------------
     // Uniform mode: unit = (pair of row tiles, split) with num_splits key ranges. Tail
@@ -363,7 +380,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bar.rescaled, 2);
         mbar_init(&bar.stats_full, 4);
         mbar_init(&bar.sync_bar, 1);
-        mbar_init(&bar.drain, 1);
+        // S leader: one drain commit per MMA issuer that runs (one block: only warp 1)
+        mbar_init(&bar.drain, (s_role && nb > 1) ? 2 : 1);
         bar.cmd = 0;
         bar.abort_flag = 0;
         fence_mbar_init();
@@ -388,82 +406,86 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             // ------- TMA producer: Q_pe once, then this CTA's half of each key chunk -------
             if (elect_one() && nb > 0) {
-                tma_prefetch_desc(&map_ks);
-                tma_prefetch_desc(&map_kpe);
                 if (leader) mbar_arrive_expect_tx(&bar.qpe_full, 2 * kQpeBytes);
                 tma_load_2d_pair(qpe_tile, &map_qpe, map_to_rank(&bar.qpe_full, lead_rank), 0,
                                  (int)((int64_t)b * p.rows_seq + r0));
+                // The key chunks are loaded by the O-CTAs (their copy engines carry less than
+                // this one, which sends P); the leader only arms the pair's barriers: a slot's
+                // next use is armed once the pair's MMAs have released it.
                 RingPos kr, rr;
-                bool going = true;
+                bool going = leader;
                 for (int j = 0; j < nb && going && !aborted(bar); ++j) {
-                    const int key0 = key_base + (kb0 + j) * kKeys + kpair * kHalfKeys;   // this CTA's 64 keys
-                    for (int c = 0; c < 2 && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
-                        // the pair's MMAs have read the slot's previous contents
+                    for (int c = 0; c < 2 && going; ++c) {
                         if (kr.n >= kNK &&
-                            !(going = wait_cluster_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -2)))
+                            !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -2)))
                             break;
                         if (kr.n >= kNK) KDT_TC_TRACE(kEvKEmpty, kr.n - kNK);
-                        if (leader) mbar_arrive_expect_tx(&bar.kfull[kr.slot], 2 * kKSlotBytes);
-                        tma_load_4d_pair(kring + kr.slot * kKSlotBytes, &map_ks, map_to_rank(&bar.kfull[kr.slot], lead_rank),
-                                         0, key0, 4 * c, b);
-                        KDT_TC_TRACE(kEvKIssue, kr.n);
+                        mbar_arrive_expect_tx(&bar.kfull[kr.slot], 2 * kKSlotBytes);
                         ring_advance<kNK>(kr);
                     }
                     if (!going) break;
                     if (rr.n >= kNR &&
-                        !(going = wait_cluster_or_abort(bar, &bar.rempty[rr.slot], rr.phase ^ 1, p.err, -2)))
+                        !(going = wait_or_abort(bar, &bar.rempty[rr.slot], rr.phase ^ 1, p.err, -2)))
                         break;
-                    if (leader) mbar_arrive_expect_tx(&bar.rfull[rr.slot], 2 * kKSub);
-                    tma_load_3d_pair(rring + rr.slot * kKSub, &map_kpe, map_to_rank(&bar.rfull[rr.slot], lead_rank), 0,
-                                     key0, b);
+                    mbar_arrive_expect_tx(&bar.rfull[rr.slot], 2 * kKSub);
                     ring_advance<kNR>(rr);
                 }
-                // drain: the MMA commits for the last uses of every slot mean this CTA's
-                // copies have landed and been read; none may be in flight at exit
+                // drain (both S-CTAs): the MMA commits for the last uses of every slot mean
+                // the copies into this CTA have landed and been read
+                if (!leader) {
+                    kr.n = rr.n = 0;
+                    for (int u = 0; u < 2 * nb; ++u) ring_advance<kNK>(kr);
+                    for (int u = 0; u < nb; ++u) ring_advance<kNR>(rr);
+                }
                 ring_drain<kNK>(bar.kempty, kr);
                 ring_drain<kNR>(bar.rempty, rr);
             }
-        } else if (warp == 1) {
-            // ---------------- MMA issuer (leader): S = Q K^T for 256 rows -----------------
-            if (leader && elect_one() && nb > 0) {
+        } else if (warp == 1 || warp == 2) {
+            // ---------------- MMA issuers (leader): S = Q K^T for 256 rows -----------------
+            // Two issuing threads, warp 1 for even blocks and warp 2 for odd ones: the tensor
+            // queue is shallow, so while one thread waits on a barrier or commits, the other's
+            // MMAs keep the pipe busy. A ring slot may serve both threads in turn; its uses
+            // still complete in order, because a use's copy is only issued after the slot's
+            // previous use was released, and the score buffers follow block parity.
+            const int par = warp - 1;
+            if (leader && elect_one() && nb > par) {
                 const uint32_t idesc = idesc_bf16_f32(2 * kRows, kKeys, 0, 0);
-                bool ok = wait_cluster_or_abort(bar, &bar.q_ready, 0, p.err, -3) &&
-                          wait_cluster_or_abort(bar, &bar.qpe_full, 0, p.err, -3);
+                bool ok = wait_or_abort(bar, &bar.q_ready, 0, p.err, -3) &&
+                          wait_or_abort(bar, &bar.qpe_full, 0, p.err, -3);
                 tc_fence_after();
-                RingPos kr, rr;
-                for (int j = 0; j < nb && ok; ++j) {
+                for (int j = par; j < nb && ok; j += 2) {
                     const int buf = j & 1;
-                    if (j >= 2 && !(ok = wait_cluster_or_abort(bar, &bar.sempty[buf], ((j >> 1) - 1) & 1, p.err, -4)))
+                    if (j >= 2 && !(ok = wait_or_abort(bar, &bar.sempty[buf], ((j >> 1) - 1) & 1, p.err, -4)))
                         break;
                     tc_fence_after();
                     KDT_TC_TRACE(kEvSMmaStart, j);
                     const uint32_t d = tmem_s0 + buf * kKeys;
                     for (int c = 0; c < 2; ++c) {
-                        if (!(ok = wait_cluster_or_abort(bar, &bar.kfull[kr.slot], kr.phase, p.err, -5))) break;
+                        const int u = 2 * j + c;                    // latent chunk use
+                        const int slot = u % kNK;
+                        if (!(ok = wait_or_abort(bar, &bar.kfull[slot], (uint32_t)(u / kNK) & 1, p.err, -5))) break;
                         tc_fence_after();
-                        KDT_TC_TRACE(kEvKFull, kr.n);
-                        const uint32_t kaddr = smem_u32(kring + kr.slot * kKSlotBytes);
+                        KDT_TC_TRACE(kEvKFull, u);
+                        const uint32_t kaddr = smem_u32(kring + slot * kKSlotBytes);
                         for (int t = 0; t < 4; ++t)                // sub-tile t: dims 256c + 64t .. +64
                             for (int kk = 0; kk < 4; ++kk) {
                                 const uint64_t bdesc = sdesc_sw128(kaddr + t * kKSub + kk * 32, 16, 1024);
                                 mma_ts_pair(d, tmem_q + 128 * c + 32 * t + 8 * kk, bdesc, idesc,
                                             (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
                             }
-                        mma_commit_pair(&bar.kempty[kr.slot], kMaskS);   // slot free in both S-CTAs
-                        ring_advance<kNK>(kr);
+                        KDT_TC_TRACE(kEvKIssued, u);
+                        mma_commit_pair(&bar.kempty[slot], kMaskAll);   // slot free: S-CTAs and their loaders
                     }
                     if (!ok) break;
-                    if (!(ok = wait_cluster_or_abort(bar, &bar.rfull[rr.slot], rr.phase, p.err, -5))) break;
+                    const int rslot = j % kNR;
+                    if (!(ok = wait_or_abort(bar, &bar.rfull[rslot], (uint32_t)(j / kNR) & 1, p.err, -5))) break;
                     tc_fence_after();
-                    {
-                        const uint32_t raddr = smem_u32(rring + rr.slot * kKSub);
-                        for (int kk = 0; kk < 4; ++kk)             // rope dims
-                            mma_ss_pair(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
-                                        sdesc_sw128(raddr + kk * 32, 16, 1024), idesc, 1u);
-                        mma_commit_pair(&bar.rempty[rr.slot], kMaskS);
-                        ring_advance<kNR>(rr);
-                    }
-                    if (!ok) break;
+                    KDT_TC_TRACE(kEvRFull, j);
+                    const uint32_t raddr = smem_u32(rring + rslot * kKSub);
+                    for (int kk = 0; kk < 4; ++kk)                 // rope dims
+                        mma_ss_pair(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
+                                    sdesc_sw128(raddr + kk * 32, 16, 1024), idesc, 1u);
+                    mma_commit_pair(&bar.rempty[rslot], kMaskAll);
                     mma_commit_pair(&bar.sfull[buf], kMaskS);
                     KDT_TC_TRACE(kEvSMmaIssued, j);
                 }
@@ -507,7 +529,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 const int buf = j & 1;
                 const int ss = j % kNS;                            // staging slot here
                 const int ps = j % kNP;                            // P slot in the O-CTA
-                ok = ok && warp_wait_cluster(bar, &bar.sfull[buf], (j >> 1) & 1, p.err, -6);
+                ok = ok && warp_wait(bar, &bar.sfull[buf], (j >> 1) & 1, p.err, -6);
                 float x[64];
                 float mx = -INFINITY;
                 if (ok) {
@@ -558,8 +580,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 // the O-CTA's P slot is free once P.V of block j - kNP has run; this CTA's
                 // staging slot once the copy of block j - kNS has landed
-                ok = (j < kNP || warp_wait_cluster(bar, &bar.pempty[ps], ((j / kNP) - 1) & 1, p.err, -7)) &&
-                     (j < kNS || warp_wait_cluster(bar, &bar.sfree[ss], ((j / kNS) - 1) & 1, p.err, -19));
+                ok = (j < kNP || warp_wait(bar, &bar.pempty[ps], ((j / kNP) - 1) & 1, p.err, -7)) &&
+                     (j < kNS || warp_wait(bar, &bar.sfree[ss], ((j / kNS) - 1) & 1, p.err, -19));
                 if (ok) {
                     if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxSlot, j);
                     unsigned char *slot_base = smem + kOffPStage + ss * kPSlotBytes;
@@ -603,11 +625,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             if (!fail && ok && warp == 4) {
                 for (int ps = 0; ps < kNP && ps < nb; ++ps) {
                     const int j_last = ps + ((nb - 1 - ps) / kNP) * kNP;
-                    ok = warp_wait_cluster(bar, &bar.pempty[ps], (j_last / kNP) & 1, p.err, -18) && ok;
+                    ok = warp_wait(bar, &bar.pempty[ps], (j_last / kNP) & 1, p.err, -18) && ok;
                 }
                 for (int ss = 0; ss < kNS && ss < nb; ++ss) {
                     const int j_last = ss + ((nb - 1 - ss) / kNS) * kNS;
-                    ok = warp_wait_cluster(bar, &bar.sfree[ss], (j_last / kNS) & 1, p.err, -20) && ok;
+                    ok = warp_wait(bar, &bar.sfree[ss], (j_last / kNS) & 1, p.err, -20) && ok;
                 }
             }
             // final statistics for the O-CTA epilogue: (m, l) with l summed over both halves
@@ -637,7 +659,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < nb && !aborted(bar); ++j) {
                     const int key0 = key_base + (kb0 + j) * kKeys;
                     for (int h = 0; h < 2; ++h) {
-                        if (issued >= kNV && !wait_cluster_or_abort(bar, &bar.vempty[slot], phase ^ 1, p.err, -8))
+                        if (issued >= kNV && !wait_or_abort(bar, &bar.vempty[slot], phase ^ 1, p.err, -8))
                             break;
                         if (leader) mbar_arrive_expect_tx(&bar.vfull[slot], 2 * kVSlotBytes);
                         // latent dims [256h + 128k, +128): two sub-tiles in one request
@@ -677,7 +699,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                         // let every P.V issued so far finish, then hand O to the CTAs whose
                         // rows need the rescale (the others count as done at once)
                         mma_commit_pair(&bar.sync_bar, 0x4);
-                        if (!(ok = wait_cluster_or_abort(bar, &bar.sync_bar, sync_phase, p.err, -15))) break;
+                        if (!(ok = wait_or_abort(bar, &bar.sync_bar, sync_phase, p.err, -15))) break;
                         sync_phase ^= 1;
                         tc_fence_before();
                         for (uint32_t k = 0; k < 2; ++k) {
@@ -694,7 +716,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t paddr = smem_u32(pbase + ps * kPSlotBytes);
                     for (int h = 0; h < 2; ++h) {
-                        if (!(ok = wait_cluster_or_abort(bar, &bar.vfull[slot], phase, p.err, -10))) break;
+                        if (!(ok = wait_or_abort(bar, &bar.vfull[slot], phase, p.err, -10))) break;
                         tc_fence_after();
                         KDT_TC_TRACE(kEvVFull, 2 * j + h);
                         const uint32_t vaddr = smem_u32(vbase + slot * kVSlotBytes);
@@ -717,12 +739,47 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 drain_mmas(bar, kMaskO);
             }
+        } else if (warp == 3) {
+            // ------- key loader: S-CTA k's half of each key block, into its shared memory -------
+            // Multicast to that one CTA with pair semantics: the bytes complete on the S
+            // leader's barrier, which counts both S-CTAs' halves.
+            if (elect_one() && nb > 0) {
+                tma_prefetch_desc(&map_ks);
+                tma_prefetch_desc(&map_kpe);
+                const uint16_t dst_mask = (uint16_t)(1u << kpair);
+                unsigned char *kring = smem + kOffKRing;     // same offsets as in the S-CTA
+                unsigned char *rring = smem + kOffRRing;
+                RingPos kr, rr;
+                bool going = true;
+                for (int j = 0; j < nb && going && !aborted(bar); ++j) {
+                    const int key0 = key_base + (kb0 + j) * kKeys + kpair * kHalfKeys;   // S-CTA k's 64 keys
+                    for (int c = 0; c < 2 && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
+                        if (kr.n >= kNK &&
+                            !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -21)))
+                            break;
+                        tma_load_4d_pair_mc(kring + kr.slot * kKSlotBytes, &map_ks, map_to_rank(&bar.kfull[kr.slot], 0),
+                                            0, key0, 4 * c, b, dst_mask);
+                        KDT_TC_TRACE(kEvKIssue, kr.n);
+                        ring_advance<kNK>(kr);
+                    }
+                    if (!going) break;
+                    if (rr.n >= kNR &&
+                        !(going = wait_or_abort(bar, &bar.rempty[rr.slot], rr.phase ^ 1, p.err, -21)))
+                        break;
+                    tma_load_3d_pair_mc(rring + rr.slot * kKSub, &map_kpe, map_to_rank(&bar.rfull[rr.slot], 0), 0, key0,
+                                        b, dst_mask);
+                    ring_advance<kNR>(rr);
+                }
+                // every copy this CTA issued has landed and been read before it may exit
+                ring_drain<kNK>(bar.kempty, kr);
+                ring_drain<kNR>(bar.rempty, rr);
+            }
         } else if (warp == 2) {
             // ---------------- P watcher: P of each block landed, and does O need a rescale? --
             for (int j = 0; j < nb; ++j) {
                 const int ps = j % kNP;
                 if (lane == 0) mbar_arrive_expect_tx(&bar.pfull[ps], kPTx);   // P + alpha of block j
-                if (!warp_wait_cluster(bar, &bar.pfull[ps], (j / kNP) & 1, p.err, -11)) break;
+                if (!warp_wait(bar, &bar.pfull[ps], (j / kNP) & 1, p.err, -11)) break;
                 if (lane == 0) KDT_TC_TRACE(kEvCorrIn, j);
                 const float4 a4 = reinterpret_cast<const float4 *>(pbase + ps * kPSlotBytes + kPBytes)[lane];
                 const bool need =
@@ -787,7 +844,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < kDc; c += 4) *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (lrow) *lrow = -INFINITY;
                 }
-            } else if (ok && warp_wait_cluster(bar, &bar.drain, 0, p.err, -13) &&
+            } else if (ok && warp_wait(bar, &bar.drain, 0, p.err, -13) &&
                        warp_wait_cluster(bar, &bar.stats_full, 0, p.err, -14)) {
                 tc_fence_after();
                 const float2 st = stats_s[row];
