@@ -79,6 +79,8 @@ enum TraceEvent {
     kEvKEmpty,           // S producer: the pair's MMAs finished reading key chunk u
     kEvKIssued,          // S MMA thread: the MMAs of key chunk u are issued
     kEvRFull,            // S MMA thread: rope chunk of block j landed
+    kEvSoftmaxMax,       // softmax warp 4: row maxima of both halves agreed
+    kEvSoftmaxStaged,    // softmax warp 4: its rows of P staged
     kNumTraceEvents
 };
 
@@ -139,9 +141,10 @@ struct Barriers {
     uint64_t q_ready;              // leader: both CTAs' Q_nope stored in TMEM (16 arrivals)
     uint64_t pempty[kNP];          // each S-CTA: O-CTA P slot free again (O pair's MMA commit)
     uint64_t sfree[kNS];           // each S-CTA: the copy out of a staging slot has landed
+    uint64_t staged[kNS][2];       // each S-CTA: the four warps of a half have staged their rows
     // O pair
     uint64_t pfull[kNP];           // each O-CTA: P + alpha of a block landed from its S-CTA
-    uint64_t pready[2][kNP];       // leader: P slot filled in O-CTA k, its rescale flag written
+    uint64_t pready[kNP];          // leader: P slot filled in both O-CTAs, their rescale flags written
     uint64_t vfull[kNV];           // leader: both halves of a value chunk landed
     uint64_t vempty[kNV];          // each O-CTA: its half of the chunk was read
     // Rare rescale hand-over: the MMA thread lets its P.V drain, then sends `go` with a
@@ -299,6 +302,30 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Visibility of keys [key0, key0 + 64) for one query row as a 64-bit mask (bit c: key
+// key0 + c): keys before 0 are padding (hidden), prefix keys [0, P) are visible, and tree
+// key P + t is visible when bit t of the row's packed ancestor bits is set. The tree part
+// of a window spans at most three 32-bit words.
+__device__ __forceinline__ uint64_t vis_mask64(const uint32_t *visrow, int W, int key0, int P) {
+    uint64_t m = 0;
+    const int p_lo = max(key0, 0) - key0, p_hi = min(key0 + 64, P) - key0;   // prefix keys, as c
+    if (p_hi > p_lo) {
+        const uint64_t below_hi = p_hi >= 64 ? ~0ull : ((1ull << p_hi) - 1);
+        m |= below_hi & ~((1ull << p_lo) - 1);
+    }
+    const int c_lo = max(key0, P) - key0;                                      // first tree key, as c
+    if (c_lo < 64) {
+        const int ta = key0 + c_lo - P;                                        // its tree index (>= 0)
+        const int wi = ta >> 5, sh = ta & 31;
+        const uint64_t w0 = wi < W ? __ldg(visrow + wi) : 0u;
+        const uint64_t w1 = wi + 1 < W ? __ldg(visrow + wi + 1) : 0u;
+        const uint64_t w2 = wi + 2 < W ? __ldg(visrow + wi + 2) : 0u;
+        const uint64_t bits = ((w0 | (w1 << 32)) >> sh) | (sh ? (w2 << (64 - sh)) : 0ull);   // tree bits ta..ta+63
+        m |= bits << c_lo;
+    }
+    return m;
+}
+
 // TMEM-address helpers: lane field in bits [31:16].
 __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, uint32_t col) {
     return base + ((uint32_t)(32 * (warp & 3)) << 16) + col;
@@ -370,11 +397,14 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNP; ++i) {
             mbar_init(&bar.pempty[i], 1);
             mbar_init(&bar.pfull[i], 1);
-            mbar_init(&bar.pready[0][i], 1);
-            mbar_init(&bar.pready[1][i], 1);
+            mbar_init(&bar.pready[i], 2);
             bar.need[0][i] = bar.need[1][i] = 0;
         }
-        for (int i = 0; i < kNS; ++i) mbar_init(&bar.sfree[i], 1);
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(&bar.sfree[i], 1);
+            mbar_init(&bar.staged[i][0], 4);
+            mbar_init(&bar.staged[i][1], 4);
+        }
         for (int i = 0; i < kNV; ++i) { mbar_init(&bar.vfull[i], 1); mbar_init(&bar.vempty[i], 1); }
         mbar_init(&bar.go, 1);
         mbar_init(&bar.rescaled, 2);
@@ -491,6 +521,24 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 drain_mmas(bar, 0x1);
             }
+        } else if (warp == 3) {
+            // ---------------- P copier: each half of P to the O-CTA once staged ---------------
+            if (elect_one()) {
+                for (int j = 0; j < nb; ++j) {
+                    const int ss = j % kNS, ps = j % kNP;
+                    const uint32_t par = (uint32_t)(j / kNS) & 1;
+                    bool ok = true;
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        if (!(ok = wait_or_abort(bar, &bar.staged[ss][h], par, p.err, -22))) break;
+                        const uint32_t off = (uint32_t)h * (kPBytes / 2);
+                        bulk_copy_to_peer(smem_u32(smem + kOffP + ps * kPSlotBytes + off),
+                                          smem + kOffPStage + ss * kPSlotBytes + off,
+                                          h == 0 ? kPBytes / 2 : kPBytes / 2 + kRows * 4, &bar.pfull[ps], o_rank);
+                        if (h == 0) KDT_TC_TRACE(kEvSoftmaxSent, j);
+                    }
+                    if (!ok) break;
+                }
+            }
         } else if (warp >= 4) {
             // ---------------- Q_nope -> TMEM, then softmax ---------------------------------
             // Eight warps: warp w serves the 32 rows of TMEM lane quadrant (w % 4); warps 4-7
@@ -552,16 +600,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxLoaded, j);
                     const int key0 = key_base + (kb0 + j) * kKeys + 64 * half;
                     if (key0 < 0 || key0 + 64 > P) {               // leading pad or tree keys: mask
+                        const uint64_t vm = vis_mask64(visrow, p.W, key0, P);
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const int key = key0 + c;
-                            bool vis = key >= 0;
-                            if (vis && key >= P) {
-                                const int t = key - P;
-                                vis = (__ldg(visrow + (t >> 5)) >> (t & 31)) & 1u;
-                            }
-                            if (!vis) x[c] = -INFINITY;
-                        }
+                        for (int c = 0; c < 64; ++c)
+                            if (!((vm >> c) & 1ull)) x[c] = -INFINITY;
                     }
 #pragma unroll
                     for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
@@ -571,6 +613,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     fail = true;
                     break;
                 }
+                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxMax, j);
                 mx = fmaxf(mx, rowmax_s[(buf * 2 + (half ^ 1)) * kRows + row]);
                 float alpha = 1.f;
                 if (mx > m_run + kRescaleThreshold || (m_run == -INFINITY && mx > -INFINITY)) {
@@ -605,18 +648,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     // the rescale factors follow the second half of P, which carries them
                     if (half == 1) reinterpret_cast<float *>(slot_base + kPBytes)[row] = alpha;
                     fence_proxy_async_smem();                      // staging visible to the copy engine
-                }
-                // Each half of P goes to the O-CTA in its own copy once its four warps are
-                // done. A failure here is carried in `ok` to the next all-warp barrier, so
-                // the two halves never part ways.
-                const bool half_fail = half == 0 ? barrier_or<3, 128>(!ok) : barrier_or<4, 128>(!ok);
-                if (half_fail) {
-                    ok = false;
-                } else if (lane == 0 && (warp & 3) == 0) {
-                    const uint32_t off = (uint32_t)half * (kPBytes / 2);
-                    bulk_copy_to_peer(smem_u32(smem + kOffP + ps * kPSlotBytes + off), smem + kOffPStage + ss * kPSlotBytes + off,
-                                      half == 0 ? kPBytes / 2 : kPBytes / 2 + kRows * 4, &bar.pfull[ps], o_rank);
-                    if (half == 0) KDT_TC_TRACE(kEvSoftmaxSent, j);
+                    __syncwarp();
+                    // hand the rows to the copy thread without waiting for the other warps
+                    if (lane == 0) mbar_arrive(&bar.staged[ss][half]);
+                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxStaged, j);
                 }
             }
             // The O pair's MMA commits (pempty) and the O-CTA's watcher (sfree) arrive
@@ -689,9 +724,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < nb && ok; ++j) {
                     const int ps = j % kNP;
                     const uint32_t par = (uint32_t)(j / kNP) & 1;
-                    if (!(ok = wait_cluster_or_abort(bar, &bar.pready[0][ps], par, p.err, -9) &&
-                               wait_cluster_or_abort(bar, &bar.pready[1][ps], par, p.err, -9)))
-                        break;
+                    if (!(ok = wait_cluster_or_abort(bar, &bar.pready[ps], par, p.err, -9))) break;
                     KDT_TC_TRACE(kEvOMmaStart, j);
                     const uint32_t n0 = *reinterpret_cast<volatile uint32_t *>(&bar.need[0][ps]);
                     const uint32_t n1 = *reinterpret_cast<volatile uint32_t *>(&bar.need[1][ps]);
@@ -787,7 +820,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_remote_cta(&bar.sfree[j % kNS], (uint32_t)kpair);   // its staging slot is reusable
                     st_cluster_u32(map_to_rank(&bar.need[kpair][ps], lead_rank), need ? 1u : 0u);
-                    mbar_arrive_remote(&bar.pready[kpair][ps], lead_rank);          // release: flag first
+                    mbar_arrive_remote(&bar.pready[ps], lead_rank);                 // release: flag first
                 }
                 __syncwarp();
             }
