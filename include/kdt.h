@@ -181,8 +181,9 @@ kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const flo
  * device array of KDT_NOALLOC_SCRATCH_BYTES inside libkdt.so, present on every GPU
  * that loads the library until the process exits. Nothing is allocated: no
  * cudaMalloc, no cudaFree, no allocating library routine.
- *  - Size limit: if the call needs more scratch than KDT_NOALLOC_SCRATCH_BYTES, an
- *    automatic split count (num_splits == 0) is lowered until the partials fit;
+ *  - Size limit: 64 MiB, enough for the bf16 tensor-core path's partial states on
+ *    any GPU it supports. If the call needs more scratch, an SIMT call's automatic
+ *    split count (num_splits == 0) is lowered until the partials fit;
  *    if the call still does not fit, or an explicit num_splits does not fit, it
  *    returns KDT_ERR_WORKSPACE and launches nothing.
  *  - Set-up: the first call made on a device (with that device current) looks up
@@ -194,7 +195,7 @@ kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const flo
  *    other host threads) race on the array: order them on one stream or serialise
  *    them.
  */
-#define KDT_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+#define KDT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
 kdt_status kdt_verify_attn_noalloc(const kdt_verify_args *a, cudaStream_t stream);
 

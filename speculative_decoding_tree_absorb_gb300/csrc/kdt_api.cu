@@ -30,7 +30,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Plan {
     int impl = KDT_IMPL_SIMT;
     int splits = 1;
-    int tail_units = 0, tail_splits = 0;   // tensor path: split only the last partial wave
+    int tc_clusters = 1;                   // tensor path: resident clusters the work is split across
     int blocks_per_split = 1;
     int ctas = 0;
     int launches = 0;
@@ -83,39 +83,33 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     const int unit_tiles = (int)((rows_seq + unit_rows - 1) / unit_rows);   // work units per sequence
     const int nblk = (a->max_kv_len + unit_keys - 1) / unit_keys;
     const int64_t base = (int64_t)unit_tiles * a->B;
-    // concurrent units: one CTA per SM for SIMT, the resident 4-CTA clusters for tcgen05
-    const int64_t slots = tc ? tc_max_clusters() : sm_count();
-    int splits;
-    if (a->num_splits > 0) {
-        splits = a->num_splits;
-    } else if (tc && base >= slots) {
-        // Enough units for full waves: keep whole units, and cut only the units of the
-        // last partial wave into key ranges so that wave occupies every cluster.
-        splits = 1;
-        const int64_t rem = base % slots;
-        if (rem > 0) {
-            int ts = (int)(slots / rem);
-            if (ts > kMaxSplits) ts = kMaxSplits;
-            const int cap = nblk / 2 > 1 ? nblk / 2 : 1;
-            if (ts > cap) ts = cap;
-            if (ts >= 2) {
-                p.tail_units = (int)rem;
-                p.tail_splits = ts;
-            }
-        }
+    if (tc) {
+        // One cluster per resident slot, each taking an equal share of all units' key
+        // blocks (the split adapts on the device to the actual prefix lengths); caller
+        // splits do not apply.
+        p.tc_clusters = tc_max_clusters();
+        p.splits = 1;
+        p.blocks_per_split = nblk;
+        p.ctas = 4 * p.tc_clusters;
     } else {
-        // fill about two waves, with at least 4 key blocks per split
-        const int64_t want = (2LL * slots + base - 1) / base;
-        splits = (int)(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
-        const int cap = nblk / 4 > 1 ? nblk / 4 : 1;
-        if (splits > cap) splits = cap;
+        // SIMT: one CTA per SM at a time; fill about two waves, with at least 4 key blocks
+        // per split, unless the caller fixed the splits
+        const int64_t slots = sm_count();
+        int splits;
+        if (a->num_splits > 0) {
+            splits = a->num_splits;
+        } else {
+            const int64_t want = (2LL * slots + base - 1) / base;
+            splits = (int)(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
+            const int cap = nblk / 4 > 1 ? nblk / 4 : 1;
+            if (splits > cap) splits = cap;
+        }
+        if (splits > kMaxSplits) splits = kMaxSplits;
+        if (splits > nblk) splits = nblk;
+        p.blocks_per_split = (nblk + splits - 1) / splits;
+        p.splits = (nblk + p.blocks_per_split - 1) / p.blocks_per_split;
+        p.ctas = (int)(base * p.splits);
     }
-    if (splits > kMaxSplits) splits = kMaxSplits;
-    if (splits > nblk) splits = nblk;
-    p.blocks_per_split = (nblk + splits - 1) / splits;
-    p.splits = (nblk + p.blocks_per_split - 1) / p.blocks_per_split;
-    p.ctas = (int)((p.tail_splits > 0 ? base - p.tail_units + (int64_t)p.tail_units * p.tail_splits
-                                      : base * p.splits) * (tc ? 4 : 1));
     size_t off = 0;
     if (a->parent) {
         const int W = (a->T + 31) / 32;
@@ -123,9 +117,11 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         p.vis_bytes = (size_t)a->B * a->T * W * sizeof(uint32_t);
         off = align_up(off + p.vis_bytes);
     }
-    if (p.splits > 1 || p.tail_splits > 0) {
-        const int64_t prow = p.tail_splits > 0 ? (int64_t)p.tail_units * unit_rows : rows_total;
-        const int ns = p.tail_splits > 0 ? p.tail_splits : p.splits;
+    const bool tc_pieces = tc && p.tc_clusters > 1;
+    if (p.splits > 1 || tc_pieces) {
+        // SIMT: [splits][rows_total]; tensor path: [2 * clusters][256] piece states
+        const int64_t prow = tc_pieces ? (int64_t)2 * p.tc_clusters * unit_rows : rows_total;
+        const int ns = tc_pieces ? 1 : p.splits;
         p.po_off = off;
         p.po_bytes = (size_t)ns * prow * kDc * sizeof(float);
         off = align_up(off + p.po_bytes);
@@ -134,7 +130,7 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         off = align_up(off + p.pl_bytes);
     }
     p.ws_bytes = off;
-    p.launches = (a->parent ? 1 : 0) + 1 + ((p.splits > 1 || p.tail_splits > 0) ? 1 : 0);
+    p.launches = (a->parent ? 1 : 0) + 1 + ((p.splits > 1 || tc_pieces) ? 1 : 0);
     *pl = p;
     return KDT_OK;
 }
@@ -212,12 +208,11 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     vp.num_splits = p.splits;
     vp.blocks_per_split = p.blocks_per_split;
     vp.rows_total = (int64_t)a->B * a->T * a->H;
-    const bool partials = p.splits > 1 || p.tail_splits > 0;
+    const bool partials = p.splits > 1 || (p.impl == KDT_IMPL_TCGEN05 && p.tc_clusters > 1);
     vp.part_o = partials ? reinterpret_cast<float *>(ws + p.po_off) : nullptr;
     vp.part_lse = partials ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
     vp.err = a->err;
-    vp.tail_units = p.tail_units;
-    vp.tail_splits = p.tail_splits;
+    vp.tc_clusters = p.tc_clusters;
 
     if (a->parent) {
         uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);
@@ -230,13 +225,7 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     const cudaError_t e = p.impl == KDT_IMPL_TCGEN05 ? launch_verify_tc(vp, stream)
                                                      : launch_verify_simt(vp, a->dtype, stream);
     if (e != cudaSuccess) return KDT_ERR_CUDA;
-    if (p.tail_splits > 0) {
-        const int rows_seq = a->T * a->H;
-        const int unit_tiles = (rows_seq + tc_rows_per_unit() - 1) / tc_rows_per_unit();
-        if (launch_merge_tail(vp.part_o, vp.part_lse, p.tail_splits, p.tail_units, a->B * unit_tiles - p.tail_units,
-                              unit_tiles, tc_rows_per_unit(), rows_seq, a->out, a->lse, stream) != cudaSuccess)
-            return KDT_ERR_CUDA;
-    } else if (p.splits > 1) {
+    if (p.impl == KDT_IMPL_SIMT && p.splits > 1) {
         if (launch_merge_splits(vp.part_o, vp.part_lse, p.splits, vp.rows_total, a->out, a->lse, stream) !=
             cudaSuccess)
             return KDT_ERR_CUDA;

@@ -29,12 +29,9 @@ struct VerifyParams {
     int blocks_per_split;      // key blocks (of the kernel's block size) per split
     int64_t rows_total;        // B*T*H
     int32_t *err;              // caller error word (tensor-core path: negative = pipeline timeout)
-    // Tail splitting (tensor-core path, num_splits == 1): the last `tail_units` work
-    // units (tc_rows_per_unit() rows each) are each cut into `tail_splits` key ranges
-    // whose partial states land in part_o/part_lse compactly
-    // ([tail_splits][tail_units * rows per unit][512]) and are merged by
-    // launch_merge_tail. tail_splits == 0: off.
-    int tail_units, tail_splits;
+    // Tensor-core path: the resident clusters the work is split across; part_o/part_lse
+    // then hold [2 * tc_clusters][256] partial states (unused when tc_clusters == 1).
+    int tc_clusters;
 };
 
 // K0: parent -> packed ancestor bits.
@@ -46,22 +43,17 @@ constexpr int kSimtRows = 64;
 constexpr int kSimtKeys = 64;
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, cudaStream_t s);
 
-// K1: tcgen05 verify (bf16 inputs), 4-CTA clusters (two CTA pairs) of two 128-row
-// tiles x 128-key blocks.
+// K1: tcgen05 verify (bf16 inputs): one 4-CTA cluster (two CTA pairs) per resident slot,
+// each taking an equal share of the (256-row unit, 128-key block) work; launch_verify_tc
+// also merges the units cut by the split.
 int tc_rows_per_unit();   // query rows of one work unit (256)
-int tc_max_clusters();    // 4-CTA clusters resident at once on the current device
+int tc_max_clusters();    // 4-CTA clusters resident at once on the current device (<= 48)
 int tc_keys_per_block();
 cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t s);
 
 // K2: merge the split partials into out/lse.
 cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int num_splits, int64_t rows,
                                 float *out, float *lse, cudaStream_t s);
-
-// K2 for tail splitting: merge compact partials of the last `tail_tiles` units of
-// `rows_per_tile` rows (unit index = b * row_tiles + unit within the sequence).
-cudaError_t launch_merge_tail(const float *part_o, const float *part_lse, int splits, int tail_tiles,
-                              int first_tile, int row_tiles, int rows_per_tile, int rows_seq, float *out, float *lse,
-                              cudaStream_t s);
 
 // Public two-state merge.
 cudaError_t launch_merge_two(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,

@@ -22,7 +22,7 @@
 
 namespace {
 
-// Fixed scratch: KDT_NOALLOC_SCRATCH_BYTES (16 MiB) per device, 256-byte aligned.
+// Fixed scratch: KDT_NOALLOC_SCRATCH_BYTES (64 MiB) per device, 256-byte aligned.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDT_NOALLOC_SCRATCH_BYTES];
 
 // Device address of g_noalloc_scratch, looked up once per device (on the first call

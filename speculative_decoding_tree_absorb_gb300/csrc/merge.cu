@@ -76,25 +76,6 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_splits_kernel(const f
     merge_row(part_o, part_lse, S, rows, row, out + row * kDc, lse ? lse + row : nullptr);
 }
 
-// Same merge for compact tail partials: compact row k belongs to row tile
-// first_tile + k / rows_per_tile, i.e. sequence b = tile / row_tiles and local row
-// (tile % row_tiles) * rows_per_tile + k % rows_per_tile; rows past the sequence end
-// are skipped.
-__global__ void __launch_bounds__(kWarpsPerCta * 32) merge_tail_kernel(const float *__restrict__ part_o,
-                                                                       const float *__restrict__ part_lse, int S,
-                                                                       int64_t nrows, int first_tile, int row_tiles,
-                                                                       int rows_per_tile, int rows_seq,
-                                                                       float *__restrict__ out,
-                                                                       float *__restrict__ lse) {
-    const int64_t k = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    if (k >= nrows) return;
-    const int tile = first_tile + (int)(k / rows_per_tile);
-    const int local = (tile % row_tiles) * rows_per_tile + (int)(k % rows_per_tile);
-    if (local >= rows_seq) return;
-    const int64_t row = (int64_t)(tile / row_tiles) * rows_seq + local;
-    merge_row(part_o, part_lse, S, nrows, k, out + row * kDc, lse ? lse + row : nullptr);
-}
-
 __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_two_kernel(const float *o_a, const float *lse_a,
                                                                       const float *o_b, const float *lse_b,
                                                                       int64_t rows, int D, float *o,
@@ -128,17 +109,6 @@ cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int 
     if (rows == 0) return cudaSuccess;
     const int64_t ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
     merge_splits_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, s>>>(part_o, part_lse, num_splits, rows, out, lse);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_merge_tail(const float *part_o, const float *part_lse, int splits, int tail_tiles,
-                              int first_tile, int row_tiles, int rows_per_tile, int rows_seq, float *out, float *lse,
-                              cudaStream_t s) {
-    const int64_t nrows = (int64_t)tail_tiles * rows_per_tile;
-    if (nrows == 0) return cudaSuccess;
-    const int64_t ctas = (nrows + kWarpsPerCta - 1) / kWarpsPerCta;
-    merge_tail_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, s>>>(part_o, part_lse, splits, nrows, first_tile, row_tiles,
-                                                                  rows_per_tile, rows_seq, out, lse);
     return cudaGetLastError();
 }
 

@@ -120,9 +120,9 @@ constexpr int kOffRowMax = kOffPStage + kNS * kPSlotBytes;  // S: [2 blocks][2 h
 constexpr int kOffLSum = kOffRowMax + 2 * 2 * kRows * 4;    // S: [128] partial row sums
 constexpr int kOffP = 0;                                    // O: 3 x 33 KB P + alpha
 constexpr int kOffV = kOffP + kNP * kPSlotBytes;            // O: 3 x 32 KB
-constexpr int kOffStats = kOffV + kNV * kVSlotBytes;        // O: [128] x (m, l)
+constexpr int kOffStats = kOffV + kNV * kVSlotBytes;        // O: [2 items][128] x (m, l)
 constexpr int kSEnd = kOffLSum + kRows * 4;
-constexpr int kOEnd = kOffStats + kRows * 8;
+constexpr int kOEnd = kOffStats + 2 * kRows * 8;
 constexpr int kTileBytes = kSEnd > kOEnd ? kSEnd : kOEnd;
 constexpr int kSmemBytes = kTileBytes + 1024;               // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -137,7 +137,8 @@ struct Barriers {
     uint64_t rempty[kNR];          // each S-CTA: its rope chunk was read
     uint64_t sfull[2];             // each S-CTA: scores of a block are in its TMEM
     uint64_t sempty[2];            // leader: both CTAs' softmax warps have read the buffer (16 arrivals)
-    uint64_t qpe_full;             // leader: both Q_pe tiles landed
+    uint64_t qpe_full;             // leader: both Q_pe tiles of the item landed
+    uint64_t qpe_empty;            // each S-CTA: the item's last rope MMAs read its Q_pe tile
     uint64_t q_ready;              // leader: both CTAs' Q_nope stored in TMEM (16 arrivals)
     uint64_t pempty[kNP];          // each S-CTA: O-CTA P slot free again (O pair's MMA commit)
     uint64_t sfree[kNS];           // each S-CTA: the copy out of a staging slot has landed
@@ -152,11 +153,16 @@ struct Barriers {
     // rows need it, and waits for `rescaled` (one arrival per O-CTA).
     uint64_t go;                   // each O-CTA: a command is in `cmd`
     uint64_t rescaled;             // leader: rows of O rescaled (or no rescale needed) per O-CTA
-    uint64_t stats_full;           // each O-CTA: final (m, l) of its rows from its S-CTA
+    uint64_t stats_full[2];        // each O-CTA: an item's (m, l) of its rows from its S-CTA (by item parity)
+    uint64_t stats_empty[2];       // each S-CTA: the O-CTA epilogue has read that buffer
+    uint64_t o_done;               // each O-CTA: every P.V of the item has completed
+    uint64_t o_free;               // O leader: both O-CTAs' epilogues have read O (8 arrivals)
     uint64_t sync_bar;             // leader: MMA thread's own completion probe (mid-stream)
     uint64_t drain;                // completion of all MMAs of the pair before TMEM is read or freed
     uint32_t need[2][kNP];         // leader: per-CTA "some row of O needs a rescale" per P slot
     uint32_t cmd;                  // each O-CTA: correction command
+    int kseen[2];                  // S leader: latest latent chunk use each MMA issuer saw land
+    int work_u0, work_kb0, work_count;   // this cluster's work range (see the decomposition below)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -165,17 +171,90 @@ struct TcParams {
     int B, T, H, W;
     int rows_seq;          // T*H
     int row_tiles;         // ceil(rows_seq / 128)
-    int num_splits, blocks_per_split;
     int64_t rows_total;
     const __nv_bfloat16 *q_nope;
     const int32_t *prefix_len;
     const uint32_t *vis;
     float scale_log2;
-    float *out, *lse, *part_o, *part_lse;
+    float *out, *lse;
+    float *part_o, *part_lse;      // [2 * clusters][256] partial states of units cut by the work split
     int32_t *err;
-    int tail_units, tail_splits;   // tail splitting (see VerifyParams); 0 = off
     int pairs_per_seq;             // work units (two row tiles each) per sequence
 };
+
+// ---- work decomposition ----------------------------------------------------------------
+// The work is every unit's key blocks, units in order (unit = b * pairs_per_seq + pair,
+// blocks 0 .. nblk(b) - 1). Cluster c of C takes the contiguous range
+// [W c / C, W (c + 1) / C) of it, so every cluster gets the same number of blocks (+-1)
+// whatever the wave count; the ranges are derived from prefix_len on the device, the same
+// way in every CTA. A unit cut by a range boundary is processed in pieces: each piece
+// writes its normalised partial state (o, lse) into slot 2c (the cluster's first item) or
+// 2c + 1 (its last item), and a merge pass combines them.
+__device__ __forceinline__ int seq_blocks(const TcParams &p, int b) {
+    return (p.prefix_len[b] + p.T + kKeys - 1) / kKeys;
+}
+
+__device__ __forceinline__ int64_t total_blocks(const TcParams &p) {
+    int64_t w = 0;
+    for (int b = 0; b < p.B; ++b) w += (int64_t)p.pairs_per_seq * seq_blocks(p, b);
+    return w;
+}
+
+// Unit holding flattened block s, its first flattened block and its block count.
+__device__ __forceinline__ void locate_block(const TcParams &p, int64_t s, int &u, int64_t &start, int &nblk) {
+    int64_t acc = 0;
+    for (int b = 0; b < p.B; ++b) {
+        const int nb = seq_blocks(p, b);
+        const int64_t seq = (int64_t)p.pairs_per_seq * nb;
+        if (s < acc + seq) {
+            const int k = (int)((s - acc) / nb);
+            u = b * p.pairs_per_seq + k;
+            start = acc + (int64_t)k * nb;
+            nblk = nb;
+            return;
+        }
+        acc += seq;
+    }
+    u = p.B * p.pairs_per_seq;
+    start = acc;
+    nblk = 0;
+}
+
+struct Item {
+    int b, rt0;            // sequence; first of the unit's two row tiles
+    int P, nblk, key_base; // prefix length, key blocks of the unit, first key of block 0 (<= 0)
+    int kb0, nb;           // blocks [kb0, kb0 + nb) of the unit
+    bool whole;            // the unit's whole key range: write the final rows
+    int slot;              // partial-state slot otherwise
+};
+
+struct WorkIter {
+    int u, kb, left, taken;
+};
+
+__device__ __forceinline__ bool next_item(const TcParams &p, WorkIter &w, int c, Item &it) {
+    if (w.left <= 0) return false;
+    const int b = w.u / p.pairs_per_seq;
+    it.b = b;
+    it.rt0 = 2 * (w.u % p.pairs_per_seq);
+    it.P = p.prefix_len[b];
+    const int kv_len = it.P + p.T;
+    it.nblk = (kv_len + kKeys - 1) / kKeys;
+    it.key_base = kv_len - it.nblk * kKeys;
+    it.kb0 = w.kb;
+    it.nb = min(it.nblk - w.kb, w.left);
+    it.whole = it.kb0 == 0 && it.nb == it.nblk;
+    it.slot = 2 * c + (w.taken == 0 ? 0 : 1);
+    w.left -= it.nb;
+    ++w.taken;
+    if (w.kb + it.nb == it.nblk) {
+        ++w.u;
+        w.kb = 0;
+    } else {
+        w.kb += it.nb;
+    }
+    return true;
+}
 
 __device__ __forceinline__ bool aborted(const Barriers &bar) {
     return *reinterpret_cast<const volatile int *>(&bar.abort_flag) != 0;
@@ -326,6 +405,65 @@ __device__ __forceinline__ uint64_t vis_mask64(const uint32_t *visrow, int W, in
     return m;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Largest scaled score of a row's 64 raw scores (scale > 0: scale * max; else scale * min).
+__device__ __forceinline__ float scaled_max64(const float (&x)[64], float scale) {
+    float r;
+    if (scale >= 0.f) {
+        r = fmax3(x[0], x[1], x[2]);
+#pragma unroll
+        for (int c = 3; c < 63; c += 2) r = fmax3(r, x[c], x[c + 1]);
+        r = fmaxf(r, x[63]);
+    } else {
+        r = fmin3(x[0], x[1], x[2]);
+#pragma unroll
+        for (int c = 3; c < 63; c += 2) r = fmin3(r, x[c], x[c + 1]);
+        r = fminf(r, x[63]);
+    }
+    return r * scale;
+}
+
+// p = 2^(scale * x - m) for 64 keys of one row, packed to bf16 into a 128-byte
+// swizzled row of a P tile; returns the fp32 sum of the p. kScaled: x already holds
+// scale * score (hidden keys -inf) and m may be -inf (all hidden so far: p = 0).
+template <bool kScaled>
+__device__ __forceinline__ float stage_p_row(const float (&x)[64], float scale, float m, unsigned char *dst_row,
+                                             int row) {
+    float lsum = 0.f;
+    const bool live = !kScaled || m > -INFINITY;
+    const float nm = -m;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {                          // 8 chunks of 8 keys
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float e0, e1;
+            if (kScaled) {
+                e0 = live ? fast_exp2(x[u * 8 + 2 * q] + nm) : 0.f;
+                e1 = live ? fast_exp2(x[u * 8 + 2 * q + 1] + nm) : 0.f;
+            } else {
+                e0 = fast_exp2(fmaf(x[u * 8 + 2 * q], scale, nm));
+                e1 = fast_exp2(fmaf(x[u * 8 + 2 * q + 1], scale, nm));
+            }
+            lsum += e0 + e1;
+            w[q] = pack_bf16x2(e0, e1);
+        }
+        *reinterpret_cast<uint4 *>(dst_row + ((u ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return lsum;
+}
+
 // TMEM-address helpers: lane field in bits [31:16].
 __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, uint32_t col) {
     return base + ((uint32_t)(32 * (warp & 3)) << 16) + col;
@@ -351,48 +489,24 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t o_rank = 2u + (uint32_t)kpair;  // the O-CTA an S-CTA feeds
     constexpr uint16_t kMaskS = 0x3, kMaskO = 0xC, kMaskAll = 0xF;
 
-    // ---- unit -> (b, two row tiles, key range) -------------------------------------
-    // Uniform mode: unit = (pair of row tiles, split) with num_splits key ranges. Tail
-    // mode (tail_splits > 0, num_splits == 1): units before the last tail_units are
-    // whole; each of the last tail_units is cut into tail_splits key ranges so the final
-    // wave of clusters is as full as the others.
-    const int unit = blockIdx.x >> 2;
-    const int units = p.B * p.pairs_per_seq;
-    const int first_tail = units - p.tail_units;
-    int pair, split, nsplit;
-    if (p.tail_splits > 0) {
-        if (unit < first_tail) {
-            pair = unit;
-            split = 0;
-            nsplit = 1;
-        } else {
-            pair = first_tail + (unit - first_tail) / p.tail_splits;
-            split = (unit - first_tail) % p.tail_splits;
-            nsplit = p.tail_splits;
-        }
-    } else {
-        pair = unit / p.num_splits;
-        split = unit % p.num_splits;
-        nsplit = p.num_splits;
-    }
-    const int b = pair / p.pairs_per_seq;
-    const int rt = 2 * (pair % p.pairs_per_seq) + kpair;   // past the sequence when row_tiles is odd
-    const int P = p.prefix_len[b];
-    const int kv_len = P + p.T;
-    const int nblk = (kv_len + kKeys - 1) / kKeys;
-    const int bps = p.tail_splits > 0 ? (nblk + nsplit - 1) / nsplit : p.blocks_per_split;
-    const int kb0 = split * bps;
-    const int kb1 = min(nblk, kb0 + bps);
-    const int nb = kb1 > kb0 ? kb1 - kb0 : 0;       // blocks of this unit (0: empty split)
-    const int key_base = kv_len - nblk * kKeys;     // first key of block 0 (<= 0)
-    const int r0 = rt * kRows;
-
     // ---- set-up: barriers, TMEM ------------------------------------------------------
     if (threadIdx.x == 0) {
+        {
+            const int64_t W = total_blocks(p);
+            const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
+            const int64_t s0 = W * c / C, s1 = W * (c + 1) / C;
+            int u0, nblk0;
+            int64_t start0;
+            locate_block(p, s0, u0, start0, nblk0);
+            bar.work_u0 = u0;
+            bar.work_kb0 = (int)(s0 - start0);
+            bar.work_count = (int)(s1 - s0);
+        }
         for (int i = 0; i < kNK; ++i) { mbar_init(&bar.kfull[i], 1); mbar_init(&bar.kempty[i], 1); }
         for (int i = 0; i < kNR; ++i) { mbar_init(&bar.rfull[i], 1); mbar_init(&bar.rempty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&bar.sfull[i], 1); mbar_init(&bar.sempty[i], 16); }
         mbar_init(&bar.qpe_full, 1);
+        mbar_init(&bar.qpe_empty, 1);
         mbar_init(&bar.q_ready, 16);
         for (int i = 0; i < kNP; ++i) {
             mbar_init(&bar.pempty[i], 1);
@@ -408,10 +522,17 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNV; ++i) { mbar_init(&bar.vfull[i], 1); mbar_init(&bar.vempty[i], 1); }
         mbar_init(&bar.go, 1);
         mbar_init(&bar.rescaled, 2);
-        mbar_init(&bar.stats_full, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.stats_full[i], 4);
+            mbar_init(&bar.stats_empty[i], 4);
+        }
+        mbar_init(&bar.o_done, 1);
+        mbar_init(&bar.o_free, 8);
+        bar.kseen[0] = bar.kseen[1] = -1;
         mbar_init(&bar.sync_bar, 1);
-        // S leader: one drain commit per MMA issuer that runs (one block: only warp 1)
-        mbar_init(&bar.drain, (s_role && nb > 1) ? 2 : 1);
+        // one drain commit per MMA issuer that runs: two in the S leader (one for a single
+        // block), one in the O leader
+        mbar_init(&bar.drain, (s_role && bar.work_count > 1) ? 2 : 1);
         bar.cmd = 0;
         bar.abort_flag = 0;
         fence_mbar_init();
@@ -426,6 +547,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bar.tmem_base;
 
+    // Every role walks the same sequence of items of this cluster's work range; per-block
+    // state (ring slots, buffers, parities) follows the cluster-wide block counter g.
+    const WorkIter w0 = {bar.work_u0, bar.work_kb0, bar.work_count, 0};
+    const int G = bar.work_count;                  // key blocks of this cluster
+    const int cl = blockIdx.x >> 2;
+
     if (s_role) {
         // =============================== S-CTA ===============================
         unsigned char *qpe_tile = smem + kOffQpe;
@@ -434,99 +561,139 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t tmem_q = tmem;                 // Q_nope: columns [0, 256)
         const uint32_t tmem_s0 = tmem + 256;          // score buffers at 256 and 384
         if (warp == 0) {
-            // ------- TMA producer: Q_pe once, then this CTA's half of each key chunk -------
-            if (elect_one() && nb > 0) {
-                if (leader) mbar_arrive_expect_tx(&bar.qpe_full, 2 * kQpeBytes);
-                tma_load_2d_pair(qpe_tile, &map_qpe, map_to_rank(&bar.qpe_full, lead_rank), 0,
-                                 (int)((int64_t)b * p.rows_seq + r0));
-                // The key chunks are loaded by the O-CTAs (their copy engines carry less than
-                // this one, which sends P); the leader only arms the pair's barriers: a slot's
-                // next use is armed once the pair's MMAs have released it.
+            // ------- Q_pe per item; the leader arms the key rings ---------------------------
+            // The key chunks are loaded by the O-CTAs (their copy engines carry less than
+            // this one, which sends P); the leader only arms the pair's barriers: a slot's
+            // next use is armed once the pair's MMAs have released it.
+            if (elect_one() && G > 0) {
                 RingPos kr, rr;
-                bool going = leader;
-                for (int j = 0; j < nb && going && !aborted(bar); ++j) {
-                    for (int c = 0; c < 2 && going; ++c) {
-                        if (kr.n >= kNK &&
-                            !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -2)))
-                            break;
-                        if (kr.n >= kNK) KDT_TC_TRACE(kEvKEmpty, kr.n - kNK);
-                        mbar_arrive_expect_tx(&bar.kfull[kr.slot], 2 * kKSlotBytes);
-                        ring_advance<kNK>(kr);
-                    }
-                    if (!going) break;
-                    if (rr.n >= kNR &&
-                        !(going = wait_or_abort(bar, &bar.rempty[rr.slot], rr.phase ^ 1, p.err, -2)))
+                bool going = true;
+                WorkIter w = w0;
+                Item it;
+                int ii = 0;
+                while (going && !aborted(bar) && next_item(p, w, cl, it)) {
+                    // this CTA's Q_pe tile is free once the previous item's rope MMAs read it
+                    if (ii > 0 && !(going = wait_or_abort(bar, &bar.qpe_empty, (uint32_t)(ii - 1) & 1, p.err, -24)))
                         break;
-                    mbar_arrive_expect_tx(&bar.rfull[rr.slot], 2 * kKSub);
-                    ring_advance<kNR>(rr);
+                    if (leader) mbar_arrive_expect_tx(&bar.qpe_full, 2 * kQpeBytes);
+                    tma_load_2d_pair(qpe_tile, &map_qpe, map_to_rank(&bar.qpe_full, lead_rank), 0,
+                                     (int)((int64_t)it.b * p.rows_seq + (it.rt0 + kpair) * kRows));
+                    ++ii;
+                    for (int j = 0; leader && j < it.nb && going; ++j) {
+                        for (int c = 0; c < 2 && going; ++c) {
+                            if (kr.n >= kNK &&
+                                !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -2)))
+                                break;
+                            if (kr.n >= kNK) KDT_TC_TRACE(kEvKEmpty, kr.n - kNK);
+                            mbar_arrive_expect_tx(&bar.kfull[kr.slot], 2 * kKSlotBytes);
+                            ring_advance<kNK>(kr);
+                        }
+                        if (!going) break;
+                        if (rr.n >= kNR &&
+                            !(going = wait_or_abort(bar, &bar.rempty[rr.slot], rr.phase ^ 1, p.err, -2)))
+                            break;
+                        mbar_arrive_expect_tx(&bar.rfull[rr.slot], 2 * kKSub);
+                        ring_advance<kNR>(rr);
+                    }
                 }
                 // drain (both S-CTAs): the MMA commits for the last uses of every slot mean
                 // the copies into this CTA have landed and been read
                 if (!leader) {
-                    kr.n = rr.n = 0;
-                    for (int u = 0; u < 2 * nb; ++u) ring_advance<kNK>(kr);
-                    for (int u = 0; u < nb; ++u) ring_advance<kNR>(rr);
+                    kr = RingPos{};
+                    rr = RingPos{};
+                    for (int u = 0; u < 2 * G; ++u) ring_advance<kNK>(kr);
+                    for (int u = 0; u < G; ++u) ring_advance<kNR>(rr);
                 }
                 ring_drain<kNK>(bar.kempty, kr);
                 ring_drain<kNR>(bar.rempty, rr);
+                if (ii > 0) mbar_wait(&bar.qpe_empty, (uint32_t)(ii - 1) & 1, kWaitLimit);
             }
         } else if (warp == 1 || warp == 2) {
             // ---------------- MMA issuers (leader): S = Q K^T for 256 rows -----------------
             // Two issuing threads, warp 1 for even blocks and warp 2 for odd ones: the tensor
             // queue is shallow, so while one thread waits on a barrier or commits, the other's
-            // MMAs keep the pipe busy. A ring slot may serve both threads in turn; its uses
-            // still complete in order, because a use's copy is only issued after the slot's
-            // previous use was released, and the score buffers follow block parity.
+            // MMAs keep the pipe busy. Latent ring slots serve both threads in turn, so before
+            // waiting on a slot's use u a thread makes sure the other thread has already seen
+            // use u - kNK land (a parity wait can only tell adjacent phases apart). Rope slots
+            // and score buffers follow block parity.
             const int par = warp - 1;
-            if (leader && elect_one() && nb > par) {
+            if (leader && elect_one() && G > par) {
                 const uint32_t idesc = idesc_bf16_f32(2 * kRows, kKeys, 0, 0);
-                bool ok = wait_or_abort(bar, &bar.q_ready, 0, p.err, -3) &&
-                          wait_or_abort(bar, &bar.qpe_full, 0, p.err, -3);
-                tc_fence_after();
-                for (int j = par; j < nb && ok; j += 2) {
-                    const int buf = j & 1;
-                    if (j >= 2 && !(ok = wait_or_abort(bar, &bar.sempty[buf], ((j >> 1) - 1) & 1, p.err, -4)))
-                        break;
+                volatile int *seen_mine = &bar.kseen[par];
+                volatile int *seen_other = &bar.kseen[par ^ 1];
+                bool ok = true;
+                WorkIter w = w0;
+                Item it;
+                int ii = 0, g = 0;
+                while (ok && next_item(p, w, cl, it)) {
+                    // this item's rows of Q are in tensor memory and its Q_pe tile landed
+                    ok = wait_or_abort(bar, &bar.q_ready, (uint32_t)ii & 1, p.err, -3) &&
+                         wait_or_abort(bar, &bar.qpe_full, (uint32_t)ii & 1, p.err, -3);
                     tc_fence_after();
-                    KDT_TC_TRACE(kEvSMmaStart, j);
-                    const uint32_t d = tmem_s0 + buf * kKeys;
-                    for (int c = 0; c < 2; ++c) {
-                        const int u = 2 * j + c;                    // latent chunk use
-                        const int slot = u % kNK;
-                        if (!(ok = wait_or_abort(bar, &bar.kfull[slot], (uint32_t)(u / kNK) & 1, p.err, -5))) break;
+                    for (int j = 0; j < it.nb && ok; ++j, ++g) {
+                        if ((g & 1) != par) continue;
+                        const int buf = g & 1;
+                        if (g >= 2 && !(ok = wait_or_abort(bar, &bar.sempty[buf], (uint32_t)((g >> 1) - 1) & 1, p.err, -4)))
+                            break;
                         tc_fence_after();
-                        KDT_TC_TRACE(kEvKFull, u);
-                        const uint32_t kaddr = smem_u32(kring + slot * kKSlotBytes);
-                        for (int t = 0; t < 4; ++t)                // sub-tile t: dims 256c + 64t .. +64
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t bdesc = sdesc_sw128(kaddr + t * kKSub + kk * 32, 16, 1024);
-                                mma_ts_pair(d, tmem_q + 128 * c + 32 * t + 8 * kk, bdesc, idesc,
-                                            (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
+                        KDT_TC_TRACE(kEvSMmaStart, g);
+                        const uint32_t d = tmem_s0 + buf * kKeys;
+                        for (int c = 0; c < 2; ++c) {
+                            const int u = 2 * g + c;                // latent chunk use
+                            const int slot = u % kNK;
+                            // the slot's previous use belongs to the other thread when its block
+                            // has the other parity: wait until that thread has seen it land
+                            const int prev = u - kNK;
+                            if (prev >= 0 && (((prev >> 1) & 1) != par)) {
+                                const uint64_t t0 = global_ns();
+                                while (*seen_other < prev) {
+                                    if (aborted(bar) || global_ns() - t0 > kWaitLimit) {
+                                        set_abort(bar, p.err, -25);
+                                        ok = false;
+                                        break;
+                                    }
+                                }
+                                if (!ok) break;
                             }
-                        KDT_TC_TRACE(kEvKIssued, u);
-                        mma_commit_pair(&bar.kempty[slot], kMaskAll);   // slot free: S-CTAs and their loaders
+                            if (!(ok = wait_or_abort(bar, &bar.kfull[slot], (uint32_t)(u / kNK) & 1, p.err, -5))) break;
+                            *seen_mine = u;
+                            tc_fence_after();
+                            KDT_TC_TRACE(kEvKFull, u);
+                            const uint32_t kaddr = smem_u32(kring + slot * kKSlotBytes);
+                            for (int t = 0; t < 4; ++t)            // sub-tile t: dims 256c + 64t .. +64
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t bdesc = sdesc_sw128(kaddr + t * kKSub + kk * 32, 16, 1024);
+                                    mma_ts_pair(d, tmem_q + 128 * c + 32 * t + 8 * kk, bdesc, idesc,
+                                                (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
+                                }
+                            KDT_TC_TRACE(kEvKIssued, u);
+                            mma_commit_pair(&bar.kempty[slot], kMaskAll);   // slot free: S-CTAs and their loaders
+                        }
+                        if (!ok) break;
+                        const int rslot = g % kNR;
+                        if (!(ok = wait_or_abort(bar, &bar.rfull[rslot], (uint32_t)(g / kNR) & 1, p.err, -5))) break;
+                        tc_fence_after();
+                        KDT_TC_TRACE(kEvRFull, g);
+                        const uint32_t raddr = smem_u32(rring + rslot * kKSub);
+                        for (int kk = 0; kk < 4; ++kk)             // rope dims
+                            mma_ss_pair(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
+                                        sdesc_sw128(raddr + kk * 32, 16, 1024), idesc, 1u);
+                        mma_commit_pair(&bar.rempty[rslot], kMaskAll);
+                        mma_commit_pair(&bar.sfull[buf], kMaskS);
+                        // the item's last block: both CTAs' Q_pe tiles may be refilled once it ran
+                        if (j == it.nb - 1) mma_commit_pair(&bar.qpe_empty, kMaskS);
+                        KDT_TC_TRACE(kEvSMmaIssued, g);
                     }
-                    if (!ok) break;
-                    const int rslot = j % kNR;
-                    if (!(ok = wait_or_abort(bar, &bar.rfull[rslot], (uint32_t)(j / kNR) & 1, p.err, -5))) break;
-                    tc_fence_after();
-                    KDT_TC_TRACE(kEvRFull, j);
-                    const uint32_t raddr = smem_u32(rring + rslot * kKSub);
-                    for (int kk = 0; kk < 4; ++kk)                 // rope dims
-                        mma_ss_pair(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
-                                    sdesc_sw128(raddr + kk * 32, 16, 1024), idesc, 1u);
-                    mma_commit_pair(&bar.rempty[rslot], kMaskAll);
-                    mma_commit_pair(&bar.sfull[buf], kMaskS);
-                    KDT_TC_TRACE(kEvSMmaIssued, j);
+                    ++ii;
                 }
                 drain_mmas(bar, 0x1);
             }
         } else if (warp == 3) {
             // ---------------- P copier: each half of P to the O-CTA once staged ---------------
             if (elect_one()) {
-                for (int j = 0; j < nb; ++j) {
-                    const int ss = j % kNS, ps = j % kNP;
-                    const uint32_t par = (uint32_t)(j / kNS) & 1;
+                for (int g = 0; g < G; ++g) {
+                    const int ss = g % kNS, ps = g % kNP;
+                    const uint32_t par = (uint32_t)(g / kNS) & 1;
                     bool ok = true;
                     for (int h = 0; h < 2 && ok; ++h) {
                         if (!(ok = wait_or_abort(bar, &bar.staged[ss][h], par, p.err, -22))) break;
@@ -534,149 +701,160 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                         bulk_copy_to_peer(smem_u32(smem + kOffP + ps * kPSlotBytes + off),
                                           smem + kOffPStage + ss * kPSlotBytes + off,
                                           h == 0 ? kPBytes / 2 : kPBytes / 2 + kRows * 4, &bar.pfull[ps], o_rank);
-                        if (h == 0) KDT_TC_TRACE(kEvSoftmaxSent, j);
+                        if (h == 0) KDT_TC_TRACE(kEvSoftmaxSent, g);
                     }
                     if (!ok) break;
                 }
             }
         } else if (warp >= 4) {
-            // ---------------- Q_nope -> TMEM, then softmax ---------------------------------
+            // ---------------- per item: Q_nope -> TMEM, softmax, statistics -----------------
             // Eight warps: warp w serves the 32 rows of TMEM lane quadrant (w % 4); warps 4-7
             // take keys 0..63 of each block, warps 8-11 keys 64..127.
             const int half = (warp - 4) >> 2;
             const int row = 32 * (warp & 3) + lane;
-            const int R = r0 + row;
-            const bool row_valid = R < p.rows_seq;
-            {
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)b * p.rows_seq + R) * kDc);
-                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {     // 4 x 32 columns = 256 bf16
-                    uint32_t w[32];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 v = row_valid ? __ldg(src + c8 * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
-                        w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
-                    }
-                    tmem_st32(tmem_lane_addr(tmem_q, warp, c8 * 32), w);
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote_cta(&bar.q_ready, lead_rank);
-            }
-            const int qi = min(R, p.rows_seq - 1) / p.H;
-            const uint32_t *visrow = p.vis + ((int64_t)b * p.T + qi) * p.W;
             float *rowmax_s = reinterpret_cast<float *>(smem + kOffRowMax);
             float *lsum_s = reinterpret_cast<float *>(smem + kOffLSum);
-            float m_run = -INFINITY;                               // log2 units, same in both halves
-            float l_run = 0.f;                                     // this half's share of the row sum
             bool ok = true;
             bool fail = false;
-            for (int j = 0; j < nb; ++j) {
-                // No warp leaves this loop on its own: every iteration meets the other seven
-                // at the named barriers, which OR their failures.
-                const int buf = j & 1;
-                const int ss = j % kNS;                            // staging slot here
-                const int ps = j % kNP;                            // P slot in the O-CTA
-                ok = ok && warp_wait(bar, &bar.sfull[buf], (j >> 1) & 1, p.err, -6);
-                float x[64];
-                float mx = -INFINITY;
-                if (ok) {
-                    tc_fence_after();
-                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxIn, j);
-                    uint32_t r0v[32], r1v[32];
-                    const uint32_t sbase = tmem_s0 + buf * kKeys + 64 * half;
-                    tmem_ld32(tmem_lane_addr(sbase, warp, 0), r0v);
-                    tmem_ld32(tmem_lane_addr(sbase, warp, 32), r1v);
-                    tmem_wait_ld();
-                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxLd, j);
+            WorkIter w = w0;
+            Item it;
+            int ii = 0, g = 0;
+            while (!fail && next_item(p, w, cl, it)) {
+                const int R = (it.rt0 + kpair) * kRows + row;
+                const bool row_valid = R < p.rows_seq;
+                {   // Q_nope of this item's rows: tensor memory is free, every MMA of the
+                    // previous item ran before its last scores could be read
+                    const uint4 *src =
+                        reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)it.b * p.rows_seq + R) * kDc);
+                    for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {     // 4 x 32 columns = 256 bf16
+                        uint32_t wq[32];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        x[q] = __uint_as_float(r0v[q]) * p.scale_log2;
-                        x[32 + q] = __uint_as_float(r1v[q]) * p.scale_log2;
+                        for (int q = 0; q < 8; ++q) {
+                            const uint4 v = row_valid ? __ldg(src + c8 * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+                            wq[4 * q] = v.x; wq[4 * q + 1] = v.y; wq[4 * q + 2] = v.z; wq[4 * q + 3] = v.w;
+                        }
+                        tmem_st32(tmem_lane_addr(tmem_q, warp, c8 * 32), wq);
                     }
+                    tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_remote_cta(&bar.sempty[buf], lead_rank);   // buffer may be overwritten
-                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxLoaded, j);
-                    const int key0 = key_base + (kb0 + j) * kKeys + 64 * half;
-                    if (key0 < 0 || key0 + 64 > P) {               // leading pad or tree keys: mask
-                        const uint64_t vm = vis_mask64(visrow, p.W, key0, P);
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (!((vm >> c) & 1ull)) x[c] = -INFINITY;
-                    }
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
-                    rowmax_s[(buf * 2 + half) * kRows + row] = mx;
+                    if (lane == 0) mbar_arrive_remote_cta(&bar.q_ready, lead_rank);
                 }
-                if (barrier_or<2, 256>(!ok)) {
-                    fail = true;
-                    break;
-                }
-                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxMax, j);
-                mx = fmaxf(mx, rowmax_s[(buf * 2 + (half ^ 1)) * kRows + row]);
-                float alpha = 1.f;
-                if (mx > m_run + kRescaleThreshold || (m_run == -INFINITY && mx > -INFINITY)) {
-                    alpha = (m_run == -INFINITY) ? 1.f : fast_exp2(m_run - mx);
-                    m_run = mx;
-                    l_run *= alpha;
-                }
-                // the O-CTA's P slot is free once P.V of block j - kNP has run; this CTA's
-                // staging slot once the copy of block j - kNS has landed
-                ok = (j < kNP || warp_wait(bar, &bar.pempty[ps], ((j / kNP) - 1) & 1, p.err, -7)) &&
-                     (j < kNS || warp_wait(bar, &bar.sfree[ss], ((j / kNS) - 1) & 1, p.err, -19));
-                if (ok) {
-                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxSlot, j);
-                    unsigned char *slot_base = smem + kOffPStage + ss * kPSlotBytes;
-                    unsigned char *stage = slot_base + half * (kPBytes / 2);
-                    float lsum = 0.f;
-                    const bool live = m_run > -INFINITY;
+                const int qi = min(R, p.rows_seq - 1) / p.H;
+                const uint32_t *visrow = p.vis + ((int64_t)it.b * p.T + qi) * p.W;
+                float m_run = -INFINITY;                           // log2 units, same in both halves
+                float l_run = 0.f;                                 // this half's share of the row sum
+                for (int j = 0; j < it.nb; ++j, ++g) {
+                    // No warp leaves this loop on its own: every iteration meets the other seven
+                    // at the named barrier, which ORs their failures.
+                    const int buf = g & 1;
+                    const int ss = g % kNS;                        // staging slot here
+                    const int ps = g % kNP;                        // P slot in the O-CTA
+                    ok = ok && warp_wait(bar, &bar.sfull[buf], (uint32_t)(g >> 1) & 1, p.err, -6);
+                    float x[64];
+                    float mx = -INFINITY;
+                    bool masked = false;                            // block half holds hidden keys
+                    if (ok) {
+                        tc_fence_after();
+                        if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxIn, g);
+                        uint32_t r0v[32], r1v[32];
+                        const uint32_t sbase = tmem_s0 + buf * kKeys + 64 * half;
+                        tmem_ld32(tmem_lane_addr(sbase, warp, 0), r0v);
+                        tmem_ld32(tmem_lane_addr(sbase, warp, 32), r1v);
+                        tmem_wait_ld();
+                        if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxLd, g);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {                  // 8 chunks of 8 keys
-                        uint32_t w[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float e0 = live ? fast_exp2(x[u * 8 + 2 * q] - m_run) : 0.f;
-                            const float e1 = live ? fast_exp2(x[u * 8 + 2 * q + 1] - m_run) : 0.f;
-                            lsum += e0 + e1;
-                            w[q] = pack_bf16x2(e0, e1);
+                        for (int q = 0; q < 32; ++q) {             // raw scores
+                            x[q] = __uint_as_float(r0v[q]);
+                            x[32 + q] = __uint_as_float(r1v[q]);
                         }
-                        *reinterpret_cast<uint4 *>(stage + row * 128 + ((u ^ (row & 7)) << 4)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote_cta(&bar.sempty[buf], lead_rank);   // buffer may be overwritten
+                        if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxLoaded, g);
+                        const int key0 = it.key_base + (it.kb0 + j) * kKeys + 64 * half;
+                        masked = key0 < 0 || key0 + 64 > it.P;     // leading pad or tree keys
+                        if (masked) {   // scale now, hidden keys -inf (also right for scale 0)
+                            const uint64_t vm = vis_mask64(visrow, p.W, key0, it.P);
+#pragma unroll
+                            for (int c = 0; c < 64; ++c) x[c] = ((vm >> c) & 1ull) ? x[c] * p.scale_log2 : -INFINITY;
+#pragma unroll
+                            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+                        } else {        // all visible: raw scores kept, the scale goes into the exponent
+                            mx = scaled_max64(x, p.scale_log2);
+                        }
+                        rowmax_s[(buf * 2 + half) * kRows + row] = mx;
                     }
-                    l_run += lsum;
-                    // the rescale factors follow the second half of P, which carries them
-                    if (half == 1) reinterpret_cast<float *>(slot_base + kPBytes)[row] = alpha;
-                    fence_proxy_async_smem();                      // staging visible to the copy engine
-                    __syncwarp();
-                    // hand the rows to the copy thread without waiting for the other warps
-                    if (lane == 0) mbar_arrive(&bar.staged[ss][half]);
-                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxStaged, j);
+                    if (barrier_or<2, 256>(!ok)) {
+                        fail = true;
+                        break;
+                    }
+                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxMax, g);
+                    mx = fmaxf(mx, rowmax_s[(buf * 2 + (half ^ 1)) * kRows + row]);
+                    float alpha = 1.f;
+                    if (mx > m_run + kRescaleThreshold || (m_run == -INFINITY && mx > -INFINITY)) {
+                        alpha = (m_run == -INFINITY) ? 1.f : fast_exp2(m_run - mx);
+                        m_run = mx;
+                        l_run *= alpha;
+                    }
+                    // the O-CTA's P slot is free once P.V of block g - kNP has run; this CTA's
+                    // staging slot once the copy of block g - kNS has landed
+                    ok = (g < kNP || warp_wait(bar, &bar.pempty[ps], (uint32_t)((g / kNP) - 1) & 1, p.err, -7)) &&
+                         (g < kNS || warp_wait(bar, &bar.sfree[ss], (uint32_t)((g / kNS) - 1) & 1, p.err, -19));
+                    if (ok) {
+                        if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxSlot, g);
+                        unsigned char *slot_base = smem + kOffPStage + ss * kPSlotBytes;
+                        unsigned char *stage_row = slot_base + half * (kPBytes / 2) + row * 128;
+                        // an all-visible half has finite scores, so m_run is finite here
+                        l_run += masked ? stage_p_row<true>(x, p.scale_log2, m_run, stage_row, row)
+                                        : stage_p_row<false>(x, p.scale_log2, m_run, stage_row, row);
+                        // the rescale factors follow the second half of P, which carries them
+                        if (half == 1) reinterpret_cast<float *>(slot_base + kPBytes)[row] = alpha;
+                        fence_proxy_async_smem();                  // staging visible to the copy engine
+                        __syncwarp();
+                        // hand the rows to the copy thread without waiting for the other warps
+                        if (lane == 0) mbar_arrive(&bar.staged[ss][half]);
+                        if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvSoftmaxStaged, g);
+                    }
                 }
+                if (fail) break;
+                // this item's statistics for the O-CTA epilogue: (m, l), l over both halves
+                if (half == 1) lsum_s[row] = l_run;
+                fail = barrier_or<2, 256>(!ok);
+                if (fail) break;
+                const int sb = ii & 1;                            // statistics buffer of this item
+                if (half == 0) {
+                    // the O-CTA has read this buffer's previous contents (item ii - 2)
+                    ok = ii < 2 || warp_wait(bar, &bar.stats_empty[sb], (uint32_t)((ii >> 1) - 1) & 1, p.err, -26);
+                    if (ok) {
+                        const uint32_t dst = map_to_rank(smem + kOffStats + (sb * kRows + row) * 8, o_rank);
+                        st_cluster_f32(dst, m_run);
+                        st_cluster_f32(dst + 4, l_run + lsum_s[row]);
+                        publish_remote_stores();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote(&bar.stats_full[sb], o_rank);
+                    }
+                }
+                // lsum_s is rewritten at the end of the next item only after this barrier
+                fail = barrier_or<2, 256>(!ok);
+                ++ii;
             }
-            // The O pair's MMA commits (pempty) and the O-CTA's watcher (sfree) arrive
-            // here; the arrivals for the last blocks are consumed before this CTA may
-            // leave, so none can land in the shared memory of a CTA that later runs here.
+            // The O pair's MMA commits (pempty), the O-CTA's watcher (sfree) and its epilogue
+            // (stats_empty) arrive here; the arrivals still due are consumed before this CTA
+            // may leave, so none can land in the shared memory of a CTA that later runs here.
             if (!fail && ok && warp == 4) {
-                for (int ps = 0; ps < kNP && ps < nb; ++ps) {
-                    const int j_last = ps + ((nb - 1 - ps) / kNP) * kNP;
-                    ok = warp_wait(bar, &bar.pempty[ps], (j_last / kNP) & 1, p.err, -18) && ok;
+                for (int ps = 0; ps < kNP && ps < G; ++ps) {
+                    const int g_last = ps + ((G - 1 - ps) / kNP) * kNP;
+                    ok = warp_wait(bar, &bar.pempty[ps], (uint32_t)(g_last / kNP) & 1, p.err, -18) && ok;
                 }
-                for (int ss = 0; ss < kNS && ss < nb; ++ss) {
-                    const int j_last = ss + ((nb - 1 - ss) / kNS) * kNS;
-                    ok = warp_wait(bar, &bar.sfree[ss], (j_last / kNS) & 1, p.err, -20) && ok;
+                for (int ss = 0; ss < kNS && ss < G; ++ss) {
+                    const int g_last = ss + ((G - 1 - ss) / kNS) * kNS;
+                    ok = warp_wait(bar, &bar.sfree[ss], (uint32_t)(g_last / kNS) & 1, p.err, -20) && ok;
                 }
-            }
-            // final statistics for the O-CTA epilogue: (m, l) with l summed over both halves
-            if (half == 1) lsum_s[row] = l_run;
-            fail = barrier_or<2, 256>(fail || !ok) || fail;
-            if (!fail && half == 0 && nb > 0) {
-                const uint32_t dst = map_to_rank(smem + kOffStats + row * 8, o_rank);
-                st_cluster_f32(dst, m_run);
-                st_cluster_f32(dst + 4, l_run + lsum_s[row]);
-                publish_remote_stores();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(&bar.stats_full, o_rank);
+                for (int sb = 0; sb < 2 && sb < ii; ++sb) {
+                    const int i_last = sb + ((ii - 1 - sb) / 2) * 2;
+                    ok = warp_wait(bar, &bar.stats_empty[sb], (uint32_t)(i_last >> 1) & 1, p.err, -27) && ok;
+                }
             }
         }
     } else {
@@ -686,89 +864,104 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         const float2 *stats_s = reinterpret_cast<const float2 *>(smem + kOffStats);
         if (warp == 0) {
             // ------- TMA producer: this CTA's 128 of each 256 latent columns of V -------
-            if (elect_one() && nb > 0) {
+            if (elect_one() && G > 0) {
                 tma_prefetch_desc(&map_vs);
-                int slot = 0;
-                uint32_t phase = 0;
-                int issued = 0;
-                for (int j = 0; j < nb && !aborted(bar); ++j) {
-                    const int key0 = key_base + (kb0 + j) * kKeys;
-                    for (int h = 0; h < 2; ++h) {
-                        if (issued >= kNV && !wait_or_abort(bar, &bar.vempty[slot], phase ^ 1, p.err, -8))
-                            break;
-                        if (leader) mbar_arrive_expect_tx(&bar.vfull[slot], 2 * kVSlotBytes);
-                        // latent dims [256h + 128k, +128): two sub-tiles in one request
-                        tma_load_4d_pair(vbase + slot * kVSlotBytes, &map_vs, map_to_rank(&bar.vfull[slot], lead_rank),
-                                         0, key0, 4 * h + 2 * kpair, b);
-                        KDT_TC_TRACE(kEvVIssue, issued);
-                        ++issued;
-                        if (++slot == kNV) { slot = 0; phase ^= 1; }
+                RingPos vr;
+                bool going = true;
+                WorkIter w = w0;
+                Item it;
+                while (going && !aborted(bar) && next_item(p, w, cl, it)) {
+                    for (int j = 0; j < it.nb && going; ++j) {
+                        const int key0 = it.key_base + (it.kb0 + j) * kKeys;
+                        for (int h = 0; h < 2; ++h) {
+                            if (vr.n >= kNV &&
+                                !(going = wait_or_abort(bar, &bar.vempty[vr.slot], vr.phase ^ 1, p.err, -8)))
+                                break;
+                            if (leader) mbar_arrive_expect_tx(&bar.vfull[vr.slot], 2 * kVSlotBytes);
+                            // latent dims [256h + 128k, +128): two sub-tiles in one request
+                            tma_load_4d_pair(vbase + vr.slot * kVSlotBytes, &map_vs,
+                                             map_to_rank(&bar.vfull[vr.slot], lead_rank), 0, key0, 4 * h + 2 * kpair, it.b);
+                            KDT_TC_TRACE(kEvVIssue, vr.n);
+                            ring_advance<kNV>(vr);
+                        }
                     }
                 }
-                const int outstanding = issued < kNV ? issued : kNV;
-                int s = slot;
-                uint32_t ph = phase;
-                for (int k = 0; k < outstanding; ++k) {
-                    if (--s < 0) { s = kNV - 1; ph ^= 1; }
-                    mbar_wait_cluster(&bar.vempty[s], ph, kWaitLimit);
-                }
+                ring_drain<kNV>(bar.vempty, vr);
             }
         } else if (warp == 1) {
             // ---------------- MMA issuer (leader): O += P V for 256 rows --------------------
-            if (leader && elect_one() && nb > 0) {
+            if (leader && elect_one() && G > 0) {
                 const uint32_t idesc = idesc_bf16_f32(2 * kRows, 256, 0, 1);
-                int slot = 0;
-                uint32_t phase = 0;
+                RingPos vr;
                 uint32_t rs_phase = 0, sync_phase = 0;
                 bool ok = true;
-                for (int j = 0; j < nb && ok; ++j) {
-                    const int ps = j % kNP;
-                    const uint32_t par = (uint32_t)(j / kNP) & 1;
-                    if (!(ok = wait_cluster_or_abort(bar, &bar.pready[ps], par, p.err, -9))) break;
-                    KDT_TC_TRACE(kEvOMmaStart, j);
-                    const uint32_t n0 = *reinterpret_cast<volatile uint32_t *>(&bar.need[0][ps]);
-                    const uint32_t n1 = *reinterpret_cast<volatile uint32_t *>(&bar.need[1][ps]);
-                    if (n0 | n1) {
-                        // let every P.V issued so far finish, then hand O to the CTAs whose
-                        // rows need the rescale (the others count as done at once)
-                        mma_commit_pair(&bar.sync_bar, 0x4);
-                        if (!(ok = wait_or_abort(bar, &bar.sync_bar, sync_phase, p.err, -15))) break;
-                        sync_phase ^= 1;
-                        tc_fence_before();
-                        for (uint32_t k = 0; k < 2; ++k) {
-                            if (k == 0 ? n0 : n1) {
-                                st_cluster_u32(map_to_rank(&bar.cmd, 2 + k), (uint32_t)ps);
-                                mbar_arrive_remote(&bar.go, 2 + k);      // release: command first
-                            } else {
-                                mbar_arrive(&bar.rescaled);
+                WorkIter w = w0;
+                Item it;
+                int ii = 0, g = 0;
+                while (ok && next_item(p, w, cl, it)) {
+                    // the previous item's epilogue has read O out of tensor memory
+                    if (ii > 0 && !(ok = wait_cluster_or_abort(bar, &bar.o_free, (uint32_t)(ii - 1) & 1, p.err, -28)))
+                        break;
+                    for (int j = 0; j < it.nb && ok; ++j, ++g) {
+                        const int ps = g % kNP;
+                        if (!(ok = wait_cluster_or_abort(bar, &bar.pready[ps], (uint32_t)(g / kNP) & 1, p.err, -9))) break;
+                        KDT_TC_TRACE(kEvOMmaStart, g);
+                        const uint32_t n0 = *reinterpret_cast<volatile uint32_t *>(&bar.need[0][ps]);
+                        const uint32_t n1 = *reinterpret_cast<volatile uint32_t *>(&bar.need[1][ps]);
+                        if (n0 | n1) {
+                            // let every P.V issued so far finish, then hand O to the CTAs whose
+                            // rows need the rescale (the others count as done at once)
+                            mma_commit_pair(&bar.sync_bar, 0x4);
+                            if (!(ok = wait_or_abort(bar, &bar.sync_bar, sync_phase, p.err, -15))) break;
+                            sync_phase ^= 1;
+                            tc_fence_before();
+                            for (uint32_t k = 0; k < 2; ++k) {
+                                if (k == 0 ? n0 : n1) {
+                                    st_cluster_u32(map_to_rank(&bar.cmd, 2 + k), (uint32_t)ps);
+                                    mbar_arrive_remote(&bar.go, 2 + k);      // release: command first
+                                } else {
+                                    mbar_arrive(&bar.rescaled);
+                                }
                             }
+                            if (!(ok = wait_cluster_or_abort(bar, &bar.rescaled, rs_phase, p.err, -16))) break;
+                            rs_phase ^= 1;
                         }
-                        if (!(ok = wait_cluster_or_abort(bar, &bar.rescaled, rs_phase, p.err, -16))) break;
-                        rs_phase ^= 1;
-                    }
-                    tc_fence_after();
-                    const uint32_t paddr = smem_u32(pbase + ps * kPSlotBytes);
-                    for (int h = 0; h < 2; ++h) {
-                        if (!(ok = wait_or_abort(bar, &bar.vfull[slot], phase, p.err, -10))) break;
                         tc_fence_after();
-                        KDT_TC_TRACE(kEvVFull, 2 * j + h);
-                        const uint32_t vaddr = smem_u32(vbase + slot * kVSlotBytes);
-                        for (int kk = 0; kk < kKeys / 16; ++kk) {
-                            const uint64_t adesc = sdesc_sw128(paddr + (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bdesc = sdesc_sw128(vaddr + kk * 2048, kVSub, 1024);
-                            mma_ss_pair(tmem + 256 * h, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                        const uint32_t paddr = smem_u32(pbase + ps * kPSlotBytes);
+                        for (int h = 0; h < 2; ++h) {
+                            if (!(ok = wait_or_abort(bar, &bar.vfull[vr.slot], vr.phase, p.err, -10))) break;
+                            tc_fence_after();
+                            KDT_TC_TRACE(kEvVFull, vr.n);
+                            const uint32_t vaddr = smem_u32(vbase + vr.slot * kVSlotBytes);
+                            for (int kk = 0; kk < kKeys / 16; ++kk) {
+                                const uint64_t adesc =
+                                    sdesc_sw128(paddr + (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32, 16, 1024);
+                                const uint64_t bdesc = sdesc_sw128(vaddr + kk * 2048, kVSub, 1024);
+                                // the item's first block starts O afresh
+                                mma_ss_pair(tmem + 256 * h, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            mma_commit_pair(&bar.vempty[vr.slot], kMaskO);   // slot free in both O-CTAs
+                            ring_advance<kNV>(vr);
                         }
-                        mma_commit_pair(&bar.vempty[slot], kMaskO);   // slot free in both O-CTAs
-                        if (++slot == kNV) { slot = 0; phase ^= 1; }
+                        if (!ok) break;
+                        KDT_TC_TRACE(kEvOMmaIssued, g);
+                        // P slot ps of both O-CTAs is free again: tell both S-CTAs
+                        mma_commit_pair(&bar.pempty[ps], kMaskS);
                     }
                     if (!ok) break;
-                    KDT_TC_TRACE(kEvOMmaIssued, j);
-                    // P slot ps of both O-CTAs is free again: tell both S-CTAs
-                    mma_commit_pair(&bar.pempty[ps], kMaskS);
+                    // the item's P.V is complete once this arrives; the epilogues then read O
+                    mma_commit_pair(&bar.o_done, kMaskO);
+                    for (uint32_t k = 0; k < 2; ++k) {   // end the correction loop of this item
+                        st_cluster_u32(map_to_rank(&bar.cmd, 2 + k), kCmdDone);
+                        mbar_arrive_remote(&bar.go, 2 + k);
+                    }
+                    ++ii;
                 }
-                for (uint32_t k = 0; k < 2; ++k) {       // release the correction warps
-                    st_cluster_u32(map_to_rank(&bar.cmd, 2 + k), kCmdDone);
-                    mbar_arrive_remote(&bar.go, 2 + k);
+                if (!ok) {   // release the correction warps of an item left unfinished
+                    for (uint32_t k = 0; k < 2; ++k) {
+                        st_cluster_u32(map_to_rank(&bar.cmd, 2 + k), kCmdDone);
+                        mbar_arrive_remote(&bar.go, 2 + k);
+                    }
                 }
                 drain_mmas(bar, kMaskO);
             }
@@ -776,7 +969,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             // ------- key loader: S-CTA k's half of each key block, into its shared memory -------
             // Multicast to that one CTA with pair semantics: the bytes complete on the S
             // leader's barrier, which counts both S-CTAs' halves.
-            if (elect_one() && nb > 0) {
+            if (elect_one() && G > 0) {
                 tma_prefetch_desc(&map_ks);
                 tma_prefetch_desc(&map_kpe);
                 const uint16_t dst_mask = (uint16_t)(1u << kpair);
@@ -784,24 +977,28 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 unsigned char *rring = smem + kOffRRing;
                 RingPos kr, rr;
                 bool going = true;
-                for (int j = 0; j < nb && going && !aborted(bar); ++j) {
-                    const int key0 = key_base + (kb0 + j) * kKeys + kpair * kHalfKeys;   // S-CTA k's 64 keys
-                    for (int c = 0; c < 2 && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
-                        if (kr.n >= kNK &&
-                            !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -21)))
+                WorkIter w = w0;
+                Item it;
+                while (going && !aborted(bar) && next_item(p, w, cl, it)) {
+                    for (int j = 0; j < it.nb && going; ++j) {
+                        const int key0 = it.key_base + (it.kb0 + j) * kKeys + kpair * kHalfKeys;   // S-CTA k's 64 keys
+                        for (int c = 0; c < 2 && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
+                            if (kr.n >= kNK &&
+                                !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -21)))
+                                break;
+                            tma_load_4d_pair_mc(kring + kr.slot * kKSlotBytes, &map_ks,
+                                                map_to_rank(&bar.kfull[kr.slot], 0), 0, key0, 4 * c, it.b, dst_mask);
+                            KDT_TC_TRACE(kEvKIssue, kr.n);
+                            ring_advance<kNK>(kr);
+                        }
+                        if (!going) break;
+                        if (rr.n >= kNR &&
+                            !(going = wait_or_abort(bar, &bar.rempty[rr.slot], rr.phase ^ 1, p.err, -21)))
                             break;
-                        tma_load_4d_pair_mc(kring + kr.slot * kKSlotBytes, &map_ks, map_to_rank(&bar.kfull[kr.slot], 0),
-                                            0, key0, 4 * c, b, dst_mask);
-                        KDT_TC_TRACE(kEvKIssue, kr.n);
-                        ring_advance<kNK>(kr);
+                        tma_load_3d_pair_mc(rring + rr.slot * kKSub, &map_kpe, map_to_rank(&bar.rfull[rr.slot], 0), 0,
+                                            key0, it.b, dst_mask);
+                        ring_advance<kNR>(rr);
                     }
-                    if (!going) break;
-                    if (rr.n >= kNR &&
-                        !(going = wait_or_abort(bar, &bar.rempty[rr.slot], rr.phase ^ 1, p.err, -21)))
-                        break;
-                    tma_load_3d_pair_mc(rring + rr.slot * kKSub, &map_kpe, map_to_rank(&bar.rfull[rr.slot], 0), 0, key0,
-                                        b, dst_mask);
-                    ring_advance<kNR>(rr);
                 }
                 // every copy this CTA issued has landed and been read before it may exit
                 ring_drain<kNK>(bar.kempty, kr);
@@ -809,78 +1006,85 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             }
         } else if (warp == 2) {
             // ---------------- P watcher: P of each block landed, and does O need a rescale? --
-            for (int j = 0; j < nb; ++j) {
-                const int ps = j % kNP;
-                if (lane == 0) mbar_arrive_expect_tx(&bar.pfull[ps], kPTx);   // P + alpha of block j
-                if (!warp_wait(bar, &bar.pfull[ps], (j / kNP) & 1, p.err, -11)) break;
-                if (lane == 0) KDT_TC_TRACE(kEvCorrIn, j);
+            for (int g = 0; g < G; ++g) {
+                const int ps = g % kNP;
+                if (lane == 0) mbar_arrive_expect_tx(&bar.pfull[ps], kPTx);   // P + alpha of block g
+                if (!warp_wait(bar, &bar.pfull[ps], (uint32_t)(g / kNP) & 1, p.err, -11)) break;
+                if (lane == 0) KDT_TC_TRACE(kEvCorrIn, g);
+                // factors other than 1 only occur once a row has a running maximum, i.e. not in
+                // the first block of an item, whose P.V starts O afresh
                 const float4 a4 = reinterpret_cast<const float4 *>(pbase + ps * kPSlotBytes + kPBytes)[lane];
-                const bool need =
-                    j > 0 && __any_sync(0xffffffffu, a4.x != 1.f || a4.y != 1.f || a4.z != 1.f || a4.w != 1.f);
+                const bool need = __any_sync(0xffffffffu, a4.x != 1.f || a4.y != 1.f || a4.z != 1.f || a4.w != 1.f);
                 if (lane == 0) {
-                    mbar_arrive_remote_cta(&bar.sfree[j % kNS], (uint32_t)kpair);   // its staging slot is reusable
+                    mbar_arrive_remote_cta(&bar.sfree[g % kNS], (uint32_t)kpair);   // its staging slot is reusable
                     st_cluster_u32(map_to_rank(&bar.need[kpair][ps], lead_rank), need ? 1u : 0u);
                     mbar_arrive_remote(&bar.pready[ps], lead_rank);                 // release: flag first
                 }
                 __syncwarp();
             }
         } else if (warp >= 4 && warp < 8) {
-            // ---------------- correction (rare rescale) and epilogue -------------------------
+            // ---------------- correction (rare rescale) and epilogue, per item ----------------
             // Warps 4-7 only (one per TMEM lane quadrant): named barrier 1 counts 128 threads.
-            // They sleep on `go` until the MMA thread hands O over for a rescale or ends.
+            // They sleep on `go` until the MMA thread hands O over for a rescale or ends the item.
             const int row = 32 * (warp & 3) + lane;
             bool ok = true;
-            for (uint32_t e = 0; nb > 0; ++e) {
-                ok = warp_wait_cluster(bar, &bar.go, e & 1, p.err, -12);
+            uint32_t e = 0;                                     // `go` events so far
+            WorkIter w = w0;
+            Item it;
+            int ii = 0;
+            while (ok && next_item(p, w, cl, it)) {
+                for (;; ++e) {
+                    ok = warp_wait_cluster(bar, &bar.go, e & 1, p.err, -12);
+                    if (barrier_or<1, 128>(!ok)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t cmd = *reinterpret_cast<volatile uint32_t *>(&bar.cmd);
+                    if (cmd == kCmdDone) {
+                        ++e;
+                        break;
+                    }
+                    // every P.V before the block in P slot `cmd` has completed: rescale this
+                    // CTA's rows of O by that block's factors (rows that need none multiply by 1)
+                    const float a = reinterpret_cast<const float *>(pbase + (cmd % kNP) * kPSlotBytes + kPBytes)[row];
+                    tc_fence_after();
+                    for (int c = 0; c < 512 / 32; ++c) {
+                        uint32_t r[32];
+                        const uint32_t addr = tmem_lane_addr(tmem, warp, c * 32);
+                        tmem_ld32(addr, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * a);
+                        tmem_st32(addr, r);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    barrier_or<1, 128>(false);             // all four warps' stores done
+                    if (threadIdx.x == 128) mbar_arrive_remote(&bar.rescaled, lead_rank);
+                }
+                if (!ok) break;
+                // epilogue of the item: o = O / l, lse = ln2 (m + log2 l); whole units write the
+                // final rows, pieces their partial state
+                const int sb = ii & 1;
+                ok = warp_wait(bar, &bar.o_done, (uint32_t)ii & 1, p.err, -13) &&
+                     warp_wait_cluster(bar, &bar.stats_full[sb], (uint32_t)(ii >> 1) & 1, p.err, -14);
                 if (barrier_or<1, 128>(!ok)) {
                     ok = false;
                     break;
                 }
-                const uint32_t cmd = *reinterpret_cast<volatile uint32_t *>(&bar.cmd);
-                if (cmd == kCmdDone) break;
-                // every P.V before the block in P slot `cmd` has completed: rescale this CTA's
-                // rows of O by that block's factors (rows that need none multiply by 1)
-                const float a = reinterpret_cast<const float *>(pbase + (cmd % kNP) * kPSlotBytes + kPBytes)[row];
                 tc_fence_after();
-                for (int c = 0; c < 512 / 32; ++c) {
-                    uint32_t r[32];
-                    const uint32_t addr = tmem_lane_addr(tmem, warp, c * 32);
-                    tmem_ld32(addr, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * a);
-                    tmem_st32(addr, r);
+                const int R = (it.rt0 + kpair) * kRows + row;
+                const int64_t grow = (int64_t)it.b * p.rows_seq + R;
+                float *orow, *lrow;
+                if (it.whole) {
+                    orow = p.out + grow * kDc;
+                    lrow = p.lse ? p.lse + grow : nullptr;
+                } else {
+                    const int64_t k = (int64_t)it.slot * (2 * kRows) + kpair * kRows + row;
+                    orow = p.part_o + k * kDc;
+                    lrow = p.part_lse + k;
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                barrier_or<1, 128>(false);                 // all four warps' stores done
-                if (threadIdx.x == 128) mbar_arrive_remote(&bar.rescaled, lead_rank);
-            }
-            // epilogue
-            const int R = r0 + row;
-            const int64_t grow = (int64_t)b * p.rows_seq + R;
-            float *orow, *lrow;
-            if (nsplit == 1) {
-                orow = p.out + grow * kDc;
-                lrow = p.lse ? p.lse + grow : nullptr;
-            } else if (p.tail_splits > 0) {                  // compact tail partials
-                const int64_t nrows = (int64_t)p.tail_units * 2 * kRows;
-                const int64_t k = ((int64_t)(pair - first_tail) * 2 + kpair) * kRows + row;
-                orow = p.part_o + ((int64_t)split * nrows + k) * kDc;
-                lrow = p.part_lse + (int64_t)split * nrows + k;
-            } else {
-                orow = p.part_o + ((int64_t)split * p.rows_total + grow) * kDc;
-                lrow = p.part_lse + (int64_t)split * p.rows_total + grow;
-            }
-            if (nb == 0) {
-                if (R < p.rows_seq) {
-                    for (int c = 0; c < kDc; c += 4) *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (lrow) *lrow = -INFINITY;
-                }
-            } else if (ok && warp_wait(bar, &bar.drain, 0, p.err, -13) &&
-                       warp_wait_cluster(bar, &bar.stats_full, 0, p.err, -14)) {
-                tc_fence_after();
-                const float2 st = stats_s[row];
+                const float2 st = stats_s[sb * kRows + row];
                 const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
                 for (int c = 0; c < 512 / 32; ++c) {
                     uint32_t r[32];
@@ -895,6 +1099,14 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (R < p.rows_seq && lrow) *lrow = st.y > 0.f ? 0.6931471805599453f * (st.x + log2f(st.y)) : -INFINITY;
+                // O may be overwritten and the statistics buffer refilled
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_remote(&bar.o_free, lead_rank);
+                    mbar_arrive_remote_cta(&bar.stats_empty[sb], (uint32_t)kpair);
+                }
+                ++ii;
             }
         }
     }
@@ -914,6 +1126,74 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();            // no CTA leaves while another may still touch its shared memory
     tc_fence_after();
     if (warp == 0) tmem_dealloc_pair(tmem, 512);
+}
+
+// Combines the pieces of each unit cut by a boundary of the work split. Block (c - 1, y)
+// serves boundary c when c is the first boundary inside its unit, rows 8y .. 8y + 7 of
+// the unit's 256 (one warp per row, 16 columns per lane): the normalised partial states
+// (o_k, lse_k) of the pieces combine exactly as the log-sum-exp merge of disjoint key
+// sets, processed one piece after another.
+constexpr int kMaxClusters = 48;   // partial states then fit the no-alloc scratch
+
+__global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int C) {
+    __shared__ int s_valid, s_n, s_b, s_rt0;
+    __shared__ int s_slot[kMaxClusters + 1];
+    const int c = blockIdx.x + 1;
+    if (threadIdx.x == 0) {
+        s_valid = 0;
+        const int64_t W = total_blocks(p);
+        const int64_t sc = W * c / C, sprev = W * (c - 1) / C;
+        int u, nblk;
+        int64_t start;
+        locate_block(p, sc, u, start, nblk);
+        if (nblk > 0 && sc > start && sprev <= start) {
+            int n = 0;
+            s_slot[n++] = 2 * (c - 1) + (sprev == start ? 0 : 1);   // the piece that starts the unit
+            for (int cc = c; cc < C && n <= kMaxClusters; ++cc) {
+                const int64_t lo = W * cc / C, hi = W * (cc + 1) / C;
+                if (lo >= start + nblk) break;
+                if (hi > lo) s_slot[n++] = 2 * cc;                 // pieces that start a cluster's range
+            }
+            s_n = n;
+            s_b = u / p.pairs_per_seq;
+            s_rt0 = 2 * (u % p.pairs_per_seq);
+            s_valid = 1;
+        }
+    }
+    __syncthreads();
+    if (!s_valid) return;
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.y * 8 + (threadIdx.x >> 5);        // row of the unit, 0..255
+    const int R = s_rt0 * kRows + r;
+    if (R >= p.rows_seq) return;
+    float M = -INFINITY, sum = 0.f;
+    float4 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < s_n; ++k) {
+        const int64_t idx = (int64_t)s_slot[k] * (2 * kRows) + r;
+        const float l = p.part_lse[idx];
+        if (l == -INFINITY) continue;                          // no visible key in this piece
+        const float Mn = fmaxf(M, l);
+        const float so = M == -INFINITY ? 0.f : expf(M - Mn);
+        const float wk = expf(l - Mn);
+        const float4 *src = reinterpret_cast<const float4 *>(p.part_o + idx * kDc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v = __ldg(src + lane + 32 * q);
+            acc[q] = make_float4(acc[q].x * so + wk * v.x, acc[q].y * so + wk * v.y, acc[q].z * so + wk * v.z,
+                                 acc[q].w * so + wk * v.w);
+        }
+        sum = sum * so + wk;
+        M = Mn;
+    }
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    const int64_t grow = (int64_t)s_b * p.rows_seq + R;
+    float4 *dst = reinterpret_cast<float4 *>(p.out + grow * kDc);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        dst[lane + 32 * q] = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+    if (lane == 0 && p.lse) p.lse[grow] = sum > 0.f ? M + logf(sum) : -INFINITY;
 }
 
 }  // namespace
@@ -942,8 +1222,10 @@ int tc_max_clusters() {
     if (cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
         cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
         cudaGetLastError();    // clear the query's error; plan with the SM count instead
-        return sm_count() / 4 > 0 ? sm_count() / 4 : 1;
+        const int f = sm_count() / 4;
+        return f < 1 ? 1 : (f > kMaxClusters ? kMaxClusters : f);
     }
+    if (n > kMaxClusters) n = kMaxClusters;
     cached[slot].store(n, std::memory_order_relaxed);
     return n;
 }
@@ -1015,8 +1297,6 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     p.W = vp.W;
     p.rows_seq = vp.T * vp.H;
     p.row_tiles = (p.rows_seq + kRows - 1) / kRows;
-    p.num_splits = vp.num_splits;
-    p.blocks_per_split = vp.blocks_per_split;
     p.rows_total = vp.rows_total;
     p.q_nope = static_cast<const __nv_bfloat16 *>(vp.q_nope);
     p.prefix_len = vp.prefix_len;
@@ -1027,16 +1307,18 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     p.part_o = vp.part_o;
     p.part_lse = vp.part_lse;
     p.err = vp.err;
-    p.tail_units = vp.tail_units;
-    p.tail_splits = vp.tail_splits;
     p.pairs_per_seq = (p.row_tiles + 1) / 2;
-    const int64_t base = (int64_t)p.B * p.pairs_per_seq;
-    const int64_t units = p.tail_splits > 0 ? base - p.tail_units + (int64_t)p.tail_units * p.tail_splits
-                                            : base * p.num_splits;
+    const int C = vp.tc_clusters;
+    if (C < 1 || C > kMaxClusters || (C > 1 && (!p.part_o || !p.part_lse))) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    verify_tc_kernel<<<(unsigned)(4 * units), kThreads, kSmemBytes, s>>>(map_ks, map_vs, map_kpe, map_qpe, p);
-    return cudaGetLastError();
+    verify_tc_kernel<<<(unsigned)(4 * C), kThreads, kSmemBytes, s>>>(map_ks, map_vs, map_kpe, map_qpe, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (C > 1) {
+        merge_pieces_kernel<<<dim3((unsigned)(C - 1), 2 * kRows / 8), 256, 0, s>>>(p, C);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace kdt

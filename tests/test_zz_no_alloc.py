@@ -78,6 +78,6 @@ def test_noalloc_fits_automatic_splits_and_rejects_oversize(kdt):
     out = torch.empty((c.B, c.T, c.H, 512), device="cuda")
     a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
                       max_kv_len=c.max_kv_len, scale=c.scale, out=out, impl="simt", num_splits=16)
-    assert kdt.workspace_size(a) > (16 << 20)
+    assert kdt.workspace_size(a) > (64 << 20)
     st = kdt.lib().kdt_verify_attn_noalloc(ctypes.byref(a), None)
     assert st == kdt.kdt.KDT_ERR_WORKSPACE
