@@ -81,6 +81,12 @@ enum TraceEvent {
     kEvRFull,            // S MMA thread: rope chunk of block j landed
     kEvSoftmaxMax,       // softmax warp 4: row maxima of both halves agreed
     kEvSoftmaxStaged,    // softmax warp 4: its rows of P staged
+    kEvQReady,           // softmax warp 4: Q_nope of item i in TMEM (index = item)
+    kEvStatsSent,        // softmax warp 4: statistics of item i sent
+    kEvOFree,            // O MMA thread: O of item i - 1 read out, item i may start
+    kEvEpiIn,            // epilogue warp 4: P.V and statistics of item i complete
+    kEvEpiOut,           // epilogue warp 4: O of item i written
+    kEvQpeIssued,        // S producer: Q_pe of item i requested
     kNumTraceEvents
 };
 
@@ -88,6 +94,8 @@ constexpr int kRows = 128;             // query rows per CTA (the pair's MMA has
 constexpr int kKeys = 128;             // keys per block (S MMA N, P.V K)
 constexpr int kHalfKeys = kKeys / 2;   // keys of a block held by one S-CTA
 constexpr int kThreads = 384;          // 12 warps
+constexpr int kQPrefetchBlocks = 6;               // blocks before an item's end that warm L2 with the next Q
+constexpr uint32_t kQPrefetchChunk = 32768;       // bytes per L2 prefetch request
 // Operand tiles are [rows x 64 bf16] with 128-byte rows, 128B-swizzled.
 constexpr int kKSub = kHalfKeys * 128;            // S-CTA key sub-tile [64 keys x 64 dims]: 8 KB
 constexpr int kVSub = kKeys * 128;                // O-CTA value sub-tile [128 keys x 64 dims]: 16 KB
@@ -162,7 +170,9 @@ struct Barriers {
     uint32_t need[2][kNP];         // leader: per-CTA "some row of O needs a rescale" per P slot
     uint32_t cmd;                  // each O-CTA: correction command
     int kseen[2];                  // S leader: latest latent chunk use each MMA issuer saw land
-    int work_u0, work_kb0, work_count;   // this cluster's work range (see the decomposition below)
+    int work_wleft;                      // this cluster's whole units (see the decomposition below)
+    int work_u0, work_kb0, work_left;    // its tail range
+    int work_count;                      // its key blocks
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -183,32 +193,49 @@ struct TcParams {
 };
 
 // ---- work decomposition ----------------------------------------------------------------
-// The work is every unit's key blocks, units in order (unit = b * pairs_per_seq + pair,
-// blocks 0 .. nblk(b) - 1). Cluster c of C takes the contiguous range
-// [W c / C, W (c + 1) / C) of it, so every cluster gets the same number of blocks (+-1)
-// whatever the wave count; the ranges are derived from prefix_len on the device, the same
-// way in every CTA. A unit cut by a range boundary is processed in pieces: each piece
-// writes its normalised partial state (o, lse) into slot 2c (the cluster's first item) or
+// A unit is two row tiles (256 rows) of one sequence, unit = b * pairs_per_seq + pair; its
+// work is key blocks 0 .. nblk(b) - 1, taken in order. With C clusters:
+//  * when every sequence has the same block count, the first (units / C) * C units go out
+//    whole, round robin (cluster c takes units c, c + C, ...): the clusters running at the
+//    same time then walk the same few sequences' keys in step and share them in L2;
+//  * the remaining units (all of them when lengths differ) form the tail: their blocks,
+//    units in order, are split into C contiguous ranges [Wt c / C, Wt (c + 1) / C), so every
+//    cluster gets the same number of blocks (+-1) whatever the wave count.
+// Everything is derived from prefix_len on the device, the same way in every CTA. A tail
+// unit cut by a range boundary is processed in pieces: each piece writes its normalised
+// partial state (o, lse) into slot 2c (the first item of the cluster's tail range) or
 // 2c + 1 (its last item), and a merge pass combines them.
 __device__ __forceinline__ int seq_blocks(const TcParams &p, int b) {
     return (p.prefix_len[b] + p.T + kKeys - 1) / kKeys;
 }
 
-__device__ __forceinline__ int64_t total_blocks(const TcParams &p) {
+// First unit of the tail.
+__device__ __forceinline__ int tail_first_unit(const TcParams &p, int C) {
+    const int units = p.B * p.pairs_per_seq;
+    const int nb0 = seq_blocks(p, 0);
+    for (int b = 1; b < p.B; ++b)
+        if (seq_blocks(p, b) != nb0) return 0;
+    return (units / C) * C;
+}
+
+// Blocks of the tail (units u_first ..).
+__device__ __forceinline__ int64_t tail_blocks(const TcParams &p, int u_first) {
     int64_t w = 0;
-    for (int b = 0; b < p.B; ++b) w += (int64_t)p.pairs_per_seq * seq_blocks(p, b);
+    for (int b = u_first / p.pairs_per_seq, k0 = u_first % p.pairs_per_seq; b < p.B; ++b, k0 = 0)
+        w += (int64_t)(p.pairs_per_seq - k0) * seq_blocks(p, b);
     return w;
 }
 
-// Unit holding flattened block s, its first flattened block and its block count.
-__device__ __forceinline__ void locate_block(const TcParams &p, int64_t s, int &u, int64_t &start, int &nblk) {
+// Tail unit holding tail block s, its first tail block and its block count.
+__device__ __forceinline__ void locate_block(const TcParams &p, int u_first, int64_t s, int &u, int64_t &start,
+                                             int &nblk) {
     int64_t acc = 0;
-    for (int b = 0; b < p.B; ++b) {
+    for (int b = u_first / p.pairs_per_seq, k0 = u_first % p.pairs_per_seq; b < p.B; ++b, k0 = 0) {
         const int nb = seq_blocks(p, b);
-        const int64_t seq = (int64_t)p.pairs_per_seq * nb;
+        const int64_t seq = (int64_t)(p.pairs_per_seq - k0) * nb;
         if (s < acc + seq) {
             const int k = (int)((s - acc) / nb);
-            u = b * p.pairs_per_seq + k;
+            u = b * p.pairs_per_seq + k0 + k;
             start = acc + (int64_t)k * nb;
             nblk = nb;
             return;
@@ -229,18 +256,33 @@ struct Item {
 };
 
 struct WorkIter {
-    int u, kb, left, taken;
+    int wu, wleft;         // next whole unit (stride C) and whole units left
+    int u, kb, left, taken;   // tail range: unit, block, blocks left, tail items taken
 };
 
-__device__ __forceinline__ bool next_item(const TcParams &p, WorkIter &w, int c, Item &it) {
-    if (w.left <= 0) return false;
-    const int b = w.u / p.pairs_per_seq;
+__device__ __forceinline__ void fill_item(const TcParams &p, int u, Item &it) {
+    const int b = u / p.pairs_per_seq;
     it.b = b;
-    it.rt0 = 2 * (w.u % p.pairs_per_seq);
+    it.rt0 = 2 * (u % p.pairs_per_seq);
     it.P = p.prefix_len[b];
     const int kv_len = it.P + p.T;
     it.nblk = (kv_len + kKeys - 1) / kKeys;
     it.key_base = kv_len - it.nblk * kKeys;
+}
+
+__device__ __forceinline__ bool next_item(const TcParams &p, WorkIter &w, int c, int C, Item &it) {
+    if (w.wleft > 0) {
+        fill_item(p, w.wu, it);
+        it.kb0 = 0;
+        it.nb = it.nblk;
+        it.whole = true;
+        it.slot = 0;
+        w.wu += C;
+        --w.wleft;
+        return true;
+    }
+    if (w.left <= 0) return false;
+    fill_item(p, w.u, it);
     it.kb0 = w.kb;
     it.nb = min(it.nblk - w.kb, w.left);
     it.whole = it.kb0 == 0 && it.nb == it.nblk;
@@ -492,15 +534,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // ---- set-up: barriers, TMEM ------------------------------------------------------
     if (threadIdx.x == 0) {
         {
-            const int64_t W = total_blocks(p);
             const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
-            const int64_t s0 = W * c / C, s1 = W * (c + 1) / C;
+            const int u_first = tail_first_unit(p, C);
+            const int64_t Wt = tail_blocks(p, u_first);
+            const int64_t s0 = Wt * c / C, s1 = Wt * (c + 1) / C;
             int u0, nblk0;
             int64_t start0;
-            locate_block(p, s0, u0, start0, nblk0);
+            locate_block(p, u_first, s0, u0, start0, nblk0);
+            bar.work_wleft = u_first / C;
             bar.work_u0 = u0;
             bar.work_kb0 = (int)(s0 - start0);
-            bar.work_count = (int)(s1 - s0);
+            bar.work_left = (int)(s1 - s0);
+            bar.work_count = bar.work_wleft * (u_first > 0 ? seq_blocks(p, 0) : 0) + bar.work_left;
         }
         for (int i = 0; i < kNK; ++i) { mbar_init(&bar.kfull[i], 1); mbar_init(&bar.kempty[i], 1); }
         for (int i = 0; i < kNR; ++i) { mbar_init(&bar.rfull[i], 1); mbar_init(&bar.rempty[i], 1); }
@@ -549,9 +594,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 
     // Every role walks the same sequence of items of this cluster's work range; per-block
     // state (ring slots, buffers, parities) follows the cluster-wide block counter g.
-    const WorkIter w0 = {bar.work_u0, bar.work_kb0, bar.work_count, 0};
+    const int cl = blockIdx.x >> 2, ncl = gridDim.x >> 2;
+    const WorkIter w0 = {cl, bar.work_wleft, bar.work_u0, bar.work_kb0, bar.work_left, 0};
     const int G = bar.work_count;                  // key blocks of this cluster
-    const int cl = blockIdx.x >> 2;
 
     if (s_role) {
         // =============================== S-CTA ===============================
@@ -571,15 +616,35 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 WorkIter w = w0;
                 Item it;
                 int ii = 0;
-                while (going && !aborted(bar) && next_item(p, w, cl, it)) {
+                while (going && !aborted(bar) && next_item(p, w, cl, ncl, it)) {
                     // this CTA's Q_pe tile is free once the previous item's rope MMAs read it
                     if (ii > 0 && !(going = wait_or_abort(bar, &bar.qpe_empty, (uint32_t)(ii - 1) & 1, p.err, -24)))
                         break;
                     if (leader) mbar_arrive_expect_tx(&bar.qpe_full, 2 * kQpeBytes);
                     tma_load_2d_pair(qpe_tile, &map_qpe, map_to_rank(&bar.qpe_full, lead_rank), 0,
                                      (int)((int64_t)it.b * p.rows_seq + (it.rt0 + kpair) * kRows));
+                    KDT_TC_TRACE(kEvQpeIssued, ii);
                     ++ii;
+                    // a few blocks before the item ends, warm L2 with the next item's rows of Q
+                    // (the pair's 256 rows are contiguous): its load then sits between two
+                    // items on the tensor pipes' critical path
+                    const int j_pf = it.nb > kQPrefetchBlocks ? it.nb - kQPrefetchBlocks : 0;
                     for (int j = 0; leader && j < it.nb && going; ++j) {
+                        if (j == j_pf) {
+                            WorkIter wn = w;
+                            Item nx;
+                            if (next_item(p, wn, cl, ncl, nx)) {
+                                const int r0 = nx.rt0 * kRows;
+                                const int nrows = min(2 * kRows, p.rows_seq - r0);
+                                const unsigned char *qsrc = reinterpret_cast<const unsigned char *>(
+                                    p.q_nope + ((int64_t)nx.b * p.rows_seq + r0) * kDc);
+                                const uint32_t bytes = (uint32_t)nrows * kDc * 2;
+                                for (uint32_t o = 0; o < bytes; o += kQPrefetchChunk)
+                                    prefetch_l2_bulk(qsrc + o, min(kQPrefetchChunk, bytes - o));
+                                for (int k = 0; k < 2 && r0 + k * kRows < p.rows_seq; ++k)
+                                    tma_prefetch_2d(&map_qpe, 0, (int)((int64_t)nx.b * p.rows_seq + r0 + k * kRows));
+                            }
+                        }
                         for (int c = 0; c < 2 && going; ++c) {
                             if (kr.n >= kNK &&
                                 !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -2)))
@@ -625,7 +690,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 WorkIter w = w0;
                 Item it;
                 int ii = 0, g = 0;
-                while (ok && next_item(p, w, cl, it)) {
+                while (ok && next_item(p, w, cl, ncl, it)) {
                     // this item's rows of Q are in tensor memory and its Q_pe tile landed
                     ok = wait_or_abort(bar, &bar.q_ready, (uint32_t)ii & 1, p.err, -3) &&
                          wait_or_abort(bar, &bar.qpe_full, (uint32_t)ii & 1, p.err, -3);
@@ -716,30 +781,45 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             float *lsum_s = reinterpret_cast<float *>(smem + kOffLSum);
             bool ok = true;
             bool fail = false;
+            // Q_nope of an item's rows into tensor memory, 16 loads in flight per thread
+            auto load_q = [&](const Item &q) {
+                const int Rq = (q.rt0 + kpair) * kRows + row;
+                const bool valid = Rq < p.rows_seq;
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)q.b * p.rows_seq + Rq) * kDc) + 32 * half;
+#pragma unroll
+                for (int r2 = 0; r2 < 2; ++r2) {
+                    uint4 v[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = valid ? __ldg(src + 16 * r2 + k) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t wq[32];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            wq[4 * k] = v[8 * h + k].x;
+                            wq[4 * k + 1] = v[8 * h + k].y;
+                            wq[4 * k + 2] = v[8 * h + k].z;
+                            wq[4 * k + 3] = v[8 * h + k].w;
+                        }
+                        tmem_st32(tmem_lane_addr(tmem_q, warp, (4 * half + 2 * r2 + h) * 32), wq);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote_cta(&bar.q_ready, lead_rank);
+            };
             WorkIter w = w0;
             Item it;
             int ii = 0, g = 0;
-            while (!fail && next_item(p, w, cl, it)) {
+            bool have = next_item(p, w, cl, ncl, it);
+            if (have) {
+                load_q(it);
+                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvQReady, 0);
+            }
+            while (!fail && have) {
                 const int R = (it.rt0 + kpair) * kRows + row;
-                const bool row_valid = R < p.rows_seq;
-                {   // Q_nope of this item's rows: tensor memory is free, every MMA of the
-                    // previous item ran before its last scores could be read
-                    const uint4 *src =
-                        reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)it.b * p.rows_seq + R) * kDc);
-                    for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {     // 4 x 32 columns = 256 bf16
-                        uint32_t wq[32];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const uint4 v = row_valid ? __ldg(src + c8 * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
-                            wq[4 * q] = v.x; wq[4 * q + 1] = v.y; wq[4 * q + 2] = v.z; wq[4 * q + 3] = v.w;
-                        }
-                        tmem_st32(tmem_lane_addr(tmem_q, warp, c8 * 32), wq);
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote_cta(&bar.q_ready, lead_rank);
-                }
                 const int qi = min(R, p.rows_seq - 1) / p.H;
                 const uint32_t *visrow = p.vis + ((int64_t)it.b * p.T + qi) * p.W;
                 float m_run = -INFINITY;                           // log2 units, same in both halves
@@ -834,10 +914,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive_remote(&bar.stats_full[sb], o_rank);
                     }
+                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvStatsSent, ii);
+                }
+                ++ii;
+                // the next item's Q_nope: tensor memory is free, every MMA of this item ran
+                // before its last scores could be read
+                have = next_item(p, w, cl, ncl, it);
+                if (have && ok) {
+                    load_q(it);
+                    if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvQReady, ii);
                 }
                 // lsum_s is rewritten at the end of the next item only after this barrier
                 fail = barrier_or<2, 256>(!ok);
-                ++ii;
             }
             // The O pair's MMA commits (pempty), the O-CTA's watcher (sfree) and its epilogue
             // (stats_empty) arrive here; the arrivals still due are consumed before this CTA
@@ -870,7 +958,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 bool going = true;
                 WorkIter w = w0;
                 Item it;
-                while (going && !aborted(bar) && next_item(p, w, cl, it)) {
+                while (going && !aborted(bar) && next_item(p, w, cl, ncl, it)) {
                     for (int j = 0; j < it.nb && going; ++j) {
                         const int key0 = it.key_base + (it.kb0 + j) * kKeys;
                         for (int h = 0; h < 2; ++h) {
@@ -898,10 +986,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 WorkIter w = w0;
                 Item it;
                 int ii = 0, g = 0;
-                while (ok && next_item(p, w, cl, it)) {
+                while (ok && next_item(p, w, cl, ncl, it)) {
                     // the previous item's epilogue has read O out of tensor memory
                     if (ii > 0 && !(ok = wait_cluster_or_abort(bar, &bar.o_free, (uint32_t)(ii - 1) & 1, p.err, -28)))
                         break;
+                    KDT_TC_TRACE(kEvOFree, ii);
                     for (int j = 0; j < it.nb && ok; ++j, ++g) {
                         const int ps = g % kNP;
                         if (!(ok = wait_cluster_or_abort(bar, &bar.pready[ps], (uint32_t)(g / kNP) & 1, p.err, -9))) break;
@@ -979,7 +1068,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 bool going = true;
                 WorkIter w = w0;
                 Item it;
-                while (going && !aborted(bar) && next_item(p, w, cl, it)) {
+                while (going && !aborted(bar) && next_item(p, w, cl, ncl, it)) {
                     for (int j = 0; j < it.nb && going; ++j) {
                         const int key0 = it.key_base + (it.kb0 + j) * kKeys + kpair * kHalfKeys;   // S-CTA k's 64 keys
                         for (int c = 0; c < 2 && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
@@ -1032,7 +1121,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             WorkIter w = w0;
             Item it;
             int ii = 0;
-            while (ok && next_item(p, w, cl, it)) {
+            while (ok && next_item(p, w, cl, ncl, it)) {
                 for (;; ++e) {
                     ok = warp_wait_cluster(bar, &bar.go, e & 1, p.err, -12);
                     if (barrier_or<1, 128>(!ok)) {
@@ -1072,6 +1161,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvEpiIn, ii);
                 tc_fence_after();
                 const int R = (it.rt0 + kpair) * kRows + row;
                 const int64_t grow = (int64_t)it.b * p.rows_seq + R;
@@ -1106,6 +1196,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     mbar_arrive_remote(&bar.o_free, lead_rank);
                     mbar_arrive_remote_cta(&bar.stats_empty[sb], (uint32_t)kpair);
                 }
+                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvEpiOut, ii);
                 ++ii;
             }
         }
@@ -1141,18 +1232,19 @@ __global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int
     const int c = blockIdx.x + 1;
     if (threadIdx.x == 0) {
         s_valid = 0;
-        const int64_t W = total_blocks(p);
+        const int u_first = tail_first_unit(p, C);
+        const int64_t W = tail_blocks(p, u_first);
         const int64_t sc = W * c / C, sprev = W * (c - 1) / C;
         int u, nblk;
         int64_t start;
-        locate_block(p, sc, u, start, nblk);
+        locate_block(p, u_first, sc, u, start, nblk);
         if (nblk > 0 && sc > start && sprev <= start) {
             int n = 0;
             s_slot[n++] = 2 * (c - 1) + (sprev == start ? 0 : 1);   // the piece that starts the unit
             for (int cc = c; cc < C && n <= kMaxClusters; ++cc) {
                 const int64_t lo = W * cc / C, hi = W * (cc + 1) / C;
                 if (lo >= start + nblk) break;
-                if (hi > lo) s_slot[n++] = 2 * cc;                 // pieces that start a cluster's range
+                if (hi > lo) s_slot[n++] = 2 * cc;                 // pieces that start a cluster's tail range
             }
             s_n = n;
             s_b = u / p.pairs_per_seq;

@@ -219,8 +219,8 @@ def test_running_max_jumps_force_output_rescale(kdt, oracle_mod, dtype):
 
 
 def test_tail_tiles_split_to_fill_the_last_wave(kdt, oracle_mod):
-    # 2 sequences x 40 row tiles = 80 tiles: more than one wave of 2-CTA clusters, with
-    # a partial last wave whose tiles are cut into key ranges and merged afterwards.
+    # 2 sequences x 20 units of 256 rows, 6 key blocks each: one wave of whole units on the
+    # resident clusters, then a tail of units cut into key ranges and merged afterwards.
     import torch
     case = wl.make_case("tail", B=2, T=40, H=128, prefix=(700, 650), dtype="bf16", tree="geometric", seed=17)
     d = G.to_device(case)
@@ -231,7 +231,7 @@ def test_tail_tiles_split_to_fill_the_last_wave(kdt, oracle_mod):
     assert pl["impl"] == "tcgen05" and pl["num_launches"] == 3          # visibility, attention, tail merge
     out_g, lse_g, err = G.run(case, impl="auto", dev_tensors=d)
     assert err == 0
-    rows_tail = np.arange(case.rows - 4 * 128 - 256, case.rows)         # the last tiles, both sides of a cut
+    rows_tail = np.arange(case.rows - 5 * 256, case.rows)               # the tail units and the last whole one
     rows = np.unique(np.concatenate([rows_tail, _sample_rows(case, 128, seed=4)]))
     ref_out, ref_lse = oracle_mod.verify_attn_rows(case, rows)
     _compare(case, out_g.reshape(-1, 512)[rows], lse_g.reshape(-1)[rows], ref_out, ref_lse, "tail")
