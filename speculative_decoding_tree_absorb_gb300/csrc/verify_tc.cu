@@ -87,6 +87,9 @@ enum TraceEvent {
     kEvEpiIn,            // epilogue warp 4: P.V and statistics of item i complete
     kEvEpiOut,           // epilogue warp 4: O of item i written
     kEvQpeIssued,        // S producer: Q_pe of item i requested
+    kEvItemEnd0,         // softmax warp 4: item i's blocks done, at the statistics barrier
+    kEvItemEnd1,         // softmax warp 8: the same
+    kEvItemBar,          // softmax warp 4: statistics barrier passed
     kNumTraceEvents
 };
 
@@ -129,8 +132,9 @@ constexpr int kOffLSum = kOffRowMax + 2 * 2 * kRows * 4;    // S: [128] partial 
 constexpr int kOffP = 0;                                    // O: 3 x 33 KB P + alpha
 constexpr int kOffV = kOffP + kNP * kPSlotBytes;            // O: 3 x 32 KB
 constexpr int kOffStats = kOffV + kNV * kVSlotBytes;        // O: [2 items][128] x (m, l)
+constexpr int kOffEpi = kOffStats + 2 * kRows * 8;          // O: 4 x [32 rows][32 fp32] epilogue transpose
 constexpr int kSEnd = kOffLSum + kRows * 4;
-constexpr int kOEnd = kOffStats + 2 * kRows * 8;
+constexpr int kOEnd = kOffEpi + 4 * 32 * 32 * 4;
 constexpr int kTileBytes = kSEnd > kOEnd ? kSEnd : kOEnd;
 constexpr int kSmemBytes = kTileBytes + 1024;               // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -307,13 +311,6 @@ __device__ __forceinline__ bool aborted(const Barriers &bar) {
 __device__ __forceinline__ void drain_mmas(Barriers &bar, uint16_t mask) {
     mma_commit_pair(&bar.drain, mask);
     mbar_wait(&bar.drain, 0, kWaitLimit);
-}
-
-// Order this thread's DSMEM stores (generic proxy) before a later release-arrive
-// by another lane, and make them visible to the peer's tensor-core reads.
-__device__ __forceinline__ void publish_remote_stores() {
-    asm volatile("fence.proxy.async;" ::: "memory");
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 
 __device__ __forceinline__ void set_abort(Barriers &bar, int32_t *err, int code) {
@@ -568,7 +565,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bar.go, 1);
         mbar_init(&bar.rescaled, 2);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar.stats_full[i], 4);
+            mbar_init(&bar.stats_full[i], 4 * 32);
             mbar_init(&bar.stats_empty[i], 4);
         }
         mbar_init(&bar.o_done, 1);
@@ -900,8 +897,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 if (fail) break;
                 // this item's statistics for the O-CTA epilogue: (m, l), l over both halves
                 if (half == 1) lsum_s[row] = l_run;
+                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvItemEnd0, ii);
+                if (warp == 8 && lane == 0) KDT_TC_TRACE(kEvItemEnd1, ii);
                 fail = barrier_or<2, 256>(!ok);
                 if (fail) break;
+                if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvItemBar, ii);
                 const int sb = ii & 1;                            // statistics buffer of this item
                 if (half == 0) {
                     // the O-CTA has read this buffer's previous contents (item ii - 2)
@@ -910,9 +910,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint32_t dst = map_to_rank(smem + kOffStats + (sb * kRows + row) * 8, o_rank);
                         st_cluster_f32(dst, m_run);
                         st_cluster_f32(dst + 4, l_run + lsum_s[row]);
-                        publish_remote_stores();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_remote(&bar.stats_full[sb], o_rank);
+                        // every lane releases its own two stores: no fence on this path
+                        mbar_arrive_remote(&bar.stats_full[sb], o_rank);
                     }
                     if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvStatsSent, ii);
                 }
@@ -1176,17 +1175,31 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 const float2 st = stats_s[sb * kRows + row];
                 const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+                // Each thread holds one row; the rows go out through a per-warp transpose in
+                // shared memory so that every store instruction writes whole 128-byte lines
+                // (four rows x 128 bytes). 16-byte slot q of staged row r sits at q ^ (r & 7),
+                // which keeps both the row-wise writes and the line-wise reads conflict-free.
+                float *stg = reinterpret_cast<float *>(smem + kOffEpi) + (warp & 3) * 32 * 32;
+                const int rsub = lane >> 3, qsub = lane & 7;      // read side: row 4i + rsub, slot qsub
+                float *orow0 = orow - (int64_t)lane * kDc;        // row 0 of this warp's 32
+                const int rows_ok = p.rows_seq - (R - lane);      // rows of the 32 that exist
                 for (int c = 0; c < 512 / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tmem_lane_addr(tmem, warp, c * 32), r);
                     tmem_wait_ld();
-                    if (R < p.rows_seq) {
 #pragma unroll
-                        for (int q = 0; q < 32; q += 4)
-                            *reinterpret_cast<float4 *>(orow + c * 32 + q) =
-                                make_float4(__uint_as_float(r[q]) * inv, __uint_as_float(r[q + 1]) * inv,
-                                            __uint_as_float(r[q + 2]) * inv, __uint_as_float(r[q + 3]) * inv);
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4 *>(stg + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+                            make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                        __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + rsub;
+                        const float4 v = *reinterpret_cast<const float4 *>(stg + rr * 32 + ((qsub ^ (rr & 7)) << 2));
+                        if (rr < rows_ok) *reinterpret_cast<float4 *>(orow0 + (int64_t)rr * kDc + c * 32 + 4 * qsub) = v;
                     }
+                    __syncwarp();
                 }
                 if (R < p.rows_seq && lrow) *lrow = st.y > 0.f ? 0.6931471805599453f * (st.x + log2f(st.y)) : -INFINITY;
                 // O may be overwritten and the statistics buffer refilled
