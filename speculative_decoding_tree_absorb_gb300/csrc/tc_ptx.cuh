@@ -150,6 +150,22 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes
                  : "memory");
 }
 
+// Warm L2 with one box of a 3-D / 4-D tensor map (boxes partly outside the tensor are
+// clipped like loads).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 // Warm L2 with one box of a 2-D tensor map.
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -99,11 +99,13 @@ constexpr int kHalfKeys = kKeys / 2;   // keys of a block held by one S-CTA
 constexpr int kThreads = 384;          // 12 warps
 constexpr int kQPrefetchBlocks = 6;               // blocks before an item's end that warm L2 with the next Q
 constexpr uint32_t kQPrefetchChunk = 32768;       // bytes per L2 prefetch request
+constexpr int kKvPrefetchBlocks = 4;              // key blocks the L2 prefetch runs ahead of the loads
 // Operand tiles are [rows x 64 bf16] with 128-byte rows, 128B-swizzled.
 constexpr int kKSub = kHalfKeys * 128;            // S-CTA key sub-tile [64 keys x 64 dims]: 8 KB
 constexpr int kVSub = kKeys * 128;                // O-CTA value sub-tile [128 keys x 64 dims]: 16 KB
 // Tiles travel as 32 KB requests from 4-D views of the cache (few, large requests:
 // the copy engine's cost is per request).
+constexpr int kKChunks = 2;                       // latent key chunks per block
 constexpr int kKSlotBytes = 4 * kKSub;            // S latent ring slot: 64 keys x 256 latent dims
 constexpr int kNK = 3;                            // S-CTA latent key ring slots (96 KB, 1.5 blocks)
 constexpr int kNR = 4;                            // S-CTA rope key ring slots of kKSub (32 KB, four blocks)
@@ -124,7 +126,7 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 // Shared-memory layout (same offsets in every CTA of the cluster; roles use
 // different parts). All tiles 1024-byte aligned for the 128B swizzle.
 constexpr int kOffQpe = 0;                                  // S: Q_pe tile 16 KB
-constexpr int kOffKRing = kOffQpe + kQpeBytes;              // S: 4 x 32 KB
+constexpr int kOffKRing = kOffQpe + kQpeBytes;              // S: 3 x 32 KB latent keys
 constexpr int kOffRRing = kOffKRing + kNK * kKSlotBytes;   // S: 4 x 8 KB rope keys
 constexpr int kOffPStage = kOffRRing + kNR * kKSub;         // S: 2 x 33 KB staging of P + alpha
 constexpr int kOffRowMax = kOffPStage + kNS * kPSlotBytes;  // S: [2 blocks][2 halves][128] partial maxima
@@ -642,7 +644,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                                     tma_prefetch_2d(&map_qpe, 0, (int)((int64_t)nx.b * p.rows_seq + r0 + k * kRows));
                             }
                         }
-                        for (int c = 0; c < 2 && going; ++c) {
+                        for (int c = 0; c < kKChunks && going; ++c) {
                             if (kr.n >= kNK &&
                                 !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -2)))
                                 break;
@@ -663,7 +665,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!leader) {
                     kr = RingPos{};
                     rr = RingPos{};
-                    for (int u = 0; u < 2 * G; ++u) ring_advance<kNK>(kr);
+                    for (int u = 0; u < kKChunks * G; ++u) ring_advance<kNK>(kr);
                     for (int u = 0; u < G; ++u) ring_advance<kNR>(rr);
                 }
                 ring_drain<kNK>(bar.kempty, kr);
@@ -700,13 +702,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         KDT_TC_TRACE(kEvSMmaStart, g);
                         const uint32_t d = tmem_s0 + buf * kKeys;
-                        for (int c = 0; c < 2; ++c) {
-                            const int u = 2 * g + c;                // latent chunk use
+                        for (int c = 0; c < kKChunks; ++c) {
+                            const int u = kKChunks * g + c;         // latent chunk use
                             const int slot = u % kNK;
                             // the slot's previous use belongs to the other thread when its block
                             // has the other parity: wait until that thread has seen it land
                             const int prev = u - kNK;
-                            if (prev >= 0 && (((prev >> 1) & 1) != par)) {
+                            if (prev >= 0 && (((prev / kKChunks) & 1) != par)) {
                                 const uint64_t t0 = global_ns();
                                 while (*seen_other < prev) {
                                     if (aborted(bar) || global_ns() - t0 > kWaitLimit) {
@@ -1065,12 +1067,31 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 unsigned char *rring = smem + kOffRRing;
                 RingPos kr, rr;
                 bool going = true;
+                // L2 prefetch cursor, kKvPrefetchBlocks blocks ahead of the loads: the clusters
+                // on one sequence ask for each block at about the same time, so without it every
+                // one of them waits for the same DRAM fetch
+                WorkIter wp = w0;
+                Item ip;
+                int jp = 0;
+                bool pf = next_item(p, wp, cl, ncl, ip);
+                auto prefetch_block = [&]() {
+                    if (!pf) return;
+                    const int pk0 = ip.key_base + (ip.kb0 + jp) * kKeys + kpair * kHalfKeys;
+                    for (int c = 0; c < kKChunks; ++c) tma_prefetch_4d(&map_ks, 0, pk0, 4 * c, ip.b);
+                    tma_prefetch_3d(&map_kpe, 0, pk0, ip.b);
+                    if (++jp == ip.nb) {
+                        jp = 0;
+                        pf = next_item(p, wp, cl, ncl, ip);
+                    }
+                };
+                for (int k = 0; k < kKvPrefetchBlocks; ++k) prefetch_block();
                 WorkIter w = w0;
                 Item it;
                 while (going && !aborted(bar) && next_item(p, w, cl, ncl, it)) {
                     for (int j = 0; j < it.nb && going; ++j) {
+                        prefetch_block();
                         const int key0 = it.key_base + (it.kb0 + j) * kKeys + kpair * kHalfKeys;   // S-CTA k's 64 keys
-                        for (int c = 0; c < 2 && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
+                        for (int c = 0; c < kKChunks && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
                             if (kr.n >= kNK &&
                                 !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -21)))
                                 break;
