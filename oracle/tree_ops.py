@@ -1,0 +1,121 @@
+"""CPU oracle for the steps around tree-verify attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import this module; the library never calls it and shares no code with it.
+Plain numpy (float64) and Python loops, one function per step, each following its
+definition as stated below.
+
+Parity status per function (how each is pinned is in ``tests/test_oracle_tree_ops.py``):
+  rope_neox        -- pinned (complex-exponential form of the rotation, identity at
+                      position 0, norm preservation, scores depend only on the position
+                      difference, rotation by p then q equals rotation by p + q)
+  tree_positions   -- pinned (chain and star trees, depth from explicit paths)
+  tree_accept      -- pinned (brute force over all root paths on random trees with
+                      distinct sibling tokens; all-match chain; no-match root)
+  kv_compact       -- pinned (identity on a chain path; rows compared one by one with
+                      the rows the path names)
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------- NeoX RoPE --
+def rope_neox(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
+    """NeoX rotary embedding ("The Query-Split Kernel: A Pivotal Edit ...", "Input
+    Knowledge: What One Must Understand to Grasp This Edit": the vector is split in half
+    and each half is rotated by a position-dependent angle, the angles in float64).
+
+    For a vector x of even width d and position p: for j < d/2, with the frequency
+    w_j = base ** (-2 j / d) and the angle a_j = p * w_j,
+        y[j]       = x[j] cos a_j - x[j + d/2] sin a_j
+        y[j + d/2] = x[j + d/2] cos a_j + x[j] sin a_j.
+    x: float array [..., d]; pos: integer array of shape x.shape[:-1] (or broadcastable).
+    Returns float64 [..., d].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    if d % 2:
+        raise ValueError("rope width must be even")
+    half = d // 2
+    j = np.arange(half, dtype=np.float64)
+    w = np.power(float(base), -2.0 * j / d)                        # [half]
+    a = np.asarray(pos, dtype=np.float64)[..., None] * w          # [..., half]
+    c, s = np.cos(a), np.sin(a)
+    x1, x2 = x[..., :half], x[..., half:]
+    y = np.empty_like(x)
+    y[..., :half] = x1 * c - x2 * s
+    y[..., half:] = x2 * c + x1 * s
+    return y
+
+
+def tree_positions(parent: np.ndarray, prefix_len: np.ndarray) -> np.ndarray:
+    """Rotary position of tree node i: prefix_len[b] + depth(i), depth(root) = 0 (the
+    root is the token after the committed prefix and a node sits one step after its
+    parent; the forward pass takes token ids with their positions, "The Architecture of
+    an Inference Engine ...", "What the Message Actually Says").
+    parent int [B,T] in topological order; returns int64 [B,T]."""
+    parent = np.asarray(parent)
+    B, T = parent.shape
+    depth = np.zeros((B, T), dtype=np.int64)
+    for b in range(B):
+        for i in range(T):
+            p = int(parent[b, i])
+            depth[b, i] = 0 if p < 0 else depth[b, p] + 1
+    return depth + np.asarray(prefix_len, dtype=np.int64)[:, None]
+
+
+# ------------------------------------------------------- greedy tree accept --
+def tree_accept(parent: np.ndarray, tok: np.ndarray, target: np.ndarray):
+    """Greedy walk of a verified tree (the third Phase-1 kernel, a greedy walk deciding
+    which draft tokens are accepted: "The Moment of Truth: Validating a Custom CUDA
+    Attention Kernel ...", "Context: Building a Native DDTree Inference Engine").
+
+    Node 0 is the root. tok[i] is node i's draft token, target[i] the target model's
+    greedy next token after node i. From the root, repeatedly move to the child c of the
+    current node with tok[c] == target[current] (the lowest such index if several);
+    stop when there is none. Returns per sequence (path, bonus): the node indices from
+    the root to the last accepted node, and target[last] (the token the target adds).
+    parent/tok/target int [B,T]."""
+    parent = np.asarray(parent)
+    tok = np.asarray(tok)
+    target = np.asarray(target)
+    B, T = parent.shape
+    res = []
+    for b in range(B):
+        path = [0]
+        cur = 0
+        while True:
+            nxt = -1
+            for c in range(T):
+                if int(parent[b, c]) == cur and int(tok[b, c]) == int(target[b, cur]):
+                    nxt = c
+                    break
+            if nxt < 0:
+                break
+            path.append(nxt)
+            cur = nxt
+        res.append((path, int(target[b, cur])))
+    return res
+
+
+def kv_compact(c_kv: np.ndarray, k_pe: np.ndarray, prefix_len: np.ndarray, paths):
+    """Post-verify cache compaction (the cache is compacted after acceptance to drop the
+    unaccepted branches: "The Architecture of an Inference Engine ...", "The Context:
+    Building an Engine from Scratch" and "Input Knowledge Required"). The tree's rows sit
+    at prefix_len[b] + t; the accepted path's k-th node moves to row prefix_len[b] + k,
+    and the new prefix length is prefix_len[b] + len(path). Rows past the new length
+    keep whatever they held. c_kv [B,L,Dc], k_pe [B,L,Dr] (any dtype, copied as stored).
+    Returns (c_kv', k_pe', new_prefix_len)."""
+    c2 = np.array(c_kv, copy=True)
+    k2 = np.array(k_pe, copy=True)
+    newp = np.array(prefix_len, dtype=np.int64, copy=True)
+    for b, path in enumerate(paths):
+        p0 = int(prefix_len[b])
+        src_c = [np.array(c_kv[b, p0 + t]) for t in path]
+        src_k = [np.array(k_pe[b, p0 + t]) for t in path]
+        for k in range(len(path)):
+            c2[b, p0 + k] = src_c[k]
+            k2[b, p0 + k] = src_k[k]
+        newp[b] = p0 + len(path)
+    return c2, k2, newp

@@ -1,0 +1,178 @@
+"""Pins for the oracle of the steps around tree-verify attention (CPU only).
+
+Each check ties the oracle to something other than its own formula: the complex form of
+the rotation, invariants RoPE is built to have, brute force over tree paths, and row by
+row comparisons with the rows a path names.
+"""
+import numpy as np
+import pytest
+
+import workloads as wl
+from oracle import tree_ops as ot
+
+
+def _vecs(seed, n, d):
+    return wl.normal(seed, "rope_x", n * d).reshape(n, d)
+
+
+# ------------------------------------------------------------------ RoPE pins --
+@pytest.mark.parametrize("d,base", [(2, 10000.0), (8, 10000.0), (64, 10000.0), (64, 50000.0)])
+def test_rope_matches_complex_exponential_form(d, base):
+    # NeoX pairs element j with j + d/2: as a complex number z_j = x_j + i x_{j+d/2}, the
+    # rotation multiplies z_j by exp(i p w_j), w_j = 1 / base^(2j/d).
+    x = _vecs(1, 40, d)
+    pos = np.arange(40) * 37 + 3
+    y = ot.rope_neox(x, pos, base)
+    inv_freq = 1.0 / (base ** (np.arange(0, d, 2, dtype=np.float64) / d))
+    z = (x[:, : d // 2] + 1j * x[:, d // 2:]) * np.exp(1j * pos[:, None] * inv_freq[None, :])
+    np.testing.assert_allclose(y[:, : d // 2], z.real, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(y[:, d // 2:], z.imag, rtol=0, atol=1e-12)
+
+
+def test_rope_known_value_single_pair():
+    # width 2: the only frequency is 1, so position 1 turns (1, 0) by one radian
+    y = ot.rope_neox(np.array([[1.0, 0.0]]), np.array([1]), 10000.0)
+    np.testing.assert_allclose(y[0], [0.5403023058681398, 0.8414709848078965], rtol=0, atol=1e-15)
+
+
+def test_rope_position_zero_is_identity():
+    x = _vecs(2, 16, 64)
+    assert np.array_equal(ot.rope_neox(x, np.zeros(16, dtype=np.int64), 10000.0), x)
+
+
+def test_rope_preserves_pair_norms():
+    x = _vecs(3, 32, 64)
+    y = ot.rope_neox(x, np.arange(32) * 1000 + 17, 10000.0)
+    nx = x[:, :32] ** 2 + x[:, 32:] ** 2
+    ny = y[:, :32] ** 2 + y[:, 32:] ** 2
+    np.testing.assert_allclose(ny, nx, rtol=1e-12, atol=1e-14)
+
+
+def test_rope_scores_depend_only_on_position_difference():
+    q = _vecs(4, 8, 64)
+    k = _vecs(5, 8, 64)
+    m = np.array([0, 5, 100, 8192, 9000, 1, 77, 4096])
+    n = np.array([3, 5, 90, 8000, 9000, 0, 70, 4100])
+    for shift in (1, 1000, 20000):
+        a = np.sum(ot.rope_neox(q, m, 10000.0) * ot.rope_neox(k, n, 10000.0), axis=1)
+        b = np.sum(ot.rope_neox(q, m + shift, 10000.0) * ot.rope_neox(k, n + shift, 10000.0), axis=1)
+        np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-9)
+
+
+def test_rope_composes_additively():
+    x = _vecs(6, 12, 64)
+    p = np.arange(12) * 311
+    q = np.arange(12) * 97 + 5
+    np.testing.assert_allclose(ot.rope_neox(ot.rope_neox(x, p, 10000.0), q, 10000.0),
+                               ot.rope_neox(x, p + q, 10000.0), rtol=1e-10, atol=1e-10)
+
+
+# --------------------------------------------------------------- positions --
+def test_positions_on_chain_star_and_random_trees():
+    assert ot.tree_positions(wl.tree_chain(5)[None], np.array([7])).tolist() == [[7, 8, 9, 10, 11]]
+    assert ot.tree_positions(wl.tree_star(5)[None], np.array([7])).tolist() == [[7, 8, 8, 8, 8]]
+    par = wl.tree_uniform(11, "pos", 40)
+    pos = ot.tree_positions(par[None], np.array([100]))[0]
+    for i in range(40):
+        d, j = 0, i
+        while par[j] >= 0:
+            j = int(par[j])
+            d += 1
+        assert pos[i] == 100 + d
+
+
+# ------------------------------------------------------------ accept pins --
+def _distinct_sibling_tokens(par, seed):
+    """Draft tokens in a 6-token alphabet with distinct tokens among siblings."""
+    T = par.shape[0]
+    tok = np.zeros(T, dtype=np.int64)
+    perm = (wl.raw_u64(seed, "tok", T) % 6).astype(np.int64)
+    used = {}
+    for c in range(1, T):
+        s = used.setdefault(int(par[c]), set())
+        t = int(perm[c])
+        while t in s:
+            t = (t + 1) % 1000
+        s.add(t)
+        tok[c] = t
+    return tok
+
+
+def _brute_accept(par, tok, tgt):
+    """Deepest node whose every root-path edge matches, by enumerating all nodes."""
+    T = par.shape[0]
+    best = 0
+    best_depth = 0
+    for i in range(T):
+        ok, d, j = True, 0, i
+        while par[j] >= 0:
+            p = int(par[j])
+            if tok[j] != tgt[p]:
+                ok = False
+                break
+            j = p
+            d += 1
+        if ok and d > best_depth:
+            best, best_depth = i, d
+    path = [best]
+    while par[path[-1]] >= 0:
+        path.append(int(par[path[-1]]))
+    return path[::-1], int(tgt[best])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_accept_equals_brute_force_on_random_trees(seed):
+    T = 3 + seed * 5
+    par = (wl.tree_uniform(seed, "acc", T) if seed % 2 else wl.tree_geometric(seed, "acc", T))
+    tok = _distinct_sibling_tokens(par, seed)
+    tgt = (wl.raw_u64(seed, "tgt", T) % 4).astype(np.int64)    # small alphabet: matches happen
+    (path, bonus), = ot.tree_accept(par[None], tok[None], tgt[None])
+    assert (path, bonus) == _brute_accept(par, tok, tgt)
+
+
+def test_accept_all_match_chain_and_no_match_root():
+    T = 9
+    par = wl.tree_chain(T)
+    tgt = np.arange(T) + 100
+    tok = np.concatenate([[0], tgt[:-1]])                        # node i drafts target[i-1]
+    (path, bonus), = ot.tree_accept(par[None], tok[None], tgt[None])
+    assert path == list(range(T)) and bonus == tgt[-1]
+    tok2 = tok + 1
+    (path, bonus), = ot.tree_accept(par[None], tok2[None], tgt[None])
+    assert path == [0] and bonus == tgt[0]
+
+
+# ----------------------------------------------------------- compaction pins --
+def test_compact_chain_path_is_identity():
+    c = wl.normal(1, "c", 2 * 20 * 8).reshape(2, 20, 8)
+    k = wl.normal(2, "k", 2 * 20 * 4).reshape(2, 20, 4)
+    pre = np.array([5, 9])
+    c2, k2, newp = ot.kv_compact(c, k, pre, [[0, 1, 2], [0, 1, 2, 3, 4]])
+    assert np.array_equal(c2, c) and np.array_equal(k2, k) and newp.tolist() == [8, 14]
+
+
+def test_compact_moves_named_rows_and_nothing_else():
+    B, L, T = 3, 40, 10
+    c = wl.normal(3, "c", B * L * 8).reshape(B, L, 8)
+    k = wl.normal(4, "k", B * L * 4).reshape(B, L, 4)
+    pre = np.array([0, 7, 25])
+    paths = [[0, 2, 5, 9], [0], [0, 1, 3]]
+    c2, k2, newp = ot.kv_compact(c, k, pre, paths)
+    assert newp.tolist() == [4, 8, 28]
+    for b in range(B):
+        n = len(paths[b])
+        for r in range(L):
+            if pre[b] <= r < pre[b] + n:
+                src = pre[b] + paths[b][r - pre[b]]
+                assert np.array_equal(c2[b, r], c[b, src]) and np.array_equal(k2[b, r], k[b, src])
+            else:
+                assert np.array_equal(c2[b, r], c[b, r]) and np.array_equal(k2[b, r], k[b, r])
+
+
+def test_accept_prefers_lowest_index_among_equal_sibling_tokens():
+    # the definition's tie rule: several children drafting the target's token -> lowest index
+    par = np.array([-1, 0, 0, 0, 2, 3])
+    tok = np.array([0, 5, 7, 7, 9, 9])
+    tgt = np.array([7, 0, 9, 9, 1, 1])
+    (path, bonus), = ot.tree_accept(par[None], tok[None], tgt[None])
+    assert path == [0, 2, 4] and bonus == 1
