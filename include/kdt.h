@@ -112,6 +112,11 @@ typedef struct {
     int32_t *err;           /* device int32 error word for the parent path, or NULL */
     int impl;               /* kdt_impl */
     int num_splits;         /* KV splits per row tile; 0 = choose automatically */
+    int64_t q_nope_row_stride; /* elements between consecutive (b,i,h) rows of q_nope; 0 = 512
+                                  (contiguous). Lets the kernels read a combined [.., 512 + 64]
+                                  query buffer where it lies (stride 576, q_pe = q_nope + 512)
+                                  instead of a split copy. Else >= 512, a multiple of 8. */
+    int64_t q_pe_row_stride;   /* the same for q_pe; 0 = 64, else >= 64, a multiple of 8 */
 } kdt_verify_args;
 
 /*
@@ -198,6 +203,82 @@ kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const flo
 #define KDT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
 kdt_status kdt_verify_attn_noalloc(const kdt_verify_args *a, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * The steps next to verify in a DDTree step: rotary embedding of the tree's rope
+ * parts before it, the greedy accept walk and the cache compaction after it.
+ * ------------------------------------------------------------------------------ */
+
+/* Arguments of kdt_rope_neox. */
+typedef struct {
+    int B, T, H;            /* sequences, tree nodes per sequence (1..4096), heads (1..1024) */
+    int D_r;                /* rope width: even, 2..256 */
+    kdt_dtype dtype;        /* element type of q and k_pe */
+    void *q;                /* device, or NULL: the rope part of query row (b,i,h) is the D_r
+                               elements at q + ((b*T + i)*H + h) * q_row_stride; rotated in place.
+                               Point it at the rope slice of a combined [.., D_c + D_r] query
+                               buffer to rotate that buffer where it lies. */
+    int64_t q_row_stride;   /* elements between consecutive (b,i,h) rows, >= D_r */
+    void *k_pe;             /* device [B, L, D_r], or NULL: rows prefix_len[b] + i (the tree's
+                               new key rows) rotated in place; rows outside [0, L) are skipped */
+    int64_t kv_row_stride;  /* L, >= T (used with k_pe) */
+    const int32_t *prefix_len; /* device [B] (used with k_pe) */
+    const int32_t *pos;     /* device [B,T]: rotary position of tree node i (normally
+                               prefix_len[b] + depth(i), the root at depth 0) */
+    double base;            /* angle base (theta), > 0, e.g. 10000 */
+} kdt_rope_args;
+
+/*
+ * kdt_rope_neox -- NeoX rotary embedding in place (page "The Query-Split Kernel: A
+ * Pivotal Edit ...", sections "The Reasoning Chain" -- rope applied in place on the rope
+ * portion of the query buffer -- and "Input Knowledge" -- NeoX variant, float64 angles).
+ * For a vector x of width d at position p and j < d/2, with a_j = p * base^(-2j/d) in
+ * float64:
+ *   (x_j, x_{j+d/2}) <- (x_j cos a_j - x_{j+d/2} sin a_j,  x_{j+d/2} cos a_j + x_j sin a_j),
+ * products and sums rounded in float64, the results rounded once (to nearest) to the
+ * element type. Every head of node (b,i) and its key row use pos[b,i].
+ * Errors: KDT_ERR_NULL_ARG (pos NULL, both q and k_pe NULL, k_pe without prefix_len),
+ * KDT_ERR_BAD_SHAPE, KDT_ERR_UNSUPPORTED (dtype), KDT_ERR_CUDA.
+ */
+kdt_status kdt_rope_neox(const kdt_rope_args *a, cudaStream_t stream);
+
+/*
+ * kdt_tree_accept -- greedy walk of a verified draft tree (page "The Moment of Truth
+ * ...", section "Context": the accept kernel walks the tree greedily to decide which
+ * draft tokens are accepted). Node 0 is the root; from it, move to the child c of the
+ * current node with tok[c] == target[current] (the lowest index if several), until no
+ * child matches.
+ *   parent   device int32 [B,T], -1 <= parent[b,i] < i (as for kdt_build_visibility)
+ *   tok      device int32 [B,T]: node i's draft token (tok[b,0] unused)
+ *   target   device int32 [B,T]: the target model's greedy next token after node i
+ *   acc_nodes device int32 [B,T] out: the accepted path (node indices from the root),
+ *            then -1
+ *   n_acc    device int32 [B] out: path length, >= 1 (the root always stays)
+ *   bonus    device int32 [B] out: target[last node of the path], the token the
+ *            target model adds after the accepted ones
+ *   err      device int32, may be NULL: zeroed, then 1 + (b*T + i) of the first parent
+ *            entry outside [-1, i); such entries are skipped.
+ * Errors: KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE (B < 0, T < 1, T > 4096), KDT_ERR_CUDA.
+ */
+kdt_status kdt_tree_accept(const int32_t *parent, const int32_t *tok, const int32_t *target, int B, int T,
+                           int32_t *acc_nodes, int32_t *n_acc, int32_t *bonus, int32_t *err,
+                           cudaStream_t stream);
+
+/*
+ * kdt_kv_compact -- drop the unaccepted branches from the cache (page "The Architecture
+ * of an Inference Engine ...", sections "The Context" and "Input Knowledge Required").
+ * The tree's rows sit at cache rows prefix_len[b] + t; the k-th node of the accepted
+ * path moves to row prefix_len[b] + k of both c_kv [B,L,D_c] and k_pe [B,L,D_r], in
+ * place. With update_prefix != 0, prefix_len[b] += n_acc[b] afterwards. Rows past the
+ * new length keep what they held. Path entries that are not increasing tree indices, or
+ * that point past row L, are not copied.
+ * D_c and D_r times the element size must be multiples of 16 bytes; c_kv and k_pe
+ * 16-byte aligned. Errors: KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE, KDT_ERR_UNSUPPORTED,
+ * KDT_ERR_CUDA.
+ */
+kdt_status kdt_kv_compact(void *c_kv, void *k_pe, kdt_dtype dtype, int D_c, int D_r, int B, int T,
+                          int64_t kv_row_stride, int32_t *prefix_len, const int32_t *acc_nodes,
+                          const int32_t *n_acc, int update_prefix, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

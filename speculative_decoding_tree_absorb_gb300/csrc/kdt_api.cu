@@ -57,6 +57,9 @@ kdt_status check_args(const kdt_verify_args *a) {
         !aligned16(a->out) || (reinterpret_cast<uintptr_t>(a->lse) & 3u))
         return KDT_ERR_BAD_SHAPE;
     if (!(a->scale == a->scale) || isinf(a->scale)) return KDT_ERR_BAD_SHAPE;
+    if ((a->q_nope_row_stride && (a->q_nope_row_stride < kDc || a->q_nope_row_stride % 8)) ||
+        (a->q_pe_row_stride && (a->q_pe_row_stride < kDr || a->q_pe_row_stride % 8)))
+        return KDT_ERR_BAD_SHAPE;
     return KDT_OK;
 }
 
@@ -199,6 +202,8 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     vp.L = a->kv_row_stride;
     vp.q_nope = a->q_nope;
     vp.q_pe = a->q_pe;
+    vp.q_nope_stride = a->q_nope_row_stride ? a->q_nope_row_stride : kDc;
+    vp.q_pe_stride = a->q_pe_row_stride ? a->q_pe_row_stride : kDr;
     vp.c_kv = a->c_kv;
     vp.k_pe = a->k_pe;
     vp.prefix_len = a->prefix_len;

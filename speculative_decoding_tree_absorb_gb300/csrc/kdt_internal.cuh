@@ -12,6 +12,18 @@ namespace kdt {
 constexpr int kDc = 512;   // latent width of the MLA cache
 constexpr int kDr = 64;    // rope width
 constexpr int kDqk = kDc + kDr;
+
+// err <- min(err, v) treating 0 as "no error yet" (v >= 1): the first offending entry
+// of a malformed tree, whatever order the threads find them in.
+__device__ __forceinline__ void record_error(int32_t *err, int32_t v) {
+    if (!err) return;
+    int32_t old = *reinterpret_cast<volatile int32_t *>(err);
+    while (old == 0 || v < old) {
+        int32_t seen = atomicCAS(err, old, v);
+        if (seen == old) break;
+        old = seen;
+    }
+}
 constexpr int kMaxSplits = 32;
 constexpr int kMaxT = 4096;
 
@@ -20,6 +32,7 @@ struct VerifyParams {
     int B, T, H, W;            // W = ceil(T/32) visibility words per query
     int64_t L;                 // cache rows per sequence
     const void *q_nope, *q_pe, *c_kv, *k_pe;
+    int64_t q_nope_stride, q_pe_stride;   // elements between consecutive (b,i,h) query rows
     const int32_t *prefix_len;
     const uint32_t *vis;       // [B,T,W]
     float scale_log2;          // scale * log2(e): scores are kept in base-2 units

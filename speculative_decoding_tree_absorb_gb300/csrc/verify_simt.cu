@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_simt_kernel(const VerifyPa
                 float v[8];
                 // Q rows beyond the sequence's T*H rows read as zero
                 if (r0 + lr < rows_seq) {
-                    if (dglob < kDc) load8(q_nope + (q_row0 + lr) * kDc + dglob, v);
-                    else load8(q_pe + (q_row0 + lr) * kDr + (dglob - kDc), v);
+                    if (dglob < kDc) load8(q_nope + (q_row0 + lr) * p.q_nope_stride + dglob, v);
+                    else load8(q_pe + (q_row0 + lr) * p.q_pe_stride + (dglob - kDc), v);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) v[e] = 0.f;

@@ -189,6 +189,7 @@ struct TcParams {
     int row_tiles;         // ceil(rows_seq / 128)
     int64_t rows_total;
     const __nv_bfloat16 *q_nope;
+    int64_t q_stride;              // elements between consecutive query rows of q_nope
     const int32_t *prefix_len;
     const uint32_t *vis;
     float scale_log2;
@@ -636,8 +637,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                                 const int r0 = nx.rt0 * kRows;
                                 const int nrows = min(2 * kRows, p.rows_seq - r0);
                                 const unsigned char *qsrc = reinterpret_cast<const unsigned char *>(
-                                    p.q_nope + ((int64_t)nx.b * p.rows_seq + r0) * kDc);
-                                const uint32_t bytes = (uint32_t)nrows * kDc * 2;
+                                    p.q_nope + ((int64_t)nx.b * p.rows_seq + r0) * p.q_stride);
+                                const uint32_t bytes = (uint32_t)((nrows - 1) * p.q_stride + kDc) * 2;
                                 for (uint32_t o = 0; o < bytes; o += kQPrefetchChunk)
                                     prefetch_l2_bulk(qsrc + o, min(kQPrefetchChunk, bytes - o));
                                 for (int k = 0; k < 2 && r0 + k * kRows < p.rows_seq; ++k)
@@ -785,7 +786,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 const int Rq = (q.rt0 + kpair) * kRows + row;
                 const bool valid = Rq < p.rows_seq;
                 const uint4 *src =
-                    reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)q.b * p.rows_seq + Rq) * kDc) + 32 * half;
+                    reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)q.b * p.rows_seq + Rq) * p.q_stride) + 32 * half;
 #pragma unroll
                 for (int r2 = 0; r2 < 2; ++r2) {
                     uint4 v[16];
@@ -1412,7 +1413,7 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     }
     {
         cuuint64_t dims[2] = {(cuuint64_t)kDr, (cuuint64_t)vp.rows_total};
-        cuuint64_t strides[1] = {(cuuint64_t)kDr * 2};
+        cuuint64_t strides[1] = {(cuuint64_t)vp.q_pe_stride * 2};   // rows may sit inside a combined buffer
         cuuint32_t box[2] = {64, kRows};
         if (!make_map(&map_qpe, vp.q_pe, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
@@ -1425,6 +1426,7 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     p.row_tiles = (p.rows_seq + kRows - 1) / kRows;
     p.rows_total = vp.rows_total;
     p.q_nope = static_cast<const __nv_bfloat16 *>(vp.q_nope);
+    p.q_stride = vp.q_nope_stride;
     p.prefix_len = vp.prefix_len;
     p.vis = vp.vis;
     p.scale_log2 = vp.scale_log2;

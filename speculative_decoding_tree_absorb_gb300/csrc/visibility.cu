@@ -16,17 +16,6 @@
 namespace kdt {
 namespace {
 
-// err <- min(err, v) treating 0 as "no error yet" (v >= 1).
-__device__ void record_error(int32_t *err, int32_t v) {
-    if (!err) return;
-    int32_t old = *reinterpret_cast<volatile int32_t *>(err);
-    while (old == 0 || v < old) {
-        int32_t seen = atomicCAS(err, old, v);
-        if (seen == old) break;
-        old = seen;
-    }
-}
-
 __global__ void build_visibility_kernel(const int32_t *__restrict__ parent, int T, int W,
                                         uint32_t *__restrict__ vis, int32_t *err) {
     const int b = blockIdx.x;

@@ -24,7 +24,7 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 # Names the header declares (checked by the CPU test suite against include/kdt.h).
 EXPORTS = ("kdt_status_str", "kdt_version", "kdt_build_visibility", "kdt_verify_attn",
            "kdt_verify_attn_workspace_size", "kdt_verify_attn_plan", "kdt_merge_attn_states",
-           "kdt_verify_attn_noalloc")
+           "kdt_verify_attn_noalloc", "kdt_rope_neox", "kdt_tree_accept", "kdt_kv_compact")
 
 
 class KdtError(RuntimeError):
@@ -46,6 +46,18 @@ class VerifyArgs(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("err", ctypes.c_void_p),
         ("impl", ctypes.c_int), ("num_splits", ctypes.c_int),
+        ("q_nope_row_stride", ctypes.c_int64), ("q_pe_row_stride", ctypes.c_int64),
+    ]
+
+
+class RopeArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("D_r", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("q", ctypes.c_void_p), ("q_row_stride", ctypes.c_int64),
+        ("k_pe", ctypes.c_void_p), ("kv_row_stride", ctypes.c_int64),
+        ("prefix_len", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+        ("base", ctypes.c_double),
     ]
 
 
@@ -83,6 +95,13 @@ def lib():
         L.kdt_merge_attn_states.restype = ctypes.c_int
         L.kdt_verify_attn_noalloc.argtypes = [ctypes.POINTER(VerifyArgs), vp]
         L.kdt_verify_attn_noalloc.restype = ctypes.c_int
+        L.kdt_rope_neox.argtypes = [ctypes.POINTER(RopeArgs), vp]
+        L.kdt_rope_neox.restype = ctypes.c_int
+        L.kdt_tree_accept.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp]
+        L.kdt_tree_accept.restype = ctypes.c_int
+        L.kdt_kv_compact.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int64, vp, vp, vp, ctypes.c_int, vp]
+        L.kdt_kv_compact.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -137,7 +156,20 @@ def make_args(q_nope, q_pe, c_kv, k_pe, prefix_len, *, parent=None, vis=None, ma
     a.err = None if err is None else err.data_ptr()
     a.impl = IMPLS[impl] if isinstance(impl, str) else int(impl)
     a.num_splits = int(num_splits)
+    a.q_nope_row_stride = _row_stride(q_nope)
+    a.q_pe_row_stride = _row_stride(q_pe)
     return a
+
+
+def _row_stride(q):
+    """0 for a contiguous [B,T,H,d] tensor; else the element stride between (b,i,h) rows
+    of a view with a contiguous last dim and equally spaced rows (e.g. a slice of a
+    combined [B,T,H,576] query buffer)."""
+    if q.is_contiguous():
+        return 0
+    if q.stride(3) != 1 or q.stride(2) * q.shape[2] != q.stride(1) or q.stride(1) * q.shape[1] != q.stride(0):
+        raise ValueError("query views must have a contiguous last dim and equally spaced (b,i,h) rows")
+    return int(q.stride(2))
 
 
 def plan(args: VerifyArgs) -> dict:
@@ -214,3 +246,51 @@ def verify_attn_noalloc(q_nope, q_pe, c_kv, k_pe, prefix_len, *, out, lse=None, 
                   scale=scale, out=out, lse=lse, err=err, impl=impl, num_splits=num_splits)
     _check(lib().kdt_verify_attn_noalloc(ctypes.byref(a), _stream_ptr(stream)), "kdt_verify_attn_noalloc")
     return out, lse
+
+
+def rope_neox(pos, *, q=None, k_pe=None, prefix_len=None, base=10000.0, stream=None):
+    """NeoX rotary embedding in place (kdt_rope_neox).
+
+    ``q``: a [B,T,H,d] view whose last dim is contiguous -- e.g. the rope slice
+    ``q_comb[..., 512:]`` of a combined [B,T,H,576] query buffer (its row stride is
+    taken from the view). ``k_pe``: the [B,L,d] key cache; rows prefix_len[b] + i are
+    rotated. ``pos`` int32 [B,T]. Returns nothing: the tensors are updated in place.
+    """
+    a = RopeArgs()
+    a.B, a.T = pos.shape
+    ref = q if q is not None else k_pe
+    a.dtype = _dtype_code(ref)
+    if q is not None:
+        if q.stride(3) != 1 or q.stride(2) * q.shape[2] != q.stride(1) or q.stride(1) * q.shape[1] != q.stride(0):
+            raise ValueError("q must be a [B,T,H,d] view with equally spaced (b,i,h) rows and a contiguous last dim")
+        a.H, a.D_r = q.shape[2], q.shape[3]
+        a.q, a.q_row_stride = q.data_ptr(), q.stride(2)
+    else:
+        a.H, a.D_r = 1, k_pe.shape[2]
+    if k_pe is not None:
+        a.k_pe, a.kv_row_stride = k_pe.data_ptr(), k_pe.shape[1]
+        a.prefix_len = None if prefix_len is None else prefix_len.data_ptr()
+    a.pos = pos.data_ptr()
+    a.base = float(base)
+    _check(lib().kdt_rope_neox(ctypes.byref(a), _stream_ptr(stream)), "kdt_rope_neox")
+
+
+def tree_accept(parent, tok, target, err=None, stream=None):
+    """Greedy accept walk (kdt_tree_accept). Returns (acc_nodes [B,T], n_acc [B], bonus [B]) int32."""
+    import torch
+    B, T = parent.shape
+    dev = parent.device
+    acc = torch.empty((B, T), dtype=torch.int32, device=dev)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    _check(lib().kdt_tree_accept(_ptr(parent), _ptr(tok), _ptr(target), B, T, _ptr(acc), _ptr(n), _ptr(bonus),
+                                 _ptr(err), _stream_ptr(stream)), "kdt_tree_accept")
+    return acc, n, bonus
+
+
+def kv_compact(c_kv, k_pe, prefix_len, acc_nodes, n_acc, update_prefix=True, stream=None):
+    """Move the accepted path's cache rows to prefix_len + k, in place (kdt_kv_compact)."""
+    B, T = acc_nodes.shape
+    _check(lib().kdt_kv_compact(_ptr(c_kv), _ptr(k_pe), _dtype_code(c_kv), c_kv.shape[2], k_pe.shape[2], B, T,
+                                c_kv.shape[1], _ptr(prefix_len), _ptr(acc_nodes), _ptr(n_acc),
+                                1 if update_prefix else 0, _stream_ptr(stream)), "kdt_kv_compact")

@@ -136,3 +136,22 @@ def test_plan_and_workspace_are_host_only(kdt):
     if clusters > 1:
         assert p["workspace_bytes"] >= 2 * clusters * 256 * (512 + 1) * 4 and p["num_launches"] == 3
     assert _status(kdt, _args(kdt, dtype=0, impl=2)) == kdt.kdt.KDT_ERR_UNSUPPORTED   # fp32 on tensor cores
+
+
+def test_tree_op_host_checks(kdt):
+    lib = kdt.lib()
+    K = kdt.kdt
+    assert lib.kdt_tree_accept(None, None, None, -1, 4, None, None, None, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_tree_accept(None, None, None, 2, 0, None, None, None, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_tree_accept(None, None, None, 2, 5, None, None, None, None, None) == K.KDT_ERR_NULL_ARG
+    assert lib.kdt_kv_compact(None, None, K.KDT_BF16, 512, 64, 2, 5, 3, None, None, None, 1, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_kv_compact(None, None, K.KDT_BF16, 500, 64, 2, 5, 100, None, None, None, 1, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_kv_compact(None, None, 7, 512, 64, 2, 5, 100, None, None, None, 1, None) == K.KDT_ERR_UNSUPPORTED
+    assert lib.kdt_kv_compact(None, None, K.KDT_BF16, 512, 64, 2, 5, 100, None, None, None, 1, None) == K.KDT_ERR_NULL_ARG
+    a = K.RopeArgs()
+    a.B, a.T, a.H, a.D_r, a.dtype, a.base = 2, 4, 8, 63, K.KDT_BF16, 10000.0
+    assert lib.kdt_rope_neox(ctypes.byref(a), None) == K.KDT_ERR_BAD_SHAPE
+    a.D_r = 64
+    assert lib.kdt_rope_neox(ctypes.byref(a), None) == K.KDT_ERR_NULL_ARG
+    a.base = -1.0
+    assert lib.kdt_rope_neox(ctypes.byref(a), None) == K.KDT_ERR_BAD_SHAPE
