@@ -14,8 +14,13 @@ Parity status per function (how each is pinned is in ``tests/test_oracle_tree_op
                       distinct sibling tokens; all-match chain; no-match root)
   kv_compact       -- pinned (identity on a chain path; rows compared one by one with
                       the rows the path names)
+  tree_build       -- pinned (brute force: every node of the full K-ary candidate tree
+                      sorted by the selection order, first N taken; path-score and depth
+                      invariants; single-candidate chain)
 """
 from __future__ import annotations
+
+import heapq
 
 import numpy as np
 
@@ -119,3 +124,52 @@ def kv_compact(c_kv: np.ndarray, k_pe: np.ndarray, prefix_len: np.ndarray, paths
             k2[b, p0 + k] = src_k[k]
         newp[b] = p0 + len(path)
     return c2, k2, newp
+
+
+# ------------------------------------------------------- best-first builder --
+def tree_build(cand_tok: np.ndarray, cand_lp: np.ndarray, N: int, root_tok=None):
+    """Best-first draft tree ("The Architecture of an Inference Engine ...", section "The
+    Context": a GPU best-first tree builder constructs the draft tree on the device,
+    replacing a per-request CPU heap).
+
+    The drafter gives, for every depth d = 1..D ahead of the root, K candidate tokens
+    cand_tok[b, d-1, :] with log-probabilities cand_lp[b, d-1, :] (the same candidates
+    below every node of depth d-1). A node's score is the float32 sum of the
+    log-probabilities on its path (root 0). Starting from the root, the tree grows by the
+    best node not yet in it whose parent is, N times. "Best" is the order: higher score,
+    then lower depth, then lower parent index, then lower candidate rank, where a depth's
+    candidates are ranked by log-probability, highest first, ties by position.
+    Nodes are numbered in the order they join (root 0), so parents precede children.
+    Returns int32 parent [B,N+1], tok [B,N+1] (tok[b,0] = root_tok[b] or -1), depth
+    [B,N+1] and float32 score [B,N+1]."""
+    cand_tok = np.asarray(cand_tok)
+    cand_lp = np.asarray(cand_lp, dtype=np.float32)
+    B, D, K = cand_lp.shape
+    T = N + 1
+    parent = np.full((B, T), -1, dtype=np.int32)
+    tok = np.full((B, T), -1, dtype=np.int32)
+    depth = np.zeros((B, T), dtype=np.int32)
+    score = np.zeros((B, T), dtype=np.float32)
+    for b in range(B):
+        # rank of each candidate: log-probability descending, ties by position
+        order = [sorted(range(K), key=lambda k: (-float(cand_lp[b, d, k]), k)) for d in range(D)]
+        if root_tok is not None:
+            tok[b, 0] = int(root_tok[b])
+        heap = []
+
+        def push(par, d, r):                         # candidate of rank r at depth d (1-based) under par
+            k = order[d - 1][r]
+            sc = np.float32(score[b, par] + cand_lp[b, d - 1, k])
+            heapq.heappush(heap, (-float(sc), d, par, r, sc))
+
+        if D > 0:
+            for r in range(K):
+                push(0, 1, r)
+        for n in range(1, T):
+            _, d, par, r, sc = heapq.heappop(heap)
+            parent[b, n], depth[b, n], score[b, n] = par, d, sc
+            tok[b, n] = int(cand_tok[b, d - 1, order[d - 1][r]])
+            if d < D:
+                for r2 in range(K):
+                    push(n, d + 1, r2)
+    return parent, tok, depth, score

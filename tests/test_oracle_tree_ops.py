@@ -176,3 +176,84 @@ def test_accept_prefers_lowest_index_among_equal_sibling_tokens():
     tgt = np.array([7, 0, 9, 9, 1, 1])
     (path, bonus), = ot.tree_accept(par[None], tok[None], tgt[None])
     assert path == [0, 2, 4] and bonus == 1
+
+
+# ------------------------------------------------------------- builder pins --
+def _cands(seed, B, D, K, quant):
+    """Distinct tokens per depth; log-probabilities <= 0, quantised to force score ties."""
+    lp = -np.abs(wl.normal(seed, "lp", B * D * K)).reshape(B, D, K)
+    if quant:
+        lp = -np.round(-lp * 2.0) / 2.0
+    tok = (np.arange(B * D * K).reshape(B, D, K) * 7 + 3).astype(np.int32)
+    return tok, lp.astype(np.float32)
+
+
+def _brute_build(tok, lp, N):
+    """Every node of the full candidate tree (rank paths up to depth D), float32 path
+    scores, sorted by the selection order with parents compared recursively; first N."""
+    import functools
+    D, K = lp.shape
+    order = [sorted(range(K), key=lambda k: (-float(lp[d, k]), k)) for d in range(D)]
+    score = {(): np.float32(0.0)}
+    nodes = []
+    frontier = [()]
+    for d in range(1, D + 1):
+        nxt = []
+        for path in frontier:
+            for r in range(K):
+                p2 = path + (r,)
+                score[p2] = np.float32(score[path] + lp[d - 1, order[d - 1][r]])
+                nxt.append(p2)
+        nodes += nxt
+        frontier = nxt
+
+    def cmp(a, b):
+        if a == b:
+            return 0
+        if score[a] != score[b]:
+            return -1 if score[a] > score[b] else 1
+        if len(a) != len(b):
+            return -1 if len(a) < len(b) else 1
+        c = cmp(a[:-1], b[:-1]) if a[:-1] != b[:-1] else 0
+        if c:
+            return c
+        return -1 if a[-1] < b[-1] else 1
+
+    chosen = sorted(nodes, key=functools.cmp_to_key(cmp))[:N]
+    index = {(): 0}
+    for n, path in enumerate(chosen, start=1):
+        index[path] = n
+    par = [-1] + [index[p[:-1]] for p in chosen]
+    tk = [-1] + [int(tok[len(p) - 1, order[len(p) - 1][p[-1]]]) for p in chosen]
+    dep = [0] + [len(p) for p in chosen]
+    sc = [np.float32(0.0)] + [score[p] for p in chosen]
+    return par, tk, dep, sc
+
+
+@pytest.mark.parametrize("seed,D,K,quant", [(0, 1, 3, False), (1, 3, 2, True), (2, 4, 3, True), (3, 3, 4, False),
+                                            (4, 5, 2, True), (5, 2, 5, True)])
+def test_build_equals_brute_force_selection_order(seed, D, K, quant):
+    tok, lp = _cands(seed, 2, D, K, quant)
+    total = sum(K ** d for d in range(1, D + 1))
+    for N in sorted({1, total // 2, total}):
+        par, tk, dep, sc = ot.tree_build(tok, lp, N)
+        for b in range(2):
+            ep, et, ed, es = _brute_build(tok[b], lp[b], N)
+            assert par[b].tolist() == ep and tk[b].tolist() == et and dep[b].tolist() == ed
+            assert np.array_equal(sc[b], np.array(es, dtype=np.float32))
+
+
+def test_build_invariants_and_single_candidate_chain():
+    tok, lp = _cands(9, 3, 6, 4, False)
+    par, tk, dep, sc = ot.tree_build(tok, lp, 40, root_tok=np.array([5, 6, 7]))
+    assert tk[:, 0].tolist() == [5, 6, 7]
+    lp_of = {(b, int(tok[b, d, k])): lp[b, d, k] for b in range(3) for d in range(6) for k in range(4)}
+    for b in range(3):
+        for n in range(1, 41):
+            p = par[b, n]
+            assert 0 <= p < n and dep[b, n] == dep[b, p] + 1
+            assert sc[b, n] == np.float32(sc[b, p] + lp_of[(b, int(tk[b, n]))])
+        assert np.all(np.diff(sc[b]) <= 0)                     # log-probs <= 0: scores never rise
+    tok1, lp1 = _cands(10, 1, 8, 1, False)
+    par, tk, dep, sc = ot.tree_build(tok1, lp1, 8)
+    assert par[0].tolist() == list(range(-1, 8)) and dep[0].tolist() == list(range(9))

@@ -25,6 +25,13 @@ MUTANTS = {
     "compact_prefix_short": ("newp[b] = p0 + len(path)", "newp[b] = p0 + len(path) - 1"),
     "compact_source_unshifted": ("src_c = [np.array(c_kv[b, p0 + t]) for t in path]",
                                  "src_c = [np.array(c_kv[b, t]) for t in path]"),
+    "build_tie_rank_before_parent": ("heapq.heappush(heap, (-float(sc), d, par, r, sc))",
+                                     "heapq.heappush(heap, (-float(sc), d, r * 1000 + par, r, sc))"),
+    "build_score_without_parent": ("sc = np.float32(score[b, par] + cand_lp[b, d - 1, k])",
+                                   "sc = np.float32(cand_lp[b, d - 1, k])"),
+    "build_depth_tie_ignored": ("heapq.heappush(heap, (-float(sc), d, par, r, sc))",
+                                "heapq.heappush(heap, (-float(sc), 0, par, r, sc))"),
+    "build_children_same_depth": ("push(n, d + 1, r2)", "push(n, d, r2)"),
 }
 
 PINS = [
@@ -40,6 +47,8 @@ PINS = [
     (P.test_accept_prefers_lowest_index_among_equal_sibling_tokens, {}),
     (P.test_compact_chain_path_is_identity, {}),
     (P.test_compact_moves_named_rows_and_nothing_else, {}),
+    (P.test_build_equals_brute_force_selection_order, dict(seed=2, D=4, K=3, quant=True)),
+    (P.test_build_invariants_and_single_candidate_chain, {}),
 ]
 
 
@@ -62,6 +71,6 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name):
     for pin, kw in PINS:
         try:
             pin(**kw)
-        except AssertionError:
+        except Exception:                  # a failed check, or the mutant breaking outright
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutant {name}"
