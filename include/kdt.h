@@ -209,6 +209,29 @@ kdt_status kdt_verify_attn_noalloc(const kdt_verify_args *a, cudaStream_t stream
  * parts before it, the greedy accept walk and the cache compaction after it.
  * ------------------------------------------------------------------------------ */
 
+/*
+ * kdt_tree_build -- best-first draft tree on the device (page "The Architecture of an
+ * Inference Engine ...", section "The Context": the tree builder constructs the draft
+ * tree on the GPU instead of with a per-request CPU heap).
+ * For every depth d = 1..D ahead of the root the drafter gives K candidates,
+ * cand_tok[b,d-1,:] with log-probabilities cand_lp[b,d-1,:], the same below every node of
+ * depth d-1. A node's score is the float32 sum of the log-probabilities on its path (the
+ * root's is 0). The tree grows N times by the best node not yet in it whose parent is:
+ * higher score, then lower depth, then lower parent index, then lower candidate rank
+ * (a depth's candidates ranked by log-probability, highest first, ties by position; NaN
+ * counts as -inf). Nodes are numbered in the order they join, the root 0, so the output
+ * is in topological order and feeds kdt_build_visibility / kdt_verify_attn directly.
+ *   cand_tok  device int32 [B,D,K];  cand_lp  device float32 [B,D,K]
+ *   root_tok  device int32 [B] or NULL: tok[b,0] (else -1)
+ *   parent, tok  device int32 [B,N+1] out; depth (int32) and score (float32) [B,N+1]
+ *            out, each may be NULL
+ * Sizes: 1 <= D <= 64, 1 <= K <= 32, 1 <= N <= 4095 and N <= K + K^2 + ... + K^D.
+ * Errors: KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE, KDT_ERR_CUDA.
+ */
+kdt_status kdt_tree_build(const int32_t *cand_tok, const float *cand_lp, int B, int D, int K, int N,
+                          const int32_t *root_tok, int32_t *parent, int32_t *tok, int32_t *depth, float *score,
+                          cudaStream_t stream);
+
 /* Arguments of kdt_rope_neox. */
 typedef struct {
     int B, T, H;            /* sequences, tree nodes per sequence (1..4096), heads (1..1024) */

@@ -1,6 +1,7 @@
-// The steps next to tree-verify attention in a DDTree step: the NeoX rotary embedding
-// of the tree's query and key rope parts before verify, and after it the greedy accept
-// walk and the compaction of the cache rows of the accepted path.
+// The steps next to tree-verify attention in a DDTree step: the best-first draft-tree
+// builder and the NeoX rotary embedding of the tree's query and key rope parts before
+// verify, and after it the greedy accept walk and the compaction of the cache rows of
+// the accepted path.
 //
 // RoPE: page "The Query-Split Kernel: A Pivotal Edit ...", sections "The Reasoning Chain"
 // (rope applied in place on the rope portion of the combined query buffer) and "Input
@@ -8,7 +9,8 @@
 // of Truth: Validating a Custom CUDA Attention Kernel ...", section "Context" (a greedy
 // walk deciding which draft tokens are accepted), and page "The Architecture of an
 // Inference Engine ...", sections "The Context" and "Input Knowledge Required" (the
-// cache is compacted after acceptance to drop the unaccepted branches).
+// cache is compacted after acceptance to drop the unaccepted branches; the tree is built
+// best-first on the device instead of with a per-request CPU heap).
 #include <climits>
 
 #include "kdt_internal.cuh"
@@ -121,6 +123,123 @@ __global__ void kv_compact_kernel(uint4 *c_kv, uint4 *k_pe, int c_vec, int r_vec
     if (update_prefix && threadIdx.x == 0) prefix_len[b] = (int32_t)(p0 + n);
 }
 
+// ------------------------------------------------------------ best-first builder --
+// A frontier entry: the candidate of rank `rank` at depth `depth` below node `par`.
+struct FrontierEntry {
+    float score;
+    int depth, par, rank;
+};
+
+// Selection order: higher score, then lower depth, lower parent, lower rank. Entries are
+// unique in (depth, par, rank), so this is a strict total order and the warp's argmin
+// does not depend on the reduction order.
+__device__ __forceinline__ bool before(const FrontierEntry &a, const FrontierEntry &b) {
+    if (a.score != b.score) return a.score > b.score;
+    if (a.depth != b.depth) return a.depth < b.depth;
+    if (a.par != b.par) return a.par < b.par;
+    return a.rank < b.rank;
+}
+
+constexpr int kMaxBuildDepth = 64, kMaxBuildK = 32, kMaxBuildN = kMaxT - 1;
+
+size_t build_smem_bytes(int D, int K, int N) {
+    const size_t lists = (size_t)D * K * 8, scores = ((size_t)(N + 1) * 4 + 15) / 16 * 16;
+    return lists + scores + (size_t)(N + 2) * sizeof(FrontierEntry);
+}
+
+// One warp per sequence. The candidates of every depth are ranked (log-probability
+// descending, ties by position; NaN counts as -inf). The frontier holds, for every node
+// in the tree, only its best child not yet taken: children below a node are ranked like
+// the candidates, so when a node's child of rank r joins, its sibling of rank r + 1 and
+// its own first child are pushed. That yields the same joins as pushing all children.
+__global__ void __launch_bounds__(32) tree_build_kernel(const int32_t *__restrict__ cand_tok,
+                                                        const float *__restrict__ cand_lp, int D, int K, int N,
+                                                        const int32_t *root_tok, int32_t *parent, int32_t *tok,
+                                                        int32_t *depth, float *score) {
+    extern __shared__ __align__(16) unsigned char bsm[];
+    float *s_lp = reinterpret_cast<float *>(bsm);                      // [D][K] ranked
+    int32_t *s_tok = reinterpret_cast<int32_t *>(s_lp + D * K);        // [D][K]
+    float *n_score = reinterpret_cast<float *>(s_tok + D * K);         // [N + 1]
+    FrontierEntry *fr = reinterpret_cast<FrontierEntry *>(bsm + (size_t)D * K * 8 + ((size_t)(N + 1) * 4 + 15) / 16 * 16);
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int T = N + 1;
+    const int64_t ob = (int64_t)b * T;
+    for (int d = 0; d < D; ++d) {
+        float v = -INFINITY;
+        int32_t t = -1;
+        if (lane < K) {
+            v = cand_lp[((int64_t)b * D + d) * K + lane];
+            if (v != v) v = -INFINITY;
+            t = cand_tok[((int64_t)b * D + d) * K + lane];
+        }
+        int rank = 0;
+        for (int j = 0; j < K; ++j) {
+            const float vj = __shfl_sync(0xffffffffu, v, j);
+            rank += (vj > v || (vj == v && j < lane)) ? 1 : 0;
+        }
+        if (lane < K) {
+            s_lp[d * K + rank] = v;
+            s_tok[d * K + rank] = t;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        n_score[0] = 0.f;
+        parent[ob] = -1;
+        tok[ob] = root_tok ? root_tok[b] : -1;
+        if (depth) depth[ob] = 0;
+        if (score) score[ob] = 0.f;
+        fr[0] = FrontierEntry{__fadd_rn(0.f, s_lp[0]), 1, 0, 0};
+    }
+    int F = 1;                                          // frontier size, the same in every lane
+    __syncwarp();
+    for (int n = 1; n < T && F > 0; ++n) {
+        int best = -1;
+        FrontierEntry be{0.f, 0, 0, 0};
+        for (int i = lane; i < F; i += 32) {
+            const FrontierEntry e = fr[i];
+            if (best < 0 || before(e, be)) {
+                best = i;
+                be = e;
+            }
+        }
+        for (int off = 16; off; off >>= 1) {
+            FrontierEntry o;
+            const int oi = __shfl_down_sync(0xffffffffu, best, off);
+            o.score = __shfl_down_sync(0xffffffffu, be.score, off);
+            o.depth = __shfl_down_sync(0xffffffffu, be.depth, off);
+            o.par = __shfl_down_sync(0xffffffffu, be.par, off);
+            o.rank = __shfl_down_sync(0xffffffffu, be.rank, off);
+            if (lane + off < 32 && oi >= 0 && (best < 0 || before(o, be))) {
+                best = oi;
+                be = o;
+            }
+        }
+        best = __shfl_sync(0xffffffffu, best, 0);
+        be.score = __shfl_sync(0xffffffffu, be.score, 0);
+        be.depth = __shfl_sync(0xffffffffu, be.depth, 0);
+        be.par = __shfl_sync(0xffffffffu, be.par, 0);
+        be.rank = __shfl_sync(0xffffffffu, be.rank, 0);
+        __syncwarp();
+        const bool sib = be.rank + 1 < K, child = be.depth < D;
+        if (lane == 0) {
+            fr[best] = fr[F - 1];                       // take the entry out
+            n_score[n] = be.score;
+            parent[ob + n] = be.par;
+            tok[ob + n] = s_tok[(be.depth - 1) * K + be.rank];
+            if (depth) depth[ob + n] = be.depth;
+            if (score) score[ob + n] = be.score;
+            int f = F - 1;
+            if (sib)
+                fr[f++] = FrontierEntry{__fadd_rn(n_score[be.par], s_lp[(be.depth - 1) * K + be.rank + 1]), be.depth,
+                                        be.par, be.rank + 1};
+            if (child) fr[f++] = FrontierEntry{__fadd_rn(be.score, s_lp[be.depth * K]), be.depth + 1, n, 0};
+        }
+        F = F - 1 + (sib ? 1 : 0) + (child ? 1 : 0);
+        __syncwarp();
+    }
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -129,6 +248,27 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 using namespace kdt;
 
 extern "C" {
+
+kdt_status kdt_tree_build(const int32_t *cand_tok, const float *cand_lp, int B, int D, int K, int N,
+                          const int32_t *root_tok, int32_t *parent, int32_t *tok, int32_t *depth, float *score,
+                          cudaStream_t stream) {
+    if (B < 0 || D < 1 || D > kMaxBuildDepth || K < 1 || K > kMaxBuildK || N < 1 || N > kMaxBuildN)
+        return KDT_ERR_BAD_SHAPE;
+    int64_t avail = 0, level = 1;                      // nodes below the root: K + K^2 + ... + K^D
+    for (int d = 0; d < D && avail < N; ++d) {
+        level *= K;
+        avail += level;
+    }
+    if (avail < N) return KDT_ERR_BAD_SHAPE;
+    if (B == 0) return KDT_OK;
+    if (!cand_tok || !cand_lp || !parent || !tok) return KDT_ERR_NULL_ARG;
+    const size_t smem = build_smem_bytes(D, K, N);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return KDT_ERR_CUDA;
+    tree_build_kernel<<<B, 32, smem, stream>>>(cand_tok, cand_lp, D, K, N, root_tok, parent, tok, depth, score);
+    return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
+}
 
 kdt_status kdt_rope_neox(const kdt_rope_args *a, cudaStream_t stream) {
     if (!a) return KDT_ERR_NULL_ARG;

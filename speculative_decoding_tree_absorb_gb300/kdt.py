@@ -24,7 +24,7 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 # Names the header declares (checked by the CPU test suite against include/kdt.h).
 EXPORTS = ("kdt_status_str", "kdt_version", "kdt_build_visibility", "kdt_verify_attn",
            "kdt_verify_attn_workspace_size", "kdt_verify_attn_plan", "kdt_merge_attn_states",
-           "kdt_verify_attn_noalloc", "kdt_rope_neox", "kdt_tree_accept", "kdt_kv_compact")
+           "kdt_verify_attn_noalloc", "kdt_rope_neox", "kdt_tree_accept", "kdt_kv_compact", "kdt_tree_build")
 
 
 class KdtError(RuntimeError):
@@ -102,6 +102,9 @@ def lib():
         L.kdt_kv_compact.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int64, vp, vp, vp, ctypes.c_int, vp]
         L.kdt_kv_compact.restype = ctypes.c_int
+        L.kdt_tree_build.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp,
+                                     vp, vp]
+        L.kdt_tree_build.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -294,3 +297,18 @@ def kv_compact(c_kv, k_pe, prefix_len, acc_nodes, n_acc, update_prefix=True, str
     _check(lib().kdt_kv_compact(_ptr(c_kv), _ptr(k_pe), _dtype_code(c_kv), c_kv.shape[2], k_pe.shape[2], B, T,
                                 c_kv.shape[1], _ptr(prefix_len), _ptr(acc_nodes), _ptr(n_acc),
                                 1 if update_prefix else 0, _stream_ptr(stream)), "kdt_kv_compact")
+
+
+def tree_build(cand_tok, cand_lp, N, root_tok=None, stream=None):
+    """Best-first draft tree (kdt_tree_build). cand_tok int32 / cand_lp float32 [B,D,K].
+    Returns (parent, tok, depth) int32 [B,N+1] and score float32 [B,N+1]."""
+    import torch
+    B, D, K = cand_lp.shape
+    dev = cand_lp.device
+    parent = torch.empty((B, N + 1), dtype=torch.int32, device=dev)
+    tok = torch.empty_like(parent)
+    depth = torch.empty_like(parent)
+    score = torch.empty((B, N + 1), dtype=torch.float32, device=dev)
+    _check(lib().kdt_tree_build(_ptr(cand_tok), _ptr(cand_lp), B, D, K, int(N), _ptr(root_tok), _ptr(parent),
+                                _ptr(tok), _ptr(depth), _ptr(score), _stream_ptr(stream)), "kdt_tree_build")
+    return parent, tok, depth, score

@@ -155,3 +155,13 @@ def test_tree_op_host_checks(kdt):
     assert lib.kdt_rope_neox(ctypes.byref(a), None) == K.KDT_ERR_NULL_ARG
     a.base = -1.0
     assert lib.kdt_rope_neox(ctypes.byref(a), None) == K.KDT_ERR_BAD_SHAPE
+
+
+def test_tree_build_host_checks(kdt):
+    lib = kdt.lib()
+    K = kdt.kdt
+    assert lib.kdt_tree_build(None, None, 1, 0, 4, 3, None, None, None, None, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_tree_build(None, None, 1, 4, 33, 3, None, None, None, None, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_tree_build(None, None, 1, 2, 2, 7, None, None, None, None, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert lib.kdt_tree_build(None, None, 1, 2, 2, 6, None, None, None, None, None, None) == K.KDT_ERR_NULL_ARG
+    assert lib.kdt_tree_build(None, None, 1, 64, 32, 4096, None, None, None, None, None, None) == K.KDT_ERR_BAD_SHAPE

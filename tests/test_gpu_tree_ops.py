@@ -242,3 +242,84 @@ def test_device_chain_rope_verify_accept_compact(kdt, oracle_mod):
     assert _ulp_diff(bits(d["k_pe"]), rk, "bf16").max() <= 1
     assert d["prefix_len"].cpu().numpy().tolist() == rp.tolist()
     assert sum(len(p) for p, _ in res) > B                                  # some draft token was accepted
+
+
+# ------------------------------------------------------------------ builder --
+def _cand(seed, B, D, K, quant):
+    lp = -np.abs(wl.normal(seed, "blp", B * D * K)).reshape(B, D, K)
+    if quant:                                            # ties in scores and within a depth
+        lp = -np.round(-lp * 2.0) / 2.0
+    tok = (wl.raw_u64(seed, "btok", B * D * K) % 50000).astype(np.int32).reshape(B, D, K)
+    return tok, lp.astype(np.float32)
+
+
+@pytest.mark.parametrize("B,D,K,N,quant", [(4, 8, 4, 63, False), (2, 16, 8, 255, False), (3, 4, 3, 60, True),
+                                           (2, 5, 1, 5, False), (2, 3, 3, 39, True), (1, 64, 32, 4095, False),
+                                           (5, 12, 6, 127, True)])
+def test_build_bit_exact(kdt, B, D, K, N, quant):
+    import torch
+    tok, lp = _cand(D * 100 + K, B, D, K, quant)
+    root = np.arange(B, dtype=np.int32) + 11
+    g = kdt.tree_build(torch.from_numpy(tok).cuda(), torch.from_numpy(lp).cuda(), N,
+                       root_tok=torch.from_numpy(root).cuda())
+    g = [t.cpu().numpy() for t in g]
+    r = ot.tree_build(tok, lp, N, root_tok=root)
+    for name, a, e in zip(("parent", "tok", "depth", "score"), g, r):
+        assert np.array_equal(a, e), f"{name} differs at {np.argwhere(a != e)[:5].tolist()}"
+
+
+def test_device_step_from_builder(kdt, oracle_mod):
+    """Build the tree from synthetic drafter candidates, then visibility, positions, RoPE,
+    verify from the combined query buffer, accept and compaction, all queued on the device
+    before one synchronisation; the oracle runs the same step on the same inputs."""
+    import dataclasses
+
+    import torch
+    from tests import gpu_util as G
+    from tests import helpers as H
+    B, D, K, N, Hh = 3, 8, 4, 47, 16
+    T = N + 1
+    case = wl.make_case("step", B=B, T=T, H=Hh, prefix=(600, 1200, 333), dtype="bf16", tree="chain", seed=21)
+    ctok, clp = _cand(21, B, D, K, False)
+    tgt_h = (wl.raw_u64(21, "tgt", B * T) % 50000).astype(np.int32).reshape(B, T)
+    # the oracle's tree; targets agree with the draft on a few nodes so some are accepted
+    r_par, r_tok, r_dep, _ = ot.tree_build(ctok, clp, N)
+    for b in range(B):
+        for i in range(1, T):
+            if i % 3 == 1:
+                tgt_h[b, r_par[b, i]] = r_tok[b, i]
+    d = G.to_device(case)
+    comb = torch.cat([d["q_nope"], d["q_pe"]], dim=-1).contiguous()
+    # -- device
+    par, tok, dep, _ = kdt.tree_build(torch.from_numpy(ctok).cuda(), torch.from_numpy(clp).cuda(), N)
+    pos = (d["prefix_len"][:, None] + dep).to(torch.int32)
+    kdt.rope_neox(pos, q=comb[..., 512:], k_pe=d["k_pe"], prefix_len=d["prefix_len"], base=10000.0)
+    vis = kdt.build_visibility(par)
+    out, lse = kdt.verify_attn(comb[..., :512], comb[..., 512:], d["c_kv"], d["k_pe"], d["prefix_len"], vis=vis,
+                               scale=case.scale, max_kv_len=case.max_kv_len)
+    acc, n_acc, bonus = kdt.tree_accept(par, tok, torch.from_numpy(tgt_h).cuda())
+    kdt.kv_compact(d["c_kv"], d["k_pe"], d["prefix_len"], acc, n_acc)
+    torch.cuda.synchronize()
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    # -- oracle
+    assert np.array_equal(par.cpu().numpy(), r_par) and np.array_equal(tok.cpu().numpy(), r_tok)
+    pos_h = ot.tree_positions(r_par, case.prefix_len)
+    assert np.array_equal(pos.cpu().numpy(), pos_h)
+    r_qpe = _round(ot.rope_neox(_widen(case.q_pe, "bf16"), pos_h[:, :, None], 10000.0), "bf16")
+    r_kpe = case.k_pe.copy()
+    for b in range(B):
+        rr = case.prefix_len[b] + np.arange(T)
+        r_kpe[b, rr] = _round(ot.rope_neox(_widen(case.k_pe[b, rr], "bf16"), pos_h[b], 10000.0), "bf16")
+    rows = np.arange(B * T * Hh)[::5]
+    rcase = dataclasses.replace(case, q_pe=r_qpe, k_pe=r_kpe, parent=r_par)
+    ref_o, ref_l = oracle_mod.verify_attn_rows(rcase, rows)
+    H.assert_close(out.reshape(-1, 512)[rows].cpu().numpy(), ref_o, *H.TOL["bf16"], "step out")
+    H.assert_close(lse.reshape(-1)[rows].cpu().numpy(), ref_l, *H.TOL["bf16"], "step lse")
+    res = ot.tree_accept(r_par, r_tok, tgt_h)
+    assert n_acc.cpu().numpy().tolist() == [len(p) for p, _ in res]
+    assert bonus.cpu().numpy().tolist() == [bn for _, bn in res]
+    assert max(len(p) for p, _ in res) > 1
+    rc, rk, rp = ot.kv_compact(case.c_kv, r_kpe, case.prefix_len, [p for p, _ in res])
+    assert np.array_equal(bits(d["c_kv"]), rc)
+    assert _ulp_diff(bits(d["k_pe"]), rk, "bf16").max() <= 1
+    assert d["prefix_len"].cpu().numpy().tolist() == rp.tolist()
