@@ -200,6 +200,74 @@ def run_reference(args, case, counts):
     return line
 
 
+def run_tree_ops(args, case, dev):
+    """Time the steps next to verify on this workload's shapes: best-first tree build from
+    synthetic drafter candidates (depth 16, 8 per depth, T - 1 nodes), NeoX RoPE in place
+    on a combined [B,T,H,576] query buffer and the tree's key rows, greedy accept, and
+    compaction of the accepted rows. CUDA events around each call, L2 flushed before each."""
+    import torch
+    import speculative_decoding_tree_absorb_gb300 as kdt
+
+    def conv(x):
+        if case.dtype == "bf16":
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(x).to(dev)
+
+    B, T, H = case.B, case.T, case.H
+    D, K, N = 16, 8, T - 1
+    lp = -np.abs(wl.normal(77, "bench_lp", B * D * K)).reshape(B, D, K).astype(np.float32)
+    ctok = (wl.raw_u64(77, "bench_tok", B * D * K) % 160000).astype(np.int32).reshape(B, D, K)
+    ctok_d, lp_d = torch.from_numpy(ctok).to(dev), torch.from_numpy(lp).to(dev)
+    comb = torch.cat([conv(case.q_nope), conv(case.q_pe)], dim=-1).contiguous()
+    c_kv, k_pe = conv(case.c_kv), conv(case.k_pe)
+    prefix = torch.from_numpy(case.prefix_len.astype(np.int32)).to(dev)
+    parent, tok, depth, _ = kdt.tree_build(ctok_d, lp_d, N)
+    pos = (prefix[:, None] + depth).to(torch.int32)
+    target = torch.from_numpy((wl.raw_u64(77, "bench_tgt", B * T) % 2).astype(np.int32).reshape(B, T)).to(dev)
+    tok = torch.remainder(tok, 2).to(torch.int32)                 # two-token alphabet: paths of a few nodes
+    acc, n_acc, _ = kdt.tree_accept(parent, tok, target)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    esz = 2 if case.dtype == "bf16" else 4
+    ops = {
+        "tree_build": (lambda: kdt.tree_build(ctok_d, lp_d, N), B * D * K * 8 + 4 * B * T * 4, "latency"),
+        "rope_neox": (lambda: kdt.rope_neox(pos, q=comb[..., 512:], k_pe=k_pe, prefix_len=prefix),
+                      2 * (B * T * H + B * T) * 64 * esz, "fp64"),
+        "tree_accept": (lambda: kdt.tree_accept(parent, tok, target), 3 * B * T * 4 + B * T * 4 + 8 * B, "latency"),
+        "kv_compact": (lambda: kdt.kv_compact(c_kv, k_pe, prefix, acc, n_acc, update_prefix=False),
+                       None, "latency"),
+    }
+    moved = int((n_acc - 1).clamp(min=0).sum().item())
+    peaks = load_peaks()
+    res = {}
+    for name, (fn, nbytes, bound) in ops.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        times = []
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) * 1e3)
+        if nbytes is None:
+            nbytes = 2 * moved * (512 + 64) * esz
+        us = statistics.mean(times)
+        res[name] = {"us": us, "us_median": statistics.median(times), "bytes": nbytes,
+                     "gbs": nbytes / (us * 1e-6) / 1e9, "frac_hbm": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                     "bound": bound}
+    res["rope_neox"]["fp64_flops"] = 6 * (B * T * H + B * T) * 32
+    return {"metric": "tree-step op time", "unit": "us", "higher_is_better": False, "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "dtype": "bf16" if case.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": workload_name(args.config), "B": B, "H": H, "T": T,
+                       "builder": {"depth": D, "per_depth": K, "nodes": N}, "accepted_rows_moved": moved,
+                       "l2": "flushed before each call"},
+            "ops": res, "hbm_peak_gbs": peaks["hbm_gbs"]}
+
+
 def workload_name(name):
     d = wl.CONFIGS[name]
     pre = d["prefix"]
@@ -219,6 +287,8 @@ def main():
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tree-ops", action="store_true",
+                    help="time the steps around verify (tree build, RoPE, accept, compaction) instead")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -253,6 +323,10 @@ def main():
     case = make_workload(args.config)
     counts = workload_counts(case)
     dev = torch.device("cuda", local_rank)
+    if args.tree_ops:
+        if rank == 0:
+            print(json.dumps(run_tree_ops(args, case, dev)), flush=True)
+        return 0
 
     def conv(x):
         if case.dtype == "bf16":

@@ -116,9 +116,9 @@ constexpr int kPBytes = kRows * kKeys * 2;        // P tile of one CTA: 32 KB (t
 constexpr int kPSlotBytes = kPBytes + 1024;       // 32 KB P + alpha[128] (+ pad to 1 KB alignment)
 constexpr uint32_t kPTx = kPBytes + kRows * 4;    // bytes copied into a P slot per block
 constexpr int kNS = 2;                            // S-CTA staging slots (free once the copy landed)
-constexpr int kNP = 3;                            // O-CTA P slots (free once P.V of the block ran)
+constexpr int kNP = 4;                            // O-CTA P slots (free once P.V of the block ran)
 constexpr int kVSlotBytes = 2 * kVSub;            // O ring slot: 128 keys x 128 latent dims
-constexpr int kNV = 3;                            // O-CTA value ring slots (96 KB)
+constexpr int kNV = 2;                            // O-CTA value ring slots (64 KB)
 constexpr uint32_t kCmdDone = 0xffffffffu;        // correction command: no more rescales
 constexpr uint64_t kWaitLimit = 200000000ull;     // ns a wait may poll before giving up
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
@@ -131,8 +131,8 @@ constexpr int kOffRRing = kOffKRing + kNK * kKSlotBytes;   // S: 4 x 8 KB rope k
 constexpr int kOffPStage = kOffRRing + kNR * kKSub;         // S: 2 x 33 KB staging of P + alpha
 constexpr int kOffRowMax = kOffPStage + kNS * kPSlotBytes;  // S: [2 blocks][2 halves][128] partial maxima
 constexpr int kOffLSum = kOffRowMax + 2 * 2 * kRows * 4;    // S: [128] partial row sums
-constexpr int kOffP = 0;                                    // O: 3 x 33 KB P + alpha
-constexpr int kOffV = kOffP + kNP * kPSlotBytes;            // O: 3 x 32 KB
+constexpr int kOffP = 0;                                    // O: 4 x 33 KB P + alpha
+constexpr int kOffV = kOffP + kNP * kPSlotBytes;            // O: 2 x 32 KB values
 constexpr int kOffStats = kOffV + kNV * kVSlotBytes;        // O: [2 items][128] x (m, l)
 constexpr int kOffEpi = kOffStats + 2 * kRows * 8;          // O: 4 x [32 rows][32 fp32] epilogue transpose
 constexpr int kSEnd = kOffLSum + kRows * 4;
