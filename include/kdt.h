@@ -255,11 +255,12 @@ typedef struct {
  * kdt_rope_neox -- NeoX rotary embedding in place (page "The Query-Split Kernel: A
  * Pivotal Edit ...", sections "The Reasoning Chain" -- rope applied in place on the rope
  * portion of the query buffer -- and "Input Knowledge" -- NeoX variant, float64 angles).
- * For a vector x of width d at position p and j < d/2, with a_j = p * base^(-2j/d) in
- * float64:
- *   (x_j, x_{j+d/2}) <- (x_j cos a_j - x_{j+d/2} sin a_j,  x_{j+d/2} cos a_j + x_j sin a_j),
- * products and sums rounded in float64, the results rounded once (to nearest) to the
- * element type. Every head of node (b,i) and its key row use pos[b,i].
+ * For a vector x of width d at position p and j < d/2: a_j = p * base^(-2j/d) in float64,
+ * c_j and s_j its cosine and sine rounded to float32, then in float32
+ *   (x_j, x_{j+d/2}) <- (x_j c_j - x_{j+d/2} s_j,  x_{j+d/2} c_j + x_j s_j),
+ * each product and sum rounded to nearest on its own (no fused multiply-add), the
+ * results rounded to nearest (even) to the element type. Every head of node (b,i) and
+ * its key row use pos[b,i].
  * Errors: KDT_ERR_NULL_ARG (pos NULL, both q and k_pe NULL, k_pe without prefix_len),
  * KDT_ERR_BAD_SHAPE, KDT_ERR_UNSUPPORTED (dtype), KDT_ERR_CUDA.
  */

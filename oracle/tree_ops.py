@@ -29,28 +29,33 @@ import numpy as np
 def rope_neox(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
     """NeoX rotary embedding ("The Query-Split Kernel: A Pivotal Edit ...", "Input
     Knowledge: What One Must Understand to Grasp This Edit": the vector is split in half
-    and each half is rotated by a position-dependent angle, the angles in float64).
+    and each half is rotated by a position-dependent angle, the angles taken in float64
+    to match a numpy reference; the engine itself computes in float32, "The Architecture
+    of an Inference Engine ...", "The Context: Building an Engine from Scratch").
 
-    For a vector x of even width d and position p: for j < d/2, with the frequency
-    w_j = base ** (-2 j / d) and the angle a_j = p * w_j,
-        y[j]       = x[j] cos a_j - x[j + d/2] sin a_j
-        y[j + d/2] = x[j + d/2] cos a_j + x[j] sin a_j.
-    x: float array [..., d]; pos: integer array of shape x.shape[:-1] (or broadcastable).
-    Returns float64 [..., d].
+    For a vector x of even width d (values exact in float32) at position p, and j < d/2:
+        w_j = base ** (-2 j / d),  a_j = p * w_j                      (float64)
+        c_j = fl32(cos a_j),  s_j = fl32(sin a_j)                       (float64, rounded once)
+        y[j]       = fl32( fl32(x[j] c_j)       - fl32(x[j + d/2] s_j) )
+        y[j + d/2] = fl32( fl32(x[j + d/2] c_j) + fl32(x[j] s_j) )
+    every float32 product and sum rounded to nearest on its own (no fused multiply-add).
+    x: array [..., d]; pos: integer array of shape x.shape[:-1] (or broadcastable).
+    Returns float32 [..., d].
     """
-    x = np.asarray(x, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float32)
     d = x.shape[-1]
     if d % 2:
         raise ValueError("rope width must be even")
     half = d // 2
     j = np.arange(half, dtype=np.float64)
-    w = np.power(float(base), -2.0 * j / d)                        # [half]
-    a = np.asarray(pos, dtype=np.float64)[..., None] * w          # [..., half]
-    c, s = np.cos(a), np.sin(a)
+    w = np.power(float(base), -2.0 * j / d)                        # [half], float64
+    a = np.asarray(pos, dtype=np.float64)[..., None] * w          # [..., half], float64
+    c = np.cos(a).astype(np.float32)
+    s = np.sin(a).astype(np.float32)
     x1, x2 = x[..., :half], x[..., half:]
-    y = np.empty_like(x)
-    y[..., :half] = x1 * c - x2 * s
-    y[..., half:] = x2 * c + x1 * s
+    y = np.empty(x.shape, dtype=np.float32)
+    y[..., :half] = (x1 * c) - (x2 * s)
+    y[..., half:] = (x2 * c) + (x1 * s)
     return y
 
 

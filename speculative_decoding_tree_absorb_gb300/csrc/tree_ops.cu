@@ -5,13 +5,14 @@
 //
 // RoPE: page "The Query-Split Kernel: A Pivotal Edit ...", sections "The Reasoning Chain"
 // (rope applied in place on the rope portion of the combined query buffer) and "Input
-// Knowledge" (NeoX variant, angles in float64). Accept and compaction: page "The Moment
+// Knowledge" (NeoX variant, angles in float64; the engine computes in float32). Accept and compaction: page "The Moment
 // of Truth: Validating a Custom CUDA Attention Kernel ...", section "Context" (a greedy
 // walk deciding which draft tokens are accepted), and page "The Architecture of an
 // Inference Engine ...", sections "The Context" and "Input Knowledge Required" (the
 // cache is compacted after acceptance to drop the unaccepted branches; the tree is built
 // best-first on the device instead of with a per-request CPU heap).
 #include <climits>
+#include <cmath>
 
 #include "kdt_internal.cuh"
 
@@ -20,37 +21,43 @@ namespace {
 
 constexpr int kMaxRopeHalf = 128;   // rope widths up to 256
 
-__device__ __forceinline__ double widen(float v) { return (double)v; }
-__device__ __forceinline__ double widen(__nv_bfloat16 v) { return (double)__bfloat162float(v); }
-template <typename E> __device__ __forceinline__ E narrow(double v);
-template <> __device__ __forceinline__ float narrow<float>(double v) { return __double2float_rn(v); }
-template <> __device__ __forceinline__ __nv_bfloat16 narrow<__nv_bfloat16>(double v) { return __double2bfloat16(v); }
+__device__ __forceinline__ float widen(float v) { return v; }
+__device__ __forceinline__ float widen(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename E> __device__ __forceinline__ E narrow(float v);
+template <> __device__ __forceinline__ float narrow<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 narrow<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-// One CTA per tree node (b, i). The node's angles a_j = pos * base^(-2j/d) and their
-// cosines and sines are taken once in float64; then every head's query vector and the
-// node's key row (cache row prefix_len[b] + i) are rotated in place: for j < d/2,
+// Angle frequencies w_j = base^(-2j/d), float64, computed on the host.
+struct RopeFreqs {
+    double w[kMaxRopeHalf];
+};
+
+// One CTA per tree node (b, i). Its angles a_j = pos * w_j are taken in float64 and their
+// cosines and sines rounded once to float32; then every head's query vector and the
+// node's key row (cache row prefix_len[b] + i) are rotated in place in float32: for j < d/2,
 //   (x_j, x_{j+d/2}) <- (x_j c_j - x_{j+d/2} s_j,  x_{j+d/2} c_j + x_j s_j),
-// each product and sum rounded in float64, the result rounded once to the element type.
-// A thread owns a whole pair, so the in-place update needs no synchronisation.
+// each product and sum rounded to nearest on its own (no fused multiply-add), the result
+// rounded once more to the element type. A thread owns a whole pair, so the in-place
+// update needs no synchronisation.
 template <typename E>
 __global__ void rope_neox_kernel(E *q, int64_t q_stride, int H, E *k_pe, int64_t L, const int32_t *prefix_len,
-                                 const int32_t *pos, int T, int d, double base) {
-    __shared__ double cs[kMaxRopeHalf], sn[kMaxRopeHalf];
+                                 const int32_t *pos, int T, int d, const __grid_constant__ RopeFreqs freqs) {
+    __shared__ float cs[kMaxRopeHalf], sn[kMaxRopeHalf];
     const int node = blockIdx.x;                       // b * T + i
     const int b = node / T, i = node - b * T;
     const int half = d / 2;
     const double p = (double)pos[node];
     for (int j = threadIdx.x; j < half; j += blockDim.x) {
-        const double a = p * pow(base, (-2.0 * (double)j) / (double)d);
-        cs[j] = cos(a);
-        sn[j] = sin(a);
+        const double a = p * freqs.w[j];
+        cs[j] = (float)cos(a);
+        sn[j] = (float)sin(a);
     }
     __syncthreads();
     auto rotate = [&](E *x, int j) {
-        const double x1 = widen(x[j]), x2 = widen(x[j + half]);
-        const double c = cs[j], s = sn[j];
-        x[j] = narrow<E>(__dsub_rn(__dmul_rn(x1, c), __dmul_rn(x2, s)));
-        x[j + half] = narrow<E>(__dadd_rn(__dmul_rn(x2, c), __dmul_rn(x1, s)));
+        const float x1 = widen(x[j]), x2 = widen(x[j + half]);
+        const float c = cs[j], s = sn[j];
+        x[j] = narrow<E>(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
+        x[j + half] = narrow<E>(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
     };
     if (q)
         for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
@@ -124,27 +131,27 @@ __global__ void kv_compact_kernel(uint4 *c_kv, uint4 *k_pe, int c_vec, int r_vec
 }
 
 // ------------------------------------------------------------ best-first builder --
-// A frontier entry: the candidate of rank `rank` at depth `depth` below node `par`.
-struct FrontierEntry {
-    float score;
-    int depth, par, rank;
-};
+// A frontier entry -- the candidate of rank `rank` at depth `depth` below node `par`,
+// with its path score -- packed into one 64-bit key whose unsigned order is the selection
+// order: higher score (high word: the float's bits mapped to an order-preserving integer,
+// complemented), then lower depth, lower parent, lower rank (low word). Entries are unique
+// in (depth, par, rank), so the warp minimum is one entry whatever the reduction order.
+__device__ __forceinline__ uint64_t pack_key(float score, int depth, int par, int rank) {
+    uint32_t u = __float_as_uint(score == 0.f ? 0.f : score);    // one zero
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);            // ascending with the float
+    return ((uint64_t)(~u) << 32) | ((uint32_t)depth << 17) | ((uint32_t)par << 5) | (uint32_t)rank;
+}
 
-// Selection order: higher score, then lower depth, lower parent, lower rank. Entries are
-// unique in (depth, par, rank), so this is a strict total order and the warp's argmin
-// does not depend on the reduction order.
-__device__ __forceinline__ bool before(const FrontierEntry &a, const FrontierEntry &b) {
-    if (a.score != b.score) return a.score > b.score;
-    if (a.depth != b.depth) return a.depth < b.depth;
-    if (a.par != b.par) return a.par < b.par;
-    return a.rank < b.rank;
+__device__ __forceinline__ float key_score(uint64_t key) {
+    const uint32_t u = ~(uint32_t)(key >> 32);
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
 constexpr int kMaxBuildDepth = 64, kMaxBuildK = 32, kMaxBuildN = kMaxT - 1;
 
 size_t build_smem_bytes(int D, int K, int N) {
     const size_t lists = (size_t)D * K * 8, scores = ((size_t)(N + 1) * 4 + 15) / 16 * 16;
-    return lists + scores + (size_t)(N + 2) * sizeof(FrontierEntry);
+    return lists + scores + (size_t)(N + 2) * sizeof(uint64_t);
 }
 
 // One warp per sequence. The candidates of every depth are ranked (log-probability
@@ -152,6 +159,7 @@ size_t build_smem_bytes(int D, int K, int N) {
 // in the tree, only its best child not yet taken: children below a node are ranked like
 // the candidates, so when a node's child of rank r joins, its sibling of rank r + 1 and
 // its own first child are pushed. That yields the same joins as pushing all children.
+// Each join is two warp-wide minimum reductions over the packed keys.
 __global__ void __launch_bounds__(32) tree_build_kernel(const int32_t *__restrict__ cand_tok,
                                                         const float *__restrict__ cand_lp, int D, int K, int N,
                                                         const int32_t *root_tok, int32_t *parent, int32_t *tok,
@@ -160,7 +168,7 @@ __global__ void __launch_bounds__(32) tree_build_kernel(const int32_t *__restric
     float *s_lp = reinterpret_cast<float *>(bsm);                      // [D][K] ranked
     int32_t *s_tok = reinterpret_cast<int32_t *>(s_lp + D * K);        // [D][K]
     float *n_score = reinterpret_cast<float *>(s_tok + D * K);         // [N + 1]
-    FrontierEntry *fr = reinterpret_cast<FrontierEntry *>(bsm + (size_t)D * K * 8 + ((size_t)(N + 1) * 4 + 15) / 16 * 16);
+    uint64_t *fr = reinterpret_cast<uint64_t *>(bsm + (size_t)D * K * 8 + ((size_t)(N + 1) * 4 + 15) / 16 * 16);
     const int b = blockIdx.x, lane = threadIdx.x;
     const int T = N + 1;
     const int64_t ob = (int64_t)b * T;
@@ -189,51 +197,39 @@ __global__ void __launch_bounds__(32) tree_build_kernel(const int32_t *__restric
         tok[ob] = root_tok ? root_tok[b] : -1;
         if (depth) depth[ob] = 0;
         if (score) score[ob] = 0.f;
-        fr[0] = FrontierEntry{__fadd_rn(0.f, s_lp[0]), 1, 0, 0};
+        fr[0] = pack_key(__fadd_rn(0.f, s_lp[0]), 1, 0, 0);
     }
     int F = 1;                                          // frontier size, the same in every lane
     __syncwarp();
     for (int n = 1; n < T && F > 0; ++n) {
-        int best = -1;
-        FrontierEntry be{0.f, 0, 0, 0};
+        uint64_t mine = ~0ull;
+        int slot = -1;
         for (int i = lane; i < F; i += 32) {
-            const FrontierEntry e = fr[i];
-            if (best < 0 || before(e, be)) {
-                best = i;
-                be = e;
+            const uint64_t k = fr[i];
+            if (k < mine) {
+                mine = k;
+                slot = i;
             }
         }
-        for (int off = 16; off; off >>= 1) {
-            FrontierEntry o;
-            const int oi = __shfl_down_sync(0xffffffffu, best, off);
-            o.score = __shfl_down_sync(0xffffffffu, be.score, off);
-            o.depth = __shfl_down_sync(0xffffffffu, be.depth, off);
-            o.par = __shfl_down_sync(0xffffffffu, be.par, off);
-            o.rank = __shfl_down_sync(0xffffffffu, be.rank, off);
-            if (lane + off < 32 && oi >= 0 && (best < 0 || before(o, be))) {
-                best = oi;
-                be = o;
-            }
-        }
-        best = __shfl_sync(0xffffffffu, best, 0);
-        be.score = __shfl_sync(0xffffffffu, be.score, 0);
-        be.depth = __shfl_sync(0xffffffffu, be.depth, 0);
-        be.par = __shfl_sync(0xffffffffu, be.par, 0);
-        be.rank = __shfl_sync(0xffffffffu, be.rank, 0);
-        __syncwarp();
-        const bool sib = be.rank + 1 < K, child = be.depth < D;
+        const uint32_t hi = __reduce_min_sync(0xffffffffu, (uint32_t)(mine >> 32));
+        const uint32_t lo = __reduce_min_sync(0xffffffffu, (uint32_t)(mine >> 32) == hi ? (uint32_t)mine : ~0u);
+        const uint64_t best = ((uint64_t)hi << 32) | lo;
+        const int owner = __ffs(__ballot_sync(0xffffffffu, mine == best)) - 1;
+        const int best_slot = __shfl_sync(0xffffffffu, slot, owner);
+        const float bscore = key_score(best);
+        const int bdepth = (int)(lo >> 17), bpar = (int)((lo >> 5) & 0xfffu), brank = (int)(lo & 31u);
+        const bool sib = brank + 1 < K, child = bdepth < D;
         if (lane == 0) {
-            fr[best] = fr[F - 1];                       // take the entry out
-            n_score[n] = be.score;
-            parent[ob + n] = be.par;
-            tok[ob + n] = s_tok[(be.depth - 1) * K + be.rank];
-            if (depth) depth[ob + n] = be.depth;
-            if (score) score[ob + n] = be.score;
+            fr[best_slot] = fr[F - 1];                  // take the entry out
+            n_score[n] = bscore;
+            parent[ob + n] = bpar;
+            tok[ob + n] = s_tok[(bdepth - 1) * K + brank];
+            if (depth) depth[ob + n] = bdepth;
+            if (score) score[ob + n] = bscore;
             int f = F - 1;
             if (sib)
-                fr[f++] = FrontierEntry{__fadd_rn(n_score[be.par], s_lp[(be.depth - 1) * K + be.rank + 1]), be.depth,
-                                        be.par, be.rank + 1};
-            if (child) fr[f++] = FrontierEntry{__fadd_rn(be.score, s_lp[be.depth * K]), be.depth + 1, n, 0};
+                fr[f++] = pack_key(__fadd_rn(n_score[bpar], s_lp[(bdepth - 1) * K + brank + 1]), bdepth, bpar, brank + 1);
+            if (child) fr[f++] = pack_key(__fadd_rn(bscore, s_lp[bdepth * K]), bdepth + 1, n, 0);
         }
         F = F - 1 + (sib ? 1 : 0) + (child ? 1 : 0);
         __syncwarp();
@@ -280,15 +276,17 @@ kdt_status kdt_rope_neox(const kdt_rope_args *a, cudaStream_t stream) {
     if (!a->pos || (!a->q && !a->k_pe)) return KDT_ERR_NULL_ARG;
     if (a->q && a->q_row_stride < a->D_r) return KDT_ERR_BAD_SHAPE;
     if (a->k_pe && (!a->prefix_len || a->kv_row_stride < a->T)) return a->prefix_len ? KDT_ERR_BAD_SHAPE : KDT_ERR_NULL_ARG;
+    RopeFreqs f;
+    for (int j = 0; j < a->D_r / 2; ++j) f.w[j] = pow(a->base, (-2.0 * (double)j) / (double)a->D_r);
     const int threads = 256;
     if (a->dtype == KDT_F32)
         rope_neox_kernel<float><<<a->B * a->T, threads, 0, stream>>>(
             static_cast<float *>(a->q), a->q_row_stride, a->H, static_cast<float *>(a->k_pe), a->kv_row_stride,
-            a->prefix_len, a->pos, a->T, a->D_r, a->base);
+            a->prefix_len, a->pos, a->T, a->D_r, f);
     else
         rope_neox_kernel<__nv_bfloat16><<<a->B * a->T, threads, 0, stream>>>(
             static_cast<__nv_bfloat16 *>(a->q), a->q_row_stride, a->H, static_cast<__nv_bfloat16 *>(a->k_pe),
-            a->kv_row_stride, a->prefix_len, a->pos, a->T, a->D_r, a->base);
+            a->kv_row_stride, a->prefix_len, a->pos, a->T, a->D_r, f);
     return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
 }
 

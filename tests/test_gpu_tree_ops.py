@@ -2,12 +2,13 @@
 compaction, through the C ABI, against the CPU oracle (oracle/tree_ops.py) on the same
 seeded inputs.
 
-Bars: accept and compaction are integer and copy work -- bit-exact. RoPE computes its
-angles, products and sums in float64 on both sides and rounds once to the element type;
-the two sides may differ only where the float64 cosine, sine or power of the GPU's math
-library and of the host's differ in the last bit and the result sits on a rounding
-boundary, so the bar is at most one unit in the last place of the element type, with
-every element that is not rotated bit-exact.
+Bars: accept, compaction and the tree builder are integer, copy and float32-sum work --
+bit-exact. RoPE takes its angles in float64 and rounds their cosines and sines to
+float32 on both sides, then does the same float32 operations; the two sides may differ
+only where the float64 cosine or sine of the GPU's math library and of the host's differ
+in the last bit and straddle a float32 rounding boundary, so the bar is at most one unit
+in the last place of the element type, with every element that is not rotated
+bit-exact.
 """
 import numpy as np
 import pytest
@@ -36,11 +37,12 @@ def _stored(seed, tag, shape, dtype):
 
 
 def _widen(a, dtype):
-    return a.astype(np.float64) if dtype == "f32" else wl.bf16_bits_to_f32(a).astype(np.float64)
+    return a.astype(np.float32) if dtype == "f32" else wl.bf16_bits_to_f32(a).astype(np.float32)
 
 
 def _round(x, dtype):
-    return x.astype(np.float32) if dtype == "f32" else wl.f64_to_bf16_bits(x)
+    """float32 oracle values to the element type as stored (bf16: round to nearest even)."""
+    return x.astype(np.float32) if dtype == "f32" else wl.f64_to_bf16_bits(x.astype(np.float64))
 
 
 def _to_dev(a, dtype):

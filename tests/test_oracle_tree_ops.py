@@ -19,52 +19,58 @@ def _vecs(seed, n, d):
 @pytest.mark.parametrize("d,base", [(2, 10000.0), (8, 10000.0), (64, 10000.0), (64, 50000.0)])
 def test_rope_matches_complex_exponential_form(d, base):
     # NeoX pairs element j with j + d/2: as a complex number z_j = x_j + i x_{j+d/2}, the
-    # rotation multiplies z_j by exp(i p w_j), w_j = 1 / base^(2j/d).
-    x = _vecs(1, 40, d)
+    # rotation multiplies z_j by exp(i p w_j), w_j = 1 / base^(2j/d). The oracle rounds
+    # cos, sin, each product and each sum to float32: a few float32 ulps of the result's
+    # scale apart from the exact value.
+    x = _vecs(1, 40, d).astype(np.float32)
     pos = np.arange(40) * 37 + 3
-    y = ot.rope_neox(x, pos, base)
+    y = ot.rope_neox(x, pos, base).astype(np.float64)
     inv_freq = 1.0 / (base ** (np.arange(0, d, 2, dtype=np.float64) / d))
-    z = (x[:, : d // 2] + 1j * x[:, d // 2:]) * np.exp(1j * pos[:, None] * inv_freq[None, :])
-    np.testing.assert_allclose(y[:, : d // 2], z.real, rtol=0, atol=1e-12)
-    np.testing.assert_allclose(y[:, d // 2:], z.imag, rtol=0, atol=1e-12)
+    z = (x[:, : d // 2] + 1j * x[:, d // 2:]).astype(np.complex128) * np.exp(1j * pos[:, None] * inv_freq[None, :])
+    scale = np.abs(x).max()
+    np.testing.assert_allclose(y[:, : d // 2], z.real, rtol=0, atol=4e-7 * scale)
+    np.testing.assert_allclose(y[:, d // 2:], z.imag, rtol=0, atol=4e-7 * scale)
 
 
 def test_rope_known_value_single_pair():
     # width 2: the only frequency is 1, so position 1 turns (1, 0) by one radian
     y = ot.rope_neox(np.array([[1.0, 0.0]]), np.array([1]), 10000.0)
-    np.testing.assert_allclose(y[0], [0.5403023058681398, 0.8414709848078965], rtol=0, atol=1e-15)
+    assert y.dtype == np.float32
+    assert y[0].tolist() == [np.float32(0.5403023058681398), np.float32(0.8414709848078965)]
 
 
 def test_rope_position_zero_is_identity():
-    x = _vecs(2, 16, 64)
+    x = _vecs(2, 16, 64).astype(np.float32)
     assert np.array_equal(ot.rope_neox(x, np.zeros(16, dtype=np.int64), 10000.0), x)
 
 
 def test_rope_preserves_pair_norms():
-    x = _vecs(3, 32, 64)
-    y = ot.rope_neox(x, np.arange(32) * 1000 + 17, 10000.0)
+    x = _vecs(3, 32, 64).astype(np.float32)
+    y = ot.rope_neox(x, np.arange(32) * 1000 + 17, 10000.0).astype(np.float64)
+    x = x.astype(np.float64)
     nx = x[:, :32] ** 2 + x[:, 32:] ** 2
     ny = y[:, :32] ** 2 + y[:, 32:] ** 2
-    np.testing.assert_allclose(ny, nx, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(ny, nx, rtol=2e-6, atol=1e-7)
 
 
 def test_rope_scores_depend_only_on_position_difference():
-    q = _vecs(4, 8, 64)
-    k = _vecs(5, 8, 64)
+    q = _vecs(4, 8, 64).astype(np.float32)
+    k = _vecs(5, 8, 64).astype(np.float32)
     m = np.array([0, 5, 100, 8192, 9000, 1, 77, 4096])
     n = np.array([3, 5, 90, 8000, 9000, 0, 70, 4100])
+    dot = lambda a, b: np.sum(a.astype(np.float64) * b.astype(np.float64), axis=1)
     for shift in (1, 1000, 20000):
-        a = np.sum(ot.rope_neox(q, m, 10000.0) * ot.rope_neox(k, n, 10000.0), axis=1)
-        b = np.sum(ot.rope_neox(q, m + shift, 10000.0) * ot.rope_neox(k, n + shift, 10000.0), axis=1)
-        np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-9)
+        a = dot(ot.rope_neox(q, m, 10000.0), ot.rope_neox(k, n, 10000.0))
+        b = dot(ot.rope_neox(q, m + shift, 10000.0), ot.rope_neox(k, n + shift, 10000.0))
+        np.testing.assert_allclose(a, b, rtol=1e-5, atol=1e-5)
 
 
 def test_rope_composes_additively():
-    x = _vecs(6, 12, 64)
+    x = _vecs(6, 12, 64).astype(np.float32)
     p = np.arange(12) * 311
     q = np.arange(12) * 97 + 5
     np.testing.assert_allclose(ot.rope_neox(ot.rope_neox(x, p, 10000.0), q, 10000.0),
-                               ot.rope_neox(x, p + q, 10000.0), rtol=1e-10, atol=1e-10)
+                               ot.rope_neox(x, p + q, 10000.0), rtol=1e-5, atol=1e-5)
 
 
 # --------------------------------------------------------------- positions --

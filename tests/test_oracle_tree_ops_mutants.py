@@ -13,10 +13,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(os.path.dirname(HERE), "oracle", "tree_ops.py")
 
 MUTANTS = {
-    "rope_sin_sign_second_half": ("y[..., half:] = x2 * c + x1 * s", "y[..., half:] = x2 * c - x1 * s"),
+    "rope_sin_sign_second_half": ("y[..., half:] = (x2 * c) + (x1 * s)", "y[..., half:] = (x2 * c) - (x1 * s)"),
     "rope_frequency_exponent": ("w = np.power(float(base), -2.0 * j / d)", "w = np.power(float(base), -1.0 * j / d)"),
     "rope_interleaved_pairs": ("x1, x2 = x[..., :half], x[..., half:]", "x1, x2 = x[..., 0::2], x[..., 1::2]"),
-    "rope_cos_sin_swapped": ("c, s = np.cos(a), np.sin(a)", "s, c = np.cos(a), np.sin(a)"),
+    "rope_cos_sin_swapped": ("c = np.cos(a).astype(np.float32)", "c = np.sin(a).astype(np.float32)"),
     "positions_root_depth_one": ("depth[b, i] = 0 if p < 0 else depth[b, p] + 1",
                                  "depth[b, i] = 1 if p < 0 else depth[b, p] + 1"),
     "accept_child_own_target": ("int(tok[b, c]) == int(target[b, cur])", "int(tok[b, c]) == int(target[b, c])"),
