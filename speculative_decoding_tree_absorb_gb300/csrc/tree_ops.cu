@@ -32,20 +32,25 @@ struct RopeFreqs {
     double w[kMaxRopeHalf];
 };
 
+// V consecutive elements of type E, loaded or stored as one aligned vector.
+template <typename E, int V> struct alignas(sizeof(E) * V) Vec {
+    E v[V];
+};
+
 // One CTA per tree node (b, i). Its angles a_j = pos * w_j are taken in float64 and their
 // cosines and sines rounded once to float32; then every head's query vector and the
 // node's key row (cache row prefix_len[b] + i) are rotated in place in float32: for j < d/2,
 //   (x_j, x_{j+d/2}) <- (x_j c_j - x_{j+d/2} s_j,  x_{j+d/2} c_j + x_j s_j),
 // each product and sum rounded to nearest on its own (no fused multiply-add), the result
-// rounded once more to the element type. A thread owns a whole pair, so the in-place
-// update needs no synchronisation.
-template <typename E>
+// rounded once more to the element type. A thread owns V whole pairs (j .. j+V-1, moved
+// as vectors when the rows allow), so the in-place update needs no synchronisation.
+template <typename E, int V>
 __global__ void rope_neox_kernel(E *q, int64_t q_stride, int H, E *k_pe, int64_t L, const int32_t *prefix_len,
                                  const int32_t *pos, int T, int d, const __grid_constant__ RopeFreqs freqs) {
     __shared__ float cs[kMaxRopeHalf], sn[kMaxRopeHalf];
     const int node = blockIdx.x;                       // b * T + i
     const int b = node / T, i = node - b * T;
-    const int half = d / 2;
+    const int half = d / 2, groups = half / V;
     const double p = (double)pos[node];
     for (int j = threadIdx.x; j < half; j += blockDim.x) {
         const double a = p * freqs.w[j];
@@ -53,21 +58,28 @@ __global__ void rope_neox_kernel(E *q, int64_t q_stride, int H, E *k_pe, int64_t
         sn[j] = (float)sin(a);
     }
     __syncthreads();
-    auto rotate = [&](E *x, int j) {
-        const float x1 = widen(x[j]), x2 = widen(x[j + half]);
-        const float c = cs[j], s = sn[j];
-        x[j] = narrow<E>(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
-        x[j + half] = narrow<E>(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
+    auto rotate = [&](E *x, int j0) {
+        Vec<E, V> a1 = *reinterpret_cast<const Vec<E, V> *>(x + j0);
+        Vec<E, V> a2 = *reinterpret_cast<const Vec<E, V> *>(x + j0 + half);
+#pragma unroll
+        for (int t = 0; t < V; ++t) {
+            const float x1 = widen(a1.v[t]), x2 = widen(a2.v[t]);
+            const float c = cs[j0 + t], s = sn[j0 + t];
+            a1.v[t] = narrow<E>(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
+            a2.v[t] = narrow<E>(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
+        }
+        *reinterpret_cast<Vec<E, V> *>(x + j0) = a1;
+        *reinterpret_cast<Vec<E, V> *>(x + j0 + half) = a2;
     };
     if (q)
-        for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
-            const int h = idx / half, j = idx - h * half;
-            rotate(q + ((int64_t)node * H + h) * q_stride, j);
+        for (int idx = threadIdx.x; idx < H * groups; idx += blockDim.x) {
+            const int h = idx / groups, j0 = (idx - h * groups) * V;
+            rotate(q + ((int64_t)node * H + h) * q_stride, j0);
         }
     if (k_pe) {
         const int64_t row = (int64_t)prefix_len[b] + i;
         if (row >= 0 && row < L)                       // the caller's bound; never write outside
-            for (int j = threadIdx.x; j < half; j += blockDim.x) rotate(k_pe + ((int64_t)b * L + row) * d, j);
+            for (int g = threadIdx.x; g < groups; g += blockDim.x) rotate(k_pe + ((int64_t)b * L + row) * d, g * V);
     }
 }
 
@@ -278,15 +290,29 @@ kdt_status kdt_rope_neox(const kdt_rope_args *a, cudaStream_t stream) {
     if (a->k_pe && (!a->prefix_len || a->kv_row_stride < a->T)) return a->prefix_len ? KDT_ERR_BAD_SHAPE : KDT_ERR_NULL_ARG;
     RopeFreqs f;
     for (int j = 0; j < a->D_r / 2; ++j) f.w[j] = pow(a->base, (-2.0 * (double)j) / (double)a->D_r);
-    const int threads = 256;
-    if (a->dtype == KDT_F32)
-        rope_neox_kernel<float><<<a->B * a->T, threads, 0, stream>>>(
-            static_cast<float *>(a->q), a->q_row_stride, a->H, static_cast<float *>(a->k_pe), a->kv_row_stride,
-            a->prefix_len, a->pos, a->T, a->D_r, f);
-    else
-        rope_neox_kernel<__nv_bfloat16><<<a->B * a->T, threads, 0, stream>>>(
-            static_cast<__nv_bfloat16 *>(a->q), a->q_row_stride, a->H, static_cast<__nv_bfloat16 *>(a->k_pe),
-            a->kv_row_stride, a->prefix_len, a->pos, a->T, a->D_r, f);
+    // 16-byte vectors when every half-row starts on a 16-byte boundary, else one pair a thread
+    const int esz = a->dtype == KDT_F32 ? 4 : 2, V = 16 / esz;
+    const bool vec = (a->D_r / 2) % V == 0 && (!a->q || (aligned16(a->q) && (a->q_row_stride * esz) % 16 == 0)) &&
+                     (!a->k_pe || aligned16(a->k_pe));
+    const int threads = 128;
+    const dim3 grid(a->B * a->T);
+    if (a->dtype == KDT_F32) {
+        float *q = static_cast<float *>(a->q), *k = static_cast<float *>(a->k_pe);
+        if (vec)
+            rope_neox_kernel<float, 4><<<grid, threads, 0, stream>>>(q, a->q_row_stride, a->H, k, a->kv_row_stride,
+                                                                     a->prefix_len, a->pos, a->T, a->D_r, f);
+        else
+            rope_neox_kernel<float, 1><<<grid, threads, 0, stream>>>(q, a->q_row_stride, a->H, k, a->kv_row_stride,
+                                                                     a->prefix_len, a->pos, a->T, a->D_r, f);
+    } else {
+        __nv_bfloat16 *q = static_cast<__nv_bfloat16 *>(a->q), *k = static_cast<__nv_bfloat16 *>(a->k_pe);
+        if (vec)
+            rope_neox_kernel<__nv_bfloat16, 8><<<grid, threads, 0, stream>>>(
+                q, a->q_row_stride, a->H, k, a->kv_row_stride, a->prefix_len, a->pos, a->T, a->D_r, f);
+        else
+            rope_neox_kernel<__nv_bfloat16, 1><<<grid, threads, 0, stream>>>(
+                q, a->q_row_stride, a->H, k, a->kv_row_stride, a->prefix_len, a->pos, a->T, a->D_r, f);
+    }
     return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
 }
 

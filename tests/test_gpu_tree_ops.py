@@ -325,3 +325,17 @@ def test_device_step_from_builder(kdt, oracle_mod):
     assert np.array_equal(bits(d["c_kv"]), rc)
     assert _ulp_diff(bits(d["k_pe"]), rk, "bf16").max() <= 1
     assert d["prefix_len"].cpu().numpy().tolist() == rp.tolist()
+
+
+def test_rope_unaligned_rows_take_the_scalar_path(kdt):
+    # rows whose rope part does not start on a 16-byte boundary are rotated one pair a thread
+    import torch
+    B, T, H, d = 2, 5, 3, 64
+    buf = _stored(13, "qu", (B, T, H, d + 2), "bf16")
+    dq = _to_dev(buf, "bf16")
+    pos = (np.arange(B * T, dtype=np.int32).reshape(B, T) * 13 + 1)
+    kdt.rope_neox(torch.from_numpy(pos).cuda(), q=dq[..., 1:1 + d], base=10000.0)
+    g = _from_dev(dq, "bf16")
+    ref = _round(ot.rope_neox(_widen(buf[..., 1:1 + d], "bf16"), pos[:, :, None], 10000.0), "bf16")
+    assert _ulp_diff(g[..., 1:1 + d], ref, "bf16").max() <= 1
+    assert np.array_equal(g[..., 0], buf[..., 0]) and np.array_equal(g[..., 1 + d], buf[..., 1 + d])
