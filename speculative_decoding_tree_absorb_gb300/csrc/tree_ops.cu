@@ -120,25 +120,47 @@ __global__ void tree_accept_kernel(const int32_t *__restrict__ parent, const int
     }
 }
 
-// One CTA per sequence; the k-th accepted node's rows move to cache row prefix + k, in
-// path order. Path nodes increase along the path (a parent precedes its children), so the
-// source of step k (row prefix + path[k] >= prefix + k) is never a row an earlier step
-// wrote, and the copy is safe in place with a barrier between steps. Entries outside the
-// tree or the cache are not copied.
-__global__ void kv_compact_kernel(uint4 *c_kv, uint4 *k_pe, int c_vec, int r_vec, int64_t L, int32_t *prefix_len,
-                                  const int32_t *acc_nodes, const int32_t *n_acc, int T, int update_prefix) {
+// One CTA per sequence; the k-th accepted node's rows move to cache row prefix + k. Path
+// nodes increase along the path (a parent precedes its children), so the source of step k
+// (row prefix + path[k] >= prefix + k) is never a row an earlier step wrote. The path is
+// moved in chunks of rows staged through shared memory: every source row of a chunk is
+// read before any of its destinations is written, and later chunks read no row an
+// earlier chunk wrote. Entries outside the tree or the cache are not copied.
+constexpr int kCompactSmem = 40 * 1024;
+
+__global__ void __launch_bounds__(256) kv_compact_kernel(uint4 *c_kv, uint4 *k_pe, int c_vec, int r_vec, int64_t L,
+                                                         int32_t *prefix_len, const int32_t *acc_nodes,
+                                                         const int32_t *n_acc, int T, int update_prefix) {
+    __shared__ uint4 stage[kCompactSmem / 16];
+    __shared__ int src_row[kCompactSmem / 32];
     const int b = blockIdx.x;
     const int64_t p0 = prefix_len[b];
     const int n = min(max(n_acc[b], 0), T);
-    for (int k = 1; k < n; ++k) {
-        const int src = acc_nodes[(int64_t)b * T + k];
-        if (src == k || src < k || src >= T || p0 + src >= L || p0 < 0) continue;   // same for every thread
-        const int64_t dst_row = (int64_t)b * L + p0 + k, src_row = (int64_t)b * L + p0 + src;
-        for (int v = threadIdx.x; v < c_vec; v += blockDim.x) c_kv[dst_row * c_vec + v] = c_kv[src_row * c_vec + v];
-        for (int v = threadIdx.x; v < r_vec; v += blockDim.x) k_pe[dst_row * r_vec + v] = k_pe[src_row * r_vec + v];
+    const int row_vec = c_vec + r_vec;
+    const int chunk = kCompactSmem / 16 / row_vec;      // rows staged at a time
+    for (int k0 = 1; k0 < n; k0 += chunk) {
+        const int kn = min(chunk, n - k0);
+        for (int t = threadIdx.x; t < kn; t += blockDim.x) {
+            const int k = k0 + t, src = acc_nodes[(int64_t)b * T + k];
+            src_row[t] = (src == k || src < k || src >= T || p0 + src >= L || p0 < 0) ? -1 : src;
+        }
+        __syncthreads();
+        for (int v = threadIdx.x; v < kn * row_vec; v += blockDim.x) {
+            const int t = v / row_vec, e = v - t * row_vec, src = src_row[t];
+            if (src < 0) continue;
+            const int64_t r = (int64_t)b * L + p0 + src;
+            stage[v] = e < c_vec ? c_kv[r * c_vec + e] : k_pe[r * r_vec + (e - c_vec)];
+        }
+        __syncthreads();
+        for (int v = threadIdx.x; v < kn * row_vec; v += blockDim.x) {
+            const int t = v / row_vec, e = v - t * row_vec;
+            if (src_row[t] < 0) continue;
+            const int64_t r = (int64_t)b * L + p0 + k0 + t;
+            if (e < c_vec) c_kv[r * c_vec + e] = stage[v];
+            else k_pe[r * r_vec + (e - c_vec)] = stage[v];
+        }
         __syncthreads();
     }
-    __syncthreads();
     if (update_prefix && threadIdx.x == 0) prefix_len[b] = (int32_t)(p0 + n);
 }
 
@@ -162,8 +184,11 @@ __device__ __forceinline__ float key_score(uint64_t key) {
 constexpr int kMaxBuildDepth = 64, kMaxBuildK = 32, kMaxBuildN = kMaxT - 1;
 
 size_t build_smem_bytes(int D, int K, int N) {
-    const size_t lists = (size_t)D * K * 8, scores = ((size_t)(N + 1) * 4 + 15) / 16 * 16;
-    return lists + scores + (size_t)(N + 2) * sizeof(uint64_t);
+    // n_score and the frontier also stage the unranked candidates before the joins start
+    const size_t lists = (size_t)D * K * 8;
+    const size_t scores = ((size_t)(N + 1 > D * K ? N + 1 : D * K) * 4 + 15) / 16 * 16;
+    const size_t frontier = (size_t)(N + 2 > (D * K + 1) / 2 ? N + 2 : (D * K + 1) / 2) * sizeof(uint64_t);
+    return lists + scores + frontier;
 }
 
 // One warp per sequence. The candidates of every depth are ranked (log-probability
@@ -180,17 +205,27 @@ __global__ void __launch_bounds__(32) tree_build_kernel(const int32_t *__restric
     float *s_lp = reinterpret_cast<float *>(bsm);                      // [D][K] ranked
     int32_t *s_tok = reinterpret_cast<int32_t *>(s_lp + D * K);        // [D][K]
     float *n_score = reinterpret_cast<float *>(s_tok + D * K);         // [N + 1]
-    uint64_t *fr = reinterpret_cast<uint64_t *>(bsm + (size_t)D * K * 8 + ((size_t)(N + 1) * 4 + 15) / 16 * 16);
+    const int n_score_len = N + 1 > D * K ? N + 1 : D * K;
+    uint64_t *fr = reinterpret_cast<uint64_t *>(bsm + (size_t)D * K * 8 + ((size_t)n_score_len * 4 + 15) / 16 * 16);
     const int b = blockIdx.x, lane = threadIdx.x;
     const int T = N + 1;
     const int64_t ob = (int64_t)b * T;
+    // every candidate of the sequence in one round of loads (the ranked lists are written
+    // over these staged copies only after all of them have been read into registers)
+    float *u_lp = n_score;                                             // [D][K] unranked, scratch
+    int32_t *u_tok = reinterpret_cast<int32_t *>(fr);                  // [D][K] unranked, scratch
+    for (int i = lane; i < D * K; i += 32) {
+        u_lp[i] = cand_lp[(int64_t)b * D * K + i];
+        u_tok[i] = cand_tok[(int64_t)b * D * K + i];
+    }
+    __syncwarp();
     for (int d = 0; d < D; ++d) {
         float v = -INFINITY;
         int32_t t = -1;
         if (lane < K) {
-            v = cand_lp[((int64_t)b * D + d) * K + lane];
+            v = u_lp[d * K + lane];
             if (v != v) v = -INFINITY;
-            t = cand_tok[((int64_t)b * D + d) * K + lane];
+            t = u_tok[d * K + lane];
         }
         int rank = 0;
         for (int j = 0; j < K; ++j) {
@@ -338,7 +373,8 @@ kdt_status kdt_kv_compact(void *c_kv, void *k_pe, kdt_dtype dtype, int D_c, int 
     if (B == 0) return KDT_OK;
     if (!c_kv || !k_pe || !prefix_len || !acc_nodes || !n_acc) return KDT_ERR_NULL_ARG;
     if (!aligned16(c_kv) || !aligned16(k_pe)) return KDT_ERR_BAD_SHAPE;
-    kv_compact_kernel<<<B, 128, 0, stream>>>(static_cast<uint4 *>(c_kv), static_cast<uint4 *>(k_pe),
+    if (((int64_t)D_c * esz + (int64_t)D_r * esz) > kCompactSmem) return KDT_ERR_BAD_SHAPE;
+    kv_compact_kernel<<<B, 256, 0, stream>>>(static_cast<uint4 *>(c_kv), static_cast<uint4 *>(k_pe),
                                              D_c * esz / 16, D_r * esz / 16, kv_row_stride, prefix_len, acc_nodes,
                                              n_acc, T, update_prefix ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
