@@ -19,7 +19,7 @@
  *  - "The Moment of Truth: Validating a Custom CUDA Attention Kernel ..." --
  *    section "Context": the visibility mask comes from the draft tree.
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *  - tree node t of sequence b sits at cache row prefix_len[b] + t; the root is
  *    tree query 0 (parent -1); kv_len = prefix_len + T;
  *  - lse is the natural log of the sum of exp over the SCALED scores of the
