@@ -52,6 +52,21 @@ TRAFFIC = {
 }
 
 
+def max_over_ranks(values, dist, device):
+    """Each rank's timings -> the slowest rank's, elementwise (one all-reduce)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_tflops(flops_per_rank, world, ms_slowest):
+    """Work of all ranks (weak scaling: each rank runs its own copy) over the slowest rank's time."""
+    return flops_per_rank * world / (ms_slowest * 1e-3) / 1e12
+
+
 def kernel_src_hash(impl):
     import hashlib
     csrc = os.path.join(ROOT, "speculative_decoding_tree_absorb_gb300", "csrc")
@@ -400,10 +415,7 @@ def main():
     ms = statistics.mean(step_ms)
     ms_attn = statistics.mean(attn_ms)
     ms_attn_median = statistics.median(attn_ms)
-    if dist is not None:
-        t = torch.tensor([ms, ms_attn], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_attn = float(t[0]), float(t[1])
+    ms, ms_attn = max_over_ranks([ms, ms_attn], dist, dev)
 
     # ---- end to end through the public API with host buffers ----------------------
     pinned = {k: v.pin_memory() for k, v in host.items()}
@@ -467,7 +479,7 @@ def main():
         e2e_step()
         torch.cuda.synchronize(dev)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e_mean = statistics.mean(e2e_ms)
+    e2e_mean = max_over_ranks([statistics.mean(e2e_ms)], dist, dev)[0]
 
     # ---- parity spot check of this very run against the oracle (a few rows) --------
     if rank != 0:
@@ -478,7 +490,7 @@ def main():
 
     flops = counts["flops"]
     peaks = load_peaks()
-    tflops = flops / (ms * 1e-3) / 1e12 * world
+    tflops = whole_job_tflops(flops, world, ms)
     attn_tflops = flops / (ms_attn * 1e-3) / 1e12
     if pl["impl"] == "tcgen05":
         peak = peaks["bf16_tflops"]
@@ -529,7 +541,7 @@ def main():
                      "kernel": f"verify_{pl['impl']} (+ split merge when num_splits > 1)"},
         "algorithmic": {"flops": flops, "bytes": counts["bytes"], "kv_bytes": counts["kv_bytes"]},
         "clocks": clocks,
-        "e2e": {"value": flops * world / (e2e_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": whole_job_tflops(flops, world, e2e_mean), "unit": "TFLOP/s",
                 "ms_per_step": e2e_mean, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipeline": f"{n_chunks} chunks of whole sequences; copy in, compute and copy out on three streams"},
         "gpu_launches": launches_per_step * args.steps,
