@@ -191,8 +191,27 @@ size_t build_smem_bytes(int D, int K, int N) {
     return lists + scores + frontier;
 }
 
-// One warp per sequence. The candidates of every depth are ranked (log-probability
-// descending, ties by position; NaN counts as -inf). The frontier holds, for every node
+// The candidates of every depth, staged unranked in u_lp / u_tok, ranked into s_lp / s_tok
+// (log-probability descending, ties by position; NaN counts as -inf). Every lane ranks
+// whole entries against the K entries of their depth, all of them at once.
+__device__ __forceinline__ void rank_candidates(const float *u_lp, const int32_t *u_tok, float *s_lp,
+                                                int32_t *s_tok, int D, int K, int lane) {
+    for (int i = lane; i < D * K; i += 32) {
+        const int d = i / K, r = i - d * K;
+        float v = u_lp[i];
+        if (v != v) v = -INFINITY;
+        int rank = 0;
+        for (int j = 0; j < K; ++j) {
+            float vj = u_lp[d * K + j];
+            if (vj != vj) vj = -INFINITY;
+            rank += (vj > v || (vj == v && j < r)) ? 1 : 0;
+        }
+        s_lp[d * K + rank] = v;
+        s_tok[d * K + rank] = u_tok[i];
+    }
+}
+
+// One warp per sequence. The candidates of every depth are ranked first. The frontier holds, for every node
 // in the tree, only its best child not yet taken: children below a node are ranked like
 // the candidates, so when a node's child of rank r joins, its sibling of rank r + 1 and
 // its own first child are pushed. That yields the same joins as pushing all children.
@@ -219,24 +238,7 @@ __global__ void __launch_bounds__(32) tree_build_kernel(const int32_t *__restric
         u_tok[i] = cand_tok[(int64_t)b * D * K + i];
     }
     __syncwarp();
-    for (int d = 0; d < D; ++d) {
-        float v = -INFINITY;
-        int32_t t = -1;
-        if (lane < K) {
-            v = u_lp[d * K + lane];
-            if (v != v) v = -INFINITY;
-            t = u_tok[d * K + lane];
-        }
-        int rank = 0;
-        for (int j = 0; j < K; ++j) {
-            const float vj = __shfl_sync(0xffffffffu, v, j);
-            rank += (vj > v || (vj == v && j < lane)) ? 1 : 0;
-        }
-        if (lane < K) {
-            s_lp[d * K + rank] = v;
-            s_tok[d * K + rank] = t;
-        }
-    }
+    rank_candidates(u_lp, u_tok, s_lp, s_tok, D, K, lane);
     __syncwarp();
     if (lane == 0) {
         n_score[0] = 0.f;
@@ -283,6 +285,100 @@ __global__ void __launch_bounds__(32) tree_build_kernel(const int32_t *__restric
     }
 }
 
+// The same joins for trees of at most 32 * R nodes with nothing but the ranked lists in
+// shared memory: frontier slot s, and node n's score and fields, live in register s / 32
+// (n / 32) of lane s % 32 (n % 32). A join is the two reductions, one shuffle for the
+// parent's score and two reads of the ranked lists, computed alike in every lane; the
+// taken slot is refilled in place with the next sibling (or, with no sibling left, the
+// first child) and the child takes a fresh slot when both are pushed. The tree is
+// written out once at the end, coalesced.
+template <int R>
+__global__ void __launch_bounds__(32) tree_build_reg_kernel(const int32_t *__restrict__ cand_tok,
+                                                            const float *__restrict__ cand_lp, int D, int K, int N,
+                                                            const int32_t *root_tok, int32_t *parent, int32_t *tok,
+                                                            int32_t *depth, float *score) {
+    extern __shared__ __align__(16) unsigned char bsm[];
+    float *s_lp = reinterpret_cast<float *>(bsm);                      // [D][K] ranked
+    int32_t *s_tok = reinterpret_cast<int32_t *>(s_lp + D * K);        // [D][K] ranked
+    float *u_lp = reinterpret_cast<float *>(s_tok + D * K);            // [D][K] unranked
+    int32_t *u_tok = reinterpret_cast<int32_t *>(u_lp + D * K);        // [D][K] unranked
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int T = N + 1;
+    for (int i = lane; i < D * K; i += 32) {
+        u_lp[i] = cand_lp[(int64_t)b * D * K + i];
+        u_tok[i] = cand_tok[(int64_t)b * D * K + i];
+    }
+    __syncwarp();
+    rank_candidates(u_lp, u_tok, s_lp, s_tok, D, K, lane);
+    __syncwarp();
+    uint64_t key[R];
+    float nsc[R];
+    int32_t npar[R], nsel[R];                           // node: parent, (depth << 5) | rank
+#pragma unroll R
+    for (int j = 0; j < R; ++j) {
+        key[j] = ~0ull;                                 // empty slot: above every packed entry
+        nsc[j] = 0.f;
+        npar[j] = -1;
+        nsel[j] = 0;
+    }
+    if (lane == 0) key[0] = pack_key(__fadd_rn(0.f, s_lp[0]), 1, 0, 0);
+    int F = 1, U = 1;                                   // live entries, slots used
+    int n = 1;
+    for (; n < T && F > 0; ++n) {
+        uint64_t mine = key[0];
+#pragma unroll R
+        for (int j = 1; j < R; ++j) mine = key[j] < mine ? key[j] : mine;
+        const uint32_t hi = __reduce_min_sync(0xffffffffu, (uint32_t)(mine >> 32));
+        const uint32_t lo = __reduce_min_sync(0xffffffffu, (uint32_t)(mine >> 32) == hi ? (uint32_t)mine : ~0u);
+        const uint64_t best = ((uint64_t)hi << 32) | lo;
+        const float bscore = key_score(best);
+        const int bdepth = (int)(lo >> 17), bpar = (int)((lo >> 5) & 0xfffu), brank = (int)(lo & 31u);
+        const bool sib = brank + 1 < K, child = bdepth < D;
+        float ps = 0.f;                                 // the parent's path score
+#pragma unroll R
+        for (int j = 0; j < R; ++j) {
+            const float v = __shfl_sync(0xffffffffu, nsc[j], bpar & 31);
+            if (j == (bpar >> 5)) ps = v;
+        }
+        const uint64_t ksib =
+            sib ? pack_key(__fadd_rn(ps, s_lp[(bdepth - 1) * K + brank + 1]), bdepth, bpar, brank + 1) : ~0ull;
+        const uint64_t kchild = child ? pack_key(__fadd_rn(bscore, s_lp[bdepth * K]), bdepth + 1, n, 0) : ~0ull;
+        const uint64_t refill = sib ? ksib : kchild;
+#pragma unroll R
+        for (int j = 0; j < R; ++j) {
+            if (key[j] == best) key[j] = refill;        // entries are unique: one slot in one lane
+            if (sib && child && j == (U >> 5) && lane == (U & 31)) key[j] = kchild;
+            if (j == (n >> 5) && lane == (n & 31)) {
+                nsc[j] = bscore;
+                npar[j] = bpar;
+                nsel[j] = (bdepth << 5) | brank;
+            }
+        }
+        U += (sib && child) ? 1 : 0;
+        F += (sib ? 1 : 0) + (child ? 1 : 0) - 1;
+    }
+    const int64_t ob = (int64_t)b * T;
+#pragma unroll R
+    for (int j = 0; j < R; ++j) {
+        const int m = 32 * j + lane;
+        if (m >= n) continue;                           // n: nodes joined (all T of them when the shape allows)
+        const int dm = nsel[j] >> 5;
+        parent[ob + m] = npar[j];
+        tok[ob + m] = m == 0 ? (root_tok ? root_tok[b] : -1) : s_tok[(dm - 1) * K + (nsel[j] & 31)];
+        if (depth) depth[ob + m] = dm;
+        if (score) score[ob + m] = nsc[j];
+    }
+}
+
+template <int R>
+kdt_status launch_build_reg(const int32_t *cand_tok, const float *cand_lp, int B, int D, int K, int N,
+                            const int32_t *root_tok, int32_t *parent, int32_t *tok, int32_t *depth, float *score,
+                            cudaStream_t stream) {
+    const size_t smem = (size_t)D * K * 16;             // ranked and unranked lists: at most 32 KB
+    tree_build_reg_kernel<R><<<B, 32, smem, stream>>>(cand_tok, cand_lp, D, K, N, root_tok, parent, tok, depth, score);
+    return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -305,6 +401,10 @@ kdt_status kdt_tree_build(const int32_t *cand_tok, const float *cand_lp, int B, 
     if (avail < N) return KDT_ERR_BAD_SHAPE;
     if (B == 0) return KDT_OK;
     if (!cand_tok || !cand_lp || !parent || !tok) return KDT_ERR_NULL_ARG;
+    if (N + 1 <= 32) return launch_build_reg<1>(cand_tok, cand_lp, B, D, K, N, root_tok, parent, tok, depth, score, stream);
+    if (N + 1 <= 64) return launch_build_reg<2>(cand_tok, cand_lp, B, D, K, N, root_tok, parent, tok, depth, score, stream);
+    if (N + 1 <= 128)
+        return launch_build_reg<4>(cand_tok, cand_lp, B, D, K, N, root_tok, parent, tok, depth, score, stream);
     const size_t smem = build_smem_bytes(D, K, N);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

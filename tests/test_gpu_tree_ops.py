@@ -255,9 +255,13 @@ def _cand(seed, B, D, K, quant):
     return tok, lp.astype(np.float32)
 
 
+# N + 1 <= 32, 64, 128 take the register-resident kernel (one, two, four slots a lane),
+# larger trees the shared-memory one; the cases sit on both sides of each boundary, and
+# (3, 2, 5, 30) and (2, 1, 32, 32) use up every candidate.
 @pytest.mark.parametrize("B,D,K,N,quant", [(4, 8, 4, 63, False), (2, 16, 8, 255, False), (3, 4, 3, 60, True),
                                            (2, 5, 1, 5, False), (2, 3, 3, 39, True), (1, 64, 32, 4095, False),
-                                           (5, 12, 6, 127, True)])
+                                           (5, 12, 6, 127, True), (2, 6, 2, 31, False), (2, 7, 3, 64, True),
+                                           (2, 9, 2, 128, False), (3, 2, 5, 30, False), (2, 1, 32, 32, True)])
 def test_build_bit_exact(kdt, B, D, K, N, quant):
     import torch
     tok, lp = _cand(D * 100 + K, B, D, K, quant)
