@@ -302,6 +302,8 @@ def main():
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="chunks the end-to-end step is cut into (a divisor of B; default 4, else 2, else 1)")
     ap.add_argument("--tree-ops", action="store_true",
                     help="time the steps around verify (tree build, RoPE, accept, compaction) instead")
     args = ap.parse_args()
@@ -418,70 +420,106 @@ def main():
     ms, ms_attn = max_over_ranks([ms, ms_attn], dist, dev)
 
     # ---- end to end through the public API with host buffers ----------------------
-    pinned = {k: v.pin_memory() for k, v in host.items()}
-    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    # The step is cut into chunks of whole sequences (four by default): a
+    # chunk's inputs sit contiguous in one pinned host region and go in with one copy, its out
+    # and lse come back with one copy, and the chunk's kdt_build_visibility +
+    # kdt_verify_attn read views of the device copy. The copy of
+    # chunk k+1 in, the compute of chunk k and the copy of chunk k-1 out overlap on three
+    # streams (the host link, not the kernels, sets the pace).
+    def region(parts):
+        offs, off = {}, 0
+        for name, nbytes in parts:
+            offs[name] = (off, nbytes)
+            off += (nbytes + 255) // 256 * 256
+        return offs, off
 
-    # The step is cut into chunks of whole sequences (each chunk an independent
-    # kdt_build_visibility + kdt_verify_attn call on views of the same buffers), so that
-    # the copy of chunk k+1 in, the compute of chunk k and the copy of chunk k-1 out
-    # overlap on three streams.
-    n_chunks = min(B, 4)
-    bounds = [(B * k // n_chunks, B * (k + 1) // n_chunks) for k in range(n_chunks)]
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    def as_bytes(t):
+        return t.contiguous().view(-1).view(torch.uint8)
+
+    # four: enough overlap, while the host still queues a chunk faster than the link moves it
+    # (eight one-sequence chunks leave the host the slower side)
+    n_chunks = args.e2e_chunks or next(c for c in (4, 2, 1) if B % c == 0)
+    if n_chunks < 1 or B % n_chunks:
+        raise SystemExit("--e2e-chunks must divide B")
+    nb = B // n_chunks                                # sequences per chunk
+    in_offs, in_bytes = region([(k_, as_bytes(v[:nb]).numel()) for k_, v in host.items()])
+    out_offs, out_bytes = region([("out", nb * T * H * 512 * 4), ("lse", nb * T * H * 4)])
+    in_h = torch.empty((n_chunks, in_bytes), dtype=torch.uint8).pin_memory()
+    for c in range(n_chunks):
+        for k_, v in host.items():
+            o_, n_ = in_offs[k_]
+            in_h[c, o_:o_ + n_].copy_(as_bytes(v[c * nb:(c + 1) * nb]))
+    in_d = torch.empty((n_chunks, in_bytes), dtype=torch.uint8, device=dev)
+    out_h = torch.empty((n_chunks, out_bytes), dtype=torch.uint8).pin_memory()
+    out_d = torch.empty((n_chunks, out_bytes), dtype=torch.uint8, device=dev)
+    h2d = n_chunks * in_bytes
+    d2h = n_chunks * out_bytes
+
+    def view(buf, offs, name, dtype, shape):
+        o_, n_ = offs[name]
+        return buf[o_:o_ + n_].view(dtype).view(shape)
+
     chunk_calls = []
-    for b0, b1 in bounds:
-        ca = kdt.make_args(d["q_nope"][b0:b1], d["q_pe"][b0:b1], d["c_kv"][b0:b1], d["k_pe"][b0:b1],
-                           d["prefix_len"][b0:b1], vis=vis[b0:b1], max_kv_len=case.max_kv_len, scale=case.scale,
-                           out=out[b0:b1], lse=lse[b0:b1], err=err, impl=args.kernel_impl,
-                           num_splits=args.num_splits)
+    for c in range(n_chunks):
+        dv = {k_: view(in_d[c], in_offs, k_, v.dtype, (nb,) + tuple(v.shape[1:])) for k_, v in host.items()}
+        o_c = view(out_d[c], out_offs, "out", torch.float32, (nb, T, H, 512))
+        l_c = view(out_d[c], out_offs, "lse", torch.float32, (nb, T, H))
+        vis_c = vis[c * nb:(c + 1) * nb]
+        ca = kdt.make_args(dv["q_nope"], dv["q_pe"], dv["c_kv"], dv["k_pe"], dv["prefix_len"], vis=vis_c,
+                           max_kv_len=case.max_kv_len, scale=case.scale, out=o_c, lse=l_c, err=err,
+                           impl=args.kernel_impl, num_splits=args.num_splits)
         if kdt.workspace_size(ca) > ws_n:
             raise SystemExit("chunk workspace larger than the full call's")
-        chunk_calls.append((b0, b1, ca, ctypes.c_void_p(d["parent"][b0:b1].data_ptr()),
-                            ctypes.c_void_p(vis[b0:b1].data_ptr())))
+        chunk_calls.append((ca, ctypes.c_void_p(dv["parent"].data_ptr()), ctypes.c_void_p(vis_c.data_ptr())))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    done_in = [torch.cuda.Event() for _ in range(n_chunks)]
+    done_comp = [torch.cuda.Event() for _ in range(n_chunks)]
 
     def e2e_step():
-        done_in, done_comp = [], []
         s_in.wait_stream(stream)                      # the previous step has read its inputs
         stream.wait_stream(s_out)                     # ... and its outputs have been copied out
         with torch.cuda.stream(s_in):
-            for b0, b1 in bounds:
-                for k_, v in pinned.items():
-                    d[k_][b0:b1].copy_(v[b0:b1], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(s_in)
-                done_in.append(e)
-        for (b0, b1, ca, par_p, vis_p), e in zip(chunk_calls, done_in):
-            stream.wait_event(e)
-            st = lib.kdt_build_visibility(par_p, b1 - b0, T, vis_p, err_ptr, sptr)
+            for b in range(n_chunks):
+                in_d[b].copy_(in_h[b], non_blocking=True)
+                done_in[b].record(s_in)
+        # each chunk's copy out is queued right behind its compute, so it can start while the
+        # host is still queueing the later chunks
+        for b, (ca, par_p, vis_p) in enumerate(chunk_calls):
+            stream.wait_event(done_in[b])
+            st = lib.kdt_build_visibility(par_p, nb, T, vis_p, err_ptr, sptr)
             st2 = lib.kdt_verify_attn(ctypes.byref(ca), ws_ptr, ws_n, sptr)
             if st or st2:
                 raise kdt.KdtError(st or st2, "e2e chunk")
-            e2 = torch.cuda.Event()
-            e2.record(stream)
-            done_comp.append(e2)
-        with torch.cuda.stream(s_out):
-            for (b0, b1), e2 in zip(bounds, done_comp):
-                s_out.wait_event(e2)
-                out_h[b0:b1].copy_(out[b0:b1], non_blocking=True)
-                lse_h[b0:b1].copy_(lse[b0:b1], non_blocking=True)
+            done_comp[b].record(stream)
+            s_out.wait_event(done_comp[b])
+            with torch.cuda.stream(s_out):
+                out_h[b].copy_(out_d[b], non_blocking=True)
 
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize(dev)
-    e2e_ms = []
+    e2e_ms, enq_ms = [], []
     for _ in range(max(3, min(args.steps, 10))):
         flush.fill_(1)
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         e2e_step()
+        enq_ms.append((time.perf_counter() - t0) * 1e3)
         torch.cuda.synchronize(dev)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    # the host copy of the chunked run against the device-timed call on the same inputs: the
+    # work splits differ (and with them the bf16 rounding of P), so they agree within the
+    # path's own tolerance, not bit for bit
+    o_, n_ = out_offs["out"]
+    e2e_out = out_h[:, o_:o_ + n_].contiguous().view(torch.float32).view(B, T, H, 512)   # chunks in order
+    ref_out = out.cpu()
+    tol = 2e-2 if case.dtype == "bf16" else 1e-4
+    e2e_diff = (e2e_out - ref_out).abs()
+    if bool((e2e_diff > tol + tol * ref_out.abs()).any()):
+        raise SystemExit(f"end-to-end output differs from the device-timed call by {e2e_diff.max().item()}")
+    e2e_check = {"max_abs_diff": e2e_diff.max().item(), "mean_abs_diff": e2e_diff.mean().item()}
     e2e_mean = max_over_ranks([statistics.mean(e2e_ms)], dist, dev)[0]
 
-    # ---- parity spot check of this very run against the oracle (a few rows) --------
     if rank != 0:
         if dist is not None:
             dist.barrier()
@@ -543,7 +581,9 @@ def main():
         "clocks": clocks,
         "e2e": {"value": whole_job_tflops(flops, world, e2e_mean), "unit": "TFLOP/s",
                 "ms_per_step": e2e_mean, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipeline": f"{n_chunks} chunks of whole sequences; copy in, compute and copy out on three streams"},
+                "pipeline": f"{n_chunks} chunks of {nb} sequence(s), one copy in and one copy out each; copy "
+                            f"in, compute and copy out on three streams",
+                "host_enqueue_ms": statistics.mean(enq_ms), "vs_device_call": e2e_check},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu_baseline,
         "wall_s_timed": t_wall,
