@@ -303,7 +303,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=0,
-                    help="chunks the end-to-end step is cut into (a divisor of B; default 4, else 2, else 1)")
+                    help="chunks kdt_verify_attn_host cuts the end-to-end step into (a divisor of B; "
+                         "default 4, else 2, else 1)")
     ap.add_argument("--tree-ops", action="store_true",
                     help="time the steps around verify (tree build, RoPE, accept, compaction) instead")
     args = ap.parse_args()
@@ -419,81 +420,33 @@ def main():
     ms_attn_median = statistics.median(attn_ms)
     ms, ms_attn = max_over_ranks([ms, ms_attn], dist, dev)
 
-    # ---- end to end through the public API with host buffers ----------------------
-    # The step is cut into chunks of whole sequences (four by default): a
-    # chunk's inputs sit contiguous in one pinned host region and go in with one copy, its out
-    # and lse come back with one copy, and the chunk's kdt_build_visibility +
-    # kdt_verify_attn read views of the device copy. The copy of
-    # chunk k+1 in, the compute of chunk k and the copy of chunk k-1 out overlap on three
-    # streams (the host link, not the kernels, sets the pace).
-    def region(parts):
-        offs, off = {}, 0
-        for name, nbytes in parts:
-            offs[name] = (off, nbytes)
-            off += (nbytes + 255) // 256 * 256
-        return offs, off
-
-    def as_bytes(t):
-        return t.contiguous().view(-1).view(torch.uint8)
-
-    # four: enough overlap, while the host still queues a chunk faster than the link moves it
-    # (eight one-sequence chunks leave the host the slower side)
+    # ---- end to end through the C ABI with host buffers ------------------------------
+    # kdt_verify_attn_host: pinned host tensors in, host out and lse back. The library cuts
+    # the batch into chunks of whole sequences and overlaps each chunk's copy in, compute and
+    # copy out on three streams (the host link, not the kernels, sets the pace).
+    pinned = {k_: v.contiguous().pin_memory() for k_, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
     n_chunks = args.e2e_chunks or next(c for c in (4, 2, 1) if B % c == 0)
     if n_chunks < 1 or B % n_chunks:
         raise SystemExit("--e2e-chunks must divide B")
-    nb = B // n_chunks                                # sequences per chunk
-    in_offs, in_bytes = region([(k_, as_bytes(v[:nb]).numel()) for k_, v in host.items()])
-    out_offs, out_bytes = region([("out", nb * T * H * 512 * 4), ("lse", nb * T * H * 4)])
-    in_h = torch.empty((n_chunks, in_bytes), dtype=torch.uint8).pin_memory()
-    for c in range(n_chunks):
-        for k_, v in host.items():
-            o_, n_ = in_offs[k_]
-            in_h[c, o_:o_ + n_].copy_(as_bytes(v[c * nb:(c + 1) * nb]))
-    in_d = torch.empty((n_chunks, in_bytes), dtype=torch.uint8, device=dev)
-    out_h = torch.empty((n_chunks, out_bytes), dtype=torch.uint8).pin_memory()
-    out_d = torch.empty((n_chunks, out_bytes), dtype=torch.uint8, device=dev)
-    h2d = n_chunks * in_bytes
-    d2h = n_chunks * out_bytes
-
-    def view(buf, offs, name, dtype, shape):
-        o_, n_ = offs[name]
-        return buf[o_:o_ + n_].view(dtype).view(shape)
-
-    chunk_calls = []
-    for c in range(n_chunks):
-        dv = {k_: view(in_d[c], in_offs, k_, v.dtype, (nb,) + tuple(v.shape[1:])) for k_, v in host.items()}
-        o_c = view(out_d[c], out_offs, "out", torch.float32, (nb, T, H, 512))
-        l_c = view(out_d[c], out_offs, "lse", torch.float32, (nb, T, H))
-        vis_c = vis[c * nb:(c + 1) * nb]
-        ca = kdt.make_args(dv["q_nope"], dv["q_pe"], dv["c_kv"], dv["k_pe"], dv["prefix_len"], vis=vis_c,
-                           max_kv_len=case.max_kv_len, scale=case.scale, out=o_c, lse=l_c, err=err,
-                           impl=args.kernel_impl, num_splits=args.num_splits)
-        if kdt.workspace_size(ca) > ws_n:
-            raise SystemExit("chunk workspace larger than the full call's")
-        chunk_calls.append((ca, ctypes.c_void_p(dv["parent"].data_ptr()), ctypes.c_void_p(vis_c.data_ptr())))
+    ah = kdt.make_args(pinned["q_nope"], pinned["q_pe"], pinned["c_kv"], pinned["k_pe"], pinned["prefix_len"],
+                       parent=pinned["parent"], max_kv_len=case.max_kv_len, scale=case.scale, out=out_h, lse=lse_h,
+                       err=err, impl=args.kernel_impl, num_splits=args.num_splits)
+    dev_n = kdt.host_buffer_size(ah, n_chunks)
+    if dev_n == 0:
+        raise SystemExit("kdt_verify_attn_host rejected the arguments")
+    dev_buf = torch.empty(dev_n, dtype=torch.uint8, device=dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    done_in = [torch.cuda.Event() for _ in range(n_chunks)]
-    done_comp = [torch.cuda.Event() for _ in range(n_chunks)]
+    host_streams = [ctypes.c_void_p(x.cuda_stream) for x in (stream, s_in, s_out)]
+    dev_ptr = ctypes.c_void_p(dev_buf.data_ptr())
 
     def e2e_step():
-        s_in.wait_stream(stream)                      # the previous step has read its inputs
-        stream.wait_stream(s_out)                     # ... and its outputs have been copied out
-        with torch.cuda.stream(s_in):
-            for b in range(n_chunks):
-                in_d[b].copy_(in_h[b], non_blocking=True)
-                done_in[b].record(s_in)
-        # each chunk's copy out is queued right behind its compute, so it can start while the
-        # host is still queueing the later chunks
-        for b, (ca, par_p, vis_p) in enumerate(chunk_calls):
-            stream.wait_event(done_in[b])
-            st = lib.kdt_build_visibility(par_p, nb, T, vis_p, err_ptr, sptr)
-            st2 = lib.kdt_verify_attn(ctypes.byref(ca), ws_ptr, ws_n, sptr)
-            if st or st2:
-                raise kdt.KdtError(st or st2, "e2e chunk")
-            done_comp[b].record(stream)
-            s_out.wait_event(done_comp[b])
-            with torch.cuda.stream(s_out):
-                out_h[b].copy_(out_d[b], non_blocking=True)
+        st = lib.kdt_verify_attn_host(ctypes.byref(ah), n_chunks, dev_ptr, dev_n, *host_streams)
+        if st != 0:
+            raise kdt.KdtError(st, "kdt_verify_attn_host")
 
     for _ in range(2):
         e2e_step()
@@ -510,8 +463,7 @@ def main():
     # the host copy of the chunked run against the device-timed call on the same inputs: the
     # work splits differ (and with them the bf16 rounding of P), so they agree within the
     # path's own tolerance, not bit for bit
-    o_, n_ = out_offs["out"]
-    e2e_out = out_h[:, o_:o_ + n_].contiguous().view(torch.float32).view(B, T, H, 512)   # chunks in order
+    e2e_out = out_h
     ref_out = out.cpu()
     tol = 2e-2 if case.dtype == "bf16" else 1e-4
     e2e_diff = (e2e_out - ref_out).abs()
@@ -581,8 +533,8 @@ def main():
         "clocks": clocks,
         "e2e": {"value": whole_job_tflops(flops, world, e2e_mean), "unit": "TFLOP/s",
                 "ms_per_step": e2e_mean, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipeline": f"{n_chunks} chunks of {nb} sequence(s), one copy in and one copy out each; copy "
-                            f"in, compute and copy out on three streams",
+                "pipeline": f"kdt_verify_attn_host: {n_chunks} chunks of {B // n_chunks} sequence(s); copy in, "
+                            f"compute and copy out on three streams",
                 "host_enqueue_ms": statistics.mean(enq_ms), "vs_device_call": e2e_check},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu_baseline,

@@ -23,15 +23,17 @@
  *
  * Conventions for every entry point:
  *  - All tensor arguments are caller-owned DEVICE pointers, row-major and
- *    contiguous, 16-byte aligned, with no aliasing between inputs and outputs.
+ *    contiguous, 16-byte aligned, with no aliasing between inputs and outputs
+ *    (kdt_verify_attn_host alone takes host tensors).
  *  - Calls are asynchronous on `stream` (0 = legacy default stream). Argument
  *    checks run on the host before any launch and never synchronise. A launch
  *    failure is returned as KDT_ERR_CUDA; faults inside a kernel surface at the
  *    caller's next synchronisation.
  *  - The library allocates no memory: scratch space is the caller's `workspace`
  *    (kdt_verify_attn_noalloc, at the end, uses a fixed array inside the library
- *    instead). It keeps no other global state than a per-device cache of the SM
- *    count. Concurrent calls are safe given distinct workspaces.
+ *    instead; kdt_verify_attn_host creates and releases its events). It keeps no
+ *    other global state than a per-device cache of the SM count. Concurrent calls
+ *    are safe given distinct workspaces.
  *  - Errors found in the DATA on the device (a malformed tree) are reported
  *    through a caller-provided device word `err` (0 = ok, else 1 + the flat index
  *    b*T + i of the first offending parent entry), never by a trap.
@@ -155,6 +157,53 @@ typedef struct {
 } kdt_plan;
 
 kdt_status kdt_verify_attn_plan(const kdt_verify_args *a, kdt_plan *plan);
+
+/*
+ * kdt_verify_attn_host -- kdt_verify_attn on HOST buffers, the copies pipelined with
+ * the compute.
+ *
+ * Same arguments and results as kdt_verify_attn, except that q_nope, q_pe, c_kv,
+ * k_pe, prefix_len, parent (or vis), out and lse are HOST pointers; `err`, when
+ * given, stays a DEVICE word with the same meaning (flat index over the whole
+ * batch). Host rows must be contiguous (both row strides 0) and every host tensor
+ * 16-byte aligned. For the copies to overlap the host buffers must be page-locked
+ * (cudaHostAlloc, cudaHostRegister, a pinned torch tensor); pageable buffers give
+ * the same results with the copies serialised.
+ *
+ * The B sequences are cut into n_chunks chunks of B / n_chunks whole sequences
+ * (n_chunks must divide B; 0 = 4, else 2, else 1). Every chunk's inputs are copied
+ * into `dev_buf` on stream_in (one copy per tensor); chunk c's attention (with its
+ * visibility bits when parent is given) runs on `stream` once its inputs landed; its
+ * out and lse are copied back on stream_out right behind it. So the copy of chunk c+1
+ * in, the compute of chunk c and the copy of chunk c-1 out overlap, and the host link
+ * sets the pace. The chunks' results are those of kdt_verify_attn called on each
+ * chunk: they agree with one call over the whole batch within the path's tolerance
+ * (the work split differs), not bit for bit.
+ *
+ *   dev_buf     device scratch of kdt_verify_attn_host_buffer_size(a, n_chunks)
+ *               bytes, 256-byte aligned, no initialisation needed: every chunk's
+ *               inputs and outputs, one error word per chunk, one verify workspace.
+ *   stream      carries the compute; the call is complete -- out and lse written
+ *               on the host -- once `stream` reaches the point after the call
+ *               (synchronise it, or an event recorded on it, before reading out).
+ *               The copies in wait for the work queued on `stream` before the call.
+ *   stream_in, stream_out
+ *               two more streams, distinct from each other and from `stream`. They
+ *               should be non-blocking (cudaStreamNonBlocking) and `stream` not the
+ *               legacy default stream with blocking streams, or the copies and the
+ *               compute serialise (the results are the same).
+ * The library creates 2 * n_chunks + 2 events per call and releases them before it
+ * returns (the driver frees them once they complete).
+ * Errors: those of kdt_verify_attn; KDT_ERR_BAD_SHAPE also for an n_chunks that
+ * does not divide B, a nonzero row stride, or two equal streams; KDT_ERR_WORKSPACE
+ * for a missing, short or misaligned dev_buf.
+ */
+kdt_status kdt_verify_attn_host(const kdt_verify_args *a, int n_chunks, void *dev_buf, size_t dev_bytes,
+                                cudaStream_t stream, cudaStream_t stream_in, cudaStream_t stream_out);
+
+/* Bytes of dev_buf kdt_verify_attn_host needs for these (host-pointer) arguments and
+ * chunk count; 0 for arguments it would reject (and for B = 0). */
+size_t kdt_verify_attn_host_buffer_size(const kdt_verify_args *a, int n_chunks);
 
 /*
  * kdt_merge_attn_states -- combine two attention results over DISJOINT key sets

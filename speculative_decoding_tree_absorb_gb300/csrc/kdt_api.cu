@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <math.h>
+#include <vector>
 
 namespace kdt {
 
@@ -138,6 +139,85 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     return KDT_OK;
 }
 
+// ---------------------------------------------------------------- host entry --
+// Device buffer of kdt_verify_attn_host: for every chunk of nb sequences its inputs, its
+// out/lse, then one error word per chunk and one verify workspace the chunks share (their
+// computes run in order on one stream). Every region starts on a 256-byte boundary.
+struct HostLayout {
+    int chunks = 0, nb = 0;
+    size_t b_qn = 0, b_qp = 0, b_kv = 0, b_kp = 0, b_pre = 0, b_tree = 0, b_out = 0, b_lse = 0;
+    size_t o_qn = 0, o_qp = 0, o_kv = 0, o_kp = 0, o_pre = 0, o_tree = 0, o_out = 0, o_lse = 0;
+    size_t chunk = 0, errs_off = 0, ws_off = 0, ws_bytes = 0, total = 0;
+};
+
+// Chunk c's arguments: the caller's, with B = nb and every tensor in the device buffer.
+kdt_verify_args chunk_args(const kdt_verify_args *a, const HostLayout &L, unsigned char *base, int c) {
+    unsigned char *ch = base + (size_t)c * L.chunk;
+    kdt_verify_args d = *a;
+    d.B = L.nb;
+    d.q_nope = ch + L.o_qn;
+    d.q_pe = ch + L.o_qp;
+    d.c_kv = ch + L.o_kv;
+    d.k_pe = ch + L.o_kp;
+    d.prefix_len = reinterpret_cast<const int32_t *>(ch + L.o_pre);
+    d.parent = a->parent ? reinterpret_cast<const int32_t *>(ch + L.o_tree) : nullptr;
+    d.vis = a->vis ? reinterpret_cast<const uint32_t *>(ch + L.o_tree) : nullptr;
+    d.out = reinterpret_cast<float *>(ch + L.o_out);
+    d.lse = a->lse ? reinterpret_cast<float *>(ch + L.o_lse) : nullptr;
+    d.err = a->err ? reinterpret_cast<int32_t *>(base + L.errs_off) + c : nullptr;
+    return d;
+}
+
+kdt_status host_layout(const kdt_verify_args *a, int n_chunks, HostLayout *L) {
+    kdt_status st = check_args(a);
+    if (st != KDT_OK) return st;
+    if (a->q_nope_row_stride || a->q_pe_row_stride) return KDT_ERR_BAD_SHAPE;   // host rows are contiguous
+    HostLayout l;
+    if (a->B == 0) {
+        *L = l;
+        return KDT_OK;
+    }
+    l.chunks = n_chunks ? n_chunks : (a->B % 4 == 0 ? 4 : (a->B % 2 == 0 ? 2 : 1));
+    if (l.chunks < 1 || a->B % l.chunks) return KDT_ERR_BAD_SHAPE;
+    l.nb = a->B / l.chunks;
+    const size_t elt = a->dtype == KDT_BF16 ? 2 : 4, nb = (size_t)l.nb, rows = nb * a->T * a->H;
+    const size_t W = (size_t)(a->T + 31) / 32;
+    l.b_qn = rows * kDc * elt;
+    l.b_qp = rows * kDr * elt;
+    l.b_kv = nb * (size_t)a->kv_row_stride * kDc * elt;
+    l.b_kp = nb * (size_t)a->kv_row_stride * kDr * elt;
+    l.b_pre = nb * sizeof(int32_t);
+    l.b_tree = a->parent ? nb * a->T * sizeof(int32_t) : nb * a->T * W * sizeof(uint32_t);
+    l.b_out = rows * kDc * sizeof(float);
+    l.b_lse = a->lse ? rows * sizeof(float) : 0;
+    size_t off = 0;
+    for (auto [o, b] : {std::pair<size_t *, size_t>{&l.o_qn, l.b_qn}, {&l.o_qp, l.b_qp}, {&l.o_kv, l.b_kv},
+                        {&l.o_kp, l.b_kp}, {&l.o_pre, l.b_pre}, {&l.o_tree, l.b_tree}, {&l.o_out, l.b_out},
+                        {&l.o_lse, l.b_lse}}) {
+        *o = off;
+        off = align_up(off + b);
+    }
+    l.chunk = off;
+    l.errs_off = (size_t)l.chunks * l.chunk;
+    l.ws_off = align_up(l.errs_off + (size_t)l.chunks * sizeof(int32_t));
+    // the workspace of one chunk's call (any base gives the same size)
+    kdt_verify_args d = chunk_args(a, l, reinterpret_cast<unsigned char *>(kAlign), 0);
+    Plan p;
+    if ((st = make_plan(&d, &p)) != KDT_OK) return st;
+    l.ws_bytes = p.ws_bytes;
+    l.total = l.ws_off + l.ws_bytes;
+    *L = l;
+    return KDT_OK;
+}
+
+// err = the first chunk's nonzero word, shifted to the flat index of the whole batch
+__global__ void combine_chunk_errors(const int32_t *chunk_err, int chunks, int64_t rows_per_chunk, int32_t *err) {
+    int32_t e = 0;
+    for (int c = 0; c < chunks && e == 0; ++c)
+        if (chunk_err[c]) e = (int32_t)(chunk_err[c] + c * rows_per_chunk);
+    *err = e;
+}
+
 }  // namespace
 }  // namespace kdt
 
@@ -236,6 +316,80 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
             return KDT_ERR_CUDA;
     }
     return KDT_OK;
+}
+
+size_t kdt_verify_attn_host_buffer_size(const kdt_verify_args *a, int n_chunks) {
+    HostLayout L;
+    return host_layout(a, n_chunks, &L) == KDT_OK ? L.total : 0;
+}
+
+kdt_status kdt_verify_attn_host(const kdt_verify_args *a, int n_chunks, void *dev_buf, size_t dev_bytes,
+                                cudaStream_t stream, cudaStream_t stream_in, cudaStream_t stream_out) {
+    HostLayout L;
+    kdt_status st = host_layout(a, n_chunks, &L);
+    if (st != KDT_OK) return st;
+    if (a->B == 0) return KDT_OK;
+    if (stream == stream_in || stream == stream_out || stream_in == stream_out) return KDT_ERR_BAD_SHAPE;
+    if (!dev_buf || dev_bytes < L.total || (reinterpret_cast<uintptr_t>(dev_buf) & (kAlign - 1)))
+        return KDT_ERR_WORKSPACE;
+    unsigned char *base = static_cast<unsigned char *>(dev_buf);
+    const int C = L.chunks;
+    std::vector<cudaEvent_t> ev(2 * (size_t)C + 2, nullptr);      // start, end, copied in [C], computed [C]
+    auto release = [&]() {
+        for (cudaEvent_t e : ev)
+            if (e) cudaEventDestroy(e);                            // freed once the event completes
+    };
+    for (cudaEvent_t &e : ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            e = nullptr;
+            release();
+            return KDT_ERR_CUDA;
+        }
+    cudaEvent_t ev_start = ev[0], ev_end = ev[1];
+    cudaEvent_t *ev_in = &ev[2], *ev_comp = &ev[2 + C];
+    bool ok = true;
+    // the copies in and out follow the work queued on `stream` before this call
+    ok = ok && cudaEventRecord(ev_start, stream) == cudaSuccess &&
+         cudaStreamWaitEvent(stream_in, ev_start, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(stream_out, ev_start, 0) == cudaSuccess;
+    // every chunk's inputs, one copy per tensor, queued first
+    for (int c = 0; c < C && ok; ++c) {
+        unsigned char *ch = base + (size_t)c * L.chunk;
+        const struct {
+            size_t off;
+            const void *src;
+            size_t bytes;
+        } in[6] = {{L.o_qn, a->q_nope, L.b_qn}, {L.o_qp, a->q_pe, L.b_qp}, {L.o_kv, a->c_kv, L.b_kv},
+                   {L.o_kp, a->k_pe, L.b_kp}, {L.o_pre, a->prefix_len, L.b_pre},
+                   {L.o_tree, a->parent ? (const void *)a->parent : (const void *)a->vis, L.b_tree}};
+        for (const auto &t : in)
+            ok = ok && cudaMemcpyAsync(ch + t.off, static_cast<const unsigned char *>(t.src) + (size_t)c * t.bytes,
+                                       t.bytes, cudaMemcpyHostToDevice, stream_in) == cudaSuccess;
+        ok = ok && cudaEventRecord(ev_in[c], stream_in) == cudaSuccess;
+    }
+    // each chunk's compute, with its copy out queued right behind it
+    for (int c = 0; c < C && ok; ++c) {
+        const kdt_verify_args d = chunk_args(a, L, base, c);
+        ok = cudaStreamWaitEvent(stream, ev_in[c], 0) == cudaSuccess;
+        if (ok && (st = kdt_verify_attn(&d, base + L.ws_off, L.ws_bytes, stream)) != KDT_OK) break;
+        ok = ok && cudaEventRecord(ev_comp[c], stream) == cudaSuccess &&
+             cudaStreamWaitEvent(stream_out, ev_comp[c], 0) == cudaSuccess &&
+             cudaMemcpyAsync(static_cast<unsigned char *>(static_cast<void *>(a->out)) + (size_t)c * L.b_out, d.out,
+                             L.b_out, cudaMemcpyDeviceToHost, stream_out) == cudaSuccess;
+        if (ok && a->lse)
+            ok = cudaMemcpyAsync(reinterpret_cast<unsigned char *>(a->lse) + (size_t)c * L.b_lse, d.lse, L.b_lse,
+                                 cudaMemcpyDeviceToHost, stream_out) == cudaSuccess;
+    }
+    if (st == KDT_OK && ok && a->err) {
+        combine_chunk_errors<<<1, 1, 0, stream>>>(reinterpret_cast<const int32_t *>(base + L.errs_off), C,
+                                                  (int64_t)L.nb * a->T, a->err);
+        ok = cudaGetLastError() == cudaSuccess;
+    }
+    // the call is complete on `stream` once the last copy out has landed
+    ok = ok && cudaEventRecord(ev_end, stream_out) == cudaSuccess && cudaStreamWaitEvent(stream, ev_end, 0) == cudaSuccess;
+    release();
+    if (st != KDT_OK) return st;
+    return ok ? KDT_OK : KDT_ERR_CUDA;
 }
 
 kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,

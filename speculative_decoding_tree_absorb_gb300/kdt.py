@@ -24,7 +24,8 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 # Names the header declares (checked by the CPU test suite against include/kdt.h).
 EXPORTS = ("kdt_status_str", "kdt_version", "kdt_build_visibility", "kdt_verify_attn",
            "kdt_verify_attn_workspace_size", "kdt_verify_attn_plan", "kdt_merge_attn_states",
-           "kdt_verify_attn_noalloc", "kdt_rope_neox", "kdt_tree_accept", "kdt_kv_compact", "kdt_tree_build")
+           "kdt_verify_attn_noalloc", "kdt_rope_neox", "kdt_tree_accept", "kdt_kv_compact", "kdt_tree_build",
+           "kdt_verify_attn_host", "kdt_verify_attn_host_buffer_size")
 
 
 class KdtError(RuntimeError):
@@ -93,6 +94,10 @@ def lib():
         L.kdt_verify_attn_plan.restype = ctypes.c_int
         L.kdt_merge_attn_states.argtypes = [vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int, vp, vp, vp]
         L.kdt_merge_attn_states.restype = ctypes.c_int
+        L.kdt_verify_attn_host.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp]
+        L.kdt_verify_attn_host.restype = ctypes.c_int
+        L.kdt_verify_attn_host_buffer_size.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.c_int]
+        L.kdt_verify_attn_host_buffer_size.restype = ctypes.c_size_t
         L.kdt_verify_attn_noalloc.argtypes = [ctypes.POINTER(VerifyArgs), vp]
         L.kdt_verify_attn_noalloc.restype = ctypes.c_int
         L.kdt_rope_neox.argtypes = [ctypes.POINTER(RopeArgs), vp]
@@ -219,6 +224,40 @@ def verify_attn(q_nope, q_pe, c_kv, k_pe, prefix_len, *, parent=None, vis=None, 
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().kdt_verify_attn(ctypes.byref(a), _ptr(workspace), ws_bytes, _stream_ptr(stream)),
            "kdt_verify_attn")
+    return out, lse
+
+
+def host_buffer_size(args: VerifyArgs, n_chunks=0) -> int:
+    return int(lib().kdt_verify_attn_host_buffer_size(ctypes.byref(args), int(n_chunks)))
+
+
+def verify_attn_host(q_nope, q_pe, c_kv, k_pe, prefix_len, *, parent=None, vis=None, max_kv_len=None,
+                     scale=DEFAULT_SCALE, out=None, lse=None, err=None, impl="auto", num_splits=0, n_chunks=0,
+                     dev_buf=None, streams=None, want_lse=True, device=None):
+    """kdt_verify_attn_host: host (CPU, ideally pinned) tensors in, host out and lse back.
+
+    ``streams`` = (compute, copy in, copy out) torch streams (default: the current
+    stream and two new ones); ``dev_buf`` a device uint8 tensor of at least
+    host_buffer_size() bytes (allocated here if None). The result is complete once
+    the compute stream is synchronised. ``err`` is a device int32 word."""
+    import torch
+    B, T, H = q_nope.shape[:3]
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    if out is None:
+        out = torch.empty((B, T, H, q_nope.shape[3]), dtype=torch.float32, pin_memory=True)
+    if lse is None and want_lse:
+        lse = torch.empty((B, T, H), dtype=torch.float32, pin_memory=True)
+    a = make_args(q_nope, q_pe, c_kv, k_pe, prefix_len, parent=parent, vis=vis, max_kv_len=max_kv_len,
+                  scale=scale, out=out, lse=lse, err=err, impl=impl, num_splits=num_splits)
+    need = host_buffer_size(a, n_chunks)
+    if dev_buf is None and need > 0:
+        dev_buf = torch.empty(need, dtype=torch.uint8, device=dev)
+    nbytes = 0 if dev_buf is None else dev_buf.numel() * dev_buf.element_size()
+    if streams is None:
+        streams = (torch.cuda.current_stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    s, s_in, s_out = (ctypes.c_void_p(x.cuda_stream) for x in streams)
+    _check(lib().kdt_verify_attn_host(ctypes.byref(a), int(n_chunks), _ptr(dev_buf), nbytes, s, s_in, s_out),
+           "kdt_verify_attn_host")
     return out, lse
 
 

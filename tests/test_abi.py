@@ -113,6 +113,39 @@ def test_host_checks_reject_bad_arguments(kdt):
     assert lib.kdt_version() >= 100
 
 
+def test_host_entry_checks(kdt):
+    """kdt_verify_attn_host refuses bad arguments, chunk counts, streams and buffers before
+    any CUDA call (the stream handles below are never used)."""
+    K = kdt.kdt
+    lib = kdt.lib()
+
+    def host(a, n=0, buf=None, nbytes=0, streams=(1, 2, 3)):
+        return lib.kdt_verify_attn_host(ctypes.byref(a), n, buf, nbytes, *(ctypes.c_void_p(x) for x in streams))
+
+    def size(a, n=0):
+        return lib.kdt_verify_attn_host_buffer_size(ctypes.byref(a), n)
+
+    a = _args(kdt)                                     # B = 2, fp32, parent given: two chunks by default
+    need = size(a)
+    per_seq = (9 * 8 * 576 * 4 + 46 * 576 * 4 + 4 + 9 * 4) + (9 * 8 * 512 * 4 + 9 * 8 * 4)
+    assert need >= 2 * per_seq + kdt.workspace_size(_args(kdt, B=1))
+    assert size(a, 1) >= 2 * per_seq and size(a, 2) == need
+    assert host(a) == K.KDT_ERR_WORKSPACE                                   # no buffer
+    assert host(a, buf=0x100000, nbytes=need - 1) == K.KDT_ERR_WORKSPACE   # short
+    assert host(a, buf=0x100010, nbytes=need) == K.KDT_ERR_WORKSPACE       # not 256-byte aligned
+    assert host(a, n=3) == K.KDT_ERR_BAD_SHAPE and size(a, 3) == 0          # does not divide B
+    assert host(a, n=-1) == K.KDT_ERR_BAD_SHAPE
+    assert host(_args(kdt, q_nope_row_stride=576)) == K.KDT_ERR_BAD_SHAPE   # host rows are contiguous
+    for streams in ((1, 1, 3), (1, 2, 1), (1, 2, 2)):
+        assert host(a, buf=0x100000, nbytes=need, streams=streams) == K.KDT_ERR_BAD_SHAPE
+    assert host(_args(kdt, out=None)) == K.KDT_ERR_NULL_ARG
+    assert host(_args(kdt, D_c=256)) == K.KDT_ERR_UNSUPPORTED and size(_args(kdt, D_c=256)) == 0
+    assert host(_args(kdt, B=0)) == K.KDT_OK and size(_args(kdt, B=0)) == 0
+    # one sequence a chunk needs room for every chunk's tensors
+    b = _args(kdt, B=4)
+    assert size(b, 4) >= 4 * per_seq and size(b, 0) == size(b, 4)
+
+
 def test_plan_and_workspace_are_host_only(kdt):
     a = _args(kdt, num_splits=3)
     p = kdt.plan(a)
