@@ -10,6 +10,9 @@ Workload: the H=64, 8K-prefix, 64-node-tree configuration -- B=8, H=64, every
 prefix 8192, T=64 geometric-bias tree, bf16 q/c_kv/k_pe, fp32 out + lse -- seeded
 synthetic data (``workloads``). ``--config`` selects another configuration.
 
+The ``e2e`` figure times the same work end to end through kdt_verify_attn_host:
+pinned host inputs in, host out and lse back, the copies pipelined with the compute.
+
 Multi-GPU: each rank runs its own copy of the workload (weak scaling, no
 collective on the data path); rank 0 reports the work of all ranks over the
 slowest rank's time.
