@@ -464,13 +464,13 @@ def main():
         torch.cuda.synchronize(dev)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
     # the host copy of the chunked run against the device-timed call on the same inputs: the
-    # work splits differ (and with them the bf16 rounding of P), so they agree within the
-    # path's own tolerance, not bit for bit
+    # work splits differ (and with them the bf16 rounding of P). Each run is held to the
+    # path's tolerance against the oracle, so the two may differ by up to twice that.
     e2e_out = out_h
     ref_out = out.cpu()
     tol = 2e-2 if case.dtype == "bf16" else 1e-4
     e2e_diff = (e2e_out - ref_out).abs()
-    if bool((e2e_diff > tol + tol * ref_out.abs()).any()):
+    if bool((e2e_diff > 2 * (tol + tol * ref_out.abs())).any()):
         raise SystemExit(f"end-to-end output differs from the device-timed call by {e2e_diff.max().item()}")
     e2e_check = {"max_abs_diff": e2e_diff.max().item(), "mean_abs_diff": e2e_diff.mean().item()}
     e2e_mean = max_over_ranks([statistics.mean(e2e_ms)], dist, dev)[0]
@@ -491,9 +491,15 @@ def main():
     else:
         peak = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         bound, peak_note = "alu", "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock"
-    tensor_roof_us = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+    # the workload's compute roof: bf16 inputs may use the tensor cores; fp32 inputs need
+    # fp32 arithmetic (TF32 would not meet the fp32 tolerance), so the fp32 FMA peak
+    if case.dtype == "bf16":
+        compute_peak, compute_basis = peaks["bf16_tflops"], "bf16 tensor"
+    else:
+        compute_peak, compute_basis = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e-6, "fp32 FMA"
+    compute_roof_us = flops / (compute_peak * 1e12) * 1e6
     hbm_roof_us = counts["bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e6
-    roof_us = max(tensor_roof_us, hbm_roof_us)
+    roof_us = max(compute_roof_us, hbm_roof_us)
 
     cpu_baseline = None
     if not args.no_cpu_baseline and world >= 1:
@@ -525,8 +531,8 @@ def main():
         "us_per_call_attention_median": ms_attn_median * 1e3,
         "tflops_attention": attn_tflops,
         "kv_gbs": counts["kv_bytes"] / (ms_attn * 1e-3) / 1e9,
-        "workload_roofline": {"roofline_us": roof_us, "tensor_us": tensor_roof_us, "hbm_us": hbm_roof_us,
-                              "frac": roof_us / (ms * 1e3), "basis": f"max(FLOPs/bf16 peak, bytes/HBM) of "
+        "workload_roofline": {"roofline_us": roof_us, "compute_us": compute_roof_us, "hbm_us": hbm_roof_us,
+                              "frac": roof_us / (ms * 1e3), "basis": f"max(FLOPs/{compute_basis} peak, bytes/HBM) of "
                                                                     f"{peaks['source']} peaks"},
         "roofline": {"bound": bound, "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak, "traffic": measured_traffic(pl["impl"], args.config),
