@@ -37,8 +37,12 @@
 //    where TMA fills zeros and the mask removes the keys. Only blocks holding tree
 //    keys (or those leading zeros) evaluate the mask, from packed ancestor bits.
 //  * Online softmax in base 2 with a lazy maximum: the running max m used for
-//    exp2(x - m) is only raised when a block's max exceeds it by more than 8, so
-//    p <= 256 and O is rescaled only then (exact either way: o = O / l).
+//    exp2(x - m) is only raised when a block's max exceeds it by more than 20, so
+//    p <= 2^20 and O is rescaled only then (exact either way: o = O / l). P is
+//    rounded to bf16, whose exponent range is fp32's, so the bound only keeps l and
+//    O (fp32) far from overflow; a smaller one rescales often on caches with
+//    outlier keys (a few times larger than the rest), and every rescale drains the
+//    P.V pipe.
 //  * Every wait is bounded; on a lost arrival the kernel records a status in the
 //    caller's error word, drains its own in-flight copies and MMAs, frees TMEM and
 //    returns (no trap, no hang).
@@ -121,7 +125,7 @@ constexpr int kVSlotBytes = 2 * kVSub;            // O ring slot: 128 keys x 128
 constexpr int kNV = 2;                            // O-CTA value ring slots (64 KB)
 constexpr uint32_t kCmdDone = 0xffffffffu;        // correction command: no more rescales
 constexpr uint64_t kWaitLimit = 200000000ull;     // ns a wait may poll before giving up
-constexpr float kRescaleThreshold = 8.0f;         // log2 units
+constexpr float kRescaleThreshold = 20.0f;        // log2 units
 
 // Shared-memory layout (same offsets in every CTA of the cluster; roles use
 // different parts). All tiles 1024-byte aligned for the 128B swizzle.
