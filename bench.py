@@ -13,9 +13,10 @@ synthetic data (``workloads``). ``--config`` selects another configuration.
 The ``e2e`` figure times the same work end to end through kdt_verify_attn_host:
 pinned host inputs in, host out and lse back, the copies pipelined with the compute.
 
-Multi-GPU: each rank runs its own copy of the workload (weak scaling, no
-collective on the data path); rank 0 reports the work of all ranks over the
-slowest rank's time.
+One GPU only: the tensor-core kernel loads key tiles with cluster-multicast TMA,
+which this library issues only over the memory of the one GPU a call runs on.
+``--gpus N`` with N > 1 (or a torchrun launch with WORLD_SIZE > 1) prints one
+``unavailable`` line on rank 0 and exits before any CUDA work.
 
 ``--impl reference`` times the CPU oracle as it stands on the host cores on a
 bounded sample of the same workload (rank 0 only).
@@ -42,32 +43,30 @@ import workloads as wl  # noqa: E402
 METRIC = "verify-attn µs/call, TFLOP/s and KV GB/s at H=64; fraction of roofline"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
-SMS = 152
 FP32_LANES_PER_SM = 128
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
-# dominant kernel from an ncu capture, with the hash of the kernel source it was
-# taken on; reported only while the source is unchanged (see profiles/).
+# dominant kernel from an ncu capture, keyed by kernel family and workload, with the
+# hash of the kernel source it was taken on; reported only while that source is
+# unchanged.
 TRAFFIC = {
-    ("tcgen05", "target"): {"src_hash": "1d2145dabf728c50", "bytes": 155.65e6,
-                            "profile": "profiles/verify_tc_target.md"},
-    ("simt", "target"): {"src_hash": None, "bytes": 155.52e6, "profile": "profiles/verify_simt_target.md"},
+    ("tcgen05", "target"): {"src_hash": "1d2145dabf728c50", "bytes": 155.65e6},
 }
 
 
-def max_over_ranks(values, dist, device):
-    """Each rank's timings -> the slowest rank's, elementwise (one all-reduce)."""
-    if dist is None:
-        return [float(v) for v in values]
-    import torch
-    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return [float(v) for v in t.tolist()]
+def single_gpu_only(gpus, world):
+    """The unavailable line for a multi-GPU request, or None for one GPU."""
+    n = max(gpus, world)
+    if n <= 1:
+        return None
+    return {"metric": METRIC, "n_gpus": n,
+            "unavailable": "one GPU per call: the tensor-core kernel's cluster-multicast TMA loads are "
+                           "issued only over the memory of the GPU a call runs on, so no multi-GPU run exists"}
 
 
-def whole_job_tflops(flops_per_rank, world, ms_slowest):
-    """Work of all ranks (weak scaling: each rank runs its own copy) over the slowest rank's time."""
-    return flops_per_rank * world / (ms_slowest * 1e-3) / 1e12
+def fp32_fma_peak_tflops(sms, sm_mhz):
+    """fp32 FMA roof: SMs x 128 lanes x 2 FLOP x SM clock."""
+    return sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
 
 
 def kernel_src_hash(impl):
@@ -324,6 +323,12 @@ def main():
         print(json.dumps(run_reference(args, case, counts)), flush=True)
         return 0
 
+    multi = single_gpu_only(args.gpus, world)
+    if multi is not None:
+        if rank == 0:
+            print(json.dumps(multi), flush=True)
+        return 0
+
     import torch
     import speculative_decoding_tree_absorb_gb300 as kdt
     from speculative_decoding_tree_absorb_gb300 import build_lib
@@ -331,22 +336,14 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
     torch.cuda.set_device(local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    if rank == 0:
-        build_lib.build()
-    if dist is not None:
-        dist.barrier()
+    build_lib.build()
     kdt.lib()
 
     case = make_workload(args.config)
     counts = workload_counts(case)
     dev = torch.device("cuda", local_rank)
     if args.tree_ops:
-        if rank == 0:
-            print(json.dumps(run_tree_ops(args, case, dev)), flush=True)
+        print(json.dumps(run_tree_ops(args, case, dev)), flush=True)
         return 0
 
     def conv(x):
@@ -397,8 +394,6 @@ def main():
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
-        if dist is not None:
-            dist.barrier()
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter()
         for k in range(args.steps):
@@ -412,8 +407,6 @@ def main():
             if st or st2:
                 raise kdt.KdtError(st or st2, "timed step")
         torch.cuda.synchronize(dev)
-        if dist is not None:
-            dist.barrier()
         t_wall = time.perf_counter() - t_wall
     clocks = clk.summary()
     step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
@@ -421,7 +414,6 @@ def main():
     ms = statistics.mean(step_ms)
     ms_attn = statistics.mean(attn_ms)
     ms_attn_median = statistics.median(attn_ms)
-    ms, ms_attn = max_over_ranks([ms, ms_attn], dist, dev)
 
     # ---- end to end through the C ABI with host buffers ------------------------------
     # kdt_verify_attn_host: pinned host tensors in, host out and lse back. The library cuts
@@ -473,36 +465,32 @@ def main():
     if bool((e2e_diff > 2 * (tol + tol * ref_out.abs())).any()):
         raise SystemExit(f"end-to-end output differs from the device-timed call by {e2e_diff.max().item()}")
     e2e_check = {"max_abs_diff": e2e_diff.max().item(), "mean_abs_diff": e2e_diff.mean().item()}
-    e2e_mean = max_over_ranks([statistics.mean(e2e_ms)], dist, dev)[0]
-
-    if rank != 0:
-        if dist is not None:
-            dist.barrier()
-            dist.destroy_process_group()
-        return 0
+    e2e_mean = statistics.mean(e2e_ms)
 
     flops = counts["flops"]
     peaks = load_peaks()
-    tflops = whole_job_tflops(flops, world, ms)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = fp32_fma_peak_tflops(sms, peaks.get("sm_max_mhz", 2070.0))
+    tflops = flops / (ms * 1e-3) / 1e12
     attn_tflops = flops / (ms_attn * 1e-3) / 1e12
     if pl["impl"] == "tcgen05":
         peak = peaks["bf16_tflops"]
         bound, peak_note = "tensor", f"bf16 dense, cuBLAS burst ({peaks['source']})"
     else:
-        peak = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-        bound, peak_note = "alu", "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock"
+        peak = fp32_peak
+        bound, peak_note = "alu", f"fp32 FMA: {sms} SMs x 128 lanes x 2 FLOP x max SM clock"
     # the workload's compute roof: bf16 inputs may use the tensor cores; fp32 inputs need
     # fp32 arithmetic (TF32 would not meet the fp32 tolerance), so the fp32 FMA peak
     if case.dtype == "bf16":
         compute_peak, compute_basis = peaks["bf16_tflops"], "bf16 tensor"
     else:
-        compute_peak, compute_basis = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e-6, "fp32 FMA"
+        compute_peak, compute_basis = fp32_peak, "fp32 FMA"
     compute_roof_us = flops / (compute_peak * 1e12) * 1e6
     hbm_roof_us = counts["bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e6
     roof_us = max(compute_roof_us, hbm_roof_us)
 
     cpu_baseline = None
-    if not args.no_cpu_baseline and world >= 1:
+    if not args.no_cpu_baseline:
         ref_args = argparse.Namespace(steps=1, warmup=0, ref_seconds=args.ref_seconds, config=args.config,
                                       gpus=1)
         r = run_reference(ref_args, case, counts)
@@ -512,7 +500,7 @@ def main():
         "metric": METRIC,
         "value": tflops,
         "unit": "TFLOP/s",
-        "n_gpus": world,
+        "n_gpus": 1,
         "steps": args.steps,
         "warmup": max(3, args.warmup),
         "ms_per_step": ms,
@@ -525,7 +513,7 @@ def main():
                    "prefix": [int(x) for x in case.prefix_len[:4]] + (["..."] if B > 4 else []),
                    "kernel_impl": pl["impl"], "num_splits": pl["num_splits"],
                    "l2": "flushed between steps (256 MiB write outside the timed events)",
-                   "parallelism": f"replicas x{world} (weak scaling, no collective)"},
+                   "parallelism": "one GPU"},
         "us_per_call": ms * 1e3,
         "us_per_call_attention": ms_attn * 1e3,
         "us_per_call_attention_median": ms_attn_median * 1e3,
@@ -540,7 +528,7 @@ def main():
                      "kernel": f"verify_{pl['impl']} (+ split merge when num_splits > 1)"},
         "algorithmic": {"flops": flops, "bytes": counts["bytes"], "kv_bytes": counts["kv_bytes"]},
         "clocks": clocks,
-        "e2e": {"value": whole_job_tflops(flops, world, e2e_mean), "unit": "TFLOP/s",
+        "e2e": {"value": flops / (e2e_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_mean, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipeline": f"kdt_verify_attn_host: {n_chunks} chunks of {B // n_chunks} sequence(s); copy in, "
                             f"compute and copy out on three streams",
@@ -550,9 +538,6 @@ def main():
         "wall_s_timed": t_wall,
     }
     print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
     return 0
 
 

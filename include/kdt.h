@@ -31,9 +31,17 @@
  *    caller's next synchronisation.
  *  - The library allocates no memory: scratch space is the caller's `workspace`
  *    (kdt_verify_attn_noalloc, at the end, uses a fixed array inside the library
- *    instead; kdt_verify_attn_host creates and releases its events). It keeps no
- *    other global state than a per-device cache of the SM count. Concurrent calls
- *    are safe given distinct workspaces.
+ *    instead; kdt_verify_attn_host creates and releases its events). Its global
+ *    state: that fixed device array (KDT_NOALLOC_SCRATCH_BYTES on every GPU that
+ *    loads the library) and per-device caches of the SM count, of how many
+ *    tensor-core clusters are resident at once, and of the array's device address.
+ *    Concurrent calls are safe given distinct workspaces.
+ *  - One GPU per call: kdt_verify_attn's tensors (and its workspace) must be device
+ *    memory of the device current on the calling thread -- not host, managed or
+ *    another GPU's memory reached through unified addressing -- else the call
+ *    returns KDT_ERR_NOT_DEVICE before any launch. The tensor-core kernel loads key
+ *    tiles with cluster-multicast TMA, which this library issues only over the
+ *    memory of the GPU the call runs on.
  *  - Errors found in the DATA on the device (a malformed tree) are reported
  *    through a caller-provided device word `err` (0 = ok, else 1 + the flat index
  *    b*T + i of the first offending parent entry), never by a trap.
@@ -55,7 +63,8 @@ typedef enum {
     KDT_ERR_BAD_SHAPE = 2,    /* sizes out of range or inconsistent (B, T, H, strides, kv bounds) */
     KDT_ERR_UNSUPPORTED = 3,  /* valid but not implemented here (D_c != 512, D_r != 64, impl) */
     KDT_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than kdt_verify_attn_workspace_size() */
-    KDT_ERR_CUDA = 5          /* a CUDA runtime call or kernel launch failed */
+    KDT_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
+    KDT_ERR_NOT_DEVICE = 6    /* a tensor is not device memory of the current device */
 } kdt_status;
 
 /* Static, never-NULL English name of a status. */
@@ -113,7 +122,11 @@ typedef struct {
     float *lse;             /* device fp32 [B,T,H], or NULL */
     int32_t *err;           /* device int32 error word for the parent path, or NULL */
     int impl;               /* kdt_impl */
-    int num_splits;         /* KV splits per row tile; 0 = choose automatically */
+    int num_splits;         /* 0 = choose automatically. SIMT kernel: KV splits per 64-row tile
+                               (at most 32). Tensor-core kernel: the number of persistent
+                               4-CTA clusters its (256-row unit, 128-key block) work is cut
+                               into equal shares for (at most those resident at once); the
+                               units a share boundary cuts are merged by log-sum-exp. */
     int64_t q_nope_row_stride; /* elements between consecutive (b,i,h) rows of q_nope; 0 = 512
                                   (contiguous). Lets the kernels read a combined [.., 512 + 64]
                                   query buffer where it lies (stride 576, q_pe = q_nope + 512)
@@ -136,8 +149,9 @@ typedef struct {
  * Errors: KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE (including prefix bound violations
  * detectable on the host: max_kv_len > kv_row_stride, max_kv_len < T),
  * KDT_ERR_UNSUPPORTED (D_c != 512, D_r != 64, unknown impl, TCGEN05 with fp32),
- * KDT_ERR_WORKSPACE, KDT_ERR_CUDA. prefix_len values are device data: the caller
- * guarantees prefix_len[b] + T <= max_kv_len.
+ * KDT_ERR_WORKSPACE, KDT_ERR_NOT_DEVICE (a tensor or the workspace is not device
+ * memory of the current device), KDT_ERR_CUDA. prefix_len values are device data: the
+ * caller guarantees prefix_len[b] + T <= max_kv_len.
  */
 kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_bytes,
                            cudaStream_t stream);
@@ -196,7 +210,8 @@ kdt_status kdt_verify_attn_plan(const kdt_verify_args *a, kdt_plan *plan);
  * before it returns (the driver frees them once they complete).
  * Errors: those of kdt_verify_attn; KDT_ERR_BAD_SHAPE also for an n_chunks that
  * does not divide B, a nonzero row stride, or two equal streams; KDT_ERR_WORKSPACE
- * for a missing, short or misaligned dev_buf.
+ * for a missing, short or misaligned dev_buf; KDT_ERR_NOT_DEVICE when dev_buf or
+ * `err` is not device memory of the current device.
  */
 kdt_status kdt_verify_attn_host(const kdt_verify_args *a, int n_chunks, void *dev_buf, size_t dev_bytes,
                                 cudaStream_t stream, cudaStream_t stream_in, cudaStream_t stream_out);
@@ -241,8 +256,11 @@ kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const flo
  *    if the call still does not fit, or an explicit num_splits does not fit, it
  *    returns KDT_ERR_WORKSPACE and launches nothing.
  *  - Set-up: the first call made on a device (with that device current) looks up
- *    the array's device address with cudaGetSymbolAddress; make that first call
- *    before any stream capture on that device.
+ *    the array's device address with cudaGetSymbolAddress and keeps it for that
+ *    device; make that first call before any stream capture on that device. A
+ *    cudaDeviceReset destroys the array with the context: the kept address then
+ *    dangles, so do not call this entry point again in a process after resetting
+ *    a device it was used on.
  *  - Sharing: every call on a device uses the same array and it keeps the last
  *    call's contents. The kernels overwrite every scratch byte they read, so no
  *    clearing is needed, but calls whose work overlaps on the GPU (other streams,

@@ -3,6 +3,7 @@
 #include "kdt_internal.cuh"
 
 #include <atomic>
+#include <initializer_list>
 #include <math.h>
 #include <vector>
 
@@ -27,6 +28,29 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every tensor a verify call touches must be device memory of the current device. The
+// tensor-core kernel encodes TMA tensor maps over c_kv, k_pe and q_pe and loads key tiles
+// with cluster multicast; those are issued here over this GPU's own memory only, never
+// over host, managed or another GPU's memory reached through unified addressing.
+// NULL entries are skipped. KDT_ERR_CUDA if the query itself fails.
+kdt_status check_on_current_device(std::initializer_list<const void *> ptrs) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return KDT_ERR_CUDA;
+    }
+    for (const void *p : ptrs) {
+        if (!p) continue;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            cudaGetLastError();
+            return KDT_ERR_CUDA;
+        }
+        if (at.type != cudaMemoryTypeDevice || at.device != dev) return KDT_ERR_NOT_DEVICE;
+    }
+    return KDT_OK;
+}
 
 struct Plan {
     int impl = KDT_IMPL_SIMT;
@@ -88,11 +112,12 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     const int nblk = (a->max_kv_len + unit_keys - 1) / unit_keys;
     const int64_t base = (int64_t)unit_tiles * a->B;
     if (tc) {
-        // One cluster per resident slot, each taking an equal share of all units' key
-        // blocks (the split adapts on the device to the actual prefix lengths); caller
-        // splits do not apply.
-        p.tc_clusters = tc_max_clusters();
-        p.splits = 1;
+        // Persistent 4-CTA clusters, each taking an equal share of all units' key blocks
+        // (the split adapts on the device to the actual prefix lengths): one per resident
+        // slot, or the caller's num_splits of them (at most the resident ones).
+        const int resident = tc_max_clusters();
+        p.tc_clusters = a->num_splits > 0 && a->num_splits < resident ? a->num_splits : resident;
+        p.splits = p.tc_clusters;
         p.blocks_per_split = nblk;
         p.ctas = 4 * p.tc_clusters;
     } else {
@@ -233,6 +258,7 @@ const char *kdt_status_str(kdt_status s) {
         case KDT_ERR_UNSUPPORTED: return "unsupported configuration";
         case KDT_ERR_WORKSPACE: return "workspace missing or too small";
         case KDT_ERR_CUDA: return "CUDA error";
+        case KDT_ERR_NOT_DEVICE: return "tensor not in device memory of the current device";
     }
     return "unknown status";
 }
@@ -266,12 +292,26 @@ kdt_status kdt_verify_attn_plan(const kdt_verify_args *a, kdt_plan *out) {
 }
 
 kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    return kdt::verify_attn_checked(a, workspace, ws_bytes, stream, true, true);
+}
+
+}  // extern "C"
+
+namespace kdt {
+
+kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t ws_bytes, cudaStream_t stream,
+                               bool check_tensors, bool check_workspace) {
     Plan p;
     kdt_status st = make_plan(a, &p);
     if (st != KDT_OK) return st;
     if (a->B == 0) return KDT_OK;
     if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return KDT_ERR_WORKSPACE;
+    if (check_tensors &&
+        (st = check_on_current_device({a->q_nope, a->q_pe, a->c_kv, a->k_pe, a->prefix_len, a->parent, a->vis,
+                                       a->out, a->lse, a->err})) != KDT_OK)
+        return st;
+    if (check_workspace && p.ws_bytes > 0 && (st = check_on_current_device({workspace})) != KDT_OK) return st;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
 
     VerifyParams vp;
@@ -318,6 +358,10 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
     return KDT_OK;
 }
 
+}  // namespace kdt
+
+extern "C" {
+
 size_t kdt_verify_attn_host_buffer_size(const kdt_verify_args *a, int n_chunks) {
     HostLayout L;
     return host_layout(a, n_chunks, &L) == KDT_OK ? L.total : 0;
@@ -332,6 +376,8 @@ kdt_status kdt_verify_attn_host(const kdt_verify_args *a, int n_chunks, void *de
     if (stream == stream_in || stream == stream_out || stream_in == stream_out) return KDT_ERR_BAD_SHAPE;
     if (!dev_buf || dev_bytes < L.total || (reinterpret_cast<uintptr_t>(dev_buf) & (kAlign - 1)))
         return KDT_ERR_WORKSPACE;
+    // every chunk's device tensors and workspace lie inside dev_buf, checked once here
+    if ((st = check_on_current_device({dev_buf, a->err})) != KDT_OK) return st;
     unsigned char *base = static_cast<unsigned char *>(dev_buf);
     const int C = L.chunks;
     std::vector<cudaEvent_t> ev(2 * (size_t)C + 2, nullptr);      // start, end, copied in [C], computed [C]
@@ -371,7 +417,8 @@ kdt_status kdt_verify_attn_host(const kdt_verify_args *a, int n_chunks, void *de
     for (int c = 0; c < C && ok; ++c) {
         const kdt_verify_args d = chunk_args(a, L, base, c);
         ok = cudaStreamWaitEvent(stream, ev_in[c], 0) == cudaSuccess;
-        if (ok && (st = kdt_verify_attn(&d, base + L.ws_off, L.ws_bytes, stream)) != KDT_OK) break;
+        if (ok && (st = verify_attn_checked(&d, base + L.ws_off, L.ws_bytes, stream, false, false)) != KDT_OK)
+            break;
         ok = ok && cudaEventRecord(ev_comp[c], stream) == cudaSuccess &&
              cudaStreamWaitEvent(stream_out, ev_comp[c], 0) == cudaSuccess &&
              cudaMemcpyAsync(static_cast<unsigned char *>(static_cast<void *>(a->out)) + (size_t)c * L.b_out, d.out,

@@ -75,4 +75,11 @@ cudaError_t launch_merge_two(const float *o_a, const float *lse_a, const float *
 // Per-device SM count (cached).
 int sm_count();
 
+// kdt_verify_attn with the device-memory checks selectable: the caller's tensors
+// (check_tensors) and the workspace (check_workspace) must be device memory of the current
+// device. Entry points whose buffers are already known to be (the host pipeline's chunks
+// inside its checked device buffer, the no-allocation entry's library array) skip them.
+kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t ws_bytes, cudaStream_t stream,
+                               bool check_tensors, bool check_workspace);
+
 }  // namespace kdt

@@ -27,7 +27,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[KDT_NOALLOC_SCR
 
 // Device address of g_noalloc_scratch, looked up once per device (on the first call
 // made with that device current). In host code the symbol names a host-side stand-in,
-// not device memory, so it is never passed to a kernel directly.
+// not device memory, so it is never passed to a kernel directly. A cudaDeviceReset
+// frees the array with its context and leaves the kept address dangling; the header
+// tells callers not to use this entry point on a device after resetting it.
 std::atomic<void *> g_scratch_ptr[64];
 
 kdt_status scratch_for_current_device(void **out) {
@@ -65,7 +67,9 @@ kdt_status kdt_verify_attn_noalloc(const kdt_verify_args *a, cudaStream_t stream
     void *scratch = nullptr;
     kdt_status st = scratch_for_current_device(&scratch);
     if (st != KDT_OK) return st;
-    return kdt_verify_attn(&args, scratch, KDT_NOALLOC_SCRATCH_BYTES, stream);
+    // the caller's tensors are checked like kdt_verify_attn's; the scratch is this
+    // device's copy of the library array
+    return kdt::verify_attn_checked(&args, scratch, KDT_NOALLOC_SCRATCH_BYTES, stream, true, false);
 }
 
 }  // extern "C"

@@ -1,4 +1,4 @@
-"""kdt_verify_attn_noalloc against kdt_verify_attn, through the C ABI.
+"""kdt_verify_attn_noalloc against kdt_verify_attn and the oracle, through the C ABI.
 
 The no-allocation entry point serves callers that cannot allocate device memory
 when they call the library (for example a serving engine that reserved nearly all
@@ -49,31 +49,60 @@ def _both(kdt, case, impl, num_splits=0):
     return (out.cpu().numpy(), lse.cpu().numpy()), (ref_out, ref_lse)
 
 
-def _check(case, got, ref):
+def _check(case, got, ref, oracle_mod=None):
+    """got against the workspace entry point's result and, given the oracle, against it too."""
     atol, rtol = H.TOL[case.dtype]
     H.assert_close(got[0], ref[0], atol, rtol, f"{case.name} out")
     H.assert_close(got[1], ref[1], atol, rtol, f"{case.name} lse")
+    if oracle_mod is not None:
+        o_out, o_lse = oracle_mod.verify_attn(case)
+        H.assert_close(got[0], o_out, atol, rtol, f"{case.name} out vs oracle")
+        H.assert_close(got[1], o_lse, atol, rtol, f"{case.name} lse vs oracle")
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(kdt):
+def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(kdt, oracle_mod):
     # call 1: fp32, one sequence, several KV splits -> partials and bits in the scratch
     a = wl.make_case("noalloc_a", B=1, T=32, H=64, prefix=1500, dtype="f32", tree="window8", seed=41)
     got, ref = _both(kdt, a, impl="simt", num_splits=3)
-    _check(a, got, ref)
+    _check(a, got, ref, oracle_mod)
     # call 2: bf16, ragged batch, different tree and split count reusing the same scratch
     b = wl.make_case("noalloc_b", B=3, T=20, H=16, prefix=(900, 31, 400), dtype="bf16", tree="geometric",
                      seed=42)
     got, ref = _both(kdt, b, impl="auto", num_splits=3)
-    _check(b, got, ref)
+    _check(b, got, ref, oracle_mod)
 
 
-def test_noalloc_fits_automatic_splits_and_rejects_oversize(kdt):
+def _auto_simt_plan_over_limit(kdt):
+    """A fp32 shape whose automatic SIMT split count needs more than the fixed scratch: with
+    about two waves of CTAs wanted, B sequences of 59 row tiles (T=59, H=64) and a prefix of
+    a few key blocks per split; B is searched because the split count depends on the SM count."""
     import torch
-    # automatic splits: the library lowers the split count to fit its fixed scratch
-    c = wl.make_case("noalloc_c", B=2, T=64, H=64, prefix=2000, dtype="bf16", tree="geometric", seed=43)
-    got, ref = _both(kdt, c, impl="auto")
-    _check(c, got, ref)
+    for B in range(3, 12):
+        c = wl.make_case("noalloc_simt", B=B, T=59, H=64, prefix=640, dtype="f32", tree="uniform", seed=44)
+        d = G.to_device(c)
+        out = torch.empty((c.B, c.T, c.H, 512), device="cuda")
+        a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
+                          max_kv_len=c.max_kv_len, scale=c.scale, out=out, impl="simt")
+        if kdt.workspace_size(a) > (64 << 20):
+            return c, kdt.plan(a)
+    return None, None
+
+
+def test_noalloc_fits_automatic_splits_and_rejects_oversize(kdt, oracle_mod):
+    import torch
+    # automatic SIMT splits whose partials exceed the fixed scratch: the library lowers the
+    # split count until they fit, and the result still matches
+    c, pl = _auto_simt_plan_over_limit(kdt)
+    assert c is not None, "no fp32 shape with an automatic split plan above 64 MiB"
+    assert pl["impl"] == "simt" and pl["num_splits"] > 1
+    got, ref = _both(kdt, c, impl="simt")
+    _check(c, got, ref, oracle_mod)
+    # the bf16 tensor path's automatic plan fits as it is
+    t = wl.make_case("noalloc_c", B=2, T=64, H=64, prefix=2000, dtype="bf16", tree="geometric", seed=43)
+    got, ref = _both(kdt, t, impl="auto")
+    _check(t, got, ref, oracle_mod)
     # an explicit split count whose partials exceed the fixed scratch is refused before any launch
+    c = t
     d = G.to_device(c)
     out = torch.empty((c.B, c.T, c.H, 512), device="cuda")
     a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
