@@ -17,6 +17,10 @@ Parity status per function (how each is pinned is in ``tests/test_oracle_tree_op
   tree_build       -- pinned (brute force: every node of the full K-ary candidate tree
                       sorted by the selection order, first N taken; path-score and depth
                       invariants; single-candidate chain)
+  vc_up_proj       -- pinned (one-hot selection weights return the selected latent
+                      dims exactly; a unit latent returns the named weight row; the
+                      triangular closed forms n + 1 and n (n + 1) / 2 fix the summation
+                      range; bf16 weights widen exactly)
 """
 from __future__ import annotations
 
@@ -178,3 +182,32 @@ def tree_build(cand_tok: np.ndarray, cand_lp: np.ndarray, N: int, root_tok=None)
                 for r2 in range(K):
                     push(n, d + 1, r2)
     return parent, tok, depth, score
+
+
+# ---------------------------------------------------- value up-projection (w_vc) --
+def vc_up_proj(o: np.ndarray, w_vc: np.ndarray, w_dtype: str = "bf16") -> np.ndarray:
+    """Per-head value up-projection of the latent attention output ("The Verify-Attn
+    Kernel: A Single File Write ...", "Design Decisions and Trade-Offs": the attention
+    kernel returns the latent, and a separate matrix multiply then applies each head's
+    value weights, as SGLang structures it).
+
+        v[..., h, n] = sum_{d < D_c} o[..., h, d] * w_vc[h, d, n]
+
+    o: float32 [..., H, D_c] (the rows of a verify output, e.g. [B, T, H, 512]);
+    w_vc: [H, D_c, D_v], bf16 bit patterns (uint16) when ``w_dtype`` is "bf16", else
+    float32. Both are widened exactly to float64, each head's product is one float64
+    matrix multiply, and the result is rounded once to float32 [..., H, D_v].
+    """
+    o64 = np.asarray(o, dtype=np.float32).astype(np.float64)
+    if w_dtype == "bf16":
+        w32 = (np.asarray(w_vc, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    else:
+        w32 = np.asarray(w_vc, dtype=np.float32)
+    w64 = w32.astype(np.float64)
+    H, D_c, D_v = w64.shape
+    if o64.shape[-2:] != (H, D_c):
+        raise ValueError("o must end in [H, D_c] matching w_vc [H, D_c, D_v]")
+    v = np.empty(o64.shape[:-1] + (D_v,), dtype=np.float64)
+    for h in range(H):
+        v[..., h, :] = o64[..., h, :] @ w64[h]
+    return v.astype(np.float32)

@@ -263,3 +263,64 @@ def test_build_invariants_and_single_candidate_chain():
     tok1, lp1 = _cands(10, 1, 8, 1, False)
     par, tk, dep, sc = ot.tree_build(tok1, lp1, 8)
     assert par[0].tolist() == list(range(-1, 8)) and dep[0].tolist() == list(range(9))
+
+
+# ----------------------------------------------------- w_vc up-projection pins --
+def _bf16_bits(x):
+    return wl.f64_to_bf16_bits(np.asarray(x, dtype=np.float64))
+
+
+def test_vc_one_hot_weights_select_latent_dims_exactly():
+    # w_vc[h, d, n] = 1 iff d = sel[h, n]: v[r, h, n] = o[r, h, sel[h, n]], exactly, with a
+    # different selection per head (a head or operand mix-up picks other dims)
+    H, D_c, D_v, R = 3, 512, 128, 5
+    o = wl.normal(31, "vc_o", R * H * D_c).reshape(R, H, D_c).astype(np.float32)
+    sel = np.stack([(np.arange(D_v) * (2 * h + 3) + 7 * h + 1) % D_c for h in range(H)])
+    w = np.zeros((H, D_c, D_v))
+    for h in range(H):
+        w[h, sel[h], np.arange(D_v)] = 1.0
+    v = ot.vc_up_proj(o, _bf16_bits(w))
+    for h in range(H):
+        assert np.array_equal(v[:, h, :], o[:, h, sel[h]])
+
+
+def test_vc_unit_latent_returns_weight_row():
+    # o[r, h] = e_k: v[r, h] is row k of that head's weights (fixes which weight index
+    # runs over the latent)
+    H, D_c, D_v = 2, 512, 64
+    w = _bf16_bits(wl.normal(32, "vc_w", H * D_c * D_v).reshape(H, D_c, D_v))
+    wf = (w.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    ks = [0, 1, 255, 256, 511]
+    o = np.zeros((len(ks), H, D_c), dtype=np.float32)
+    for r, k in enumerate(ks):
+        o[r, :, k] = 1.0
+    v = ot.vc_up_proj(o, w)
+    for r, k in enumerate(ks):
+        for h in range(H):
+            assert np.array_equal(v[r, h], wf[h, k])
+
+
+def test_vc_triangular_closed_forms():
+    # w[h, d, n] = 1 for d <= n: with o = 1 every output is n + 1; with o[d] = d it is
+    # n (n + 1) / 2 -- closed forms that fix the summation range over the latent
+    H, D_c, D_v = 2, 512, 256
+    tri = (np.arange(D_c)[:, None] <= np.arange(D_v)[None, :]).astype(np.float64)
+    w = _bf16_bits(np.broadcast_to(tri, (H, D_c, D_v)))
+    n = np.arange(D_v, dtype=np.float64)
+    v1 = ot.vc_up_proj(np.ones((2, H, D_c), dtype=np.float32), w)
+    assert np.array_equal(v1, np.broadcast_to((n + 1).astype(np.float32), v1.shape))
+    od = np.broadcast_to(np.arange(D_c, dtype=np.float32), (3, H, D_c))
+    v2 = ot.vc_up_proj(od, w)
+    assert np.array_equal(v2, np.broadcast_to((n * (n + 1) / 2).astype(np.float32), v2.shape))
+
+
+def test_vc_bf16_weights_widen_exactly():
+    # bit patterns with known values: 1, -2, 0.5 + 2^-8 (the last mantissa bit), the largest
+    # finite bf16 and the smallest subnormal
+    bits = np.array([0x3F80, 0xC000, 0x3F01, 0x7F7F, 0x0001], dtype=np.uint16)
+    want = [1.0, -2.0, 0.50390625, (2 - 2 ** -7) * 2.0 ** 127, 2.0 ** -133]
+    w = bits.reshape(1, 5, 1) * np.ones((1, 1, 1), dtype=np.uint16)
+    for k in range(5):
+        o = np.zeros((1, 1, 5), dtype=np.float32)
+        o[0, 0, k] = 1.0
+        assert float(ot.vc_up_proj(o, w)[0, 0, 0]) == np.float32(want[k])

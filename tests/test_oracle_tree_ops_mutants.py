@@ -32,6 +32,15 @@ MUTANTS = {
     "build_depth_tie_ignored": ("heapq.heappush(heap, (-float(sc), d, par, r, sc))",
                                 "heapq.heappush(heap, (-float(sc), 0, par, r, sc))"),
     "build_children_same_depth": ("push(n, d + 1, r2)", "push(n, d, r2)"),
+    "vc_same_head_weights": ("v[..., h, :] = o64[..., h, :] @ w64[h]", "v[..., h, :] = o64[..., h, :] @ w64[0]"),
+    "vc_latent_range_short": ("v[..., h, :] = o64[..., h, :] @ w64[h]",
+                              "v[..., h, :] = o64[..., h, :448] @ w64[h, :448]"),
+    "vc_other_head_latent": ("v[..., h, :] = o64[..., h, :] @ w64[h]",
+                             "v[..., h, :] = o64[..., (h + 1) % H, :] @ w64[h]"),
+    "vc_widen_shift": ("astype(np.uint32) << np.uint32(16)).view(np.float32)",
+                       "astype(np.uint32) << np.uint32(15)).view(np.float32)"),
+    "vc_weight_rows_reversed": ("v[..., h, :] = o64[..., h, :] @ w64[h]",
+                                "v[..., h, :] = o64[..., h, :] @ w64[h, ::-1]"),
 }
 
 PINS = [
@@ -49,6 +58,10 @@ PINS = [
     (P.test_compact_moves_named_rows_and_nothing_else, {}),
     (P.test_build_equals_brute_force_selection_order, dict(seed=2, D=4, K=3, quant=True)),
     (P.test_build_invariants_and_single_candidate_chain, {}),
+    (P.test_vc_one_hot_weights_select_latent_dims_exactly, {}),
+    (P.test_vc_unit_latent_returns_weight_row, {}),
+    (P.test_vc_triangular_closed_forms, {}),
+    (P.test_vc_bf16_weights_widen_exactly, {}),
 ]
 
 
