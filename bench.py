@@ -285,6 +285,57 @@ def run_tree_ops(args, case, dev):
             "ops": res, "hbm_peak_gbs": peaks["hbm_gbs"]}
 
 
+def run_vc_proj(args, case, dev):
+    """Time the per-head w_vc up-projection (kdt_vc_up_proj) on this workload's verify
+    output shape: o fp32 [B*T, H, 512] -> v fp32 [B*T, H, D_v] with bf16 weights
+    [H, 512, D_v], D_v = 128. Synthetic N(0, 1) rows and N(0, 1/512) weights; CUDA events
+    around each call on its stream, L2 flushed before each. HBM-bound: the roof is the
+    algorithmic bytes (o read once, the weights once, v written once) at the measured
+    copy bandwidth."""
+    import torch
+    import speculative_decoding_tree_absorb_gb300 as kdt
+    R, H, D_v = case.B * case.T, case.H, 128
+    o = torch.from_numpy(wl.normal(91, "bench_vc_o", R * H * 512).reshape(R, H, 512).astype(np.float32)).to(dev)
+    wb = wl.f64_to_bf16_bits(wl.normal(91, "bench_vc_w", H * 512 * D_v, 1.0 / math.sqrt(512.0)))
+    w = torch.from_numpy(wb.reshape(H, 512, D_v).view(np.int16)).view(torch.bfloat16).to(dev)
+    v = torch.empty((R, H, D_v), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        kdt.vc_up_proj(o, w, out=v, err=err)
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0
+    times = []
+    with ClockSampler(dev.index or 0) as clk:
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            kdt.vc_up_proj(o, w, out=v, err=err)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) * 1e3)
+    assert int(err.item()) == 0
+    peaks = load_peaks()
+    nbytes = R * H * 512 * 4 + H * 512 * D_v * 2 + R * H * D_v * 4
+    flops = 2.0 * R * H * 512 * D_v
+    us = statistics.mean(times)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"metric": "w_vc up-projection time", "value": us, "unit": "us", "higher_is_better": False, "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "dtype": "f32 rows x bf16 weights (fp32-accurate)",
+            "data": "synthetic",
+            "config": {"workload": f"{args.config} verify output: R={R} rows (B*T), H={H}, D_c=512, D_v={D_v}",
+                       "l2": "flushed before each call"},
+            "us_median": statistics.median(times), "tflops": flops / (us * 1e-6) / 1e12,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "peak_basis": f"copy bandwidth ({peaks['source']})", "kernel": "vc_proj_kernel"},
+            "algorithmic": {"bytes": nbytes, "flops": flops,
+                            "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6},
+            "clocks": clk.summary(), "gpu_launches": args.steps}
+
+
 def workload_name(name):
     d = wl.CONFIGS[name]
     pre = d["prefix"]
@@ -309,6 +360,8 @@ def main():
                          "default 4, else 2, else 1)")
     ap.add_argument("--tree-ops", action="store_true",
                     help="time the steps around verify (tree build, RoPE, accept, compaction) instead")
+    ap.add_argument("--vc-proj", action="store_true",
+                    help="time the per-head w_vc up-projection of the verify output instead")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -344,6 +397,9 @@ def main():
     dev = torch.device("cuda", local_rank)
     if args.tree_ops:
         print(json.dumps(run_tree_ops(args, case, dev)), flush=True)
+        return 0
+    if args.vc_proj:
+        print(json.dumps(run_vc_proj(args, case, dev)), flush=True)
         return 0
 
     def conv(x):

@@ -236,6 +236,31 @@ kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const flo
                                  cudaStream_t stream);
 
 /*
+ * kdt_vc_up_proj -- per-head value up-projection of the latent attention output. The
+ * verify kernel returns the latent; "a follow-up matrix multiply applies the per-head
+ * value weights" (page "The Verify-Attn Kernel ...", section "Design Decisions and
+ * Trade-Offs"):
+ *
+ *   v[r, h, n] = sum_{d < D_c} o[r, h, d] * w_vc[h, d, n]        r < R, h < H, n < D_v
+ *
+ *   o      device fp32 [R, H, D_c]: e.g. kdt_verify_attn's `out` with R = B*T rows
+ *   w_vc   device [H, D_c, D_v] in w_dtype (bf16)
+ *   v      device fp32 [R, H, D_v], written whole; must not overlap o or w_vc
+ *   err    device int32, may be NULL: zeroed, then a negative code if an internal
+ *          pipeline wait expired (the kernel then returns early; v is incomplete)
+ * Sizes: D_c = 512, D_v 64 or 128, 1 <= H <= 1024, R >= 0, R*H <= 2^31.
+ * Arithmetic: fp32-accurate. Each o element is split into two bf16 parts whose sum is
+ * o to within 2^-18 |o|; both are multiplied by the bf16 weights on the tensor cores
+ * with fp32 accumulation.
+ * Errors: KDT_ERR_BAD_SHAPE (sizes, 16-byte alignment of o, w_vc and v),
+ * KDT_ERR_UNSUPPORTED (D_c, D_v, w_dtype other than KDT_BF16), KDT_ERR_NULL_ARG,
+ * KDT_ERR_NOT_DEVICE (a tensor not in device memory of the current device; its weights
+ * and rows are read through TMA tensor maps), KDT_ERR_CUDA.
+ */
+kdt_status kdt_vc_up_proj(const float *o, const void *w_vc, kdt_dtype w_dtype, int R, int H, int D_c, int D_v,
+                          float *v, int32_t *err, cudaStream_t stream);
+
+/*
  * kdt_verify_attn_noalloc -- kdt_verify_attn without a caller workspace.
  *
  * The method's pages have no counterpart to this entry point; it exists for

@@ -439,6 +439,20 @@ kdt_status kdt_verify_attn_host(const kdt_verify_args *a, int n_chunks, void *de
     return ok ? KDT_OK : KDT_ERR_CUDA;
 }
 
+kdt_status kdt_vc_up_proj(const float *o, const void *w_vc, kdt_dtype w_dtype, int R, int H, int D_c, int D_v,
+                          float *v, int32_t *err, cudaStream_t stream) {
+    if (R < 0 || H < 1 || H > 1024 || (int64_t)R * H > ((int64_t)1 << 31)) return KDT_ERR_BAD_SHAPE;
+    if (D_c != kDc || (D_v != 64 && D_v != 128) || w_dtype != KDT_BF16) return KDT_ERR_UNSUPPORTED;
+    if (R == 0) return KDT_OK;
+    if (!o || !w_vc || !v) return KDT_ERR_NULL_ARG;
+    if (!aligned16(o) || !aligned16(w_vc) || !aligned16(v) || (reinterpret_cast<uintptr_t>(err) & 3u))
+        return KDT_ERR_BAD_SHAPE;
+    kdt_status st = check_on_current_device({o, w_vc, v, err});
+    if (st != KDT_OK) return st;
+    if (err && cudaMemsetAsync(err, 0, sizeof(int32_t), stream) != cudaSuccess) return KDT_ERR_CUDA;
+    return launch_vc_proj(o, w_vc, R, H, D_v, v, err, stream) == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
+}
+
 kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
                                  int64_t rows, int D, float *o, float *lse, cudaStream_t stream) {
     if (rows < 0 || D < 4 || D > 4096 || (D & 3)) return KDT_ERR_BAD_SHAPE;

@@ -72,6 +72,12 @@ cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int 
 cudaError_t launch_merge_two(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
                              int64_t rows, int D, float *o, float *lse, cudaStream_t s);
 
+// K4: per-head value up-projection v[r, h, :D_v] = o[r, h, :512] . w_vc[h] (bf16 weights,
+// D_v 64 or 128), persistent tcgen05 tiles; err (may be NULL) gets a negative code if
+// an internal wait expired.
+cudaError_t launch_vc_proj(const float *o, const void *w_vc, int R, int H, int Dv, float *v, int32_t *err,
+                           cudaStream_t s);
+
 // Per-device SM count (cached).
 int sm_count();
 

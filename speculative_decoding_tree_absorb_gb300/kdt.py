@@ -26,7 +26,7 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 EXPORTS = ("kdt_status_str", "kdt_version", "kdt_build_visibility", "kdt_verify_attn",
            "kdt_verify_attn_workspace_size", "kdt_verify_attn_plan", "kdt_merge_attn_states",
            "kdt_verify_attn_noalloc", "kdt_rope_neox", "kdt_tree_accept", "kdt_kv_compact", "kdt_tree_build",
-           "kdt_verify_attn_host", "kdt_verify_attn_host_buffer_size")
+           "kdt_verify_attn_host", "kdt_verify_attn_host_buffer_size", "kdt_vc_up_proj")
 
 
 class KdtError(RuntimeError):
@@ -99,6 +99,9 @@ def lib():
         L.kdt_verify_attn_host.restype = ctypes.c_int
         L.kdt_verify_attn_host_buffer_size.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.c_int]
         L.kdt_verify_attn_host_buffer_size.restype = ctypes.c_size_t
+        L.kdt_vc_up_proj.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     vp, vp, vp]
+        L.kdt_vc_up_proj.restype = ctypes.c_int
         L.kdt_verify_attn_noalloc.argtypes = [ctypes.POINTER(VerifyArgs), vp]
         L.kdt_verify_attn_noalloc.restype = ctypes.c_int
         L.kdt_rope_neox.argtypes = [ctypes.POINTER(RopeArgs), vp]
@@ -274,6 +277,22 @@ def merge_attn_states(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
     _check(lib().kdt_merge_attn_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, D, _ptr(out),
                                        _ptr(lse), _stream_ptr(stream)), "kdt_merge_attn_states")
     return out, lse
+
+
+def vc_up_proj(o, w_vc, out=None, err=None, stream=None):
+    """Per-head value up-projection (kdt_vc_up_proj): o fp32 [..., H, 512] (e.g. the
+    verify output [B,T,H,512]), w_vc bf16 [H, 512, D_v] -> fp32 [..., H, D_v]."""
+    import torch
+    H, D_c = o.shape[-2], o.shape[-1]
+    D_v = w_vc.shape[-1]
+    if tuple(w_vc.shape[:2]) != (H, D_c):
+        raise ValueError("w_vc must be [H, D_c, D_v] matching o [..., H, D_c]")
+    R = o.numel() // (H * D_c) if o.numel() else 0
+    if out is None:
+        out = torch.empty(tuple(o.shape[:-1]) + (D_v,), dtype=torch.float32, device=o.device)
+    _check(lib().kdt_vc_up_proj(_ptr(o), _ptr(w_vc), _dtype_code(w_vc), R, H, D_c, D_v, _ptr(out), _ptr(err),
+                                _stream_ptr(stream)), "kdt_vc_up_proj")
+    return out
 
 
 def verify_attn_noalloc(q_nope, q_pe, c_kv, k_pe, prefix_len, *, out, lse=None, parent=None, vis=None,

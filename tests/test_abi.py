@@ -109,7 +109,18 @@ def test_host_checks_reject_bad_arguments(kdt):
     assert lib.kdt_build_visibility(None, 2, 5, None, None, None) == K.KDT_ERR_NULL_ARG
     assert lib.kdt_merge_attn_states(None, None, None, None, 4, 6, None, None, None) == K.KDT_ERR_BAD_SHAPE
     assert lib.kdt_merge_attn_states(None, None, None, None, 4, 512, None, None, None) == K.KDT_ERR_NULL_ARG
+    # the w_vc up-projection's host checks (fake device addresses, never dereferenced)
+    vc = lib.kdt_vc_up_proj
+    assert vc(0x10000, 0x20000, K.KDT_BF16, -1, 4, 512, 128, 0x30000, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert vc(0x10000, 0x20000, K.KDT_BF16, 8, 0, 512, 128, 0x30000, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert vc(0x10000, 0x20000, K.KDT_BF16, 8, 4, 256, 128, 0x30000, None, None) == K.KDT_ERR_UNSUPPORTED
+    assert vc(0x10000, 0x20000, K.KDT_BF16, 8, 4, 512, 100, 0x30000, None, None) == K.KDT_ERR_UNSUPPORTED
+    assert vc(0x10000, 0x20000, K.KDT_F32, 8, 4, 512, 128, 0x30000, None, None) == K.KDT_ERR_UNSUPPORTED
+    assert vc(None, 0x20000, K.KDT_BF16, 8, 4, 512, 128, 0x30000, None, None) == K.KDT_ERR_NULL_ARG
+    assert vc(0x10004, 0x20000, K.KDT_BF16, 8, 4, 512, 128, 0x30000, None, None) == K.KDT_ERR_BAD_SHAPE
+    assert vc(None, None, K.KDT_BF16, 0, 4, 512, 128, None, None, None) == K.KDT_OK     # nothing to do
     assert kdt.status_str(K.KDT_ERR_WORKSPACE) == "workspace missing or too small"
+    assert kdt.status_str(K.KDT_ERR_NOT_DEVICE).startswith("tensor not in device memory")
     assert lib.kdt_version() >= 100
 
 
