@@ -249,9 +249,10 @@ kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const flo
  *   err    device int32, may be NULL: zeroed, then a negative code if an internal
  *          pipeline wait expired (the kernel then returns early; v is incomplete)
  * Sizes: D_c = 512, D_v 64 or 128, 1 <= H <= 1024, R >= 0, R*H <= 2^31.
- * Arithmetic: fp32-accurate. Each o element is split into two bf16 parts whose sum is
- * o to within 2^-18 |o|; both are multiplied by the bf16 weights on the tensor cores
- * with fp32 accumulation.
+ * Arithmetic: each o element is split into two bf16 parts whose sum is o to within
+ * 2^-16 |o|; both are multiplied by the bf16 weights on the tensor cores with fp32
+ * accumulation, so the result meets the fp32 path's bound (1e-4 absolute + 1e-4
+ * relative) against the exact product.
  * Errors: KDT_ERR_BAD_SHAPE (sizes, 16-byte alignment of o, w_vc and v),
  * KDT_ERR_UNSUPPORTED (D_c, D_v, w_dtype other than KDT_BF16), KDT_ERR_NULL_ARG,
  * KDT_ERR_NOT_DEVICE (a tensor not in device memory of the current device; its weights

@@ -6,7 +6,7 @@ this package holds the build script and a thin ctypes binding with the same name
 from .kdt import (  # noqa: F401
     DEFAULT_SCALE, EXPORTS, IMPLS, KdtError, RopeArgs, VerifyArgs, build_visibility, host_buffer_size, kv_compact,
     lib, make_args, merge_attn_states, plan, rope_neox, status_str, tree_accept, tree_build, verify_attn,
-    verify_attn_host, verify_attn_noalloc, workspace_size,
+    vc_up_proj, verify_attn_host, verify_attn_noalloc, workspace_size,
 )
 
 __version__ = "0.1.0"

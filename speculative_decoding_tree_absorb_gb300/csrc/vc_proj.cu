@@ -11,10 +11,11 @@
 //    HBM-bound, and the tensor cores are what keeps the contraction below the memory
 //    time (fp32 FMA alone would take four times longer than the bytes).
 //  * Precision: o is fp32 and w_vc bf16. Each o element is split into two bf16 parts,
-//    hi = bf16(o) and lo = bf16(o - hi), so o = hi + lo to within 2^-18 |o|; both parts
+//    hi = bf16(o) and lo = bf16(o - hi), so o = hi + lo to within 2^-16 |o| (bf16's unit
+//    roundoff 2^-8, squared: |o - hi| <= 2^-8 |o| and lo rounds that again); both parts
 //    are multiplied by the (exact) bf16 weights on the tensor cores, accumulating in
-//    fp32 in tensor memory. The result is fp32-accurate at twice the MMA work, which
-//    still hides under the memory time.
+//    fp32 in tensor memory. The result meets the fp32 path's bound at twice the MMA
+//    work, which still hides under the memory time.
 //  * Work: tiles of 128 rows of one head (M = 128, cta_group::1), persistent CTAs (one
 //    per SM) taking tiles in head-major order, so the CTAs running at once share a few
 //    heads' weights in L2. Per 64-wide latent chunk: the fp32 rows arrive by TMA into a

@@ -80,9 +80,9 @@ def test_vc_up_proj_of_verify_output(kdt, oracle_mod):
 
 
 def test_vc_up_proj_one_hot_weights_are_exact(kdt):
-    # one-hot weights select latent dims: only the split of o into bf16 parts and its
-    # exact recombination are involved, so the result equals the selected dims to within
-    # 2^-18 of their magnitude
+    # one-hot weights select latent dims: only the split of o into two bf16 parts is
+    # involved (hi = bf16(o) is off by at most 2^-8 |o|, and lo = bf16(o - hi) by 2^-8 of
+    # that), so the result equals the selected dims to within 2^-16 of their magnitude
     Hh, R = 2, 200
     o = wl.normal(4, "vc_sel", R * Hh * 512).reshape(R, Hh, 512).astype(np.float32)
     sel = np.stack([(np.arange(128) * 5 + 11 * h) % 512 for h in range(Hh)])
@@ -92,7 +92,7 @@ def test_vc_up_proj_one_hot_weights_are_exact(kdt):
     got = _run(kdt, o, wl.f64_to_bf16_bits(w))
     for h in range(Hh):
         want = o[:, h, sel[h]].astype(np.float64)
-        assert np.all(np.abs(got[:, h] - want) <= 2.0 ** -18 * np.abs(want) + 1e-30)
+        assert np.all(np.abs(got[:, h] - want) <= 2.0 ** -16 * np.abs(want) + 1e-30)
 
 
 def test_vc_up_proj_refuses_host_memory_and_bad_sizes(kdt):
