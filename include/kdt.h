@@ -237,9 +237,9 @@ kdt_status kdt_merge_attn_states(const float *o_a, const float *lse_a, const flo
 
 /*
  * kdt_vc_up_proj -- per-head value up-projection of the latent attention output. The
- * verify kernel returns the latent; "a follow-up matrix multiply applies the per-head
- * value weights" (page "The Verify-Attn Kernel ...", section "Design Decisions and
- * Trade-Offs"):
+ * verify kernel stops at the latent, and each head's value weights are applied by a
+ * separate GEMM after it (page "The Verify-Attn Kernel ...", section "Design Decisions
+ * and Trade-Offs"):
  *
  *   v[r, h, n] = sum_{d < D_c} o[r, h, d] * w_vc[h, d, n]        r < R, h < H, n < D_v
  *

@@ -9,10 +9,11 @@
  *
  * Sources (page titles of the method's write-up):
  *  - "The Verify-Attn Kernel: A Single File Write ..." -- section "The Design
- *    Journey: From Concept to CUDA": the score is the absorbed-query dot with the
- *    cached latent plus the rope dot; a query sees only the shared prefix and its
- *    own ancestors; softmax with max subtraction; output is the latent (w_vc stays
- *    outside), section "Design Decisions and Trade-Offs"; the per-row
+ *    Journey: From Concept to CUDA": a score adds two dot products, the absorbed
+ *    query against the latent row and the rope query against the rope key; a query
+ *    sees only the shared prefix and its own ancestors; softmax with max
+ *    subtraction; output is the latent (w_vc stays outside), section "Design
+ *    Decisions and Trade-Offs"; the per-row
  *    log-sum-exp feeds the prefix/tail merge described there.
  *  - same page, section "Assumptions and the Path Forward": every query sees at
  *    least its own position.

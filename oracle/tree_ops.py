@@ -32,8 +32,8 @@ import numpy as np
 # ---------------------------------------------------------------- NeoX RoPE --
 def rope_neox(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
     """NeoX rotary embedding ("The Query-Split Kernel: A Pivotal Edit ...", "Input
-    Knowledge: What One Must Understand to Grasp This Edit": the vector is split in half
-    and each half is rotated by a position-dependent angle, the angles taken in float64
+    Knowledge: What One Must Understand to Grasp This Edit": element j pairs with element
+    j + d/2 and the pair turns by an angle that grows with the position, the angles in float64
     to match a numpy reference; the engine itself computes in float32, "The Architecture
     of an Inference Engine ...", "The Context: Building an Engine from Scratch").
 
@@ -188,8 +188,8 @@ def tree_build(cand_tok: np.ndarray, cand_lp: np.ndarray, N: int, root_tok=None)
 def vc_up_proj(o: np.ndarray, w_vc: np.ndarray, w_dtype: str = "bf16") -> np.ndarray:
     """Per-head value up-projection of the latent attention output ("The Verify-Attn
     Kernel: A Single File Write ...", "Design Decisions and Trade-Offs": the attention
-    kernel returns the latent, and a separate matrix multiply then applies each head's
-    value weights, as SGLang structures it).
+    output stays in the latent space and the value projection of each head is its own
+    GEMM afterwards, the split SGLang uses).
 
         v[..., h, n] = sum_{d < D_c} o[..., h, d] * w_vc[h, d, n]
 

@@ -300,7 +300,7 @@ kdt_status kdt_verify_attn(const kdt_verify_args *a, void *workspace, size_t ws_
 namespace kdt {
 
 kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t ws_bytes, cudaStream_t stream,
-                               bool check_tensors, bool check_workspace) {
+                               bool check_tensors, bool check_workspace, const TestHooks *hooks) {
     Plan p;
     kdt_status st = make_plan(a, &p);
     if (st != KDT_OK) return st;
@@ -338,6 +338,10 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
     vp.part_lse = partials ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
     vp.err = a->err;
     vp.tc_clusters = p.tc_clusters;
+    if (hooks) {
+        vp.wait_ns = hooks->wait_ns;
+        vp.fault = hooks->fault;
+    }
 
     if (a->parent) {
         uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);
@@ -361,6 +365,16 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
 }  // namespace kdt
 
 extern "C" {
+
+kdt_status kdt_test_verify_attn_wait_expiry(const kdt_verify_args *a, void *workspace, size_t ws_bytes,
+                                            uint32_t wait_us, cudaStream_t stream) {
+    Plan p;
+    kdt_status st = make_plan(a, &p);
+    if (st != KDT_OK) return st;
+    if (p.impl != KDT_IMPL_TCGEN05 || wait_us < 100 || wait_us > 1000000) return KDT_ERR_UNSUPPORTED;
+    const TestHooks hooks{(uint64_t)wait_us * 1000ull, 1};
+    return verify_attn_checked(a, workspace, ws_bytes, stream, true, true, &hooks);
+}
 
 size_t kdt_verify_attn_host_buffer_size(const kdt_verify_args *a, int n_chunks) {
     HostLayout L;

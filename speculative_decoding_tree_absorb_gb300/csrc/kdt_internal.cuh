@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "kdt.h"
+#include "kdt_testing.h"
 
 namespace kdt {
 
@@ -45,6 +46,10 @@ struct VerifyParams {
     // Tensor-core path: the resident clusters the work is split across; part_o/part_lse
     // then hold [2 * tc_clusters][256] partial states (unused when tc_clusters == 1).
     int tc_clusters;
+    // Tensor-core path, test hooks only: wait limit in ns (0 = the default 200 ms) and an
+    // arrival to withhold (0 = none, 1 = the first item's Q-ready arrivals).
+    uint64_t wait_ns = 0;
+    int fault = 0;
 };
 
 // K0: parent -> packed ancestor bits.
@@ -85,7 +90,12 @@ int sm_count();
 // (check_tensors) and the workspace (check_workspace) must be device memory of the current
 // device. Entry points whose buffers are already known to be (the host pipeline's chunks
 // inside its checked device buffer, the no-allocation entry's library array) skip them.
+// `hooks` (may be NULL) carries the tensor-core kernel's test hooks.
+struct TestHooks {
+    uint64_t wait_ns;
+    int fault;
+};
 kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t ws_bytes, cudaStream_t stream,
-                               bool check_tensors, bool check_workspace);
+                               bool check_tensors, bool check_workspace, const TestHooks *hooks = nullptr);
 
 }  // namespace kdt

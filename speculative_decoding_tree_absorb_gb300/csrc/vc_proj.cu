@@ -1,9 +1,9 @@
 // K4: per-head value up-projection of the latent attention output (tcgen05).
 //
 // The verify kernel returns the latent o[r, h, :512] (r = b*T + i); the head's value
-// is v[r, h, :] = o[r, h, :] . w_vc[h] with w_vc[h] of shape [512, D_v]: "a follow-up
-// matrix multiply applies the per-head value weights" (page "The Verify-Attn Kernel:
-// A Single File Write ...", section "Design Decisions and Trade-Offs").
+// is v[r, h, :] = o[r, h, :] . w_vc[h] with w_vc[h] of shape [512, D_v], a GEMM kept
+// apart from the attention kernel (page "The Verify-Attn Kernel: A Single File Write
+// ...", section "Design Decisions and Trade-Offs").
 //
 // GB300 design:
 //  * Per head this is a dense contraction M = rows x N = D_v x K = 512. Its arithmetic
@@ -18,14 +18,15 @@
 //    work, which still hides under the memory time.
 //  * Work: tiles of 128 rows of one head (M = 128, cta_group::1), persistent CTAs (one
 //    per SM) taking tiles in head-major order, so the CTAs running at once share a few
-//    heads' weights in L2. Per 64-wide latent chunk: the fp32 rows arrive by TMA into a
-//    2-slot staging ring, four converter warps write hi and lo as 128B-swizzled K-major
-//    bf16 tiles, the weights arrive by TMA as MN-major tiles, and one thread issues the
-//    MMAs. The accumulator is double-buffered in tensor memory (2 x D_v columns) so one
-//    tile's epilogue (four warps, rows transposed through shared memory into whole
-//    128-byte line stores) overlaps the next tile's loads and MMAs.
-//  * Every wait is bounded; on expiry the kernel records a negative code in the error
-//    word, lets the other roles leave, drains its MMAs, frees tensor memory and returns.
+//    heads' weights in L2. Per 64-wide latent chunk the fp32 rows arrive by TMA (two
+//    128B-swizzled [128 x 32] boxes) into a 5-slot staging ring, so about 160 KB per SM
+//    are in flight; eight converter warps (one row per thread, half a chunk per warp)
+//    write hi and lo into tensor memory with tcgen05.st, where the MMA reads its A
+//    operand, so shared memory holds only the staging, the weights and the epilogue
+//    transpose. The weights arrive by TMA as MN-major tiles; one thread issues the MMAs.
+//    The accumulator is double-buffered in tensor memory (2 x 128 columns, next to two
+//    64-column A slots) so one tile's epilogue (four warps, rows transposed through
+//    shared memory into whole 128-byte line stores) overlaps the next tile's loads.
 #include "kdt_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -39,23 +40,27 @@ using namespace tc;
 constexpr int kVRows = 128;                  // rows of a tile (MMA M)
 constexpr int kVChunk = 64;                  // latent dims per chunk (one 128-byte bf16 row)
 constexpr int kVChunks = kDc / kVChunk;      // 8
-constexpr int kVThreads = 384;               // 12 warps
-constexpr int kNF = 2;                       // fp32 staging slots
-constexpr int kNA = 2;                       // bf16 operand slots (hi + lo)
+constexpr int kVThreads = 512;               // 16 warps
+constexpr int kNF = 5;                       // fp32 staging slots
+constexpr int kNA = 2;                       // tensor-memory A slots (hi + lo of one chunk)
 constexpr int kNW = 3;                       // weight slots
-constexpr int kF32Bytes = kVRows * kVChunk * 4;     // 32 KB
-constexpr int kAHalf = kVRows * kVChunk * 2;        // 16 KB: one bf16 part
-constexpr int kASlot = 2 * kAHalf;                  // hi then lo
+constexpr int kConvWarps = 8;                // converter warps 4..11
+constexpr int kF32Box = kVRows * 32 * 4;            // [128 rows x 32 fp32], 128B-swizzled: 16 KB
+constexpr int kF32Bytes = 2 * kF32Box;              // one chunk: 32 KB
 constexpr int kWSub = kVChunk * 128;                // [64 latent rows x 64 value cols] bf16: 8 KB
 constexpr int kMaxDv = 128;
 constexpr int kWSlot = (kMaxDv / 64) * kWSub;       // 16 KB
 constexpr int kOffF = 0;
-constexpr int kOffA = kOffF + kNF * kF32Bytes;
-constexpr int kOffW = kOffA + kNA * kASlot;
+constexpr int kOffW = kOffF + kNF * kF32Bytes;
 constexpr int kOffEpi = kOffW + kNW * kWSlot;
 constexpr int kVTile = kOffEpi + 4 * 32 * 32 * 4;
 constexpr int kVSmem = kVTile + 1024;
 static_assert(kVSmem <= 227 * 1024, "shared memory budget");
+// Tensor memory: accumulators at columns [0, 256), A slot s at 256 + 64 s (hi: 32 columns
+// of packed bf16 pairs, then lo).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = kMaxDv;
+constexpr uint32_t kACol0 = 2 * kAccCols;
 constexpr uint64_t kVWaitLimit = 200000000ull;      // ns a wait may poll before giving up
 
 struct VBars {
@@ -97,6 +102,16 @@ __device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
 __device__ __forceinline__ float bf16_lo_as_f32(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float bf16_hi_as_f32(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
 
+// 32 lanes x 16 consecutive 32-bit columns: thread t of the warp writes lane (base + t).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 __global__ void __launch_bounds__(kVThreads, 1)
     vc_proj_kernel(const __grid_constant__ CUtensorMap map_o, const __grid_constant__ CUtensorMap map_w,
                    const VParams p) {
@@ -111,8 +126,8 @@ __global__ void __launch_bounds__(kVThreads, 1)
     const int my_tiles = p.tiles > (int)blockIdx.x ? (p.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNF; ++i) { mbar_init(&bar.f_full[i], 1); mbar_init(&bar.f_empty[i], 4); }
-        for (int i = 0; i < kNA; ++i) { mbar_init(&bar.a_full[i], 4); mbar_init(&bar.a_empty[i], 1); }
+        for (int i = 0; i < kNF; ++i) { mbar_init(&bar.f_full[i], 1); mbar_init(&bar.f_empty[i], kConvWarps); }
+        for (int i = 0; i < kNA; ++i) { mbar_init(&bar.a_full[i], kConvWarps); mbar_init(&bar.a_empty[i], 1); }
         for (int i = 0; i < kNW; ++i) { mbar_init(&bar.w_full[i], 1); mbar_init(&bar.w_empty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&bar.acc_full[i], 1); mbar_init(&bar.acc_empty[i], 4); }
         mbar_init(&bar.drain, 1);
@@ -120,7 +135,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&bar.tmem_base, 256);               // two accumulators of up to 128 columns
+        tmem_alloc(&bar.tmem_base, kTmemCols);         // two accumulators, two A slots
         tmem_relinquish();
     }
     tc_fence_before();
@@ -128,39 +143,44 @@ __global__ void __launch_bounds__(kVThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bar.tmem_base;
 
-    if (warp == 0) {
-        // ---------------- TMA producer: fp32 rows of o and the head's weights ----------------
+    if (warp == 0 || warp == 2) {
+        // ---------------- TMA producers: warp 0 the fp32 rows of o, warp 2 the weights -------
+        // (separate threads, so the shallower weight ring never holds up the row loads)
         if (elect_one() && my_tiles > 0) {
-            tma_prefetch_desc(&map_o);
-            tma_prefetch_desc(&map_w);
+            const bool rows = warp == 0;
+            tma_prefetch_desc(rows ? &map_o : &map_w);
+            const int depth = rows ? kNF : kNW;
+            uint64_t *full = rows ? bar.f_full : bar.w_full;
+            uint64_t *empty = rows ? bar.f_empty : bar.w_empty;
             bool ok = true;
-            int nf = 0, nw = 0;                          // staging and weight loads issued
+            int n = 0;                                   // loads issued
             for (int k = 0; k < my_tiles && ok; ++k) {
                 const int t = (int)blockIdx.x + k * (int)gridDim.x;
                 const int h = t / p.row_tiles, r0 = (t % p.row_tiles) * kVRows;
-                for (int c = 0; c < kVChunks && ok; ++c) {
+                for (int c = 0; c < kVChunks; ++c) {
                     const int g = k * kVChunks + c;
-                    const int fs = g % kNF, ws = g % kNW;
-                    if (g >= kNF && !(ok = v_wait(bar, &bar.f_empty[fs], (uint32_t)((g / kNF) - 1) & 1, p.err, -31)))
+                    const int sl = g % depth;
+                    if (g >= depth &&
+                        !(ok = v_wait(bar, &empty[sl], (uint32_t)((g / depth) - 1) & 1, p.err, rows ? -31 : -32)))
                         break;
-                    mbar_arrive_expect_tx(&bar.f_full[fs], kF32Bytes);
-                    tma_load_3d(smem + kOffF + fs * kF32Bytes, &map_o, &bar.f_full[fs], c * kVChunk, h, r0);
-                    ++nf;
-                    if (g >= kNW && !(ok = v_wait(bar, &bar.w_empty[ws], (uint32_t)((g / kNW) - 1) & 1, p.err, -32)))
-                        break;
-                    mbar_arrive_expect_tx(&bar.w_full[ws], w_bytes);
-                    for (int n = 0; n < n_sub; ++n)
-                        tma_load_3d(smem + kOffW + ws * kWSlot + n * kWSub, &map_w, &bar.w_full[ws], 64 * n,
-                                    c * kVChunk, h);
-                    ++nw;
+                    if (rows) {
+                        mbar_arrive_expect_tx(&full[sl], kF32Bytes);
+                        for (int hh = 0; hh < 2; ++hh)
+                            tma_load_3d(smem + kOffF + sl * kF32Bytes + hh * kF32Box, &map_o, &full[sl],
+                                        c * kVChunk + 32 * hh, h, r0);
+                    } else {
+                        mbar_arrive_expect_tx(&full[sl], w_bytes);
+                        for (int nn = 0; nn < n_sub; ++nn)
+                            tma_load_3d(smem + kOffW + sl * kWSlot + nn * kWSub, &map_w, &full[sl], 64 * nn,
+                                        c * kVChunk, h);
+                    }
+                    ++n;
                 }
             }
             // every copy issued has landed and been consumed before the CTA may leave
             // (bounded: on the error path a use nobody consumes times out)
-            for (int g = nf - kNF > 0 ? nf - kNF : 0; g < nf; ++g)
-                mbar_wait(&bar.f_empty[g % kNF], (uint32_t)(g / kNF) & 1, kVWaitLimit);
-            for (int g = nw - kNW > 0 ? nw - kNW : 0; g < nw; ++g)
-                mbar_wait(&bar.w_empty[g % kNW], (uint32_t)(g / kNW) & 1, kVWaitLimit);
+            for (int g = n - depth > 0 ? n - depth : 0; g < n; ++g)
+                mbar_wait(&empty[g % depth], (uint32_t)(g / depth) & 1, kVWaitLimit);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer: acc (+)= hi . W + lo . W over the 8 chunks --------------
@@ -172,20 +192,19 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 if (k >= 2 && !(ok = v_wait(bar, &bar.acc_empty[buf], (uint32_t)((k >> 1) - 1) & 1, p.err, -33)))
                     break;
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(buf * kMaxDv);
+                const uint32_t d = tmem + (uint32_t)buf * kAccCols;
                 for (int c = 0; c < kVChunks && ok; ++c) {
                     const int g = k * kVChunks + c;
                     const int as = g % kNA, ws = g % kNW;
                     if (!(ok = v_wait(bar, &bar.a_full[as], (uint32_t)(g / kNA) & 1, p.err, -34))) break;
                     if (!(ok = v_wait(bar, &bar.w_full[ws], (uint32_t)(g / kNW) & 1, p.err, -35))) break;
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smem + kOffA + as * kASlot);
+                    const uint32_t a0 = tmem + kACol0 + (uint32_t)(as * 64);
                     const uint32_t w0 = smem_u32(smem + kOffW + ws * kWSlot);
                     for (int part = 0; part < 2; ++part)
                         for (int kk = 0; kk < kVChunk / 16; ++kk) {
-                            const uint64_t adesc = sdesc_sw128(a0 + part * kAHalf + kk * 32, 16, 1024);
                             const uint64_t bdesc = sdesc_sw128(w0 + kk * 2048, kWSub, 1024);
-                            mma_ss(d, adesc, bdesc, idesc, (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                            mma_ts(d, a0 + 32 * part + 8 * kk, bdesc, idesc, (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
                         }
                     mma_commit(&bar.a_empty[as]);
                     mma_commit(&bar.w_empty[ws]);
@@ -195,9 +214,14 @@ __global__ void __launch_bounds__(kVThreads, 1)
             mma_commit(&bar.drain);                   // every MMA of this CTA has completed
             mbar_wait(&bar.drain, 0, kVWaitLimit);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- converters: fp32 -> bf16 hi and lo, 128B-swizzled K-major -----------
-        const int tid = threadIdx.x - 128;
+    } else if (warp >= 4 && warp < 4 + kConvWarps) {
+        // ---------------- converters: fp32 -> bf16 hi and lo into tensor memory ---------------
+        // Warp w serves TMEM lane quadrant w % 4 (rows 32 (w % 4) + lane, one per thread) and
+        // latent dims [32 hh, 32 hh + 32) of each chunk, hh = (w - 4) / 4: its rows of the
+        // staged box hh, 128B-swizzled (16-byte unit u of row r at u ^ (r % 8)).
+        const int q = warp & 3, hh = (warp - 4) >> 2;
+        const int row = 32 * q + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         bool ok = true;
         for (int k = 0; k < my_tiles && ok; ++k) {
             for (int c = 0; c < kVChunks && ok; ++c) {
@@ -208,24 +232,23 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     ok = __all_sync(0xffffffffu,
                                     v_wait(bar, &bar.a_empty[as], (uint32_t)((g / kNA) - 1) & 1, p.err, -37));
                 if (!ok) break;
-                const float4 *src = reinterpret_cast<const float4 *>(smem + kOffF + fs * kF32Bytes);
-                unsigned char *hi = smem + kOffA + as * kASlot;
-                unsigned char *lo = hi + kAHalf;
-#pragma unroll 4
-                for (int j = 0; j < 16; ++j) {
-                    const int f = tid + 128 * j;            // float4 f of the [128 x 64] chunk
-                    const int r = f >> 4, c4 = f & 15;
-                    const float4 x = src[f];
+                tc_fence_after();
+                const unsigned char *src = smem + kOffF + fs * kF32Bytes + hh * kF32Box + row * 128;
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src + ((u ^ (row & 7)) << 4));
                     const uint32_t h01 = pack2_bf16(x.x, x.y), h23 = pack2_bf16(x.z, x.w);
-                    const uint32_t l01 = pack2_bf16(x.x - bf16_lo_as_f32(h01), x.y - bf16_hi_as_f32(h01));
-                    const uint32_t l23 = pack2_bf16(x.z - bf16_lo_as_f32(h23), x.w - bf16_hi_as_f32(h23));
-                    // element 4 c4 of row r: 16-byte unit c4 / 2 of the row, swizzled by row % 8
-                    const uint32_t off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((c4 >> 1) ^ (r & 7))) << 4) +
-                                                    (c4 & 1) * 8);
-                    *reinterpret_cast<uint2 *>(hi + off) = make_uint2(h01, h23);
-                    *reinterpret_cast<uint2 *>(lo + off) = make_uint2(l01, l23);
+                    hi[2 * u] = h01;
+                    hi[2 * u + 1] = h23;
+                    lo[2 * u] = pack2_bf16(x.x - bf16_lo_as_f32(h01), x.y - bf16_hi_as_f32(h01));
+                    lo[2 * u + 1] = pack2_bf16(x.z - bf16_lo_as_f32(h23), x.w - bf16_hi_as_f32(h23));
                 }
-                fence_proxy_async_smem();                    // the MMA reads through the async proxy
+                const uint32_t a0 = tmem + lane_base + kACol0 + (uint32_t)(as * 64 + 16 * hh);
+                tmem_st16(a0, hi);
+                tmem_st16(a0 + 32, lo);
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&bar.a_full[as]);
@@ -233,7 +256,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 }
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 4 + kConvWarps) {
         // ---------------- epilogue: accumulator rows -> v[r, h, :] ----------------------------
         const int q = warp & 3;                              // TMEM lane quadrant of this warp
         float *stg = reinterpret_cast<float *>(smem + kOffEpi) + q * 32 * 32;
@@ -251,7 +274,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
             float *vrow0 = p.v + ((int64_t)r0 * p.H + h) * p.Dv;
             for (int cc = 0; cc < p.Dv / 32; ++cc) {
                 uint32_t rv[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kMaxDv + 32 * cc), rv);
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * kAccCols + (uint32_t)(32 * cc), rv);
                 tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
@@ -277,7 +300,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -309,13 +332,13 @@ cudaError_t launch_vc_proj(const float *o, const void *w_vc, int R, int H, int D
     memset(&map_o, 0, sizeof(map_o));
     memset(&map_w, 0, sizeof(map_w));
     {
-        // o as [R rows][H heads][512] fp32; a box is one head's 64-dim chunk of 128 rows
+        // o as [R rows][H heads][512] fp32; a box is 32 dims (128 bytes) of one head's 128 rows
         const cuuint64_t dims[3] = {(cuuint64_t)kDc, (cuuint64_t)H, (cuuint64_t)R};
         const cuuint64_t strides[2] = {(cuuint64_t)kDc * 4, (cuuint64_t)H * kDc * 4};
-        const cuuint32_t box[3] = {kVChunk, 1, kVRows};
+        const cuuint32_t box[3] = {32, 1, kVRows};
         const cuuint32_t es[3] = {1, 1, 1};
         if (fn(&map_o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(o), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }

@@ -124,7 +124,7 @@ constexpr int kNP = 4;                            // O-CTA P slots (free once P.
 constexpr int kVSlotBytes = 2 * kVSub;            // O ring slot: 128 keys x 128 latent dims
 constexpr int kNV = 2;                            // O-CTA value ring slots (64 KB)
 constexpr uint32_t kCmdDone = 0xffffffffu;        // correction command: no more rescales
-constexpr uint64_t kWaitLimit = 200000000ull;     // ns a wait may poll before giving up
+constexpr uint64_t kWaitLimit = 200000000ull;     // ns a wait may poll before giving up (default)
 constexpr float kRescaleThreshold = 20.0f;        // log2 units
 
 // Shared-memory layout (same offsets in every CTA of the cluster; roles use
@@ -185,6 +185,7 @@ struct Barriers {
     int work_count;                      // its key blocks
     uint32_t tmem_base;
     int abort_flag;
+    uint64_t wait_ns;              // how long a wait may poll before the kernel gives up
 };
 
 struct TcParams {
@@ -201,6 +202,8 @@ struct TcParams {
     float *part_o, *part_lse;      // [2 * clusters][256] partial states of units cut by the work split
     int32_t *err;
     int pairs_per_seq;             // work units (two row tiles each) per sequence
+    uint64_t wait_ns;              // wait limit (kWaitLimit unless a test shortens it)
+    int fault;                     // test hook: 1 = withhold the first item's Q-ready arrivals
 };
 
 // ---- work decomposition ----------------------------------------------------------------
@@ -209,9 +212,14 @@ struct TcParams {
 //  * when every sequence has the same block count, the first (units / C) * C units go out
 //    whole, round robin (cluster c takes units c, c + C, ...): the clusters running at the
 //    same time then walk the same few sequences' keys in step and share them in L2;
-//  * the remaining units (all of them when lengths differ) form the tail: their blocks,
-//    units in order, are split into C contiguous ranges [Wt c / C, Wt (c + 1) / C), so every
-//    cluster gets the same number of blocks (+-1) whatever the wave count.
+//  * the remaining units (all of them when lengths differ) form the tail, cut into C
+//    contiguous ranges of equal COST, units in order: a unit costs its key blocks plus
+//    kItemCost blocks for the item boundary (the epilogue, the next Q load and the pipeline
+//    refill between two items take about as long as that many blocks). In "virtual blocks"
+//    unit u spans kItemCost boundary blocks followed by its key blocks, the tail spans Wv
+//    of them, and cluster c takes the key blocks whose virtual positions fall in
+//    [Wv c / C, Wv (c + 1) / C). Equal block counts alone left clusters that met many
+//    short units (ragged prefixes) with several more boundaries than others.
 // Everything is derived from prefix_len on the device, the same way in every CTA. A tail
 // unit cut by a range boundary is processed in pieces: each piece writes its normalised
 // partial state (o, lse) into slot 2c (the first item of the cluster's tail range) or
@@ -229,33 +237,43 @@ __device__ __forceinline__ int tail_first_unit(const TcParams &p, int C) {
     return (units / C) * C;
 }
 
-// Blocks of the tail (units u_first ..).
-__device__ __forceinline__ int64_t tail_blocks(const TcParams &p, int u_first) {
+constexpr int kItemCost = 6;   // an item boundary, in key blocks of time
+
+// Virtual blocks of the tail (units u_first ..): kItemCost + the key blocks of each unit.
+__device__ __forceinline__ int64_t tail_vblocks(const TcParams &p, int u_first) {
     int64_t w = 0;
     for (int b = u_first / p.pairs_per_seq, k0 = u_first % p.pairs_per_seq; b < p.B; ++b, k0 = 0)
-        w += (int64_t)(p.pairs_per_seq - k0) * seq_blocks(p, b);
+        w += (int64_t)(p.pairs_per_seq - k0) * (kItemCost + seq_blocks(p, b));
     return w;
 }
 
-// Tail unit holding tail block s, its first tail block and its block count.
-__device__ __forceinline__ void locate_block(const TcParams &p, int u_first, int64_t s, int &u, int64_t &start,
-                                             int &nblk) {
-    int64_t acc = 0;
+// Where virtual position s of the tail falls: unit u, that unit's first key block in the
+// tail's key-block numbering (start), its block count, and pos = the first key block at
+// or after s (start when s lies in the unit's boundary part). s = Wv gives u = units and
+// pos = the tail's key-block count.
+__device__ __forceinline__ void locate_vblock(const TcParams &p, int u_first, int64_t s, int &u, int64_t &start,
+                                              int &nblk, int64_t &pos) {
+    int64_t acc_v = 0, acc_r = 0;
     for (int b = u_first / p.pairs_per_seq, k0 = u_first % p.pairs_per_seq; b < p.B; ++b, k0 = 0) {
         const int nb = seq_blocks(p, b);
-        const int64_t seq = (int64_t)(p.pairs_per_seq - k0) * nb;
-        if (s < acc + seq) {
-            const int k = (int)((s - acc) / nb);
-            u = b * p.pairs_per_seq + k0 + k;
-            start = acc + (int64_t)k * nb;
+        const int64_t vs = kItemCost + nb;                    // virtual size of one unit
+        const int64_t k = p.pairs_per_seq - k0;               // tail units of this sequence
+        if (s < acc_v + k * vs) {
+            const int64_t kk = (s - acc_v) / vs;
+            u = b * p.pairs_per_seq + k0 + (int)kk;
+            start = acc_r + kk * nb;
             nblk = nb;
+            const int64_t into = s - acc_v - kk * vs - kItemCost;   // key blocks of the unit before s
+            pos = start + (into > 0 ? into : 0);
             return;
         }
-        acc += seq;
+        acc_v += k * vs;
+        acc_r += k * nb;
     }
     u = p.B * p.pairs_per_seq;
-    start = acc;
+    start = acc_r;
     nblk = 0;
+    pos = acc_r;
 }
 
 struct Item {
@@ -317,7 +335,7 @@ __device__ __forceinline__ bool aborted(const Barriers &bar) {
 // the completion also arrives on the drain barrier of the other CTAs in `mask`.
 __device__ __forceinline__ void drain_mmas(Barriers &bar, uint16_t mask) {
     mma_commit_pair(&bar.drain, mask);
-    mbar_wait(&bar.drain, 0, kWaitLimit);
+    mbar_wait(&bar.drain, 0, bar.wait_ns);
 }
 
 __device__ __forceinline__ void set_abort(Barriers &bar, int32_t *err, int code) {
@@ -331,7 +349,7 @@ __device__ __forceinline__ void set_abort(Barriers &bar, int32_t *err, int code)
 // store (flags, commands, statistics) wait with cluster-scope acquire.
 __device__ __forceinline__ bool wait_or_abort(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err, int code) {
     if (*reinterpret_cast<volatile int *>(&bar.abort_flag)) return false;
-    if (mbar_wait(b, parity, kWaitLimit)) return true;
+    if (mbar_wait(b, parity, bar.wait_ns)) return true;
     set_abort(bar, err, code);
     return false;
 }
@@ -339,7 +357,7 @@ __device__ __forceinline__ bool wait_or_abort(Barriers &bar, uint64_t *b, uint32
 __device__ __forceinline__ bool wait_cluster_or_abort(Barriers &bar, uint64_t *b, uint32_t parity, int32_t *err,
                                                       int code) {
     if (*reinterpret_cast<volatile int *>(&bar.abort_flag)) return false;
-    if (mbar_wait_cluster(b, parity, kWaitLimit)) return true;
+    if (mbar_wait_cluster(b, parity, bar.wait_ns)) return true;
     set_abort(bar, err, code);
     return false;
 }
@@ -387,7 +405,7 @@ __device__ __forceinline__ void ring_advance(RingPos &r) {
 // Wait until the releases of the last (up to kSlots) uses of a ring have arrived: the
 // copies into those slots have landed and been read, and no arrival is still in flight.
 template <int kSlots>
-__device__ __forceinline__ void ring_drain(uint64_t *empty, const RingPos &r) {
+__device__ __forceinline__ void ring_drain(uint64_t *empty, const RingPos &r, uint64_t limit_ns) {
     const int outstanding = r.n < kSlots ? r.n : kSlots;
     int s = r.slot;
     uint32_t ph = r.phase;
@@ -396,7 +414,7 @@ __device__ __forceinline__ void ring_drain(uint64_t *empty, const RingPos &r) {
             s = kSlots - 1;
             ph ^= 1;
         }
-        mbar_wait(&empty[s], ph, kWaitLimit);
+        mbar_wait(&empty[s], ph, limit_ns);
     }
 }
 
@@ -540,15 +558,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         {
             const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
             const int u_first = tail_first_unit(p, C);
-            const int64_t Wt = tail_blocks(p, u_first);
-            const int64_t s0 = Wt * c / C, s1 = Wt * (c + 1) / C;
-            int u0, nblk0;
-            int64_t start0;
-            locate_block(p, u_first, s0, u0, start0, nblk0);
+            const int64_t Wv = tail_vblocks(p, u_first);
+            int u0, nblk0, u1, nblk1;
+            int64_t start0, pos0, start1, pos1;
+            locate_vblock(p, u_first, Wv * c / C, u0, start0, nblk0, pos0);
+            locate_vblock(p, u_first, Wv * (c + 1) / C, u1, start1, nblk1, pos1);
             bar.work_wleft = u_first / C;
             bar.work_u0 = u0;
-            bar.work_kb0 = (int)(s0 - start0);
-            bar.work_left = (int)(s1 - s0);
+            bar.work_kb0 = (int)(pos0 - start0);
+            bar.work_left = (int)(pos1 - pos0);
             bar.work_count = bar.work_wleft * (u_first > 0 ? seq_blocks(p, 0) : 0) + bar.work_left;
         }
         for (int i = 0; i < kNK; ++i) { mbar_init(&bar.kfull[i], 1); mbar_init(&bar.kempty[i], 1); }
@@ -584,6 +602,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bar.drain, (s_role && bar.work_count > 1) ? 2 : 1);
         bar.cmd = 0;
         bar.abort_flag = 0;
+        bar.wait_ns = p.wait_ns;
         fence_mbar_init();
     }
     if (warp == 0) {           // collective over the pair: both CTAs get the same columns
@@ -673,9 +692,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < kKChunks * G; ++u) ring_advance<kNK>(kr);
                     for (int u = 0; u < G; ++u) ring_advance<kNR>(rr);
                 }
-                ring_drain<kNK>(bar.kempty, kr);
-                ring_drain<kNR>(bar.rempty, rr);
-                if (ii > 0) mbar_wait(&bar.qpe_empty, (uint32_t)(ii - 1) & 1, kWaitLimit);
+                ring_drain<kNK>(bar.kempty, kr, bar.wait_ns);
+                ring_drain<kNR>(bar.rempty, rr, bar.wait_ns);
+                if (ii > 0) mbar_wait(&bar.qpe_empty, (uint32_t)(ii - 1) & 1, bar.wait_ns);
             }
         } else if (warp == 1 || warp == 2) {
             // ---------------- MMA issuers (leader): S = Q K^T for 256 rows -----------------
@@ -716,7 +735,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                             if (prev >= 0 && (((prev / kKChunks) & 1) != par)) {
                                 const uint64_t t0 = global_ns();
                                 while (*seen_other < prev) {
-                                    if (aborted(bar) || global_ns() - t0 > kWaitLimit) {
+                                    if (aborted(bar) || global_ns() - t0 > bar.wait_ns) {
                                         set_abort(bar, p.err, -25);
                                         ok = false;
                                         break;
@@ -786,7 +805,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             bool fail = false;
             // Q_nope of an item's rows into tensor memory, 16 loads in flight per thread
-            auto load_q = [&](const Item &q) {
+            auto load_q = [&](const Item &q, bool withhold) {
                 const int Rq = (q.rt0 + kpair) * kRows + row;
                 const bool valid = Rq < p.rows_seq;
                 const uint4 *src =
@@ -812,14 +831,14 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote_cta(&bar.q_ready, lead_rank);
+                if (lane == 0 && !withhold) mbar_arrive_remote_cta(&bar.q_ready, lead_rank);
             };
             WorkIter w = w0;
             Item it;
             int ii = 0, g = 0;
             bool have = next_item(p, w, cl, ncl, it);
             if (have) {
-                load_q(it);
+                load_q(it, p.fault == 1);                  // the test hook leaves Q-ready one arrival short
                 if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvQReady, 0);
             }
             while (!fail && have) {
@@ -927,7 +946,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 // before its last scores could be read
                 have = next_item(p, w, cl, ncl, it);
                 if (have && ok) {
-                    load_q(it);
+                    load_q(it, false);
                     if (warp == 4 && lane == 0) KDT_TC_TRACE(kEvQReady, ii);
                 }
                 // lsum_s is rewritten at the end of the next item only after this barrier
@@ -980,7 +999,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                ring_drain<kNV>(bar.vempty, vr);
+                ring_drain<kNV>(bar.vempty, vr, bar.wait_ns);
             }
         } else if (warp == 1) {
             // ---------------- MMA issuer (leader): O += P V for 256 rows --------------------
@@ -1115,8 +1134,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 // every copy this CTA issued has landed and been read before it may exit
-                ring_drain<kNK>(bar.kempty, kr);
-                ring_drain<kNR>(bar.rempty, rr);
+                ring_drain<kNK>(bar.kempty, kr, bar.wait_ns);
+                ring_drain<kNR>(bar.rempty, rr, bar.wait_ns);
             }
         } else if (warp == 2) {
             // ---------------- P watcher: P of each block landed, and does O need a rescale? --
@@ -1272,16 +1291,22 @@ __global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int
     if (threadIdx.x == 0) {
         s_valid = 0;
         const int u_first = tail_first_unit(p, C);
-        const int64_t W = tail_blocks(p, u_first);
-        const int64_t sc = W * c / C, sprev = W * (c - 1) / C;
-        int u, nblk;
-        int64_t start;
-        locate_block(p, u_first, sc, u, start, nblk);
+        const int64_t Wv = tail_vblocks(p, u_first);
+        // key-block position of range boundary k, as the kernel computes it
+        auto boundary = [&](int k, int &uu, int64_t &st, int &nb) {
+            int64_t pos;
+            locate_vblock(p, u_first, Wv * k / C, uu, st, nb, pos);
+            return pos;
+        };
+        int u, nblk, ud, nd;
+        int64_t start, sd;
+        const int64_t sc = boundary(c, u, start, nblk);
+        const int64_t sprev = boundary(c - 1, ud, sd, nd);
         if (nblk > 0 && sc > start && sprev <= start) {
             int n = 0;
             s_slot[n++] = 2 * (c - 1) + (sprev == start ? 0 : 1);   // the piece that starts the unit
             for (int cc = c; cc < C && n <= kMaxClusters; ++cc) {
-                const int64_t lo = W * cc / C, hi = W * (cc + 1) / C;
+                const int64_t lo = boundary(cc, ud, sd, nd), hi = boundary(cc + 1, ud, sd, nd);
                 if (lo >= start + nblk) break;
                 if (hi > lo) s_slot[n++] = 2 * cc;                 // pieces that start a cluster's tail range
             }
@@ -1440,6 +1465,8 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     p.part_lse = vp.part_lse;
     p.err = vp.err;
     p.pairs_per_seq = (p.row_tiles + 1) / 2;
+    p.wait_ns = vp.wait_ns ? vp.wait_ns : kWaitLimit;
+    p.fault = vp.fault;
     const int C = vp.tc_clusters;
     if (C < 1 || C > kMaxClusters || (C > 1 && (!p.part_o || !p.part_lse))) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);

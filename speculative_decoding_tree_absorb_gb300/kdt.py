@@ -26,7 +26,8 @@ DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 EXPORTS = ("kdt_status_str", "kdt_version", "kdt_build_visibility", "kdt_verify_attn",
            "kdt_verify_attn_workspace_size", "kdt_verify_attn_plan", "kdt_merge_attn_states",
            "kdt_verify_attn_noalloc", "kdt_rope_neox", "kdt_tree_accept", "kdt_kv_compact", "kdt_tree_build",
-           "kdt_verify_attn_host", "kdt_verify_attn_host_buffer_size", "kdt_vc_up_proj")
+           "kdt_verify_attn_host", "kdt_verify_attn_host_buffer_size", "kdt_vc_up_proj",
+           "kdt_test_verify_attn_wait_expiry")
 
 
 class KdtError(RuntimeError):
@@ -102,6 +103,9 @@ def lib():
         L.kdt_vc_up_proj.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      vp, vp, vp]
         L.kdt_vc_up_proj.restype = ctypes.c_int
+        L.kdt_test_verify_attn_wait_expiry.argtypes = [ctypes.POINTER(VerifyArgs), vp, ctypes.c_size_t,
+                                                       ctypes.c_uint32, vp]
+        L.kdt_test_verify_attn_wait_expiry.restype = ctypes.c_int
         L.kdt_verify_attn_noalloc.argtypes = [ctypes.POINTER(VerifyArgs), vp]
         L.kdt_verify_attn_noalloc.restype = ctypes.c_int
         L.kdt_rope_neox.argtypes = [ctypes.POINTER(RopeArgs), vp]
