@@ -11,12 +11,21 @@
 //
 // Design (differs from the pages' one-block-per-(b,h,i) kernel): a CTA owns 64
 // consecutive rows of one sequence -- all heads of a few tree queries -- so each
-// cache row it stages in shared memory serves 64 query rows instead of one.
-// Scores for a 64x64 (rows x keys) block are a register-tiled SIMT product (each
-// of 256 threads owns a 4x4 sub-tile); P.V accumulates a 64x512 fp32 output tile
-// (4 rows x 32 columns per thread). No atomics: every output element has one owner.
-// Split-KV: blockIdx.y takes a contiguous range of key blocks; with more than one
-// split the CTA writes a normalised partial (o_s, lse_s) that K2 merges.
+// cache row it stages in shared memory serves 64 query rows instead of one. It is the
+// fp32 path (scores, softmax and P.V all in fp32) and the small-shape path.
+//  * 16 warps, 2 rows a thread: scores as a 2 x 4 register tile of a 64 x 64 block
+//    (keys tx, tx + 16, tx + 32, tx + 48 of the 16 key lanes, so that a warp's key reads
+//    are consecutive rows), the output as 2 rows x 32 columns (64 accumulators), which
+//    keeps a thread under 128 registers and a SM at 16 resident warps.
+//  * Every operand reaches shared memory by cp.async (16-byte copies, rows past the
+//    sequence zero-filled, never read), in one ring of 4 slots filled in the order the
+//    block consumes them: per 64-key block, 18 chunks of 32 dims of Q and K for the
+//    scores, then 4 slices of 16 value rows (the latent rows again) for P.V. So the next
+//    block's first chunks load while this block's P.V runs, and the 3 loads ahead of the
+//    one in use hide the L2/DRAM latency; operands stay in their row-major global layout.
+//  * No atomics: every output element has one owner.
+// Split-KV: blockIdx.y takes a contiguous range of key blocks; with more than one split
+// the CTA writes a normalised partial (o_s, lse_s) that K2 merges.
 #include "kdt_internal.cuh"
 
 #include <math.h>
@@ -26,43 +35,62 @@ namespace {
 
 constexpr int kRows = kSimtRows;       // 64 query rows per CTA
 constexpr int kKeys = kSimtKeys;       // 64 keys per block
-constexpr int kThreads = 256;
-constexpr int kDChunk = 32;            // reduction-dim chunk staged per step
-constexpr int kVKeys = 16;             // keys per staged slice of V
-constexpr int kPad = 4;
+constexpr int kThreads = 512;
+constexpr int kDChunk = 32;            // dims per score chunk
+constexpr int kQKChunks = kDqk / kDChunk;      // 18
+constexpr int kVKeys = 16;             // value rows per P.V slice
+constexpr int kVSlices = kKeys / kVKeys;       // 4
+constexpr int kSteps = kQKChunks + kVSlices;   // loads per key block
+constexpr int kNS = 4;                 // ring slots
 
-struct __align__(16) SimtSmem {
-    float qs[kDChunk][kRows + kPad];   // Q chunk, transposed: qs[d][row]
-    float ks[kDChunk][kKeys + kPad];   // K chunk, transposed: ks[d][key]
-    float ps[kRows][kKeys + kPad];     // softmax numerators of the block
-    float vs[kVKeys][kDc];             // slice of V = c_kv rows
+// Element-type traits: shared-memory row pads (keep 16-byte alignment and spread the
+// rows over the banks) and 4-wide loads widened to fp32.
+template <typename T> struct Elt;
+template <> struct Elt<float> {
+    static constexpr int kPadQK = 4, kPadV = 4;
+    __device__ static float4 get4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+};
+template <> struct Elt<__nv_bfloat16> {
+    static constexpr int kPadQK = 8, kPadV = 8;
+    __device__ static float4 get4(const __nv_bfloat16 *p) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+    }
 };
 
-__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
+template <typename T> struct Layout {
+    static constexpr int kQKRow = kDChunk + Elt<T>::kPadQK;            // elements per staged Q/K row
+    static constexpr int kVRow = kDc + Elt<T>::kPadV;                  // elements per staged value row
+    static constexpr int kQKBytes = 2 * kRows * kQKRow * (int)sizeof(T);
+    static constexpr int kVBytes = kVKeys * kVRow * (int)sizeof(T);
+    static constexpr int kSlot = ((kQKBytes > kVBytes ? kQKBytes : kVBytes) + 127) / 128 * 128;
+    static constexpr int kPRow = kKeys + 4;                            // floats per P row
+    static constexpr int kSmem = kNS * kSlot + kRows * kPRow * 4;
+};
 
-__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        v[2 * k] = __uint_as_float(w[k] << 16);
-        v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
+// 16-byte asynchronous copy global -> shared; src_bytes 0 fills the 16 bytes with zeros
+// (the source address is then not read).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads, 1) verify_simt_kernel(const VerifyParams p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SimtSmem &sm = *reinterpret_cast<SimtSmem *>(smem_raw);
+    using L = Layout<Tin>;
+    constexpr int kEl16 = 16 / (int)sizeof(Tin);       // elements per 16-byte copy
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ps = reinterpret_cast<float *>(smem_raw + kNS * L::kSlot);     // P [64][68]
 
     const int tid = threadIdx.x;
-    const int tx = tid & 15;          // key group (S) / column group (O)
-    const int ty = tid >> 4;          // row group: rows ty*4 .. ty*4+3
+    const int tx = tid & 15;          // key lane (S) / column group (O)
+    const int ty = tid >> 4;          // rows 2 ty, 2 ty + 1
     const int b = blockIdx.z;
     const int split = blockIdx.y;
     const int rows_seq = p.T * p.H;
@@ -79,197 +107,207 @@ __global__ void __launch_bounds__(kThreads, 1) verify_simt_kernel(const VerifyPa
     const int kb0 = split * p.blocks_per_split;
     const int kb1 = min(nblk, kb0 + p.blocks_per_split);
     const int key_end = min(kv_len, kb1 * kKeys);
-
-    // query index of each of this thread's 4 rows (for the tree mask)
-    int qidx[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) qidx[i] = min(r0 + ty * 4 + i, rows_seq - 1) / p.H;
-
-    float o[4][32];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 32; ++c) o[i][c] = 0.f;
-    float m2[4], lpart[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) { m2[i] = -INFINITY; lpart[i] = 0.f; }
-
     const int64_t q_row0 = (int64_t)b * rows_seq + r0;
     const int64_t kv_row0 = (int64_t)b * p.L;
+    const int total = kb1 > kb0 ? (kb1 - kb0) * kSteps : 0;
 
-    for (int kb = kb0; kb < kb1; ++kb) {
-        const int k0 = kb * kKeys;
-        // ---------------- S = Q K^T for 64 rows x 64 keys --------------------
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    // This thread's share of the copies, fixed for the whole kernel: Q/K chunk pieces of one
+    // row (piece qk_pc of row qk_row; the Q row for the first half of the threads' pieces, the
+    // K row for the second), and value pieces of rows v_row + v_step * r.
+    constexpr int kQKPieces = kDChunk / kEl16;                 // 16-byte pieces per chunk row
+    constexpr int kQKPer = 2 * kRows * kQKPieces / kThreads;   // fp32: 2 (Q and K), bf16: 1
+    constexpr int kVPieces = kDc / kEl16;                      // 16-byte pieces per value row
+    constexpr int kVPer = kVKeys * kVPieces / kThreads;        // fp32: 4, bf16: 2
+    constexpr int kVStep = kThreads / kVPieces;
+    const int v_pc = tid % kVPieces, v_row = tid / kVPieces;
 
-        for (int dc = 0; dc < kDqk / kDChunk; ++dc) {
-            {
-                const int lr = tid >> 2, d8 = (tid & 3) * 8;
-                const int dglob = dc * kDChunk + d8;
-                float v[8];
-                // Q rows beyond the sequence's T*H rows read as zero
-                if (r0 + lr < rows_seq) {
-                    if (dglob < kDc) load8(q_nope + (q_row0 + lr) * p.q_nope_stride + dglob, v);
-                    else load8(q_pe + (q_row0 + lr) * p.q_pe_stride + (dglob - kDc), v);
-                } else {
+    // Queue load g of the sequence (block kb0 + g / kSteps, step g % kSteps) into its slot;
+    // one commit group per load, empty past the end, so that the wait counts stay uniform.
+    auto issue = [&](int g) {
+        if (g < total) {
+            const int kb = kb0 + g / kSteps, step = g % kSteps;
+            Tin *slot = reinterpret_cast<Tin *>(smem_raw + (g % kNS) * L::kSlot);
+            if (step < kQKChunks) {
+                // Q rows r0.. and K rows kb*64.. of dims [32 step, 32 step + 32)
+                const int d0 = step * kDChunk;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) sm.qs[d8 + e][lr] = v[e];
-                // keys at or beyond key_end (padding, other splits) read as zero
-                const int key = k0 + lr;
-                if (key < key_end) {
-                    if (dglob < kDc) load8(c_kv + (kv_row0 + key) * kDc + dglob, v);
-                    else load8(k_pe + (kv_row0 + key) * kDr + (dglob - kDc), v);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) sm.ks[d8 + e][lr] = v[e];
-            }
-            __syncthreads();
-#pragma unroll
-            for (int d = 0; d < kDChunk; ++d) {
-                const float4 a = *reinterpret_cast<const float4 *>(&sm.qs[d][ty * 4]);
-                const float4 k = *reinterpret_cast<const float4 *>(&sm.ks[d][tx * 4]);
-                const float av[4] = {a.x, a.y, a.z, a.w};
-                const float kvv[4] = {k.x, k.y, k.z, k.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], kvv[j], acc[i][j]);
-            }
-            __syncthreads();
-        }
-
-        // ---------------- mask, online softmax --------------------------------
-        float alpha[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float s[4];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int key = k0 + tx * 4 + j;
-                bool visible = key < key_end;
-                if (visible && key >= P) {
-                    const int t = key - P;
-                    const uint32_t w = p.vis[((int64_t)b * p.T + qidx[i]) * p.W + (t >> 5)];
-                    visible = (w >> (t & 31)) & 1u;
-                }
-                s[j] = visible ? acc[i][j] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[j]);
-            }
-#pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float mnew = fmaxf(m2[i], mx);
-            // a row with nothing visible so far keeps m = -inf: weights 0, no rescale
-            alpha[i] = (mnew == -INFINITY) ? 1.f : exp2f(m2[i] - mnew);
-            float rs = 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float pj = (mnew == -INFINITY) ? 0.f : exp2f(s[j] - mnew);
-                sm.ps[ty * 4 + i][tx * 4 + j] = pj;
-                rs += pj;
-            }
-            lpart[i] = lpart[i] * alpha[i] + rs;
-            m2[i] = mnew;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[i][c] *= alpha[i];
-
-        // ---------------- O += P V ------------------------------------------------
-        for (int vc = 0; vc < kKeys / kVKeys; ++vc) {
-            __syncthreads();   // ps written / previous slice consumed
-            {
-                const int lk = tid >> 4, d0 = (tid & 15) * 32;
-                const int key = k0 + vc * kVKeys + lk;
-                float v[8];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (key < key_end) load8(c_kv + (kv_row0 + key) * kDc + d0 + q * 8, v);
-                    else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                for (int rep = 0; rep < kQKPer; ++rep) {
+                    const int i = tid + rep * kThreads;
+                    const bool isk = i >= kRows * kQKPieces;
+                    const int rr = (i / kQKPieces) & (kRows - 1), pc = i % kQKPieces;
+                    const Tin *src;
+                    bool ok;
+                    if (!isk) {
+                        ok = r0 + rr < rows_seq;
+                        const int64_t qr = q_row0 + (ok ? rr : 0);
+                        src = d0 < kDc ? q_nope + qr * p.q_nope_stride + d0 : q_pe + qr * p.q_pe_stride + (d0 - kDc);
+                    } else {
+                        const int key = kb * kKeys + rr;
+                        ok = key < key_end;
+                        const int64_t kr = kv_row0 + (ok ? key : 0);
+                        src = d0 < kDc ? c_kv + kr * kDc + d0 : k_pe + kr * kDr + (d0 - kDc);
                     }
-                    *reinterpret_cast<float4 *>(&sm.vs[lk][d0 + q * 8]) = make_float4(v[0], v[1], v[2], v[3]);
-                    *reinterpret_cast<float4 *>(&sm.vs[lk][d0 + q * 8 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+                    cp_async16(slot + ((isk ? kRows : 0) + rr) * L::kQKRow + pc * kEl16, src + pc * kEl16,
+                               ok ? 16u : 0u);
+                }
+            } else {
+                // value rows kb*64 + 16 (step - 18) .. + 16, all 512 latent dims
+                const int k0 = kb * kKeys + (step - kQKChunks) * kVKeys;
+#pragma unroll
+                for (int rep = 0; rep < kVPer; ++rep) {
+                    const int kk = v_row + rep * kVStep;
+                    const int key = k0 + kk;
+                    const bool ok = key < key_end;
+                    cp_async16(slot + kk * L::kVRow + v_pc * kEl16,
+                               c_kv + (kv_row0 + (ok ? key : 0)) * kDc + v_pc * kEl16, ok ? 16u : 0u);
                 }
             }
-            __syncthreads();
-#pragma unroll 4
-            for (int kk = 0; kk < kVKeys; ++kk) {
-                float pr[4];
+        }
+        cp_async_commit();
+    };
+
+    // query index of each of this thread's 2 rows (for the tree mask)
+    int qidx[2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) pr[i] = sm.ps[ty * 4 + i][vc * kVKeys + kk];
+    for (int i = 0; i < 2; ++i) qidx[i] = min(r0 + 2 * ty + i, rows_seq - 1) / p.H;
+
+    float o[2][32];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[i][c] = 0.f;
+    float m2[2] = {-INFINITY, -INFINITY}, lpart[2] = {0.f, 0.f};
+    float acc[2][4];
+
+#pragma unroll
+    for (int g = 0; g < kNS - 1; ++g) issue(g);
+    for (int g = 0; g < total; ++g) {
+        cp_async_wait<kNS - 2>();      // this thread's copies of load g have landed
+        __syncthreads();               // everyone's have; everyone is done with load g - 1's slot
+        issue(g + kNS - 1);            // into the slot load g - 1 used
+        const int step = g % kSteps;
+        const int k0 = (kb0 + g / kSteps) * kKeys;
+        const Tin *slot = reinterpret_cast<const Tin *>(smem_raw + (g % kNS) * L::kSlot);
+        if (step < kQKChunks) {
+            // ---------------- S += Q K^T over 32 dims: rows 2ty+i, keys tx + 16 j -------------
+            if (step == 0) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+            }
+            const Tin *qs = slot + (2 * ty) * L::kQKRow;
+            const Tin *ks = slot + (kRows + tx) * L::kQKRow;
+#pragma unroll
+            for (int d = 0; d < kDChunk; d += 4) {
+                const float4 a0 = Elt<Tin>::get4(qs + d);
+                const float4 a1 = Elt<Tin>::get4(qs + L::kQKRow + d);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 k = Elt<Tin>::get4(ks + 16 * j * L::kQKRow + d);
+                    acc[0][j] = fmaf(a0.x, k.x, fmaf(a0.y, k.y, fmaf(a0.z, k.z, fmaf(a0.w, k.w, acc[0][j]))));
+                    acc[1][j] = fmaf(a1.x, k.x, fmaf(a1.y, k.y, fmaf(a1.z, k.z, fmaf(a1.w, k.w, acc[1][j]))));
+                }
+            }
+            if (step == kQKChunks - 1) {
+                // ---------------- mask, online softmax, P to shared memory -------------------
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    float s[4];
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int key = k0 + tx + 16 * j;
+                        bool visible = key < key_end;
+                        if (visible && key >= P) {
+                            const int t = key - P;
+                            const uint32_t w = p.vis[((int64_t)b * p.T + qidx[i]) * p.W + (t >> 5)];
+                            visible = (w >> (t & 31)) & 1u;
+                        }
+                        s[j] = visible ? acc[i][j] * p.scale_log2 : -INFINITY;
+                        mx = fmaxf(mx, s[j]);
+                    }
+#pragma unroll
+                    for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    const float mnew = fmaxf(m2[i], mx);
+                    // a row with nothing visible so far keeps m = -inf: weights 0, no rescale
+                    const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(m2[i] - mnew);
+                    float rs = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float pj = (mnew == -INFINITY) ? 0.f : exp2f(s[j] - mnew);
+                        ps[(2 * ty + i) * L::kPRow + tx + 16 * j] = pj;
+                        rs += pj;
+                    }
+                    lpart[i] = lpart[i] * alpha + rs;
+                    m2[i] = mnew;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[i][c] *= alpha;
+                }
+                // P is read after the next load's barrier
+            }
+        } else {
+            // ---------------- O += P V for 16 keys: rows 2ty+i, columns 64 c + 4 tx ------------
+            const int kk0 = (step - kQKChunks) * kVKeys;
+#pragma unroll 2
+            for (int kk = 0; kk < kVKeys; ++kk) {
+                const float p0 = ps[(2 * ty) * L::kPRow + kk0 + kk];
+                const float p1 = ps[(2 * ty + 1) * L::kPRow + kk0 + kk];
+                const Tin *vrow = slot + kk * L::kVRow + 4 * tx;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const float4 v = *reinterpret_cast<const float4 *>(&sm.vs[kk][c * 64 + tx * 4]);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        o[i][c * 4 + 0] = fmaf(pr[i], v.x, o[i][c * 4 + 0]);
-                        o[i][c * 4 + 1] = fmaf(pr[i], v.y, o[i][c * 4 + 1]);
-                        o[i][c * 4 + 2] = fmaf(pr[i], v.z, o[i][c * 4 + 2]);
-                        o[i][c * 4 + 3] = fmaf(pr[i], v.w, o[i][c * 4 + 3]);
-                    }
+                    const float4 v = Elt<Tin>::get4(vrow + 64 * c);
+                    o[0][4 * c + 0] = fmaf(p0, v.x, o[0][4 * c + 0]);
+                    o[0][4 * c + 1] = fmaf(p0, v.y, o[0][4 * c + 1]);
+                    o[0][4 * c + 2] = fmaf(p0, v.z, o[0][4 * c + 2]);
+                    o[0][4 * c + 3] = fmaf(p0, v.w, o[0][4 * c + 3]);
+                    o[1][4 * c + 0] = fmaf(p1, v.x, o[1][4 * c + 0]);
+                    o[1][4 * c + 1] = fmaf(p1, v.y, o[1][4 * c + 1]);
+                    o[1][4 * c + 2] = fmaf(p1, v.z, o[1][4 * c + 2]);
+                    o[1][4 * c + 3] = fmaf(p1, v.w, o[1][4 * c + 3]);
                 }
             }
         }
-        __syncthreads();
     }
+    cp_async_wait<0>();
 
-    // ---------------- epilogue: o = O / l, lse = ln2 * (m2 + log2 l) -------------
+    // ---------------- epilogue: o = O / l, lse = ln2 * (m2 + log2 l) -------------------------
     const bool partial = p.num_splits > 1;
     float *obase = partial ? p.part_o + (int64_t)split * p.rows_total * kDc : p.out;
     float *lbase = partial ? p.part_lse + (int64_t)split * p.rows_total : p.lse;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
         float l = lpart[i];
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        const int r = r0 + ty * 4 + i;
+        const int r = r0 + 2 * ty + i;
         if (r >= rows_seq) continue;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t grow = (int64_t)b * rows_seq + r;
         float *orow = obase + grow * kDc;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float4 v = make_float4(o[i][c * 4] * inv, o[i][c * 4 + 1] * inv, o[i][c * 4 + 2] * inv,
-                                         o[i][c * 4 + 3] * inv);
-            *reinterpret_cast<float4 *>(orow + c * 64 + tx * 4) = v;
-        }
-        if (tx == 0 && lbase) {
-            lbase[grow] = (l > 0.f) ? 0.6931471805599453f * (m2[i] + log2f(l)) : -INFINITY;
-        }
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4 *>(orow + c * 64 + tx * 4) =
+                make_float4(o[i][c * 4] * inv, o[i][c * 4 + 1] * inv, o[i][c * 4 + 2] * inv, o[i][c * 4 + 3] * inv);
+        if (tx == 0 && lbase) lbase[grow] = (l > 0.f) ? 0.6931471805599453f * (m2[i] + log2f(l)) : -INFINITY;
     }
+}
+
+template <typename Tin>
+cudaError_t launch_typed(const VerifyParams &p, cudaStream_t s) {
+    const int rows_seq = p.T * p.H;
+    const dim3 grid((rows_seq + kRows - 1) / kRows, p.num_splits, p.B);
+    const int smem = Layout<Tin>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(verify_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    verify_simt_kernel<Tin><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, cudaStream_t s) {
-    const int rows_seq = p.T * p.H;
-    const dim3 grid((rows_seq + kRows - 1) / kRows, p.num_splits, p.B);
-    const size_t smem = sizeof(SimtSmem);
-    cudaError_t e;
-    if (dt == KDT_F32) {
-        e = cudaFuncSetAttribute(verify_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        verify_simt_kernel<float><<<grid, kThreads, smem, s>>>(p);
-    } else {
-        e = cudaFuncSetAttribute(verify_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        verify_simt_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(p);
-    }
-    return cudaGetLastError();
+    return dt == KDT_F32 ? launch_typed<float>(p, s) : launch_typed<__nv_bfloat16>(p, s);
 }
 
 }  // namespace kdt
