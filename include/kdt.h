@@ -75,10 +75,14 @@ int kdt_version(void);
 
 typedef enum { KDT_F32 = 0, KDT_BF16 = 1 } kdt_dtype;
 
-/* Kernel family. AUTO picks by dtype and shape: bf16 inputs use the tcgen05
- * tensor-core kernel, fp32 inputs the SIMT kernel (which computes in fp32; the
- * tensor path would round inputs). SIMT is valid for both dtypes. */
-typedef enum { KDT_IMPL_AUTO = 0, KDT_IMPL_SIMT = 1, KDT_IMPL_TCGEN05 = 2 } kdt_impl;
+/* Kernel family. AUTO picks by shape and dtype: small problems -- B*T*H * max_kv_len at
+ * most 2^18 for bf16 inputs, 2^19 for fp32 -- go to SIMT_SMALL, the SIMT kernel on 16-row
+ * tiles with one 64-key block per split, spread over many CTAs (the tensor-core kernel's
+ * pipeline has a fixed latency of tens of microseconds); otherwise bf16 inputs use the
+ * tcgen05 tensor-core kernel and fp32 inputs the SIMT kernel on 64-row tiles (which
+ * computes in fp32; the tensor path would round inputs). kdt_verify_attn_plan reports the
+ * choice. Both SIMT forms are valid for both dtypes. */
+typedef enum { KDT_IMPL_AUTO = 0, KDT_IMPL_SIMT = 1, KDT_IMPL_TCGEN05 = 2, KDT_IMPL_SIMT_SMALL = 3 } kdt_impl;
 
 /*
  * kdt_build_visibility -- draft-tree parent array -> packed ancestor bits.

@@ -25,6 +25,14 @@ int sm_count() {
 namespace {
 
 constexpr size_t kAlign = 256;
+
+// Problems with at most this many (query row x cache row) pairs go to the SIMT kernel on
+// 16-row tiles when the caller leaves the choice to the library: the crossovers measured
+// on GB300 (device time, L2 flushed) against the tensor-core kernel for bf16 inputs (about
+// 0.6 GFLOP; below it the 16-row SIMT kernel took 0.45-0.8 of the tensor kernel's time) and
+// against the 64-row SIMT kernel for fp32 inputs (about 1.1 GFLOP; 0.1-0.8 of its time).
+constexpr int64_t kSmallShapeWorkBf16 = (int64_t)1 << 18;
+constexpr int64_t kSmallShapeWorkF32 = (int64_t)1 << 19;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -52,6 +60,9 @@ kdt_status check_on_current_device(std::initializer_list<const void *> ptrs) {
     return KDT_OK;
 }
 
+struct Plan;
+int unit_rows_of(const Plan &p);
+
 struct Plan {
     int impl = KDT_IMPL_SIMT;
     int splits = 1;
@@ -65,13 +76,16 @@ struct Plan {
     size_t ws_bytes = 0;
 };
 
+int unit_rows_of(const Plan &p) { return p.impl == KDT_IMPL_SIMT_SMALL ? kSimtSmallRows : kSimtRows; }
+
 kdt_status check_args(const kdt_verify_args *a) {
     if (!a) return KDT_ERR_NULL_ARG;
     if (a->B < 0 || a->B > 65535 || a->T < 1 || a->T > kMaxT || a->H < 1 || a->H > 1024)
         return KDT_ERR_BAD_SHAPE;
     if (a->D_c != kDc || a->D_r != kDr) return KDT_ERR_UNSUPPORTED;
     if (a->dtype != KDT_F32 && a->dtype != KDT_BF16) return KDT_ERR_UNSUPPORTED;
-    if (a->impl != KDT_IMPL_AUTO && a->impl != KDT_IMPL_SIMT && a->impl != KDT_IMPL_TCGEN05)
+    if (a->impl != KDT_IMPL_AUTO && a->impl != KDT_IMPL_SIMT && a->impl != KDT_IMPL_TCGEN05 &&
+        a->impl != KDT_IMPL_SIMT_SMALL)
         return KDT_ERR_UNSUPPORTED;
     if (a->num_splits < 0) return KDT_ERR_BAD_SHAPE;
     if (a->B == 0) return KDT_OK;
@@ -99,14 +113,22 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     }
     const int64_t rows_seq = (int64_t)a->T * a->H;
     const int64_t rows_total = rows_seq * a->B;
-    // Kernel family: bf16 inputs go to the tensor-core kernel; fp32 inputs stay on the
-    // SIMT kernel (the tensor path would round them).
-    const bool tc = a->impl == KDT_IMPL_TCGEN05 || (a->impl == KDT_IMPL_AUTO && a->dtype == KDT_BF16);
+    // Kernel family: small problems go to the SIMT kernel on 16-row tiles (the tensor-core
+    // kernel's pipeline has a fixed latency of tens of microseconds, the 64-row SIMT tile
+    // puts a whole 64 x 64 block on one SM); otherwise bf16 inputs go to the tensor-core
+    // kernel and fp32 inputs stay on the SIMT kernel (the tensor path would round them).
+    const bool small =
+        rows_total * a->max_kv_len <= (a->dtype == KDT_BF16 ? kSmallShapeWorkBf16 : kSmallShapeWorkF32);
+    int impl = a->impl;
+    if (impl == KDT_IMPL_AUTO)
+        impl = small ? KDT_IMPL_SIMT_SMALL : (a->dtype == KDT_BF16 ? KDT_IMPL_TCGEN05 : KDT_IMPL_SIMT);
+    const bool tc = impl == KDT_IMPL_TCGEN05;
     if (tc && a->dtype != KDT_BF16) return KDT_ERR_UNSUPPORTED;
     if (tc && (rows_total >= ((int64_t)1 << 31) || a->kv_row_stride >= ((int64_t)1 << 31)))
         return KDT_ERR_BAD_SHAPE;
-    p.impl = tc ? KDT_IMPL_TCGEN05 : KDT_IMPL_SIMT;
-    const int unit_rows = tc ? tc_rows_per_unit() : kSimtRows;
+    p.impl = impl;
+    const bool simt_small = impl == KDT_IMPL_SIMT_SMALL;
+    const int unit_rows = tc ? tc_rows_per_unit() : (simt_small ? kSimtSmallRows : kSimtRows);
     const int unit_keys = tc ? tc_keys_per_block() : kSimtKeys;
     const int unit_tiles = (int)((rows_seq + unit_rows - 1) / unit_rows);   // work units per sequence
     const int nblk = (a->max_kv_len + unit_keys - 1) / unit_keys;
@@ -127,6 +149,8 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         int splits;
         if (a->num_splits > 0) {
             splits = a->num_splits;
+        } else if (simt_small) {
+            splits = nblk;                  // one 64-key block per split: short chains, many CTAs
         } else {
             const int64_t want = (2LL * slots + base - 1) / base;
             splits = (int)(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
@@ -352,9 +376,9 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
         if (a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t), stream) != cudaSuccess) return KDT_ERR_CUDA;
     }
     const cudaError_t e = p.impl == KDT_IMPL_TCGEN05 ? launch_verify_tc(vp, stream)
-                                                     : launch_verify_simt(vp, a->dtype, stream);
+                                                     : launch_verify_simt(vp, a->dtype, unit_rows_of(p), stream);
     if (e != cudaSuccess) return KDT_ERR_CUDA;
-    if (p.impl == KDT_IMPL_SIMT && p.splits > 1) {
+    if (p.impl != KDT_IMPL_TCGEN05 && p.splits > 1) {
         if (launch_merge_splits(vp.part_o, vp.part_lse, p.splits, vp.rows_total, a->out, a->lse, stream) !=
             cudaSuccess)
             return KDT_ERR_CUDA;

@@ -56,10 +56,12 @@ struct VerifyParams {
 cudaError_t launch_build_visibility(const int32_t *parent, int B, int T, uint32_t *vis, int32_t *err,
                                     cudaStream_t s);
 
-// K3: SIMT verify (fp32 arithmetic, fp32 or bf16 inputs).
+// K3: SIMT verify (fp32 arithmetic, fp32 or bf16 inputs), with 64-row tiles (512 threads)
+// or, for small shapes, 16-row tiles (128 threads) spread over more CTAs.
 constexpr int kSimtRows = 64;
+constexpr int kSimtSmallRows = 16;
 constexpr int kSimtKeys = 64;
-cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, cudaStream_t s);
+cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s);
 
 // K1: tcgen05 verify (bf16 inputs): one 4-CTA cluster (two CTA pairs) per resident slot,
 // each taking an equal share of the (256-row unit, 128-key block) work; launch_verify_tc

@@ -33,9 +33,7 @@
 namespace kdt {
 namespace {
 
-constexpr int kRows = kSimtRows;       // 64 query rows per CTA
 constexpr int kKeys = kSimtKeys;       // 64 keys per block
-constexpr int kThreads = 512;
 constexpr int kDChunk = 32;            // dims per score chunk
 constexpr int kQKChunks = kDqk / kDChunk;      // 18
 constexpr int kVKeys = 16;             // value rows per P.V slice
@@ -59,10 +57,12 @@ template <> struct Elt<__nv_bfloat16> {
     }
 };
 
-template <typename T> struct Layout {
+// kRows query rows a CTA (64, or 16 for the small-shape tile), 8 threads a row.
+template <typename T, int kRows> struct Layout {
+    static constexpr int kThreads = 8 * kRows;
     static constexpr int kQKRow = kDChunk + Elt<T>::kPadQK;            // elements per staged Q/K row
     static constexpr int kVRow = kDc + Elt<T>::kPadV;                  // elements per staged value row
-    static constexpr int kQKBytes = 2 * kRows * kQKRow * (int)sizeof(T);
+    static constexpr int kQKBytes = (kRows + kKeys) * kQKRow * (int)sizeof(T);
     static constexpr int kVBytes = kVKeys * kVRow * (int)sizeof(T);
     static constexpr int kSlot = ((kQKBytes > kVBytes ? kQKBytes : kVBytes) + 127) / 128 * 128;
     static constexpr int kPRow = kKeys + 4;                            // floats per P row
@@ -81,12 +81,13 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <typename Tin>
-__global__ void __launch_bounds__(kThreads, 1) verify_simt_kernel(const VerifyParams p) {
-    using L = Layout<Tin>;
+template <typename Tin, int kRows>
+__global__ void __launch_bounds__(8 * kRows, kRows == 16 ? 2 : 1) verify_simt_kernel(const VerifyParams p) {
+    using L = Layout<Tin, kRows>;
+    constexpr int kThreads = L::kThreads;
     constexpr int kEl16 = 16 / (int)sizeof(Tin);       // elements per 16-byte copy
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    float *ps = reinterpret_cast<float *>(smem_raw + kNS * L::kSlot);     // P [64][68]
+    float *ps = reinterpret_cast<float *>(smem_raw + kNS * L::kSlot);     // P [kRows][68]
 
     const int tid = threadIdx.x;
     const int tx = tid & 15;          // key lane (S) / column group (O)
@@ -111,15 +112,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_simt_kernel(const VerifyPa
     const int64_t kv_row0 = (int64_t)b * p.L;
     const int total = kb1 > kb0 ? (kb1 - kb0) * kSteps : 0;
 
-    // This thread's share of the copies, fixed for the whole kernel: Q/K chunk pieces of one
-    // row (piece qk_pc of row qk_row; the Q row for the first half of the threads' pieces, the
-    // K row for the second), and value pieces of rows v_row + v_step * r.
+    // Copies of one load, spread over the threads: 16-byte pieces of the Q rows, then of the
+    // key rows (a Q/K chunk), or of the value rows (a value slice).
     constexpr int kQKPieces = kDChunk / kEl16;                 // 16-byte pieces per chunk row
-    constexpr int kQKPer = 2 * kRows * kQKPieces / kThreads;   // fp32: 2 (Q and K), bf16: 1
+    constexpr int kQPieces = kRows * kQKPieces;
     constexpr int kVPieces = kDc / kEl16;                      // 16-byte pieces per value row
-    constexpr int kVPer = kVKeys * kVPieces / kThreads;        // fp32: 4, bf16: 2
-    constexpr int kVStep = kThreads / kVPieces;
-    const int v_pc = tid % kVPieces, v_row = tid / kVPieces;
 
     // Queue load g of the sequence (block kb0 + g / kSteps, step g % kSteps) into its slot;
     // one commit group per load, empty past the end, so that the wait counts stay uniform.
@@ -130,36 +127,36 @@ __global__ void __launch_bounds__(kThreads, 1) verify_simt_kernel(const VerifyPa
             if (step < kQKChunks) {
                 // Q rows r0.. and K rows kb*64.. of dims [32 step, 32 step + 32)
                 const int d0 = step * kDChunk;
+                const bool nope = d0 < kDc;
+                const Tin *qbase = nope ? q_nope + d0 : q_pe + (d0 - kDc);
+                const int64_t qstride = nope ? p.q_nope_stride : p.q_pe_stride;
 #pragma unroll
-                for (int rep = 0; rep < kQKPer; ++rep) {
-                    const int i = tid + rep * kThreads;
-                    const bool isk = i >= kRows * kQKPieces;
-                    const int rr = (i / kQKPieces) & (kRows - 1), pc = i % kQKPieces;
-                    const Tin *src;
-                    bool ok;
-                    if (!isk) {
-                        ok = r0 + rr < rows_seq;
-                        const int64_t qr = q_row0 + (ok ? rr : 0);
-                        src = d0 < kDc ? q_nope + qr * p.q_nope_stride + d0 : q_pe + qr * p.q_pe_stride + (d0 - kDc);
-                    } else {
-                        const int key = kb * kKeys + rr;
-                        ok = key < key_end;
-                        const int64_t kr = kv_row0 + (ok ? key : 0);
-                        src = d0 < kDc ? c_kv + kr * kDc + d0 : k_pe + kr * kDr + (d0 - kDc);
-                    }
-                    cp_async16(slot + ((isk ? kRows : 0) + rr) * L::kQKRow + pc * kEl16, src + pc * kEl16,
+                for (int i = tid; i < kQPieces; i += kThreads) {
+                    const int rr = i / kQKPieces, pc = i % kQKPieces;
+                    const bool ok = r0 + rr < rows_seq;
+                    cp_async16(slot + rr * L::kQKRow + pc * kEl16, qbase + (q_row0 + (ok ? rr : 0)) * qstride + pc * kEl16,
                                ok ? 16u : 0u);
+                }
+                const Tin *kbase = nope ? c_kv + d0 : k_pe + (d0 - kDc);
+                const int kstride = nope ? kDc : kDr;
+#pragma unroll
+                for (int i = tid; i < kKeys * kQKPieces; i += kThreads) {
+                    const int rr = i / kQKPieces, pc = i % kQKPieces;
+                    const int key = kb * kKeys + rr;
+                    const bool ok = key < key_end;
+                    cp_async16(slot + (kRows + rr) * L::kQKRow + pc * kEl16,
+                               kbase + (kv_row0 + (ok ? key : 0)) * kstride + pc * kEl16, ok ? 16u : 0u);
                 }
             } else {
                 // value rows kb*64 + 16 (step - 18) .. + 16, all 512 latent dims
                 const int k0 = kb * kKeys + (step - kQKChunks) * kVKeys;
 #pragma unroll
-                for (int rep = 0; rep < kVPer; ++rep) {
-                    const int kk = v_row + rep * kVStep;
+                for (int i = tid; i < kVKeys * kVPieces; i += kThreads) {
+                    const int kk = i / kVPieces, pc = i % kVPieces;
                     const int key = k0 + kk;
                     const bool ok = key < key_end;
-                    cp_async16(slot + kk * L::kVRow + v_pc * kEl16,
-                               c_kv + (kv_row0 + (ok ? key : 0)) * kDc + v_pc * kEl16, ok ? 16u : 0u);
+                    cp_async16(slot + kk * L::kVRow + pc * kEl16, c_kv + (kv_row0 + (ok ? key : 0)) * kDc + pc * kEl16,
+                               ok ? 16u : 0u);
                 }
             }
         }
@@ -293,21 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1) verify_simt_kernel(const VerifyPa
     }
 }
 
-template <typename Tin>
+template <typename Tin, int kRows>
 cudaError_t launch_typed(const VerifyParams &p, cudaStream_t s) {
+    using L = Layout<Tin, kRows>;
     const int rows_seq = p.T * p.H;
     const dim3 grid((rows_seq + kRows - 1) / kRows, p.num_splits, p.B);
-    const int smem = Layout<Tin>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(verify_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(verify_simt_kernel<Tin, kRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kSmem);
     if (e != cudaSuccess) return e;
-    verify_simt_kernel<Tin><<<grid, kThreads, smem, s>>>(p);
+    verify_simt_kernel<Tin, kRows><<<grid, L::kThreads, L::kSmem, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, cudaStream_t s) {
-    return dt == KDT_F32 ? launch_typed<float>(p, s) : launch_typed<__nv_bfloat16>(p, s);
+cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s) {
+    if (rows_per_cta == kSimtSmallRows)
+        return dt == KDT_F32 ? launch_typed<float, kSimtSmallRows>(p, s) : launch_typed<__nv_bfloat16, kSimtSmallRows>(p, s);
+    return dt == KDT_F32 ? launch_typed<float, kSimtRows>(p, s) : launch_typed<__nv_bfloat16, kSimtRows>(p, s);
 }
 
 }  // namespace kdt

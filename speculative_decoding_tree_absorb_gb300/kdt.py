@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "libkdt.so")
 (KDT_OK, KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE, KDT_ERR_UNSUPPORTED, KDT_ERR_WORKSPACE, KDT_ERR_CUDA,
  KDT_ERR_NOT_DEVICE) = range(7)
 KDT_F32, KDT_BF16 = 0, 1
-IMPLS = {"auto": 0, "simt": 1, "tcgen05": 2}
+IMPLS = {"auto": 0, "simt": 1, "tcgen05": 2, "simt_small": 3}
 IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 

@@ -13,7 +13,7 @@ from tests import helpers as H
 
 pytestmark = pytest.mark.gpu
 
-IMPLS_BY_DTYPE = {"f32": ["simt"], "bf16": ["simt", "tcgen05"]}
+IMPLS_BY_DTYPE = {"f32": ["simt", "simt_small"], "bf16": ["simt", "simt_small", "tcgen05"]}
 
 
 @pytest.fixture(scope="module")
@@ -257,12 +257,15 @@ def test_auto_picks_tensor_cores_for_bf16(kdt):
     a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
                       max_kv_len=case.max_kv_len, out=out)
     assert kdt.plan(a)["impl"] == "tcgen05"
-    f = wl.make_case("plan32", B=1, T=4, H=8, prefix=30, dtype="f32", seed=1)
-    d = G.to_device(f)
-    out = torch.empty((f.B, f.T, f.H, 512), device="cuda")
-    a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
-                      max_kv_len=f.max_kv_len, out=out)
-    assert kdt.plan(a)["impl"] == "simt"
+    # small problems take the SIMT kernel on 16-row tiles, whatever the dtype; larger fp32
+    # problems the SIMT kernel on 64-row tiles
+    for dtype, prefix, want in (("f32", 30, "simt_small"), ("bf16", 30, "simt_small"), ("f32", 4000, "simt")):
+        f = wl.make_case("plan32", B=1, T=16, H=64, prefix=prefix, dtype=dtype, seed=1)
+        d = G.to_device(f)
+        out = torch.empty((f.B, f.T, f.H, 512), device="cuda")
+        a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
+                          max_kv_len=f.max_kv_len, out=out)
+        assert kdt.plan(a)["impl"] == want, (dtype, prefix)
 
 
 # ------------------------------------------------------- full-size configurations --
