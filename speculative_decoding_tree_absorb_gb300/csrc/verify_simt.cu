@@ -36,10 +36,6 @@ namespace {
 constexpr int kKeys = kSimtKeys;       // 64 keys per block
 constexpr int kDChunk = 32;            // dims per score chunk
 constexpr int kQKChunks = kDqk / kDChunk;      // 18
-constexpr int kVKeys = 16;             // value rows per P.V slice
-constexpr int kVSlices = kKeys / kVKeys;       // 4
-constexpr int kSteps = kQKChunks + kVSlices;   // loads per key block
-constexpr int kNS = 4;                 // ring slots
 
 // Element-type traits: shared-memory row pads (keep 16-byte alignment and spread the
 // rows over the banks) and 4-wide loads widened to fp32.
@@ -57,9 +53,16 @@ template <> struct Elt<__nv_bfloat16> {
     }
 };
 
-// kRows query rows a CTA (64, or 16 for the small-shape tile), 8 threads a row.
+// kRows query rows a CTA: 64 (512 threads) or the small-shape tile of 16 (128 threads).
+// Two rows a thread in both: one row a thread (twice the threads, 8-row value slices, a
+// 6-slot ring) measured slower on small shapes (the score loop then issues 5 shared-memory
+// loads per 16 FMAs and waits on shared memory).
 template <typename T, int kRows> struct Layout {
-    static constexpr int kThreads = 8 * kRows;
+    static constexpr int kRPT = 2;                                     // query rows a thread
+    static constexpr int kThreads = 16 * kRows / kRPT;
+    static constexpr int kVKeys = 16;                                  // value rows per P.V slice
+    static constexpr int kSteps = kQKChunks + kKeys / kVKeys;          // loads per key block
+    static constexpr int kNS = 4;                                      // ring slots
     static constexpr int kQKRow = kDChunk + Elt<T>::kPadQK;            // elements per staged Q/K row
     static constexpr int kVRow = kDc + Elt<T>::kPadV;                  // elements per staged value row
     static constexpr int kQKBytes = (kRows + kKeys) * kQKRow * (int)sizeof(T);
@@ -82,16 +85,17 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <typename Tin, int kRows>
-__global__ void __launch_bounds__(8 * kRows, kRows == 16 ? 2 : 1) verify_simt_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(Layout<Tin, kRows>::kThreads, kRows == 16 ? 2 : 1)
+    verify_simt_kernel(const VerifyParams p) {
     using L = Layout<Tin, kRows>;
-    constexpr int kThreads = L::kThreads;
+    constexpr int kThreads = L::kThreads, kRPT = L::kRPT, kVKeys = L::kVKeys, kSteps = L::kSteps, kNS = L::kNS;
     constexpr int kEl16 = 16 / (int)sizeof(Tin);       // elements per 16-byte copy
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float *ps = reinterpret_cast<float *>(smem_raw + kNS * L::kSlot);     // P [kRows][68]
 
     const int tid = threadIdx.x;
     const int tx = tid & 15;          // key lane (S) / column group (O)
-    const int ty = tid >> 4;          // rows 2 ty, 2 ty + 1
+    const int ty = tid >> 4;          // rows kRPT ty .. kRPT ty + kRPT - 1
     const int b = blockIdx.z;
     const int split = blockIdx.y;
     const int rows_seq = p.T * p.H;
@@ -164,17 +168,20 @@ __global__ void __launch_bounds__(8 * kRows, kRows == 16 ? 2 : 1) verify_simt_ke
     };
 
     // query index of each of this thread's 2 rows (for the tree mask)
-    int qidx[2];
+    int qidx[kRPT];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) qidx[i] = min(r0 + 2 * ty + i, rows_seq - 1) / p.H;
+    for (int i = 0; i < kRPT; ++i) qidx[i] = min(r0 + kRPT * ty + i, rows_seq - 1) / p.H;
 
-    float o[2][32];
+    float o[kRPT][32];
+    float m2[kRPT], lpart[kRPT];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kRPT; ++i) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) o[i][c] = 0.f;
-    float m2[2] = {-INFINITY, -INFINITY}, lpart[2] = {0.f, 0.f};
-    float acc[2][4];
+        m2[i] = -INFINITY;
+        lpart[i] = 0.f;
+    }
+    float acc[kRPT][4];
 
 #pragma unroll
     for (int g = 0; g < kNS - 1; ++g) issue(g);
@@ -189,27 +196,29 @@ __global__ void __launch_bounds__(8 * kRows, kRows == 16 ? 2 : 1) verify_simt_ke
             // ---------------- S += Q K^T over 32 dims: rows 2ty+i, keys tx + 16 j -------------
             if (step == 0) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                for (int i = 0; i < kRPT; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
             }
-            const Tin *qs = slot + (2 * ty) * L::kQKRow;
+            const Tin *qs = slot + (kRPT * ty) * L::kQKRow;
             const Tin *ks = slot + (kRows + tx) * L::kQKRow;
 #pragma unroll
             for (int d = 0; d < kDChunk; d += 4) {
-                const float4 a0 = Elt<Tin>::get4(qs + d);
-                const float4 a1 = Elt<Tin>::get4(qs + L::kQKRow + d);
+                float4 a[kRPT];
+#pragma unroll
+                for (int i = 0; i < kRPT; ++i) a[i] = Elt<Tin>::get4(qs + i * L::kQKRow + d);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float4 k = Elt<Tin>::get4(ks + 16 * j * L::kQKRow + d);
-                    acc[0][j] = fmaf(a0.x, k.x, fmaf(a0.y, k.y, fmaf(a0.z, k.z, fmaf(a0.w, k.w, acc[0][j]))));
-                    acc[1][j] = fmaf(a1.x, k.x, fmaf(a1.y, k.y, fmaf(a1.z, k.z, fmaf(a1.w, k.w, acc[1][j]))));
+#pragma unroll
+                    for (int i = 0; i < kRPT; ++i)
+                        acc[i][j] = fmaf(a[i].x, k.x, fmaf(a[i].y, k.y, fmaf(a[i].z, k.z, fmaf(a[i].w, k.w, acc[i][j]))));
                 }
             }
             if (step == kQKChunks - 1) {
                 // ---------------- mask, online softmax, P to shared memory -------------------
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 0; i < kRPT; ++i) {
                     float s[4];
                     float mx = -INFINITY;
 #pragma unroll
@@ -233,7 +242,7 @@ __global__ void __launch_bounds__(8 * kRows, kRows == 16 ? 2 : 1) verify_simt_ke
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float pj = (mnew == -INFINITY) ? 0.f : exp2f(s[j] - mnew);
-                        ps[(2 * ty + i) * L::kPRow + tx + 16 * j] = pj;
+                        ps[(kRPT * ty + i) * L::kPRow + tx + 16 * j] = pj;
                         rs += pj;
                     }
                     lpart[i] = lpart[i] * alpha + rs;
@@ -248,20 +257,20 @@ __global__ void __launch_bounds__(8 * kRows, kRows == 16 ? 2 : 1) verify_simt_ke
             const int kk0 = (step - kQKChunks) * kVKeys;
 #pragma unroll 2
             for (int kk = 0; kk < kVKeys; ++kk) {
-                const float p0 = ps[(2 * ty) * L::kPRow + kk0 + kk];
-                const float p1 = ps[(2 * ty + 1) * L::kPRow + kk0 + kk];
+                float pr[kRPT];
+#pragma unroll
+                for (int i = 0; i < kRPT; ++i) pr[i] = ps[(kRPT * ty + i) * L::kPRow + kk0 + kk];
                 const Tin *vrow = slot + kk * L::kVRow + 4 * tx;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const float4 v = Elt<Tin>::get4(vrow + 64 * c);
-                    o[0][4 * c + 0] = fmaf(p0, v.x, o[0][4 * c + 0]);
-                    o[0][4 * c + 1] = fmaf(p0, v.y, o[0][4 * c + 1]);
-                    o[0][4 * c + 2] = fmaf(p0, v.z, o[0][4 * c + 2]);
-                    o[0][4 * c + 3] = fmaf(p0, v.w, o[0][4 * c + 3]);
-                    o[1][4 * c + 0] = fmaf(p1, v.x, o[1][4 * c + 0]);
-                    o[1][4 * c + 1] = fmaf(p1, v.y, o[1][4 * c + 1]);
-                    o[1][4 * c + 2] = fmaf(p1, v.z, o[1][4 * c + 2]);
-                    o[1][4 * c + 3] = fmaf(p1, v.w, o[1][4 * c + 3]);
+#pragma unroll
+                    for (int i = 0; i < kRPT; ++i) {
+                        o[i][4 * c + 0] = fmaf(pr[i], v.x, o[i][4 * c + 0]);
+                        o[i][4 * c + 1] = fmaf(pr[i], v.y, o[i][4 * c + 1]);
+                        o[i][4 * c + 2] = fmaf(pr[i], v.z, o[i][4 * c + 2]);
+                        o[i][4 * c + 3] = fmaf(pr[i], v.w, o[i][4 * c + 3]);
+                    }
                 }
             }
         }
@@ -273,11 +282,11 @@ __global__ void __launch_bounds__(8 * kRows, kRows == 16 ? 2 : 1) verify_simt_ke
     float *obase = partial ? p.part_o + (int64_t)split * p.rows_total * kDc : p.out;
     float *lbase = partial ? p.part_lse + (int64_t)split * p.rows_total : p.lse;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kRPT; ++i) {
         float l = lpart[i];
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        const int r = r0 + 2 * ty + i;
+        const int r = r0 + kRPT * ty + i;
         if (r >= rows_seq) continue;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t grow = (int64_t)b * rows_seq + r;

@@ -213,12 +213,12 @@ struct TcParams {
 //    whole, round robin (cluster c takes units c, c + C, ...): the clusters running at the
 //    same time then walk the same few sequences' keys in step and share them in L2;
 //  * the remaining units (all of them when lengths differ) form the tail, cut into C
-//    contiguous ranges of equal COST, units in order: a unit costs its key blocks plus
-//    kItemCost blocks for the item boundary (the epilogue, the next Q load and the pipeline
-//    refill between two items take about as long as that many blocks). In "virtual blocks"
-//    unit u spans kItemCost boundary blocks followed by its key blocks, the tail spans Wv
-//    of them, and cluster c takes the key blocks whose virtual positions fall in
-//    [Wv c / C, Wv (c + 1) / C). Equal block counts alone left clusters that met many
+//    contiguous ranges of equal COST, units in order: when lengths differ a unit costs its
+//    key blocks plus kItemCost blocks for the item boundary (the epilogue, the next Q load
+//    and the pipeline refill between two items take about as long as that many blocks).
+//    In "virtual blocks" unit u spans kov boundary blocks followed by its key blocks, the
+//    tail spans Wv of them, and cluster c takes the key blocks whose virtual positions fall
+//    in [Wv c / C, Wv (c + 1) / C). Equal block counts alone left clusters that met many
 //    short units (ragged prefixes) with several more boundaries than others.
 // Everything is derived from prefix_len on the device, the same way in every CTA. A tail
 // unit cut by a range boundary is processed in pieces: each piece writes its normalised
@@ -228,22 +228,31 @@ __device__ __forceinline__ int seq_blocks(const TcParams &p, int b) {
     return (p.prefix_len[b] + p.T + kKeys - 1) / kKeys;
 }
 
-// First unit of the tail.
-__device__ __forceinline__ int tail_first_unit(const TcParams &p, int C) {
-    const int units = p.B * p.pairs_per_seq;
+// Whether every sequence has the same block count.
+__device__ __forceinline__ bool uniform_lengths(const TcParams &p) {
     const int nb0 = seq_blocks(p, 0);
     for (int b = 1; b < p.B; ++b)
-        if (seq_blocks(p, b) != nb0) return 0;
-    return (units / C) * C;
+        if (seq_blocks(p, b) != nb0) return false;
+    return true;
+}
+
+// First unit of the tail.
+__device__ __forceinline__ int tail_first_unit(const TcParams &p, int C) {
+    return uniform_lengths(p) ? (p.B * p.pairs_per_seq / C) * C : 0;
 }
 
 constexpr int kItemCost = 6;   // an item boundary, in key blocks of time
 
-// Virtual blocks of the tail (units u_first ..): kItemCost + the key blocks of each unit.
-__device__ __forceinline__ int64_t tail_vblocks(const TcParams &p, int u_first) {
+// Boundary blocks charged per unit: kItemCost when lengths differ. With equal lengths every
+// unit costs the same and the plain block split is already balanced (and cuts the units at
+// the same places as before the weighting, which measured a few us faster in the merge).
+__device__ __forceinline__ int item_cost(const TcParams &p) { return uniform_lengths(p) ? 0 : kItemCost; }
+
+// Virtual blocks of the tail (units u_first ..): kov + the key blocks of each unit.
+__device__ __forceinline__ int64_t tail_vblocks(const TcParams &p, int u_first, int kov) {
     int64_t w = 0;
     for (int b = u_first / p.pairs_per_seq, k0 = u_first % p.pairs_per_seq; b < p.B; ++b, k0 = 0)
-        w += (int64_t)(p.pairs_per_seq - k0) * (kItemCost + seq_blocks(p, b));
+        w += (int64_t)(p.pairs_per_seq - k0) * (kov + seq_blocks(p, b));
     return w;
 }
 
@@ -251,19 +260,19 @@ __device__ __forceinline__ int64_t tail_vblocks(const TcParams &p, int u_first) 
 // tail's key-block numbering (start), its block count, and pos = the first key block at
 // or after s (start when s lies in the unit's boundary part). s = Wv gives u = units and
 // pos = the tail's key-block count.
-__device__ __forceinline__ void locate_vblock(const TcParams &p, int u_first, int64_t s, int &u, int64_t &start,
-                                              int &nblk, int64_t &pos) {
+__device__ __forceinline__ void locate_vblock(const TcParams &p, int u_first, int kov, int64_t s, int &u,
+                                              int64_t &start, int &nblk, int64_t &pos) {
     int64_t acc_v = 0, acc_r = 0;
     for (int b = u_first / p.pairs_per_seq, k0 = u_first % p.pairs_per_seq; b < p.B; ++b, k0 = 0) {
         const int nb = seq_blocks(p, b);
-        const int64_t vs = kItemCost + nb;                    // virtual size of one unit
+        const int64_t vs = kov + nb;                          // virtual size of one unit
         const int64_t k = p.pairs_per_seq - k0;               // tail units of this sequence
         if (s < acc_v + k * vs) {
             const int64_t kk = (s - acc_v) / vs;
             u = b * p.pairs_per_seq + k0 + (int)kk;
             start = acc_r + kk * nb;
             nblk = nb;
-            const int64_t into = s - acc_v - kk * vs - kItemCost;   // key blocks of the unit before s
+            const int64_t into = s - acc_v - kk * vs - kov;         // key blocks of the unit before s
             pos = start + (into > 0 ? into : 0);
             return;
         }
@@ -557,12 +566,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         {
             const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
-            const int u_first = tail_first_unit(p, C);
-            const int64_t Wv = tail_vblocks(p, u_first);
+            const int u_first = tail_first_unit(p, C), kov = item_cost(p);
+            const int64_t Wv = tail_vblocks(p, u_first, kov);
             int u0, nblk0, u1, nblk1;
             int64_t start0, pos0, start1, pos1;
-            locate_vblock(p, u_first, Wv * c / C, u0, start0, nblk0, pos0);
-            locate_vblock(p, u_first, Wv * (c + 1) / C, u1, start1, nblk1, pos1);
+            locate_vblock(p, u_first, kov, Wv * c / C, u0, start0, nblk0, pos0);
+            locate_vblock(p, u_first, kov, Wv * (c + 1) / C, u1, start1, nblk1, pos1);
             bar.work_wleft = u_first / C;
             bar.work_u0 = u0;
             bar.work_kb0 = (int)(pos0 - start0);
@@ -1290,12 +1299,12 @@ __global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int
     const int c = blockIdx.x + 1;
     if (threadIdx.x == 0) {
         s_valid = 0;
-        const int u_first = tail_first_unit(p, C);
-        const int64_t Wv = tail_vblocks(p, u_first);
+        const int u_first = tail_first_unit(p, C), kov = item_cost(p);
+        const int64_t Wv = tail_vblocks(p, u_first, kov);
         // key-block position of range boundary k, as the kernel computes it
         auto boundary = [&](int k, int &uu, int64_t &st, int &nb) {
             int64_t pos;
-            locate_vblock(p, u_first, Wv * k / C, uu, st, nb, pos);
+            locate_vblock(p, u_first, kov, Wv * k / C, uu, st, nb, pos);
             return pos;
         };
         int u, nblk, ud, nd;
