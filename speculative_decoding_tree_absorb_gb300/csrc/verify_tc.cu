@@ -126,6 +126,7 @@ constexpr int kNV = 2;                            // O-CTA value ring slots (64 
 constexpr uint32_t kCmdDone = 0xffffffffu;        // correction command: no more rescales
 constexpr uint64_t kWaitLimit = 200000000ull;     // ns a wait may poll before giving up (default)
 constexpr float kRescaleThreshold = 20.0f;        // log2 units
+constexpr int kMaxClusters = 48;                  // partial states then fit the no-alloc scratch
 
 // Shared-memory layout (same offsets in every CTA of the cluster; roles use
 // different parts). All tiles 1024-byte aligned for the 128B swizzle.
@@ -186,6 +187,7 @@ struct Barriers {
     uint32_t tmem_base;
     int abort_flag;
     uint64_t wait_ns;              // how long a wait may poll before the kernel gives up
+    int64_t sched_B[kMaxClusters + 1];   // tail cut points of all clusters (cluster_schedule)
 };
 
 struct TcParams {
@@ -236,10 +238,6 @@ __device__ __forceinline__ bool uniform_lengths(const TcParams &p) {
     return true;
 }
 
-// First unit of the tail.
-__device__ __forceinline__ int tail_first_unit(const TcParams &p, int C) {
-    return uniform_lengths(p) ? (p.B * p.pairs_per_seq / C) * C : 0;
-}
 
 constexpr int kItemCost = 6;   // an item boundary, in key blocks of time
 
@@ -247,14 +245,6 @@ constexpr int kItemCost = 6;   // an item boundary, in key blocks of time
 // unit costs the same and the plain block split is already balanced (and cuts the units at
 // the same places as before the weighting, which measured a few us faster in the merge).
 __device__ __forceinline__ int item_cost(const TcParams &p) { return uniform_lengths(p) ? 0 : kItemCost; }
-
-// Virtual blocks of the tail (units u_first ..): kov + the key blocks of each unit.
-__device__ __forceinline__ int64_t tail_vblocks(const TcParams &p, int u_first, int kov) {
-    int64_t w = 0;
-    for (int b = u_first / p.pairs_per_seq, k0 = u_first % p.pairs_per_seq; b < p.B; ++b, k0 = 0)
-        w += (int64_t)(p.pairs_per_seq - k0) * (kov + seq_blocks(p, b));
-    return w;
-}
 
 // Where virtual position s of the tail falls: unit u, that unit's first key block in the
 // tail's key-block numbering (start), its block count, and pos = the first key block at
@@ -283,6 +273,65 @@ __device__ __forceinline__ void locate_vblock(const TcParams &p, int u_first, in
     start = acc_r;
     nblk = 0;
     pos = acc_r;
+}
+
+__device__ __forceinline__ int64_t unit_cost(const TcParams &p, int u, int kov) {
+    return kov + seq_blocks(p, u / p.pairs_per_seq);
+}
+
+// The schedule of all C clusters, computed by one whole warp (every lane gets R):
+//  * R rounds of whole units: in round k cluster c takes unit kC + c. With equal lengths
+//    R = units / C. Otherwise rounds are added while every cluster's cost stays below its
+//    fair share (the total cost / C, less one block), so the clusters running at the same
+//    time work on consecutive units -- the same one or two sequences -- and share their
+//    keys in L2.
+//  * the tail, units RC .. : its virtual blocks are cut at B[0] = 0 <= B[1] <= .. <= B[C]
+//    (written to shared memory), cluster c taking [B[c], B[c+1]): B[c] = (c S) / C - L[c]
+//    with S the total cost and L[c] the whole-unit cost of clusters 0 .. c-1, so each
+//    cluster's tail fills the rest of its fair share. With equal lengths this is the
+//    plain cut (Wt c) / C of the tail.
+__device__ __forceinline__ int cluster_schedule(const TcParams &p, int C, int kov, int lane, int64_t *B) {
+    const int U = p.B * p.pairs_per_seq;
+    const bool uniform = kov == 0;
+    const int c0 = lane, c1 = lane + 32;                      // this lane's clusters (C <= 48)
+    int64_t S = 0;                                            // total cost of all units
+    for (int b = lane; b < p.B; b += 32) S += (int64_t)p.pairs_per_seq * (kov + seq_blocks(p, b));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
+    const int64_t fair = S / C;
+    int64_t l0 = 0, l1 = 0;                                   // whole-unit cost of clusters c0, c1
+    int R = 0;
+    for (int k = 0; k < U / C; ++k) {
+        const int64_t n0 = c0 < C ? l0 + unit_cost(p, k * C + c0, kov) : 0;
+        const int64_t n1 = c1 < C ? l1 + unit_cost(p, k * C + c1, kov) : 0;
+        int64_t mx = n0 > n1 ? n0 : n1;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const int64_t o = __shfl_xor_sync(0xffffffffu, mx, off);
+            mx = o > mx ? o : mx;
+        }
+        if (!uniform && mx > fair - 1) break;
+        l0 = n0;
+        l1 = n1;
+        R = k + 1;
+    }
+    // L[c] = sum of the whole-unit costs of clusters before c (exclusive scan over 2 x 32)
+    int64_t x0 = l0, x1 = l1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int64_t y0 = __shfl_up_sync(0xffffffffu, x0, off), y1 = __shfl_up_sync(0xffffffffu, x1, off);
+        if (lane >= off) {
+            x0 += y0;
+            x1 += y1;
+        }
+    }
+    const int64_t total0 = __shfl_sync(0xffffffffu, x0, 31);
+    const int64_t L0 = x0 - l0, L1 = total0 + x1 - l1;
+    if (c0 < C) B[c0] = S * c0 / C - L0;
+    if (c1 < C) B[c1] = S * c1 / C - L1;
+    const int64_t all = total0 + __shfl_sync(0xffffffffu, x1, 31);
+    if (lane == 0) B[C] = S - all;
+    return R;
 }
 
 struct Item {
@@ -562,22 +611,28 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t o_rank = 2u + (uint32_t)kpair;  // the O-CTA an S-CTA feeds
     constexpr uint16_t kMaskS = 0x3, kMaskO = 0xC, kMaskAll = 0xF;
 
-    // ---- set-up: barriers, TMEM ------------------------------------------------------
-    if (threadIdx.x == 0) {
-        {
-            const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
-            const int u_first = tail_first_unit(p, C), kov = item_cost(p);
-            const int64_t Wv = tail_vblocks(p, u_first, kov);
+    // ---- set-up: this cluster's work, barriers, TMEM ---------------------------------
+    if (warp == 0) {
+        const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
+        const int kov = item_cost(p);
+        const int R = cluster_schedule(p, C, kov, lane, bar.sched_B);
+        __syncwarp();
+        if (lane == 0) {
+            const int u_first = R * C;
             int u0, nblk0, u1, nblk1;
             int64_t start0, pos0, start1, pos1;
-            locate_vblock(p, u_first, kov, Wv * c / C, u0, start0, nblk0, pos0);
-            locate_vblock(p, u_first, kov, Wv * (c + 1) / C, u1, start1, nblk1, pos1);
-            bar.work_wleft = u_first / C;
+            locate_vblock(p, u_first, kov, bar.sched_B[c], u0, start0, nblk0, pos0);
+            locate_vblock(p, u_first, kov, bar.sched_B[c + 1], u1, start1, nblk1, pos1);
+            int whole_blocks = 0;
+            for (int k = 0; k < R; ++k) whole_blocks += seq_blocks(p, (k * C + c) / p.pairs_per_seq);
+            bar.work_wleft = R;
             bar.work_u0 = u0;
             bar.work_kb0 = (int)(pos0 - start0);
             bar.work_left = (int)(pos1 - pos0);
-            bar.work_count = bar.work_wleft * (u_first > 0 ? seq_blocks(p, 0) : 0) + bar.work_left;
+            bar.work_count = whole_blocks + bar.work_left;
         }
+    }
+    if (threadIdx.x == 0) {
         for (int i = 0; i < kNK; ++i) { mbar_init(&bar.kfull[i], 1); mbar_init(&bar.kempty[i], 1); }
         for (int i = 0; i < kNR; ++i) { mbar_init(&bar.rfull[i], 1); mbar_init(&bar.rempty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&bar.sfull[i], 1); mbar_init(&bar.sempty[i], 16); }
@@ -1291,20 +1346,24 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 // the unit's 256 (one warp per row, 16 columns per lane): the normalised partial states
 // (o_k, lse_k) of the pieces combine exactly as the log-sum-exp merge of disjoint key
 // sets, processed one piece after another.
-constexpr int kMaxClusters = 48;   // partial states then fit the no-alloc scratch
-
 __global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int C) {
-    __shared__ int s_valid, s_n, s_b, s_rt0;
+    __shared__ int s_valid, s_n, s_b, s_rt0, s_R;
     __shared__ int s_slot[kMaxClusters + 1];
+    __shared__ int64_t s_B[kMaxClusters + 1];
     const int c = blockIdx.x + 1;
+    const int kov = item_cost(p);
+    if (threadIdx.x < 32) {
+        const int R = cluster_schedule(p, C, kov, threadIdx.x, s_B);   // the same cut points as the kernel
+        if (threadIdx.x == 0) s_R = R;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
         s_valid = 0;
-        const int u_first = tail_first_unit(p, C), kov = item_cost(p);
-        const int64_t Wv = tail_vblocks(p, u_first, kov);
+        const int u_first = s_R * C;
         // key-block position of range boundary k, as the kernel computes it
         auto boundary = [&](int k, int &uu, int64_t &st, int &nb) {
             int64_t pos;
-            locate_vblock(p, u_first, kov, Wv * k / C, uu, st, nb, pos);
+            locate_vblock(p, u_first, kov, s_B[k], uu, st, nb, pos);
             return pos;
         };
         int u, nblk, ud, nd;
