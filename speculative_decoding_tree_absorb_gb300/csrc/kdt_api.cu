@@ -73,6 +73,7 @@ struct Plan {
     size_t vis_off = 0, vis_bytes = 0;
     size_t po_off = 0, po_bytes = 0;
     size_t pl_off = 0, pl_bytes = 0;
+    size_t sched_off = 0;                  // tensor path with pieces: the work split's cut points
     size_t ws_bytes = 0;
 };
 
@@ -181,6 +182,10 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         p.pl_off = off;
         p.pl_bytes = (size_t)ns * prow * sizeof(float);
         off = align_up(off + p.pl_bytes);
+        if (tc_pieces) {
+            p.sched_off = off;
+            off = align_up(off + kTcSchedWords * sizeof(int64_t));
+        }
     }
     p.ws_bytes = off;
     p.launches = (a->parent ? 1 : 0) + 1 + ((p.splits > 1 || tc_pieces) ? 1 : 0);
@@ -362,6 +367,8 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
     vp.part_lse = partials ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
     vp.err = a->err;
     vp.tc_clusters = p.tc_clusters;
+    vp.tc_sched = (p.impl == KDT_IMPL_TCGEN05 && p.tc_clusters > 1) ? reinterpret_cast<int64_t *>(ws + p.sched_off)
+                                                                    : nullptr;
     if (hooks) {
         vp.wait_ns = hooks->wait_ns;
         vp.fault = hooks->fault;

@@ -46,6 +46,8 @@ struct VerifyParams {
     // Tensor-core path: the resident clusters the work is split across; part_o/part_lse
     // then hold [2 * tc_clusters][256] partial states (unused when tc_clusters == 1).
     int tc_clusters;
+    int64_t *tc_sched = nullptr;   // tensor path with tc_clusters > 1: the work split's cut points,
+                                   // written by the kernel for the merge pass (kTcSchedWords int64)
     // Tensor-core path, test hooks only: wait limit in ns (0 = the default 200 ms) and an
     // arrival to withhold (0 = none, 1 = the first item's Q-ready arrivals).
     uint64_t wait_ns = 0;
@@ -69,6 +71,7 @@ cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per
 int tc_rows_per_unit();   // query rows of one work unit (256)
 int tc_max_clusters();    // 4-CTA clusters resident at once on the current device (<= 48)
 int tc_keys_per_block();
+constexpr int kTcSchedWords = 2 + 48 + 1;   // R, boundary cost, cut points of up to 48 clusters
 cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t s);
 
 // K2: merge the split partials into out/lse.

@@ -127,6 +127,7 @@ constexpr uint32_t kCmdDone = 0xffffffffu;        // correction command: no more
 constexpr uint64_t kWaitLimit = 200000000ull;     // ns a wait may poll before giving up (default)
 constexpr float kRescaleThreshold = 20.0f;        // log2 units
 constexpr int kMaxClusters = 48;                  // partial states then fit the no-alloc scratch
+constexpr int kSeqTable = 64;                     // sequences whose block counts a CTA keeps in shared memory
 
 // Shared-memory layout (same offsets in every CTA of the cluster; roles use
 // different parts). All tiles 1024-byte aligned for the 128B swizzle.
@@ -188,6 +189,7 @@ struct Barriers {
     int abort_flag;
     uint64_t wait_ns;              // how long a wait may poll before the kernel gives up
     int64_t sched_B[kMaxClusters + 1];   // tail cut points of all clusters (cluster_schedule)
+    int nb_tab[kSeqTable];               // key blocks of each sequence, when B <= kSeqTable
 };
 
 struct TcParams {
@@ -206,6 +208,7 @@ struct TcParams {
     int pairs_per_seq;             // work units (two row tiles each) per sequence
     uint64_t wait_ns;              // wait limit (kWaitLimit unless a test shortens it)
     int fault;                     // test hook: 1 = withhold the first item's Q-ready arrivals
+    int64_t *sched;                // [R, kov, cut points B[0..C]] for the merge pass, or NULL
 };
 
 // ---- work decomposition ----------------------------------------------------------------
@@ -230,31 +233,29 @@ __device__ __forceinline__ int seq_blocks(const TcParams &p, int b) {
     return (p.prefix_len[b] + p.T + kKeys - 1) / kKeys;
 }
 
-// Whether every sequence has the same block count.
-__device__ __forceinline__ bool uniform_lengths(const TcParams &p) {
-    const int nb0 = seq_blocks(p, 0);
-    for (int b = 1; b < p.B; ++b)
-        if (seq_blocks(p, b) != nb0) return false;
-    return true;
-}
+// Key blocks of sequence b, from a shared-memory table of the first kSeqTable sequences
+// when the batch fits in it (the schedule reads them many times), else from prefix_len.
+struct SeqBlocks {
+    const TcParams &p;
+    const int *tab;
+    __device__ __forceinline__ int operator()(int b) const { return tab ? tab[b] : seq_blocks(p, b); }
+};
 
 
-constexpr int kItemCost = 6;   // an item boundary, in key blocks of time
-
-// Boundary blocks charged per unit: kItemCost when lengths differ. With equal lengths every
-// unit costs the same and the plain block split is already balanced (and cuts the units at
-// the same places as before the weighting, which measured a few us faster in the merge).
-__device__ __forceinline__ int item_cost(const TcParams &p) { return uniform_lengths(p) ? 0 : kItemCost; }
+// Boundary blocks charged per unit when lengths differ: an item boundary takes about as
+// long as kItemCost key blocks. With equal lengths every unit costs the same and the
+// plain block split is already balanced, so no boundary blocks are charged.
+constexpr int kItemCost = 6;
 
 // Where virtual position s of the tail falls: unit u, that unit's first key block in the
 // tail's key-block numbering (start), its block count, and pos = the first key block at
 // or after s (start when s lies in the unit's boundary part). s = Wv gives u = units and
 // pos = the tail's key-block count.
-__device__ __forceinline__ void locate_vblock(const TcParams &p, int u_first, int kov, int64_t s, int &u,
-                                              int64_t &start, int &nblk, int64_t &pos) {
+__device__ __forceinline__ void locate_vblock(const TcParams &p, const SeqBlocks &nbs, int u_first, int kov,
+                                              int64_t s, int &u, int64_t &start, int &nblk, int64_t &pos) {
     int64_t acc_v = 0, acc_r = 0;
     for (int b = u_first / p.pairs_per_seq, k0 = u_first % p.pairs_per_seq; b < p.B; ++b, k0 = 0) {
-        const int nb = seq_blocks(p, b);
+        const int nb = nbs(b);
         const int64_t vs = kov + nb;                          // virtual size of one unit
         const int64_t k = p.pairs_per_seq - k0;               // tail units of this sequence
         if (s < acc_v + k * vs) {
@@ -275,11 +276,8 @@ __device__ __forceinline__ void locate_vblock(const TcParams &p, int u_first, in
     pos = acc_r;
 }
 
-__device__ __forceinline__ int64_t unit_cost(const TcParams &p, int u, int kov) {
-    return kov + seq_blocks(p, u / p.pairs_per_seq);
-}
 
-// The schedule of all C clusters, computed by one whole warp (every lane gets R):
+// The schedule of all C clusters, computed by one whole warp (every lane gets R and kov):
 //  * R rounds of whole units: in round k cluster c takes unit kC + c. With equal lengths
 //    R = units / C. Otherwise rounds are added while every cluster's cost stays below its
 //    fair share (the total cost / C, less one block), so the clusters running at the same
@@ -290,30 +288,42 @@ __device__ __forceinline__ int64_t unit_cost(const TcParams &p, int u, int kov) 
 //    with S the total cost and L[c] the whole-unit cost of clusters 0 .. c-1, so each
 //    cluster's tail fills the rest of its fair share. With equal lengths this is the
 //    plain cut (Wt c) / C of the tail.
-__device__ __forceinline__ int cluster_schedule(const TcParams &p, int C, int kov, int lane, int64_t *B) {
+__device__ __forceinline__ int cluster_schedule(const TcParams &p, const SeqBlocks &nbs, int C, int lane,
+                                                int64_t *B, int &kov) {
     const int U = p.B * p.pairs_per_seq;
-    const bool uniform = kov == 0;
+    const int nb0 = nbs(0);
+    bool same = true;
+    for (int b = lane; b < p.B; b += 32) same = same && nbs(b) == nb0;
+    const bool uniform = __all_sync(0xffffffffu, same);
+    kov = uniform ? 0 : kItemCost;
     const int c0 = lane, c1 = lane + 32;                      // this lane's clusters (C <= 48)
     int64_t S = 0;                                            // total cost of all units
-    for (int b = lane; b < p.B; b += 32) S += (int64_t)p.pairs_per_seq * (kov + seq_blocks(p, b));
+    for (int b = lane; b < p.B; b += 32) S += (int64_t)p.pairs_per_seq * (kov + nbs(b));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
-    const int64_t fair = S / C;
     int64_t l0 = 0, l1 = 0;                                   // whole-unit cost of clusters c0, c1
-    int R = 0;
-    for (int k = 0; k < U / C; ++k) {
-        const int64_t n0 = c0 < C ? l0 + unit_cost(p, k * C + c0, kov) : 0;
-        const int64_t n1 = c1 < C ? l1 + unit_cost(p, k * C + c1, kov) : 0;
-        int64_t mx = n0 > n1 ? n0 : n1;
+    int R;
+    if (uniform) {
+        R = U / C;
+        l0 = c0 < C ? (int64_t)R * nb0 : 0;
+        l1 = c1 < C ? (int64_t)R * nb0 : 0;
+    } else {
+        const int64_t fair = S / C;
+        R = 0;
+        for (int k = 0; k < U / C; ++k) {
+            const int64_t n0 = c0 < C ? l0 + kov + nbs((k * C + c0) / p.pairs_per_seq) : 0;
+            const int64_t n1 = c1 < C ? l1 + kov + nbs((k * C + c1) / p.pairs_per_seq) : 0;
+            int64_t mx = n0 > n1 ? n0 : n1;
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            const int64_t o = __shfl_xor_sync(0xffffffffu, mx, off);
-            mx = o > mx ? o : mx;
+            for (int off = 16; off >= 1; off >>= 1) {
+                const int64_t o = __shfl_xor_sync(0xffffffffu, mx, off);
+                mx = o > mx ? o : mx;
+            }
+            if (mx > fair - 1) break;
+            l0 = n0;
+            l1 = n1;
+            R = k + 1;
         }
-        if (!uniform && mx > fair - 1) break;
-        l0 = n0;
-        l1 = n1;
-        R = k + 1;
     }
     // L[c] = sum of the whole-unit costs of clusters before c (exclusive scan over 2 x 32)
     int64_t x0 = l0, x1 = l1;
@@ -614,17 +624,30 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // ---- set-up: this cluster's work, barriers, TMEM ---------------------------------
     if (warp == 0) {
         const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
-        const int kov = item_cost(p);
-        const int R = cluster_schedule(p, C, kov, lane, bar.sched_B);
+        // the sequences' block counts, read from prefix_len once (all lanes at a time)
+        const bool tab = p.B <= kSeqTable;
+        if (tab)
+            for (int b = lane; b < p.B; b += 32) bar.nb_tab[b] = seq_blocks(p, b);
         __syncwarp();
+        const SeqBlocks nbs{p, tab ? bar.nb_tab : nullptr};
+        int kov;
+        const int R = cluster_schedule(p, nbs, C, lane, bar.sched_B, kov);
+        __syncwarp();
+        if (blockIdx.x == 0 && p.sched) {       // the cut points, for the merge pass
+            for (int k = lane; k <= C; k += 32) p.sched[2 + k] = bar.sched_B[k];
+            if (lane == 0) {
+                p.sched[0] = R;
+                p.sched[1] = kov;
+            }
+        }
         if (lane == 0) {
             const int u_first = R * C;
             int u0, nblk0, u1, nblk1;
             int64_t start0, pos0, start1, pos1;
-            locate_vblock(p, u_first, kov, bar.sched_B[c], u0, start0, nblk0, pos0);
-            locate_vblock(p, u_first, kov, bar.sched_B[c + 1], u1, start1, nblk1, pos1);
+            locate_vblock(p, nbs, u_first, kov, bar.sched_B[c], u0, start0, nblk0, pos0);
+            locate_vblock(p, nbs, u_first, kov, bar.sched_B[c + 1], u1, start1, nblk1, pos1);
             int whole_blocks = 0;
-            for (int k = 0; k < R; ++k) whole_blocks += seq_blocks(p, (k * C + c) / p.pairs_per_seq);
+            for (int k = 0; k < R; ++k) whole_blocks += nbs((k * C + c) / p.pairs_per_seq);
             bar.work_wleft = R;
             bar.work_u0 = u0;
             bar.work_kb0 = (int)(pos0 - start0);
@@ -1347,23 +1370,25 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 // (o_k, lse_k) of the pieces combine exactly as the log-sum-exp merge of disjoint key
 // sets, processed one piece after another.
 __global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int C) {
-    __shared__ int s_valid, s_n, s_b, s_rt0, s_R;
+    __shared__ int s_valid, s_n, s_b, s_rt0;
     __shared__ int s_slot[kMaxClusters + 1];
-    __shared__ int64_t s_B[kMaxClusters + 1];
+    __shared__ int s_nb[kSeqTable];
     const int c = blockIdx.x + 1;
-    const int kov = item_cost(p);
-    if (threadIdx.x < 32) {
-        const int R = cluster_schedule(p, C, kov, threadIdx.x, s_B);   // the same cut points as the kernel
-        if (threadIdx.x == 0) s_R = R;
-    }
+    const bool tab = p.B <= kSeqTable;
+    if (tab)
+        for (int b = threadIdx.x; b < p.B; b += blockDim.x) s_nb[b] = seq_blocks(p, b);
     __syncthreads();
     if (threadIdx.x == 0) {
         s_valid = 0;
-        const int u_first = s_R * C;
+        // the cut points the kernel computed and wrote
+        const int R = (int)p.sched[0], kov = (int)p.sched[1];
+        const int64_t *B = p.sched + 2;
+        const int u_first = R * C;
+        const SeqBlocks nbs{p, tab ? s_nb : nullptr};
         // key-block position of range boundary k, as the kernel computes it
         auto boundary = [&](int k, int &uu, int64_t &st, int &nb) {
             int64_t pos;
-            locate_vblock(p, u_first, kov, s_B[k], uu, st, nb, pos);
+            locate_vblock(p, nbs, u_first, kov, B[k], uu, st, nb, pos);
             return pos;
         };
         int u, nblk, ud, nd;
@@ -1535,8 +1560,9 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     p.pairs_per_seq = (p.row_tiles + 1) / 2;
     p.wait_ns = vp.wait_ns ? vp.wait_ns : kWaitLimit;
     p.fault = vp.fault;
+    p.sched = vp.tc_sched;
     const int C = vp.tc_clusters;
-    if (C < 1 || C > kMaxClusters || (C > 1 && (!p.part_o || !p.part_lse))) return cudaErrorInvalidValue;
+    if (C < 1 || C > kMaxClusters || (C > 1 && (!p.part_o || !p.part_lse || !p.sched))) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     verify_tc_kernel<<<(unsigned)(4 * C), kThreads, kSmemBytes, s>>>(map_ks, map_vs, map_kpe, map_qpe, p);
