@@ -378,6 +378,7 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
         uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);
         if (launch_build_visibility(a->parent, a->B, a->T, vis, a->err, stream) != cudaSuccess) return KDT_ERR_CUDA;
         vp.vis = vis;
+        vp.overlap_vis = true;
     } else {
         vp.vis = a->vis;
         if (a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t), stream) != cudaSuccess) return KDT_ERR_CUDA;

@@ -46,6 +46,11 @@ struct VerifyParams {
     // Tensor-core path: the resident clusters the work is split across; part_o/part_lse
     // then hold [2 * tc_clusters][256] partial states (unused when tc_clusters == 1).
     int tc_clusters;
+    // Tensor path: the kernel may start while the visibility kernel this call launched just
+    // before it still runs (programmatic dependent launch); it waits for that kernel only
+    // before its first read of the bits. Set only when the previous kernel of the stream is
+    // that visibility kernel: the kernel reads its other inputs before any wait.
+    bool overlap_vis = false;
     int64_t *tc_sched = nullptr;   // tensor path with tc_clusters > 1: the work split's cut points,
                                    // written by the kernel for the merge pass (kTcSchedWords int64)
     // Tensor-core path, test hooks only: wait limit in ns (0 = the default 200 ms) and an

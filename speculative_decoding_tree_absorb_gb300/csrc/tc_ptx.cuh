@@ -119,6 +119,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     }
 }
 
+// --------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while the previous
+// kernel of the stream still runs: griddep_wait() blocks the calling thread until that
+// kernel has completed and its memory is visible; griddep_launch_dependents() lets the
+// next kernel of the stream (if launched that way) start before this one ends. Both are
+// no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------------- fences --
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -891,6 +891,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             float *lsum_s = reinterpret_cast<float *>(smem + kOffLSum);
             bool ok = true;
             bool fail = false;
+            bool vis_ready = false;                    // the visibility bits are known to be written
             // Q_nope of an item's rows into tensor memory, 16 loads in flight per thread
             auto load_q = [&](const Item &q, bool withhold) {
                 const int Rq = (q.rt0 + kpair) * kRows + row;
@@ -965,6 +966,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                         const int key0 = it.key_base + (it.kb0 + j) * kKeys + 64 * half;
                         masked = key0 < 0 || key0 + 64 > it.P;     // leading pad or tree keys
                         if (masked) {   // scale now, hidden keys -inf (also right for scale 0)
+                            // the bits may come from the visibility kernel launched just before
+                            // this one: wait for it before the first window with tree keys
+                            if (!vis_ready && key0 + 64 > it.P) {
+                                griddep_wait();
+                                vis_ready = true;
+                            }
                             const uint64_t vm = vis_mask64(visrow, p.W, key0, it.P);
 #pragma unroll
                             for (int c = 0; c < 64; ++c) x[c] = ((vm >> c) & 1ull) ? x[c] * p.scale_log2 : -INFINITY;
@@ -1359,6 +1366,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             __nanosleep(1000);
         } while (global_ns() - t0 < 200000ull);
     }
+    griddep_launch_dependents();   // the merge pass may launch once every CTA got here
     cluster_sync();            // no CTA leaves while another may still touch its shared memory
     tc_fence_after();
     if (warp == 0) tmem_dealloc_pair(tmem, 512);
@@ -1377,6 +1385,9 @@ __global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int
     const bool tab = p.B <= kSeqTable;
     if (tab)
         for (int b = threadIdx.x; b < p.B; b += blockDim.x) s_nb[b] = seq_blocks(p, b);
+    // launched to overlap the attention kernel's end: its pieces and cut points are read
+    // only after it completed
+    griddep_wait();
     __syncthreads();
     if (threadIdx.x == 0) {
         s_valid = 0;
@@ -1565,11 +1576,28 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
     if (C < 1 || C > kMaxClusters || (C > 1 && (!p.part_o || !p.part_lse || !p.sched))) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    verify_tc_kernel<<<(unsigned)(4 * C), kThreads, kSmemBytes, s>>>(map_ks, map_vs, map_kpe, map_qpe, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // Programmatic dependent launch: this kernel overlaps the visibility kernel launched
+    // just before it in the same call (it waits for it before reading the bits), and the
+    // merge pass overlaps this kernel's end (it waits before reading the pieces).
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(4 * C));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = vp.overlap_vis ? 1 : 0;
+    if ((e = cudaLaunchKernelEx(&cfg, verify_tc_kernel, map_ks, map_vs, map_kpe, map_qpe, p)) != cudaSuccess) return e;
     if (C > 1) {
-        merge_pieces_kernel<<<dim3((unsigned)(C - 1), 2 * kRows / 8), 256, 0, s>>>(p, C);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t mc = {};
+        mc.gridDim = dim3((unsigned)(C - 1), 2 * kRows / 8);
+        mc.blockDim = dim3(256);
+        mc.stream = s;
+        mc.attrs = pdl;
+        mc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&mc, merge_pieces_kernel, p, C);
     }
     return e;
 }

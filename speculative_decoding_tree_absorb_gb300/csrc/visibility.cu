@@ -12,12 +12,14 @@
 // stops at the first entry that breaks this, which bounds every walk by T steps
 // and records the entry in the error word instead of trapping.
 #include "kdt_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace kdt {
 namespace {
 
 __global__ void build_visibility_kernel(const int32_t *__restrict__ parent, int T, int W,
                                         uint32_t *__restrict__ vis, int32_t *err) {
+    tc::griddep_launch_dependents();               // the attention kernel may start its prefix blocks
     const int b = blockIdx.x;
     const int32_t *par = parent + (int64_t)b * T;
     for (int i = threadIdx.x; i < T; i += blockDim.x) {
@@ -41,6 +43,7 @@ __global__ void build_visibility_kernel(const int32_t *__restrict__ parent, int 
 // Wide trees (T > 128): each thread zeroes its row, then sets bits word by word.
 __global__ void build_visibility_wide_kernel(const int32_t *__restrict__ parent, int T, int W,
                                              uint32_t *__restrict__ vis, int32_t *err) {
+    tc::griddep_launch_dependents();
     const int b = blockIdx.x;
     const int32_t *par = parent + (int64_t)b * T;
     for (int i = threadIdx.x; i < T; i += blockDim.x) {
