@@ -13,6 +13,7 @@
 // warp-shuffle reductions, and the weights are broadcast by shuffle while the
 // lanes stream the 512 output columns as float4s.
 #include "kdt_internal.cuh"
+#include "tc_ptx.cuh"
 
 #include <math.h>
 
@@ -71,6 +72,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_splits_kernel(const f
                                                                          int S, int64_t rows,
                                                                          float *__restrict__ out,
                                                                          float *__restrict__ lse) {
+    // launched to overlap the end of the attention kernel that wrote the partials
+    tc::griddep_wait();
     const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     if (row >= rows) return;
     merge_row(part_o, part_lse, S, rows, row, out + row * kDc, lse ? lse + row : nullptr);
@@ -108,7 +111,19 @@ cudaError_t launch_merge_splits(const float *part_o, const float *part_lse, int 
                                 float *out, float *lse, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
     const int64_t ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
-    merge_splits_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, s>>>(part_o, part_lse, num_splits, rows, out, lse);
+    // programmatic dependent launch after the split attention kernel (the kernel waits for
+    // it before reading the partials)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kWarpsPerCta * 32);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, merge_splits_kernel, part_o, part_lse, num_splits, rows, out, lse);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

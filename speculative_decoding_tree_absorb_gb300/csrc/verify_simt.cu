@@ -27,6 +27,7 @@
 // Split-KV: blockIdx.y takes a contiguous range of key blocks; with more than one split
 // the CTA writes a normalised partial (o_s, lse_s) that K2 merges.
 #include "kdt_internal.cuh"
+#include "tc_ptx.cuh"
 
 #include <math.h>
 
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(Layout<Tin, kRows>::kThreads, kRows == 16 ? 2 
         lpart[i] = 0.f;
     }
     float acc[kRPT][4];
+    bool vis_ready = false;            // the visibility bits are known to be written
 
 #pragma unroll
     for (int g = 0; g < kNS - 1; ++g) issue(g);
@@ -217,6 +219,12 @@ __global__ void __launch_bounds__(Layout<Tin, kRows>::kThreads, kRows == 16 ? 2 
             }
             if (step == kQKChunks - 1) {
                 // ---------------- mask, online softmax, P to shared memory -------------------
+                // the bits may come from the visibility kernel launched just before this one:
+                // wait for it before the first block with tree keys
+                if (!vis_ready && k0 + kKeys > P) {
+                    tc::griddep_wait();
+                    vis_ready = true;
+                }
 #pragma unroll
                 for (int i = 0; i < kRPT; ++i) {
                     float s[4];
@@ -276,6 +284,7 @@ __global__ void __launch_bounds__(Layout<Tin, kRows>::kThreads, kRows == 16 ? 2 
         }
     }
     cp_async_wait<0>();
+    tc::griddep_launch_dependents();   // the split merge may launch; it waits for this kernel's end
 
     // ---------------- epilogue: o = O / l, lse = ln2 * (m2 + log2 l) -------------------------
     const bool partial = p.num_splits > 1;
@@ -303,12 +312,22 @@ template <typename Tin, int kRows>
 cudaError_t launch_typed(const VerifyParams &p, cudaStream_t s) {
     using L = Layout<Tin, kRows>;
     const int rows_seq = p.T * p.H;
-    const dim3 grid((rows_seq + kRows - 1) / kRows, p.num_splits, p.B);
     cudaError_t e = cudaFuncSetAttribute(verify_simt_kernel<Tin, kRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmem);
     if (e != cudaSuccess) return e;
-    verify_simt_kernel<Tin, kRows><<<grid, L::kThreads, L::kSmem, s>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent launch after the visibility kernel of the same call: the kernel
+    // waits for it before its first block with tree keys
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows_seq + kRows - 1) / kRows, p.num_splits, p.B);
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kSmem;
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = p.overlap_vis ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, verify_simt_kernel<Tin, kRows>, p);
 }
 
 }  // namespace
