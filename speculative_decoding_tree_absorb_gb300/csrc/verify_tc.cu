@@ -1376,7 +1376,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 // serves boundary c when c is the first boundary inside its unit, rows 8y .. 8y + 7 of
 // the unit's 256 (one warp per row, 16 columns per lane): the normalised partial states
 // (o_k, lse_k) of the pieces combine exactly as the log-sum-exp merge of disjoint key
-// sets, processed one piece after another.
+// sets, o = sum_k e^(lse_k - M) o_k / sum_k e^(lse_k - M) with M the largest lse_k.
 __global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int C) {
     __shared__ int s_valid, s_n, s_b, s_rt0;
     __shared__ int s_slot[kMaxClusters + 1];
@@ -1426,26 +1426,42 @@ __global__ void __launch_bounds__(256) merge_pieces_kernel(const TcParams p, int
     const int r = blockIdx.y * 8 + (threadIdx.x >> 5);        // row of the unit, 0..255
     const int R = s_rt0 * kRows + r;
     if (R >= p.rows_seq) return;
-    float M = -INFINITY, sum = 0.f;
+    // the pieces' lse, 32 at a time across the lanes (one round trip for the weights), then
+    // their rows of o weighted and summed (independent loads)
+    const int n = s_n;
+    float M = -INFINITY;
+    for (int base = 0; base < n; base += 32) {
+        const float l = base + lane < n ? p.part_lse[(int64_t)s_slot[base + lane] * (2 * kRows) + r] : -INFINITY;
+        float m = l;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        M = fmaxf(M, m);
+    }
+    float sum = 0.f;
     float4 acc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < s_n; ++k) {
-        const int64_t idx = (int64_t)s_slot[k] * (2 * kRows) + r;
-        const float l = p.part_lse[idx];
-        if (l == -INFINITY) continue;                          // no visible key in this piece
-        const float Mn = fmaxf(M, l);
-        const float so = M == -INFINITY ? 0.f : expf(M - Mn);
-        const float wk = expf(l - Mn);
-        const float4 *src = reinterpret_cast<const float4 *>(p.part_o + idx * kDc);
+    for (int base = 0; base < n && M > -INFINITY; base += 32) {
+        const float l = base + lane < n ? p.part_lse[(int64_t)s_slot[base + lane] * (2 * kRows) + r] : -INFINITY;
+        const float w = l == -INFINITY ? 0.f : expf(l - M);   // a piece with no visible key weighs 0
+        float ws = w;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 v = __ldg(src + lane + 32 * q);
-            acc[q] = make_float4(acc[q].x * so + wk * v.x, acc[q].y * so + wk * v.y, acc[q].z * so + wk * v.z,
-                                 acc[q].w * so + wk * v.w);
+        for (int off = 16; off >= 1; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+        sum += ws;
+        const int cnt = n - base < 32 ? n - base : 32;
+#pragma unroll 4
+        for (int k = 0; k < cnt; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            if (wk == 0.f) continue;
+            const float4 *src =
+                reinterpret_cast<const float4 *>(p.part_o + ((int64_t)s_slot[base + k] * (2 * kRows) + r) * kDc);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = __ldg(src + lane + 32 * q);
+                acc[q] = make_float4(fmaf(wk, v.x, acc[q].x), fmaf(wk, v.y, acc[q].y), fmaf(wk, v.z, acc[q].z),
+                                     fmaf(wk, v.w, acc[q].w));
+            }
         }
-        sum = sum * so + wk;
-        M = Mn;
     }
     const float inv = sum > 0.f ? 1.f / sum : 0.f;
     const int64_t grow = (int64_t)s_b * p.rows_seq + R;
