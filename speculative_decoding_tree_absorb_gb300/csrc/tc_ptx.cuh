@@ -426,6 +426,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 //   lbo:   leading byte offset (MN-major: stride between 64-element MN blocks;
 //          ignored for K-major swizzled layouts)
 //   sbo:   stride byte offset (stride between 8-row groups)
+// The start field holds address >> 4 in 14 bits, so adding (bytes >> 4) to a descriptor
+// moves its start by `bytes` exactly while the address stays below 256 KB (all of shared
+// memory): MMA issue loops build one descriptor per tile and add constant offsets.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t start, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= (uint64_t)((start & 0x3FFFFu) >> 4);

@@ -109,8 +109,9 @@ constexpr int kKSub = kHalfKeys * 128;            // S-CTA key sub-tile [64 keys
 constexpr int kVSub = kKeys * 128;                // O-CTA value sub-tile [128 keys x 64 dims]: 16 KB
 // Tiles travel as 32 KB requests from 4-D views of the cache (few, large requests:
 // the copy engine's cost is per request).
-constexpr int kKChunks = 2;                       // latent key chunks per block
-constexpr int kKSlotBytes = 4 * kKSub;            // S latent ring slot: 64 keys x 256 latent dims
+constexpr int kKSubPerChunk = 4;                  // 64-dim sub-tiles per latent key chunk
+constexpr int kKChunks = 8 / kKSubPerChunk;       // latent key chunks per block
+constexpr int kKSlotBytes = kKSubPerChunk * kKSub;   // S latent ring slot: 64 keys x 256 latent dims
 constexpr int kNK = 3;                            // S-CTA latent key ring slots (96 KB, 1.5 blocks)
 constexpr int kNR = 4;                            // S-CTA rope key ring slots of kKSub (32 KB, four blocks)
 constexpr int kQpeBytes = kRows * 128;            // Q_pe tile of one S-CTA: 16 KB
@@ -121,13 +122,21 @@ constexpr int kPSlotBytes = kPBytes + 1024;       // 32 KB P + alpha[128] (+ pad
 constexpr uint32_t kPTx = kPBytes + kRows * 4;    // bytes copied into a P slot per block
 constexpr int kNS = 2;                            // S-CTA staging slots (free once the copy landed)
 constexpr int kNP = 4;                            // O-CTA P slots (free once P.V of the block ran)
-constexpr int kVSlotBytes = 2 * kVSub;            // O ring slot: 128 keys x 128 latent dims
+constexpr int kVSubPerChunk = 2;                  // 64-dim sub-tiles per value chunk of one O-CTA
+constexpr int kVChunks = 4 / kVSubPerChunk;       // value chunks per block (an O-CTA's 256 latent dims)
+constexpr int kVSlotBytes = kVSubPerChunk * kVSub;   // O ring slot: 128 keys x 128 latent dims
 constexpr int kNV = 2;                            // O-CTA value ring slots (64 KB)
 constexpr uint32_t kCmdDone = 0xffffffffu;        // correction command: no more rescales
 constexpr uint64_t kWaitLimit = 200000000ull;     // ns a wait may poll before giving up (default)
 constexpr float kRescaleThreshold = 20.0f;        // log2 units
 constexpr int kMaxClusters = 48;                  // partial states then fit the no-alloc scratch
 constexpr int kSeqTable = 64;                     // sequences whose block counts a CTA keeps in shared memory
+// O-CTA correction/epilogue warps: kEpiWarps / 4 per TMEM lane quadrant, each taking an
+// equal share of the 512 columns; each warp transposes [32 rows x kEpiCols] at a time.
+// Eight warps (twice the stores in flight while O drains) measured no faster than four.
+constexpr int kEpiWarps = 4;
+constexpr int kEpiGroupCols = 512 * 4 / kEpiWarps;   // TMEM columns of one warp
+constexpr int kEpiCols = 16;
 
 // Shared-memory layout (same offsets in every CTA of the cluster; roles use
 // different parts). All tiles 1024-byte aligned for the 128B swizzle.
@@ -140,9 +149,9 @@ constexpr int kOffLSum = kOffRowMax + 2 * 2 * kRows * 4;    // S: [128] partial 
 constexpr int kOffP = 0;                                    // O: 4 x 33 KB P + alpha
 constexpr int kOffV = kOffP + kNP * kPSlotBytes;            // O: 2 x 32 KB values
 constexpr int kOffStats = kOffV + kNV * kVSlotBytes;        // O: [2 items][128] x (m, l)
-constexpr int kOffEpi = kOffStats + 2 * kRows * 8;          // O: 4 x [32 rows][32 fp32] epilogue transpose
+constexpr int kOffEpi = kOffStats + 2 * kRows * 8;          // O: epilogue transpose, [32 rows][kEpiCols fp32] a warp
 constexpr int kSEnd = kOffLSum + kRows * 4;
-constexpr int kOEnd = kOffEpi + 4 * 32 * 32 * 4;
+constexpr int kOEnd = kOffEpi + kEpiWarps * 32 * kEpiCols * 4;
 constexpr int kTileBytes = kSEnd > kOEnd ? kSEnd : kOEnd;
 constexpr int kSmemBytes = kTileBytes + 1024;               // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -176,7 +185,7 @@ struct Barriers {
     uint64_t stats_full[2];        // each O-CTA: an item's (m, l) of its rows from its S-CTA (by item parity)
     uint64_t stats_empty[2];       // each S-CTA: the O-CTA epilogue has read that buffer
     uint64_t o_done;               // each O-CTA: every P.V of the item has completed
-    uint64_t o_free;               // O leader: both O-CTAs' epilogues have read O (8 arrivals)
+    uint64_t o_free;               // O leader: both O-CTAs' epilogues have read O (one arrival a warp)
     uint64_t sync_bar;             // leader: MMA thread's own completion probe (mid-stream)
     uint64_t drain;                // completion of all MMAs of the pair before TMEM is read or freed
     uint32_t need[2][kNP];         // leader: per-CTA "some row of O needs a rescale" per P slot
@@ -678,10 +687,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bar.rescaled, 2);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.stats_full[i], 4 * 32);
-            mbar_init(&bar.stats_empty[i], 4);
+            mbar_init(&bar.stats_empty[i], kEpiWarps);
         }
         mbar_init(&bar.o_done, 1);
-        mbar_init(&bar.o_free, 8);
+        mbar_init(&bar.o_free, 2 * kEpiWarps);
         bar.kseen[0] = bar.kseen[1] = -1;
         mbar_init(&bar.sync_bar, 1);
         // one drain commit per MMA issuer that runs: two in the S leader (one for a single
@@ -834,13 +843,17 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                             *seen_mine = u;
                             tc_fence_after();
                             KDT_TC_TRACE(kEvKFull, u);
-                            const uint32_t kaddr = smem_u32(kring + slot * kKSlotBytes);
-                            for (int t = 0; t < 4; ++t)            // sub-tile t: dims 256c + 64t .. +64
-                                for (int kk = 0; kk < 4; ++kk) {
-                                    const uint64_t bdesc = sdesc_sw128(kaddr + t * kKSub + kk * 32, 16, 1024);
-                                    mma_ts_pair(d, tmem_q + 128 * c + 32 * t + 8 * kk, bdesc, idesc,
-                                                (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
-                                }
+                            // descriptors as a base plus compile-time offsets: the issue loop is a
+                            // few adds per MMA, so one thread keeps up with the tensor pipe
+                            const uint64_t bdesc0 = sdesc_sw128(smem_u32(kring + slot * kKSlotBytes), 16, 1024);
+                            const uint32_t acol = tmem_q + 32 * kKSubPerChunk * c;
+                            const uint32_t acc0 = c > 0 ? 1u : 0u;
+#pragma unroll
+                            for (int t = 0; t < kKSubPerChunk; ++t)   // sub-tile t: dims 64 (kKSubPerChunk c + t) .. +64
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_ts_pair(d, acol + 32 * t + 8 * kk, bdesc0 + (uint64_t)((t * kKSub + kk * 32) >> 4),
+                                                idesc, (t > 0 || kk > 0) ? 1u : acc0);
                             KDT_TC_TRACE(kEvKIssued, u);
                             mma_commit_pair(&bar.kempty[slot], kMaskAll);   // slot free: S-CTAs and their loaders
                         }
@@ -849,10 +862,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                         if (!(ok = wait_or_abort(bar, &bar.rfull[rslot], (uint32_t)(g / kNR) & 1, p.err, -5))) break;
                         tc_fence_after();
                         KDT_TC_TRACE(kEvRFull, g);
-                        const uint32_t raddr = smem_u32(rring + rslot * kKSub);
+                        const uint64_t qdesc0 = sdesc_sw128(smem_u32(qpe_tile), 16, 1024);
+                        const uint64_t rdesc0 = sdesc_sw128(smem_u32(rring + rslot * kKSub), 16, 1024);
+#pragma unroll
                         for (int kk = 0; kk < 4; ++kk)             // rope dims
-                            mma_ss_pair(d, sdesc_sw128(smem_u32(qpe_tile) + kk * 32, 16, 1024),
-                                        sdesc_sw128(raddr + kk * 32, 16, 1024), idesc, 1u);
+                            mma_ss_pair(d, qdesc0 + (uint64_t)(kk * 2), rdesc0 + (uint64_t)(kk * 2), idesc, 1u);
                         mma_commit_pair(&bar.rempty[rslot], kMaskAll);
                         mma_commit_pair(&bar.sfull[buf], kMaskS);
                         // the item's last block: both CTAs' Q_pe tiles may be refilled once it ran
@@ -1080,14 +1094,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 while (going && !aborted(bar) && next_item(p, w, cl, ncl, it)) {
                     for (int j = 0; j < it.nb && going; ++j) {
                         const int key0 = it.key_base + (it.kb0 + j) * kKeys;
-                        for (int h = 0; h < 2; ++h) {
+                        for (int h = 0; h < kVChunks; ++h) {
                             if (vr.n >= kNV &&
                                 !(going = wait_or_abort(bar, &bar.vempty[vr.slot], vr.phase ^ 1, p.err, -8)))
                                 break;
                             if (leader) mbar_arrive_expect_tx(&bar.vfull[vr.slot], 2 * kVSlotBytes);
-                            // latent dims [256h + 128k, +128): two sub-tiles in one request
-                            tma_load_4d_pair(vbase + vr.slot * kVSlotBytes, &map_vs,
-                                             map_to_rank(&bar.vfull[vr.slot], lead_rank), 0, key0, 4 * h + 2 * kpair, it.b);
+                            // chunk h of the pair spans 2 kVSubPerChunk sub-tiles of latent dims, the
+                            // first kVSubPerChunk from O-CTA 0, the rest from O-CTA 1: one request
+                            tma_load_4d_pair(vbase + vr.slot * kVSlotBytes, &map_vs, map_to_rank(&bar.vfull[vr.slot], lead_rank),
+                                             0, key0, (2 * h + kpair) * kVSubPerChunk, it.b);
                             KDT_TC_TRACE(kEvVIssue, vr.n);
                             ring_advance<kNV>(vr);
                         }
@@ -1098,7 +1113,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         } else if (warp == 1) {
             // ---------------- MMA issuer (leader): O += P V for 256 rows --------------------
             if (leader && elect_one() && G > 0) {
-                const uint32_t idesc = idesc_bf16_f32(2 * kRows, 256, 0, 1);
+                const uint32_t idesc = idesc_bf16_f32(2 * kRows, 128 * kVSubPerChunk, 0, 1);
                 RingPos vr;
                 uint32_t rs_phase = 0, sync_phase = 0;
                 bool ok = true;
@@ -1135,19 +1150,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                             rs_phase ^= 1;
                         }
                         tc_fence_after();
-                        const uint32_t paddr = smem_u32(pbase + ps * kPSlotBytes);
-                        for (int h = 0; h < 2; ++h) {
+                        const uint64_t adesc0 = sdesc_sw128(smem_u32(pbase + ps * kPSlotBytes), 16, 1024);
+                        const uint32_t acc0 = j > 0 ? 1u : 0u;
+                        for (int h = 0; h < kVChunks; ++h) {
                             if (!(ok = wait_or_abort(bar, &bar.vfull[vr.slot], vr.phase, p.err, -10))) break;
                             tc_fence_after();
                             KDT_TC_TRACE(kEvVFull, vr.n);
-                            const uint32_t vaddr = smem_u32(vbase + vr.slot * kVSlotBytes);
-                            for (int kk = 0; kk < kKeys / 16; ++kk) {
-                                const uint64_t adesc =
-                                    sdesc_sw128(paddr + (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32, 16, 1024);
-                                const uint64_t bdesc = sdesc_sw128(vaddr + kk * 2048, kVSub, 1024);
-                                // the item's first block starts O afresh
-                                mma_ss_pair(tmem + 256 * h, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
-                            }
+                            const uint64_t bdesc0 = sdesc_sw128(smem_u32(vbase + vr.slot * kVSlotBytes), kVSub, 1024);
+                            const uint32_t dcol = tmem + 128 * kVSubPerChunk * h;
+#pragma unroll
+                            for (int kk = 0; kk < kKeys / 16; ++kk)   // the item's first block starts O afresh
+                                mma_ss_pair(dcol, adesc0 + (uint64_t)(((kk >> 2) * (kPBytes / 2) + (kk & 3) * 32) >> 4),
+                                            bdesc0 + (uint64_t)((kk * 2048) >> 4), idesc, kk > 0 ? 1u : acc0);
                             mma_commit_pair(&bar.vempty[vr.slot], kMaskO);   // slot free in both O-CTAs
                             ring_advance<kNV>(vr);
                         }
@@ -1195,7 +1209,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 auto prefetch_block = [&]() {
                     if (!pf) return;
                     const int pk0 = ip.key_base + (ip.kb0 + jp) * kKeys + kpair * kHalfKeys;
-                    for (int c = 0; c < kKChunks; ++c) tma_prefetch_4d(&map_ks, 0, pk0, 4 * c, ip.b);
+                    for (int c = 0; c < kKChunks; ++c) tma_prefetch_4d(&map_ks, 0, pk0, kKSubPerChunk * c, ip.b);
                     tma_prefetch_3d(&map_kpe, 0, pk0, ip.b);
                     if (++jp == ip.nb) {
                         jp = 0;
@@ -1209,12 +1223,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < it.nb && going; ++j) {
                         prefetch_block();
                         const int key0 = it.key_base + (it.kb0 + j) * kKeys + kpair * kHalfKeys;   // S-CTA k's 64 keys
-                        for (int c = 0; c < kKChunks && going; ++c) {   // latent dims [256c, 256c + 256): four sub-tiles
+                        for (int c = 0; c < kKChunks && going; ++c) {   // latent sub-tiles [kKSubPerChunk c, +kKSubPerChunk)
                             if (kr.n >= kNK &&
                                 !(going = wait_or_abort(bar, &bar.kempty[kr.slot], kr.phase ^ 1, p.err, -21)))
                                 break;
                             tma_load_4d_pair_mc(kring + kr.slot * kKSlotBytes, &map_ks,
-                                                map_to_rank(&bar.kfull[kr.slot], 0), 0, key0, 4 * c, it.b, dst_mask);
+                                                map_to_rank(&bar.kfull[kr.slot], 0), 0, key0, kKSubPerChunk * c, it.b, dst_mask);
                             KDT_TC_TRACE(kEvKIssue, kr.n);
                             ring_advance<kNK>(kr);
                         }
@@ -1249,11 +1263,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-        } else if (warp >= 4 && warp < 8) {
+        } else if (warp >= 4 && warp < 4 + kEpiWarps) {
             // ---------------- correction (rare rescale) and epilogue, per item ----------------
-            // Warps 4-7 only (one per TMEM lane quadrant): named barrier 1 counts 128 threads.
-            // They sleep on `go` until the MMA thread hands O over for a rescale or ends the item.
+            // Warp w serves the 32 rows of TMEM lane quadrant (w % 4) and the columns
+            // [col0, col0 + kEpiGroupCols); named barrier 1 counts these warps. They sleep on
+            // `go` until the MMA thread hands O over for a rescale or ends the item.
             const int row = 32 * (warp & 3) + lane;
+            const int col0 = ((warp - 4) >> 2) * kEpiGroupCols;
             bool ok = true;
             uint32_t e = 0;                                     // `go` events so far
             WorkIter w = w0;
@@ -1262,7 +1278,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             while (ok && next_item(p, w, cl, ncl, it)) {
                 for (;; ++e) {
                     ok = warp_wait_cluster(bar, &bar.go, e & 1, p.err, -12);
-                    if (barrier_or<1, 128>(!ok)) {
+                    if (barrier_or<1, 32 * kEpiWarps>(!ok)) {
                         ok = false;
                         break;
                     }
@@ -1275,9 +1291,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     // CTA's rows of O by that block's factors (rows that need none multiply by 1)
                     const float a = reinterpret_cast<const float *>(pbase + (cmd % kNP) * kPSlotBytes + kPBytes)[row];
                     tc_fence_after();
-                    for (int c = 0; c < 512 / 32; ++c) {
+                    for (int c = 0; c < kEpiGroupCols / 32; ++c) {
                         uint32_t r[32];
-                        const uint32_t addr = tmem_lane_addr(tmem, warp, c * 32);
+                        const uint32_t addr = tmem_lane_addr(tmem, warp, col0 + c * 32);
                         tmem_ld32(addr, r);
                         tmem_wait_ld();
 #pragma unroll
@@ -1286,7 +1302,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                     tc_fence_before();
-                    barrier_or<1, 128>(false);             // all four warps' stores done
+                    barrier_or<1, 32 * kEpiWarps>(false);  // every warp's stores done
                     if (threadIdx.x == 128) mbar_arrive_remote(&bar.rescaled, lead_rank);
                 }
                 if (!ok) break;
@@ -1295,7 +1311,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 const int sb = ii & 1;
                 ok = warp_wait(bar, &bar.o_done, (uint32_t)ii & 1, p.err, -13) &&
                      warp_wait_cluster(bar, &bar.stats_full[sb], (uint32_t)(ii >> 1) & 1, p.err, -14);
-                if (barrier_or<1, 128>(!ok)) {
+                if (barrier_or<1, 32 * kEpiWarps>(!ok)) {
                     ok = false;
                     break;
                 }
@@ -1315,32 +1331,40 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 const float2 st = stats_s[sb * kRows + row];
                 const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
                 // Each thread holds one row; the rows go out through a per-warp transpose in
-                // shared memory so that every store instruction writes whole 128-byte lines
-                // (four rows x 128 bytes). 16-byte slot q of staged row r sits at q ^ (r & 7),
-                // which keeps both the row-wise writes and the line-wise reads conflict-free.
-                float *stg = reinterpret_cast<float *>(smem + kOffEpi) + (warp & 3) * 32 * 32;
-                const int rsub = lane >> 3, qsub = lane & 7;      // read side: row 4i + rsub, slot qsub
-                float *orow0 = orow - (int64_t)lane * kDc;        // row 0 of this warp's 32
+                // shared memory so that every store instruction writes whole 32-byte sectors
+                // (eight rows x 64 bytes). 16-byte slot q of staged row r sits at
+                // q ^ ((r >> 1) & 3), which keeps both the row-wise writes and the
+                // sector-wise reads at the minimum number of shared-memory wavefronts.
+                static_assert(kEpiCols == 16, "the transpose below stages 16 columns");
+                float *stg = reinterpret_cast<float *>(smem + kOffEpi) + (warp - 4) * 32 * kEpiCols;
+                const int rsub = lane >> 2, qsub = lane & 3;      // read side: row 8i + rsub, slot qsub
+                float *orow0 = orow - (int64_t)lane * kDc + col0; // row 0 of this warp's 32, its first column
                 const int rows_ok = p.rows_seq - (R - lane);      // rows of the 32 that exist
-                for (int c = 0; c < 512 / 32; ++c) {
+                for (int c = 0; c < kEpiGroupCols / 32; ++c) {
                     uint32_t r[32];
-                    tmem_ld32(tmem_lane_addr(tmem, warp, c * 32), r);
+                    tmem_ld32(tmem_lane_addr(tmem, warp, col0 + c * 32), r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        *reinterpret_cast<float4 *>(stg + lane * 32 + ((q ^ (lane & 7)) << 2)) =
-                            make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                                        __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
-                    __syncwarp();
+                    for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int rr = 4 * i + rsub;
-                        const float4 v = *reinterpret_cast<const float4 *>(stg + rr * 32 + ((qsub ^ (rr & 7)) << 2));
-                        if (rr < rows_ok) *reinterpret_cast<float4 *>(orow0 + (int64_t)rr * kDc + c * 32 + 4 * qsub) = v;
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<float4 *>(stg + lane * kEpiCols + ((q ^ ((lane >> 1) & 3)) << 2)) =
+                                make_float4(__uint_as_float(r[16 * hh + 4 * q]) * inv, __uint_as_float(r[16 * hh + 4 * q + 1]) * inv,
+                                            __uint_as_float(r[16 * hh + 4 * q + 2]) * inv,
+                                            __uint_as_float(r[16 * hh + 4 * q + 3]) * inv);
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = 8 * i + rsub;
+                            const float4 v =
+                                *reinterpret_cast<const float4 *>(stg + rr * kEpiCols + ((qsub ^ ((rr >> 1) & 3)) << 2));
+                            if (rr < rows_ok)
+                                *reinterpret_cast<float4 *>(orow0 + (int64_t)rr * kDc + c * 32 + hh * 16 + 4 * qsub) = v;
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
-                if (R < p.rows_seq && lrow) *lrow = st.y > 0.f ? 0.6931471805599453f * (st.x + log2f(st.y)) : -INFINITY;
+                if (col0 == 0 && R < p.rows_seq && lrow) *lrow = st.y > 0.f ? 0.6931471805599453f * (st.x + log2f(st.y)) : -INFINITY;
                 // O may be overwritten and the statistics buffer refilled
                 tc_fence_before();
                 __syncwarp();
@@ -1549,8 +1573,8 @@ cudaError_t launch_verify_tc(const VerifyParams &vp, cudaStream_t s) {
         // lands as m consecutive [n x 64] 128B-swizzled sub-tiles.
         cuuint64_t dims[4] = {64, L, (cuuint64_t)(kDc / 64), (cuuint64_t)vp.B};
         cuuint64_t strides[3] = {(cuuint64_t)kDc * 2, 128, L * kDc * 2};
-        cuuint32_t box_k[4] = {64, kHalfKeys, 4, 1};    // S-CTA: its 64 keys x 256 dims
-        cuuint32_t box_v[4] = {64, kKeys, 2, 1};        // O-CTA: 128 keys x its 128 dims
+        cuuint32_t box_k[4] = {64, kHalfKeys, kKSubPerChunk, 1};   // S-CTA: its 64 keys x one chunk of dims
+        cuuint32_t box_v[4] = {64, kKeys, kVSubPerChunk, 1};       // O-CTA: 128 keys x its dims of one chunk
         if (!make_map(&map_ks, vp.c_kv, 4, dims, strides, box_k)) return cudaErrorInvalidValue;
         if (!make_map(&map_vs, vp.c_kv, 4, dims, strides, box_v)) return cudaErrorInvalidValue;
     }
