@@ -19,7 +19,7 @@
 //    keeps a thread under 128 registers and a SM at 16 resident warps.
 //  * Every operand reaches shared memory by cp.async (16-byte copies, rows past the
 //    sequence zero-filled, never read), in one ring of 4 slots filled in the order the
-//    block consumes them: per 64-key block, 18 chunks of 32 dims of Q and K for the
+//    block consumes them: per 64-key block, 9 chunks of 64 dims of Q and K for the
 //    scores, then 4 slices of 16 value rows (the latent rows again) for P.V. So the next
 //    block's first chunks load while this block's P.V runs, and the 3 loads ahead of the
 //    one in use hide the L2/DRAM latency; operands stay in their row-major global layout.
@@ -35,8 +35,8 @@ namespace kdt {
 namespace {
 
 constexpr int kKeys = kSimtKeys;       // 64 keys per block
-constexpr int kDChunk = 32;            // dims per score chunk
-constexpr int kQKChunks = kDqk / kDChunk;      // 18
+constexpr int kDChunk = 64;            // dims per score chunk (fewer, larger steps: each step ends at a barrier)
+constexpr int kQKChunks = kDqk / kDChunk;      // 9; a chunk lies wholly in the latent or the rope dims
 
 // Element-type traits: shared-memory row pads (keep 16-byte alignment and spread the
 // rows over the banks) and 4-wide loads widened to fp32.
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(Layout<Tin, kRows>::kThreads, kRows == 16 ? 2 
                                kbase + (kv_row0 + (ok ? key : 0)) * kstride + pc * kEl16, ok ? 16u : 0u);
                 }
             } else {
-                // value rows kb*64 + 16 (step - 18) .. + 16, all 512 latent dims
+                // value rows kb*64 + 16 (step - kQKChunks) .. + 16, all 512 latent dims
                 const int k0 = kb * kKeys + (step - kQKChunks) * kVKeys;
 #pragma unroll
                 for (int i = tid; i < kVKeys * kVPieces; i += kThreads) {
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(Layout<Tin, kRows>::kThreads, kRows == 16 ? 2 
         const int k0 = (kb0 + g / kSteps) * kKeys;
         const Tin *slot = reinterpret_cast<const Tin *>(smem_raw + (g % kNS) * L::kSlot);
         if (step < kQKChunks) {
-            // ---------------- S += Q K^T over 32 dims: rows 2ty+i, keys tx + 16 j -------------
+            // ---------------- S += Q K^T over 64 dims: rows 2ty+i, keys tx + 16 j -------------
             if (step == 0) {
 #pragma unroll
                 for (int i = 0; i < kRPT; ++i)
@@ -308,6 +308,297 @@ __global__ void __launch_bounds__(Layout<Tin, kRows>::kThreads, kRows == 16 ? 2 
     }
 }
 
+// The 64-row tile (the fp32 path and large bf16 shapes off the tensor path): the same
+// operand stream as above, with 2 value slices of 32 keys a block in a 3-slot ring (one
+// fewer barrier a block, measured 1 % faster than 4 slots of 16-key slices), and register
+// tiles chosen for the shared-memory bandwidth a SM has (one 128-byte wavefront a cycle
+// against four FMA instructions):
+//  * scores: warp w takes rows 8 (w / 2) .. + 8 and keys 32 (w % 2) .. + 32; a thread
+//    2 rows x 4 keys with the lanes as 4 row pairs x 8 keys, so a Q read is one broadcast
+//    wavefront and a K read 8 consecutive rows (one wavefront): 6 wavefronts for 32 FMAs.
+//    A row's maximum is combined over the two warps through shared memory.
+//  * output: warp w takes rows 16 (w / 4) .. + 16 and columns 128 (w % 4) .. + 128; a
+//    thread 4 rows x 16 columns (64 accumulators), P read transposed ([key][row]) as one
+//    16-byte load for its 4 rows and 4 16-byte value loads: 5 wavefronts for 64 FMAs.
+template <typename T> struct Layout64 {
+    static constexpr int kRows = 64, kThreads = 512, kVKeys = 32, kNS = 3;
+    static constexpr int kSteps = kQKChunks + kKeys / kVKeys;
+    static constexpr int kQKRow = kDChunk + Elt<T>::kPadQK;
+    static constexpr int kVRow = kDc + Elt<T>::kPadV;
+    static constexpr int kQKBytes = (kRows + kKeys) * kQKRow * (int)sizeof(T);
+    static constexpr int kVBytes = kVKeys * kVRow * (int)sizeof(T);
+    static constexpr int kSlot = ((kQKBytes > kVBytes ? kQKBytes : kVBytes) + 127) / 128 * 128;
+    static constexpr int kPtRow = kRows + 4;                  // floats per row of P^T ([key][row])
+    static constexpr int kOffPt = kNS * kSlot;
+    static constexpr int kOffRed = kOffPt + kKeys * kPtRow * 4;   // [2 key halves][64 rows] maxima, then sums
+    static constexpr int kOffAlpha = kOffRed + 2 * kRows * 4;     // [64] rescale factors of the block
+    static constexpr int kSmem = kOffAlpha + kRows * 4;
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(512, 1) verify_simt64_kernel(const VerifyParams p) {
+    using L = Layout64<Tin>;
+    constexpr int kThreads = L::kThreads, kVKeys = L::kVKeys, kSteps = L::kSteps, kNS = L::kNS, kR = L::kRows;
+    constexpr int kEl16 = 16 / (int)sizeof(Tin);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *pt = reinterpret_cast<float *>(smem_raw + L::kOffPt);       // P^T [64 keys][68]
+    float *red = reinterpret_cast<float *>(smem_raw + L::kOffRed);     // [2][64]
+    float *alpha_s = reinterpret_cast<float *>(smem_raw + L::kOffAlpha);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // score tile: rows sr0 + {0, 1}, keys sk0 + 8 j
+    const int kh = warp & 1;
+    const int sr0 = 8 * (warp >> 1) + 2 * (lane >> 3);
+    const int sk0 = 32 * kh + (lane & 7);
+    // output tile: rows or0 + {0..3}, columns oc0 + 32 q + {0..3}
+    const int or0 = 16 * (warp >> 2) + 4 * (lane >> 3);
+    const int oc0 = 128 * (warp & 3) + 4 * (lane & 7);
+
+    const int b = blockIdx.z;
+    const int split = blockIdx.y;
+    const int rows_seq = p.T * p.H;
+    const int r0 = blockIdx.x * kR;
+    const Tin *q_nope = static_cast<const Tin *>(p.q_nope);
+    const Tin *q_pe = static_cast<const Tin *>(p.q_pe);
+    const Tin *c_kv = static_cast<const Tin *>(p.c_kv);
+    const Tin *k_pe = static_cast<const Tin *>(p.k_pe);
+
+    const int P = p.prefix_len[b];
+    const int kv_len = P + p.T;
+    const int nblk = (kv_len + kKeys - 1) / kKeys;
+    const int kb0 = split * p.blocks_per_split;
+    const int kb1 = min(nblk, kb0 + p.blocks_per_split);
+    const int key_end = min(kv_len, kb1 * kKeys);
+    const int64_t q_row0 = (int64_t)b * rows_seq + r0;
+    const int64_t kv_row0 = (int64_t)b * p.L;
+    const int total = kb1 > kb0 ? (kb1 - kb0) * kSteps : 0;
+
+    constexpr int kQKPieces = kDChunk / kEl16;
+    constexpr int kQPieces = kR * kQKPieces;
+    constexpr int kVPieces = kDc / kEl16;
+    auto issue = [&](int g) {
+        if (g < total) {
+            const int kb = kb0 + g / kSteps, step = g % kSteps;
+            Tin *slot = reinterpret_cast<Tin *>(smem_raw + (g % kNS) * L::kSlot);
+            if (step < kQKChunks) {
+                const int d0 = step * kDChunk;
+                const bool nope = d0 < kDc;
+                const Tin *qbase = nope ? q_nope + d0 : q_pe + (d0 - kDc);
+                const int64_t qstride = nope ? p.q_nope_stride : p.q_pe_stride;
+#pragma unroll
+                for (int i = tid; i < kQPieces; i += kThreads) {
+                    const int rr = i / kQKPieces, pc = i % kQKPieces;
+                    const bool ok = r0 + rr < rows_seq;
+                    cp_async16(slot + rr * L::kQKRow + pc * kEl16, qbase + (q_row0 + (ok ? rr : 0)) * qstride + pc * kEl16,
+                               ok ? 16u : 0u);
+                }
+                const Tin *kbase = nope ? c_kv + d0 : k_pe + (d0 - kDc);
+                const int kstride = nope ? kDc : kDr;
+#pragma unroll
+                for (int i = tid; i < kKeys * kQKPieces; i += kThreads) {
+                    const int rr = i / kQKPieces, pc = i % kQKPieces;
+                    const int key = kb * kKeys + rr;
+                    const bool ok = key < key_end;
+                    cp_async16(slot + (kR + rr) * L::kQKRow + pc * kEl16,
+                               kbase + (kv_row0 + (ok ? key : 0)) * kstride + pc * kEl16, ok ? 16u : 0u);
+                }
+            } else {
+                const int k0 = kb * kKeys + (step - kQKChunks) * kVKeys;
+#pragma unroll
+                for (int i = tid; i < kVKeys * kVPieces; i += kThreads) {
+                    const int kk = i / kVPieces, pc = i % kVPieces;
+                    const int key = k0 + kk;
+                    const bool ok = key < key_end;
+                    cp_async16(slot + kk * L::kVRow + pc * kEl16, c_kv + (kv_row0 + (ok ? key : 0)) * kDc + pc * kEl16,
+                               ok ? 16u : 0u);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    int qidx[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) qidx[i] = min(r0 + sr0 + i, rows_seq - 1) / p.H;
+    float o[4][16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 16; ++c) o[i][c] = 0.f;
+    float m2[2] = {-INFINITY, -INFINITY}, lpart[2] = {0.f, 0.f};
+    float acc[2][4];
+    bool vis_ready = false;
+
+#pragma unroll
+    for (int g = 0; g < kNS - 1; ++g) issue(g);
+    for (int g = 0; g < total; ++g) {
+        cp_async_wait<kNS - 2>();
+        __syncthreads();
+        issue(g + kNS - 1);
+        const int step = g % kSteps;
+        const int k0 = (kb0 + g / kSteps) * kKeys;
+        const Tin *slot = reinterpret_cast<const Tin *>(smem_raw + (g % kNS) * L::kSlot);
+        if (step < kQKChunks) {
+            // ---------------- S += Q K^T over 64 dims -------------------------------------
+            if (step == 0) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+            }
+            const Tin *qs = slot + sr0 * L::kQKRow;
+            const Tin *ks = slot + (kR + sk0) * L::kQKRow;
+#pragma unroll
+            for (int d = 0; d < kDChunk; d += 4) {
+                const float4 a0 = Elt<Tin>::get4(qs + d), a1 = Elt<Tin>::get4(qs + L::kQKRow + d);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 k = Elt<Tin>::get4(ks + 8 * j * L::kQKRow + d);
+                    acc[0][j] = fmaf(a0.x, k.x, fmaf(a0.y, k.y, fmaf(a0.z, k.z, fmaf(a0.w, k.w, acc[0][j]))));
+                    acc[1][j] = fmaf(a1.x, k.x, fmaf(a1.y, k.y, fmaf(a1.z, k.z, fmaf(a1.w, k.w, acc[1][j]))));
+                }
+            }
+            if (step == kQKChunks - 1) {
+                // ---------------- mask, scale; this warp's row maxima ---------------------------
+                if (!vis_ready && k0 + kKeys > P) {
+                    tc::griddep_wait();
+                    vis_ready = true;
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int key = k0 + sk0 + 8 * j;
+                        bool visible = key < key_end;
+                        if (visible && key >= P) {
+                            const int t = key - P;
+                            const uint32_t w = p.vis[((int64_t)b * p.T + qidx[i]) * p.W + (t >> 5)];
+                            visible = (w >> (t & 31)) & 1u;
+                        }
+                        acc[i][j] = visible ? acc[i][j] * p.scale_log2 : -INFINITY;
+                        mx = fmaxf(mx, acc[i][j]);
+                    }
+#pragma unroll
+                    for (int off = 4; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    if ((lane & 7) == 0) red[kh * kR + sr0 + i] = mx;
+                }
+                // the other half's maxima are read after the next load's barrier
+            }
+        } else {
+            if (step == kQKChunks) {
+                // ---------------- online softmax: P^T to shared memory, rescale factors -------------
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float mx = fmaxf(red[sr0 + i], red[kR + sr0 + i]);
+                    const float mnew = fmaxf(m2[i], mx);
+                    const float al = (mnew == -INFINITY) ? 1.f : exp2f(m2[i] - mnew);
+                    float rs = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float pj = (mnew == -INFINITY) ? 0.f : exp2f(acc[i][j] - mnew);
+                        pt[(sk0 + 8 * j) * L::kPtRow + sr0 + i] = pj;
+                        rs += pj;
+                    }
+                    lpart[i] = lpart[i] * al + rs;
+                    m2[i] = mnew;
+                    if (kh == 0 && (lane & 7) == 0) alpha_s[sr0 + i] = al;
+                }
+                __syncthreads();       // P^T and the factors of every row are written
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float al = alpha_s[or0 + i];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) o[i][c] *= al;
+                }
+            }
+            // ---------------- O += P V for 32 keys -------------------------------------------
+            const int kk0 = (step - kQKChunks) * kVKeys;
+#pragma unroll 4
+            for (int kk = 0; kk < kVKeys; ++kk) {
+                const float4 pr = *reinterpret_cast<const float4 *>(pt + (kk0 + kk) * L::kPtRow + or0);
+                const Tin *vrow = slot + kk * L::kVRow + oc0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 v = Elt<Tin>::get4(vrow + 32 * q);
+                    o[0][4 * q + 0] = fmaf(pr.x, v.x, o[0][4 * q + 0]);
+                    o[0][4 * q + 1] = fmaf(pr.x, v.y, o[0][4 * q + 1]);
+                    o[0][4 * q + 2] = fmaf(pr.x, v.z, o[0][4 * q + 2]);
+                    o[0][4 * q + 3] = fmaf(pr.x, v.w, o[0][4 * q + 3]);
+                    o[1][4 * q + 0] = fmaf(pr.y, v.x, o[1][4 * q + 0]);
+                    o[1][4 * q + 1] = fmaf(pr.y, v.y, o[1][4 * q + 1]);
+                    o[1][4 * q + 2] = fmaf(pr.y, v.z, o[1][4 * q + 2]);
+                    o[1][4 * q + 3] = fmaf(pr.y, v.w, o[1][4 * q + 3]);
+                    o[2][4 * q + 0] = fmaf(pr.z, v.x, o[2][4 * q + 0]);
+                    o[2][4 * q + 1] = fmaf(pr.z, v.y, o[2][4 * q + 1]);
+                    o[2][4 * q + 2] = fmaf(pr.z, v.z, o[2][4 * q + 2]);
+                    o[2][4 * q + 3] = fmaf(pr.z, v.w, o[2][4 * q + 3]);
+                    o[3][4 * q + 0] = fmaf(pr.w, v.x, o[3][4 * q + 0]);
+                    o[3][4 * q + 1] = fmaf(pr.w, v.y, o[3][4 * q + 1]);
+                    o[3][4 * q + 2] = fmaf(pr.w, v.z, o[3][4 * q + 2]);
+                    o[3][4 * q + 3] = fmaf(pr.w, v.w, o[3][4 * q + 3]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    tc::griddep_launch_dependents();
+
+    // ---------------- epilogue: o = O / l, lse = ln2 * (m2 + log2 l) -------------------------
+    // row sums: over the 8 key lanes, then the two key halves through shared memory
+    __syncthreads();           // every read of the reduction buffer above is done
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float l = lpart[i];
+#pragma unroll
+        for (int off = 4; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if ((lane & 7) == 0) red[kh * kR + sr0 + i] = l;
+    }
+    __syncthreads();
+    const bool partial = p.num_splits > 1;
+    float *obase = partial ? p.part_o + (int64_t)split * p.rows_total * kDc : p.out;
+    float *lbase = partial ? p.part_lse + (int64_t)split * p.rows_total : p.lse;
+    if (kh == 0 && (lane & 7) == 0 && lbase) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = r0 + sr0 + i;
+            const float l = red[sr0 + i] + red[kR + sr0 + i];
+            if (r < rows_seq) lbase[(int64_t)b * rows_seq + r] = (l > 0.f) ? 0.6931471805599453f * (m2[i] + log2f(l)) : -INFINITY;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + or0 + i;
+        if (r >= rows_seq) continue;
+        const float l = red[or0 + i] + red[kR + or0 + i];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float *orow = obase + ((int64_t)b * rows_seq + r) * kDc + oc0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4 *>(orow + 32 * q) =
+                make_float4(o[i][4 * q] * inv, o[i][4 * q + 1] * inv, o[i][4 * q + 2] * inv, o[i][4 * q + 3] * inv);
+    }
+}
+
+template <typename Tin>
+cudaError_t launch_typed64(const VerifyParams &p, cudaStream_t s) {
+    using L = Layout64<Tin>;
+    const int rows_seq = p.T * p.H;
+    cudaError_t e = cudaFuncSetAttribute(verify_simt64_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows_seq + L::kRows - 1) / L::kRows, p.num_splits, p.B);
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kSmem;
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = p.overlap_vis ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, verify_simt64_kernel<Tin>, p);
+}
+
 template <typename Tin, int kRows>
 cudaError_t launch_typed(const VerifyParams &p, cudaStream_t s) {
     using L = Layout<Tin, kRows>;
@@ -335,7 +626,7 @@ cudaError_t launch_typed(const VerifyParams &p, cudaStream_t s) {
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s) {
     if (rows_per_cta == kSimtSmallRows)
         return dt == KDT_F32 ? launch_typed<float, kSimtSmallRows>(p, s) : launch_typed<__nv_bfloat16, kSimtSmallRows>(p, s);
-    return dt == KDT_F32 ? launch_typed<float, kSimtRows>(p, s) : launch_typed<__nv_bfloat16, kSimtRows>(p, s);
+    return dt == KDT_F32 ? launch_typed64<float>(p, s) : launch_typed64<__nv_bfloat16>(p, s);
 }
 
 }  // namespace kdt
