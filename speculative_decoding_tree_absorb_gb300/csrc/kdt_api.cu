@@ -130,7 +130,7 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
     p.impl = impl;
     const bool simt_small = impl == KDT_IMPL_SIMT_SMALL;
     const int unit_rows = tc ? tc_rows_per_unit() : (simt_small ? kSimtSmallRows : kSimtRows);
-    const int unit_keys = tc ? tc_keys_per_block() : kSimtKeys;
+    const int unit_keys = tc ? tc_keys_per_block() : (simt_small ? kSimtKeys : kSimtKeysTm);
     const int unit_tiles = (int)((rows_seq + unit_rows - 1) / unit_rows);   // work units per sequence
     const int nblk = (a->max_kv_len + unit_keys - 1) / unit_keys;
     const int64_t base = (int64_t)unit_tiles * a->B;
@@ -144,8 +144,9 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         p.blocks_per_split = nblk;
         p.ctas = 4 * p.tc_clusters;
     } else {
-        // SIMT: one CTA per SM at a time; fill about two waves, with at least 4 key blocks
-        // per split, unless the caller fixed the splits
+        // SIMT: one CTA per SM at a time; fill about two waves, with at least 256 keys per
+        // split (4 blocks of the 16-row tile, 2 of the 64-row tile), unless the caller fixed
+        // the splits
         const int64_t slots = sm_count();
         int splits;
         if (a->num_splits > 0) {
@@ -155,7 +156,8 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         } else {
             const int64_t want = (2LL * slots + base - 1) / base;
             splits = (int)(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
-            const int cap = nblk / 4 > 1 ? nblk / 4 : 1;
+            const int min_blocks = 256 / unit_keys;
+            const int cap = nblk / min_blocks > 1 ? nblk / min_blocks : 1;
             if (splits > cap) splits = cap;
         }
         if (splits > kMaxSplits) splits = kMaxSplits;

@@ -67,7 +67,8 @@ cudaError_t launch_build_visibility(const int32_t *parent, int B, int T, uint32_
 // or, for small shapes, 16-row tiles (128 threads) spread over more CTAs.
 constexpr int kSimtRows = 64;
 constexpr int kSimtSmallRows = 16;
-constexpr int kSimtKeys = 64;
+constexpr int kSimtKeys = 64;          // keys per block of the 16-row tile
+constexpr int kSimtKeysTm = 128;       // keys per block of the 64-row tile
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s);
 
 // K1: tcgen05 verify (bf16 inputs): one 4-CTA cluster (two CTA pairs) per resident slot,

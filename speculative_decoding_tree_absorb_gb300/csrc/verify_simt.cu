@@ -9,20 +9,21 @@
 // blocks -- the tiling that page's "Design Decisions and Trade-Offs" section
 // names for contexts beyond the single shared-memory score array.
 //
-// Design (differs from the pages' one-block-per-(b,h,i) kernel): a CTA owns 64
-// consecutive rows of one sequence -- all heads of a few tree queries -- so each
-// cache row it stages in shared memory serves 64 query rows instead of one. It is the
-// fp32 path (scores, softmax and P.V all in fp32) and the small-shape path.
-//  * 16 warps, 2 rows a thread: scores as a 2 x 4 register tile of a 64 x 64 block
-//    (keys tx, tx + 16, tx + 32, tx + 48 of the 16 key lanes, so that a warp's key reads
-//    are consecutive rows), the output as 2 rows x 32 columns (64 accumulators), which
-//    keeps a thread under 128 registers and a SM at 16 resident warps.
+// Design (differs from the pages' one-block-per-(b,h,i) kernel): a CTA owns consecutive
+// rows of one sequence -- all heads of a few tree queries -- so each cache row it stages
+// in shared memory serves all of them instead of one row. Two tiles:
+//  * the small-shape tile, 16 rows (128 threads, 2 rows a thread, 64-key blocks): scores
+//    as a 2 x 4 register tile (keys tx, tx + 16, tx + 32, tx + 48 of the 16 key lanes, so
+//    that a warp's key reads are consecutive rows), the output as 2 rows x 32 columns;
+//  * the 64-row tile (512 threads, 128-key blocks), the fp32 path: 8 x 8 register tiles
+//    in both contractions, the output tile parked in tensor memory while the scores of
+//    the next block use the registers (see verify_simt_tm_kernel below).
 //  * Every operand reaches shared memory by cp.async (16-byte copies, rows past the
-//    sequence zero-filled, never read), in one ring of 4 slots filled in the order the
-//    block consumes them: per 64-key block, 9 chunks of 64 dims of Q and K for the
-//    scores, then 4 slices of 16 value rows (the latent rows again) for P.V. So the next
-//    block's first chunks load while this block's P.V runs, and the 3 loads ahead of the
-//    one in use hide the L2/DRAM latency; operands stay in their row-major global layout.
+//    sequence zero-filled, never read), in one ring filled in the order the block
+//    consumes it: per key block, 9 chunks of 64 dims of Q and K for the scores, then
+//    slices of 16 value rows (the latent rows again) for P.V. So the next block's first
+//    chunks load while this block's P.V runs, and the loads ahead of the one in use hide
+//    the L2/DRAM latency; operands stay in their row-major global layout.
 //  * No atomics: every output element has one owner.
 // Split-KV: blockIdx.y takes a contiguous range of key blocks; with more than one split
 // the CTA writes a normalised partial (o_s, lse_s) that K2 merges.
@@ -308,51 +309,67 @@ __global__ void __launch_bounds__(Layout<Tin, kRows>::kThreads, kRows == 16 ? 2 
     }
 }
 
-// The 64-row tile (the fp32 path and large bf16 shapes off the tensor path): the same
-// operand stream as above, with 2 value slices of 32 keys a block in a 3-slot ring (one
-// fewer barrier a block, measured 1 % faster than 4 slots of 16-key slices), and register
-// tiles chosen for the shared-memory bandwidth a SM has (one 128-byte wavefront a cycle
-// against four FMA instructions):
-//  * scores: warp w takes rows 8 (w / 2) .. + 8 and keys 32 (w % 2) .. + 32; a thread
-//    2 rows x 4 keys with the lanes as 4 row pairs x 8 keys, so a Q read is one broadcast
-//    wavefront and a K read 8 consecutive rows (one wavefront): 6 wavefronts for 32 FMAs.
-//    A row's maximum is combined over the two warps through shared memory.
-//  * output: warp w takes rows 16 (w / 4) .. + 16 and columns 128 (w % 4) .. + 128; a
-//    thread 4 rows x 16 columns (64 accumulators), P read transposed ([key][row]) as one
-//    16-byte load for its 4 rows and 4 16-byte value loads: 5 wavefronts for 64 FMAs.
-template <typename T> struct Layout64 {
-    static constexpr int kRows = 64, kThreads = 512, kVKeys = 32, kNS = 3;
-    static constexpr int kSteps = kQKChunks + kKeys / kVKeys;
+// The 64-row tile with 128-key blocks and 8 x 8 register tiles in both contractions. A
+// warp-wide 16- or 8-byte shared load costs one 128-byte wavefront per 8 or 16 lanes
+// however many lanes share an address, so a lane receives at most 4 bytes a wavefront
+// while the SM issues four FMA instructions a cycle: only a tile whose every loaded
+// operand feeds 8 FMAs (8 x 8) keeps the FMA pipes busy. The 64 output accumulators and
+// the 64 score accumulators do not both fit in 128 registers, so the output tile waits in
+// tensor memory (256 columns, each thread its own lane and 64 columns) while the scores
+// of the next block are computed:
+//  * scores: warp w takes rows 8 (w / 2) .. + 8 and keys 64 (w % 2) .. + 64 of the block;
+//    lane = 8 dg + kt computes those 8 rows x keys kt + 8 j (j < 8) over the dim pairs
+//    2 dg + 8 u of every 64-dim chunk; the four dim groups' partial sums meet by two shuffle rounds,
+//    after which a lane holds rows 2 dg, 2 dg + 1 of its warp's 8 (8 keys each).
+//  * output: warp w takes rows 32 (w / 8) .. + 32 and columns 64 (w % 8) .. + 64; lane =
+//    8 rt + ct holds rows 8 rt .. + 8 of those and columns 4 ct + 32 q (q < 2, 4 each),
+//    reading P transposed ([key][row]) and 16-key value slices.
+template <typename T> struct LayoutTm {
+    static constexpr int kRows = 64, kKB = kSimtKeysTm, kThreads = 512, kVKeys = 16, kNS = 3;
+    static constexpr int kQK = kQKChunks, kSteps = kQKChunks + kKB / kVKeys;   // 9 + 8 loads a block
     static constexpr int kQKRow = kDChunk + Elt<T>::kPadQK;
     static constexpr int kVRow = kDc + Elt<T>::kPadV;
-    static constexpr int kQKBytes = (kRows + kKeys) * kQKRow * (int)sizeof(T);
+    static constexpr int kQKBytes = (kRows + kKB) * kQKRow * (int)sizeof(T);
     static constexpr int kVBytes = kVKeys * kVRow * (int)sizeof(T);
     static constexpr int kSlot = ((kQKBytes > kVBytes ? kQKBytes : kVBytes) + 127) / 128 * 128;
-    static constexpr int kPtRow = kRows + 4;                  // floats per row of P^T ([key][row])
+    static constexpr int kPtRow = kRows + 4;
     static constexpr int kOffPt = kNS * kSlot;
-    static constexpr int kOffRed = kOffPt + kKeys * kPtRow * 4;   // [2 key halves][64 rows] maxima, then sums
-    static constexpr int kOffAlpha = kOffRed + 2 * kRows * 4;     // [64] rescale factors of the block
-    static constexpr int kSmem = kOffAlpha + kRows * 4;
+    static constexpr int kOffRed = kOffPt + kKB * kPtRow * 4;     // [2 key halves][64 rows]
+    static constexpr int kOffAlpha = kOffRed + 2 * kRows * 4;     // [64]
+    static constexpr int kOffTmem = kOffAlpha + kRows * 4;        // tensor-memory base address
+    static constexpr int kSmem = kOffTmem + 16;
+    static constexpr uint32_t kTmemCols = 256;
 };
 
+// Two consecutive elements widened to fp32.
+template <typename T> __device__ __forceinline__ float2 get2(const T *p);
+template <> __device__ __forceinline__ float2 get2<float>(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+template <> __device__ __forceinline__ float2 get2<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
 template <typename Tin>
-__global__ void __launch_bounds__(512, 1) verify_simt64_kernel(const VerifyParams p) {
-    using L = Layout64<Tin>;
-    constexpr int kThreads = L::kThreads, kVKeys = L::kVKeys, kSteps = L::kSteps, kNS = L::kNS, kR = L::kRows;
+__global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyParams p) {
+    using L = LayoutTm<Tin>;
+    constexpr int kThreads = L::kThreads, kVKeys = L::kVKeys, kSteps = L::kSteps, kNS = L::kNS, kR = L::kRows,
+                  kKB = L::kKB;
     constexpr int kEl16 = 16 / (int)sizeof(Tin);
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    float *pt = reinterpret_cast<float *>(smem_raw + L::kOffPt);       // P^T [64 keys][68]
+    float *pt = reinterpret_cast<float *>(smem_raw + L::kOffPt);       // P^T [128 keys][68]
     float *red = reinterpret_cast<float *>(smem_raw + L::kOffRed);     // [2][64]
     float *alpha_s = reinterpret_cast<float *>(smem_raw + L::kOffAlpha);
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + L::kOffTmem);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // score tile: rows sr0 + {0, 1}, keys sk0 + 8 j
-    const int kh = warp & 1;
-    const int sr0 = 8 * (warp >> 1) + 2 * (lane >> 3);
-    const int sk0 = 32 * kh + (lane & 7);
-    // output tile: rows or0 + {0..3}, columns oc0 + 32 q + {0..3}
-    const int or0 = 16 * (warp >> 2) + 4 * (lane >> 3);
-    const int oc0 = 128 * (warp & 3) + 4 * (lane & 7);
+    // score tile
+    const int kh = warp & 1, dg = lane >> 3, kt = lane & 7;
+    const int srow = 8 * (warp >> 1);                 // first of the warp's 8 rows
+    const int skey = 64 * kh + kt;                    // keys skey + 8 j of the block
+    const int mrow = srow + 2 * dg;                   // rows mrow, mrow + 1 after the reduction
+    // output tile
+    const int orow = 32 * (warp >> 3) + 8 * (lane >> 3);
+    const int ocol = 64 * (warp & 7) + 4 * (lane & 7);
 
     const int b = blockIdx.z;
     const int split = blockIdx.y;
@@ -365,28 +382,42 @@ __global__ void __launch_bounds__(512, 1) verify_simt64_kernel(const VerifyParam
 
     const int P = p.prefix_len[b];
     const int kv_len = P + p.T;
-    const int nblk = (kv_len + kKeys - 1) / kKeys;
+    const int nblk = (kv_len + kKB - 1) / kKB;
     const int kb0 = split * p.blocks_per_split;
     const int kb1 = min(nblk, kb0 + p.blocks_per_split);
-    const int key_end = min(kv_len, kb1 * kKeys);
+    const int key_end = min(kv_len, kb1 * kKB);
     const int64_t q_row0 = (int64_t)b * rows_seq + r0;
     const int64_t kv_row0 = (int64_t)b * p.L;
-    const int total = kb1 > kb0 ? (kb1 - kb0) * kSteps : 0;
+    const int nb = kb1 > kb0 ? kb1 - kb0 : 0;
+    const int total = nb * kSteps;
 
+    // tensor memory for the output tile between blocks: warp w uses lanes 32 (w % 4) ..
+    // and columns 64 (w / 4) .. + 64
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_base_s, L::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem_o = *tmem_base_s + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(64 * (warp >> 2));
+
+    // Queue load g (block kb0 + g / kSteps, step g % kSteps) into its ring slot: Q rows and
+    // the block's 128 key rows of one 64-dim chunk, or 16 value rows; one commit group a
+    // load, empty past the end, so that the wait counts stay uniform.
     constexpr int kQKPieces = kDChunk / kEl16;
-    constexpr int kQPieces = kR * kQKPieces;
     constexpr int kVPieces = kDc / kEl16;
     auto issue = [&](int g) {
         if (g < total) {
             const int kb = kb0 + g / kSteps, step = g % kSteps;
             Tin *slot = reinterpret_cast<Tin *>(smem_raw + (g % kNS) * L::kSlot);
-            if (step < kQKChunks) {
+            if (step < L::kQK) {
                 const int d0 = step * kDChunk;
                 const bool nope = d0 < kDc;
                 const Tin *qbase = nope ? q_nope + d0 : q_pe + (d0 - kDc);
                 const int64_t qstride = nope ? p.q_nope_stride : p.q_pe_stride;
 #pragma unroll
-                for (int i = tid; i < kQPieces; i += kThreads) {
+                for (int i = tid; i < kR * kQKPieces; i += kThreads) {
                     const int rr = i / kQKPieces, pc = i % kQKPieces;
                     const bool ok = r0 + rr < rows_seq;
                     cp_async16(slot + rr * L::kQKRow + pc * kEl16, qbase + (q_row0 + (ok ? rr : 0)) * qstride + pc * kEl16,
@@ -395,15 +426,15 @@ __global__ void __launch_bounds__(512, 1) verify_simt64_kernel(const VerifyParam
                 const Tin *kbase = nope ? c_kv + d0 : k_pe + (d0 - kDc);
                 const int kstride = nope ? kDc : kDr;
 #pragma unroll
-                for (int i = tid; i < kKeys * kQKPieces; i += kThreads) {
+                for (int i = tid; i < kKB * kQKPieces; i += kThreads) {
                     const int rr = i / kQKPieces, pc = i % kQKPieces;
-                    const int key = kb * kKeys + rr;
+                    const int key = kb * kKB + rr;
                     const bool ok = key < key_end;
                     cp_async16(slot + (kR + rr) * L::kQKRow + pc * kEl16,
                                kbase + (kv_row0 + (ok ? key : 0)) * kstride + pc * kEl16, ok ? 16u : 0u);
                 }
             } else {
-                const int k0 = kb * kKeys + (step - kQKChunks) * kVKeys;
+                const int k0 = kb * kKB + (step - L::kQK) * kVKeys;
 #pragma unroll
                 for (int i = tid; i < kVKeys * kVPieces; i += kThreads) {
                     const int kk = i / kVPieces, pc = i % kVPieces;
@@ -419,173 +450,230 @@ __global__ void __launch_bounds__(512, 1) verify_simt64_kernel(const VerifyParam
 
     int qidx[2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) qidx[i] = min(r0 + sr0 + i, rows_seq - 1) / p.H;
-    float o[4][16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) o[i][c] = 0.f;
+    for (int i = 0; i < 2; ++i) qidx[i] = min(r0 + mrow + i, rows_seq - 1) / p.H;
     float m2[2] = {-INFINITY, -INFINITY}, lpart[2] = {0.f, 0.f};
-    float acc[2][4];
+    float o[8][8];
     bool vis_ready = false;
+    int g = 0;                                        // loads consumed so far
 
 #pragma unroll
-    for (int g = 0; g < kNS - 1; ++g) issue(g);
-    for (int g = 0; g < total; ++g) {
+    for (int k = 0; k < kNS - 1; ++k) issue(k);
+    // wait for load g, then refill the slot load g - 1 used
+    auto next_load = [&]() -> const Tin * {
         cp_async_wait<kNS - 2>();
         __syncthreads();
         issue(g + kNS - 1);
-        const int step = g % kSteps;
-        const int k0 = (kb0 + g / kSteps) * kKeys;
-        const Tin *slot = reinterpret_cast<const Tin *>(smem_raw + (g % kNS) * L::kSlot);
-        if (step < kQKChunks) {
-            // ---------------- S += Q K^T over 64 dims -------------------------------------
-            if (step == 0) {
+        return reinterpret_cast<const Tin *>(smem_raw + (g % kNS) * L::kSlot);
+    };
+
+    for (int blk = 0; blk < nb; ++blk) {
+        const int k0 = (kb0 + blk) * kKB;
+        // ---------------- S partial = Q K^T over this lane's 16 dims of each chunk -------------
+        float acc[8][8];
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-            }
-            const Tin *qs = slot + sr0 * L::kQKRow;
-            const Tin *ks = slot + (kR + sk0) * L::kQKRow;
+            for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int c = 0; c < L::kQK; ++c, ++g) {
+            const Tin *slot = next_load();
+            // lane group dg takes the dim pairs 2 dg + 8 u: the two groups of a half-warp
+            // then read disjoint banks of the 8 consecutive key rows
+            const Tin *qs = slot + srow * L::kQKRow + 2 * dg;
+            const Tin *ks = slot + (kR + skey) * L::kQKRow + 2 * dg;
+#pragma unroll 1
+            for (int d = 0; d < kDChunk; d += 8) {
+                float2 a[8];
 #pragma unroll
-            for (int d = 0; d < kDChunk; d += 4) {
-                const float4 a0 = Elt<Tin>::get4(qs + d), a1 = Elt<Tin>::get4(qs + L::kQKRow + d);
+                for (int i = 0; i < 8; ++i) a[i] = get2(qs + i * L::kQKRow + d);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 k = Elt<Tin>::get4(ks + 8 * j * L::kQKRow + d);
-                    acc[0][j] = fmaf(a0.x, k.x, fmaf(a0.y, k.y, fmaf(a0.z, k.z, fmaf(a0.w, k.w, acc[0][j]))));
-                    acc[1][j] = fmaf(a1.x, k.x, fmaf(a1.y, k.y, fmaf(a1.z, k.z, fmaf(a1.w, k.w, acc[1][j]))));
-                }
-            }
-            if (step == kQKChunks - 1) {
-                // ---------------- mask, scale; this warp's row maxima ---------------------------
-                if (!vis_ready && k0 + kKeys > P) {
-                    tc::griddep_wait();
-                    vis_ready = true;
-                }
+                for (int j = 0; j < 8; ++j) {
+                    const float2 k = get2(ks + 8 * j * L::kQKRow + d);
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int key = k0 + sk0 + 8 * j;
-                        bool visible = key < key_end;
-                        if (visible && key >= P) {
-                            const int t = key - P;
-                            const uint32_t w = p.vis[((int64_t)b * p.T + qidx[i]) * p.W + (t >> 5)];
-                            visible = (w >> (t & 31)) & 1u;
-                        }
-                        acc[i][j] = visible ? acc[i][j] * p.scale_log2 : -INFINITY;
-                        mx = fmaxf(mx, acc[i][j]);
-                    }
-#pragma unroll
-                    for (int off = 4; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    if ((lane & 7) == 0) red[kh * kR + sr0 + i] = mx;
-                }
-                // the other half's maxima are read after the next load's barrier
-            }
-        } else {
-            if (step == kQKChunks) {
-                // ---------------- online softmax: P^T to shared memory, rescale factors -------------
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float mx = fmaxf(red[sr0 + i], red[kR + sr0 + i]);
-                    const float mnew = fmaxf(m2[i], mx);
-                    const float al = (mnew == -INFINITY) ? 1.f : exp2f(m2[i] - mnew);
-                    float rs = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float pj = (mnew == -INFINITY) ? 0.f : exp2f(acc[i][j] - mnew);
-                        pt[(sk0 + 8 * j) * L::kPtRow + sr0 + i] = pj;
-                        rs += pj;
-                    }
-                    lpart[i] = lpart[i] * al + rs;
-                    m2[i] = mnew;
-                    if (kh == 0 && (lane & 7) == 0) alpha_s[sr0 + i] = al;
-                }
-                __syncthreads();       // P^T and the factors of every row are written
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float al = alpha_s[or0 + i];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) o[i][c] *= al;
-                }
-            }
-            // ---------------- O += P V for 32 keys -------------------------------------------
-            const int kk0 = (step - kQKChunks) * kVKeys;
-#pragma unroll 4
-            for (int kk = 0; kk < kVKeys; ++kk) {
-                const float4 pr = *reinterpret_cast<const float4 *>(pt + (kk0 + kk) * L::kPtRow + or0);
-                const Tin *vrow = slot + kk * L::kVRow + oc0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 v = Elt<Tin>::get4(vrow + 32 * q);
-                    o[0][4 * q + 0] = fmaf(pr.x, v.x, o[0][4 * q + 0]);
-                    o[0][4 * q + 1] = fmaf(pr.x, v.y, o[0][4 * q + 1]);
-                    o[0][4 * q + 2] = fmaf(pr.x, v.z, o[0][4 * q + 2]);
-                    o[0][4 * q + 3] = fmaf(pr.x, v.w, o[0][4 * q + 3]);
-                    o[1][4 * q + 0] = fmaf(pr.y, v.x, o[1][4 * q + 0]);
-                    o[1][4 * q + 1] = fmaf(pr.y, v.y, o[1][4 * q + 1]);
-                    o[1][4 * q + 2] = fmaf(pr.y, v.z, o[1][4 * q + 2]);
-                    o[1][4 * q + 3] = fmaf(pr.y, v.w, o[1][4 * q + 3]);
-                    o[2][4 * q + 0] = fmaf(pr.z, v.x, o[2][4 * q + 0]);
-                    o[2][4 * q + 1] = fmaf(pr.z, v.y, o[2][4 * q + 1]);
-                    o[2][4 * q + 2] = fmaf(pr.z, v.z, o[2][4 * q + 2]);
-                    o[2][4 * q + 3] = fmaf(pr.z, v.w, o[2][4 * q + 3]);
-                    o[3][4 * q + 0] = fmaf(pr.w, v.x, o[3][4 * q + 0]);
-                    o[3][4 * q + 1] = fmaf(pr.w, v.y, o[3][4 * q + 1]);
-                    o[3][4 * q + 2] = fmaf(pr.w, v.z, o[3][4 * q + 2]);
-                    o[3][4 * q + 3] = fmaf(pr.w, v.w, o[3][4 * q + 3]);
+                    for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(a[i].x, k.x, fmaf(a[i].y, k.y, acc[i][j]));
                 }
             }
         }
+        // ---------------- the four dim groups' sums: two transposing shuffle rounds ----------
+        // round 1 (partner dg ^ 2): keep rows 4 (dg >> 1) .. + 4; round 2 (dg ^ 1): keep 2.
+        float s4[4][8];
+        const bool up2 = (dg & 2) != 0, up1 = (dg & 1) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float send = up2 ? acc[i][j] : acc[4 + i][j];
+                const float keep = up2 ? acc[4 + i][j] : acc[i][j];
+                s4[i][j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+            }
+        float s[2][8];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float send = up1 ? s4[i][j] : s4[2 + i][j];
+                const float keep = up1 ? s4[2 + i][j] : s4[i][j];
+                s[i][j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+        // ---------------- mask, scale, row maxima of this warp's 64 keys ------------------------
+        if (!vis_ready && k0 + kKB > P) {            // the bits may come from the kernel just before
+            tc::griddep_wait();
+            vis_ready = true;
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int key = k0 + skey + 8 * j;
+                bool visible = key < key_end;
+                if (visible && key >= P) {
+                    const int t = key - P;
+                    const uint32_t w = p.vis[((int64_t)b * p.T + qidx[i]) * p.W + (t >> 5)];
+                    visible = (w >> (t & 31)) & 1u;
+                }
+                s[i][j] = visible ? s[i][j] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[i][j]);
+            }
+#pragma unroll
+            for (int off = 4; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (kt == 0) red[kh * kR + mrow + i] = mx;
+        }
+        // ---------------- first value slice: online softmax, P^T, rescale factors --------------
+        const Tin *vslot = next_load();              // its barrier also publishes the maxima
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float mx = fmaxf(red[mrow + i], red[kR + mrow + i]);
+            const float mnew = fmaxf(m2[i], mx);
+            const float al = (mnew == -INFINITY) ? 1.f : exp2f(m2[i] - mnew);
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float pj = (mnew == -INFINITY) ? 0.f : exp2f(s[i][j] - mnew);
+                pt[(skey + 8 * j) * L::kPtRow + mrow + i] = pj;
+                rs += pj;
+            }
+            lpart[i] = lpart[i] * al + rs;
+            m2[i] = mnew;
+            if (kh == 0 && kt == 0) alpha_s[mrow + i] = al;
+        }
+        __syncthreads();                             // P^T and every row's factor are written
+        // the output tile back from tensor memory (zero before the first block), rescaled
+        if (blk == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) o[i][c] = 0.f;
+        } else {
+            uint32_t t0[32], t1[32];
+            tc::tmem_ld32(tmem_o, t0);
+            tc::tmem_ld32(tmem_o + 32, t1);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    o[i][c] = __uint_as_float(t0[8 * i + c]);
+                    o[4 + i][c] = __uint_as_float(t1[8 * i + c]);
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float al = alpha_s[orow + i];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) o[i][c] *= al;
+        }
+        // ---------------- O += P V, 16 keys a slice ---------------------------------------------
+        for (int v = 0; v < kKB / kVKeys; ++v) {
+            if (v > 0) vslot = next_load();
+            const int kk0 = v * kVKeys;
+#pragma unroll 4
+            for (int kk = 0; kk < kVKeys; ++kk) {
+                const float4 pa = *reinterpret_cast<const float4 *>(pt + (kk0 + kk) * L::kPtRow + orow);
+                const float4 pb = *reinterpret_cast<const float4 *>(pt + (kk0 + kk) * L::kPtRow + orow + 4);
+                const float pr[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+                const Tin *vrow = vslot + kk * L::kVRow + ocol;
+                const float4 va = Elt<Tin>::get4(vrow), vb = Elt<Tin>::get4(vrow + 32);
+                const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) o[i][c] = fmaf(pr[i], vv[c], o[i][c]);
+            }
+            ++g;
+        }
+        // the tile waits in tensor memory while the next block's scores use the registers
+        if (blk + 1 < nb) {
+            uint32_t t0[32], t1[32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    t0[8 * i + c] = __float_as_uint(o[i][c]);
+                    t1[8 * i + c] = __float_as_uint(o[4 + i][c]);
+                }
+            tc::tmem_st32(tmem_o, t0);
+            tc::tmem_st32(tmem_o + 32, t1);
+            tc::tmem_wait_st();
+        }
     }
     cp_async_wait<0>();
-    tc::griddep_launch_dependents();
+    tc::griddep_launch_dependents();   // the split merge may launch; it waits for this kernel's end
 
     // ---------------- epilogue: o = O / l, lse = ln2 * (m2 + log2 l) -------------------------
-    // row sums: over the 8 key lanes, then the two key halves through shared memory
-    __syncthreads();           // every read of the reduction buffer above is done
+    __syncthreads();           // every read of the maxima buffer is done
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         float l = lpart[i];
 #pragma unroll
         for (int off = 4; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        if ((lane & 7) == 0) red[kh * kR + sr0 + i] = l;
+        if (kt == 0) red[kh * kR + mrow + i] = l;
     }
     __syncthreads();
     const bool partial = p.num_splits > 1;
     float *obase = partial ? p.part_o + (int64_t)split * p.rows_total * kDc : p.out;
     float *lbase = partial ? p.part_lse + (int64_t)split * p.rows_total : p.lse;
-    if (kh == 0 && (lane & 7) == 0 && lbase) {
+    if (kh == 0 && kt == 0 && lbase) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const int r = r0 + sr0 + i;
-            const float l = red[sr0 + i] + red[kR + sr0 + i];
+            const int r = r0 + mrow + i;
+            const float l = red[mrow + i] + red[kR + mrow + i];
             if (r < rows_seq) lbase[(int64_t)b * rows_seq + r] = (l > 0.f) ? 0.6931471805599453f * (m2[i] + log2f(l)) : -INFINITY;
         }
     }
+    if (nb > 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = r0 + or0 + i;
-        if (r >= rows_seq) continue;
-        const float l = red[or0 + i] + red[kR + or0 + i];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        float *orow = obase + ((int64_t)b * rows_seq + r) * kDc + oc0;
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + orow + i;
+            if (r >= rows_seq) continue;
+            const float l = red[orow + i] + red[kR + orow + i];
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float *orow_p = obase + ((int64_t)b * rows_seq + r) * kDc + ocol;
+            *reinterpret_cast<float4 *>(orow_p) = make_float4(o[i][0] * inv, o[i][1] * inv, o[i][2] * inv, o[i][3] * inv);
+            *reinterpret_cast<float4 *>(orow_p + 32) = make_float4(o[i][4] * inv, o[i][5] * inv, o[i][6] * inv, o[i][7] * inv);
+        }
+    } else {
+        // no key block in this split (can only happen with caller-chosen splits): zero state
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4 *>(orow + 32 * q) =
-                make_float4(o[i][4 * q] * inv, o[i][4 * q + 1] * inv, o[i][4 * q + 2] * inv, o[i][4 * q + 3] * inv);
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + orow + i;
+            if (r >= rows_seq) continue;
+            float *orow_p = obase + ((int64_t)b * rows_seq + r) * kDc + ocol;
+            *reinterpret_cast<float4 *>(orow_p) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4 *>(orow_p + 32) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(*tmem_base_s, L::kTmemCols);
 }
 
 template <typename Tin>
-cudaError_t launch_typed64(const VerifyParams &p, cudaStream_t s) {
-    using L = Layout64<Tin>;
+cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
+    using L = LayoutTm<Tin>;
     const int rows_seq = p.T * p.H;
-    cudaError_t e = cudaFuncSetAttribute(verify_simt64_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(verify_simt_tm_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
+    // programmatic dependent launch after the visibility kernel of the same call
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -596,7 +684,7 @@ cudaError_t launch_typed64(const VerifyParams &p, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = pdl;
     cfg.numAttrs = p.overlap_vis ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, verify_simt64_kernel<Tin>, p);
+    return cudaLaunchKernelEx(&cfg, verify_simt_tm_kernel<Tin>, p);
 }
 
 template <typename Tin, int kRows>
@@ -626,7 +714,7 @@ cudaError_t launch_typed(const VerifyParams &p, cudaStream_t s) {
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s) {
     if (rows_per_cta == kSimtSmallRows)
         return dt == KDT_F32 ? launch_typed<float, kSimtSmallRows>(p, s) : launch_typed<__nv_bfloat16, kSimtSmallRows>(p, s);
-    return dt == KDT_F32 ? launch_typed64<float>(p, s) : launch_typed64<__nv_bfloat16>(p, s);
+    return dt == KDT_F32 ? launch_typed_tm<float>(p, s) : launch_typed_tm<__nv_bfloat16>(p, s);
 }
 
 }  // namespace kdt
