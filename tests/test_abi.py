@@ -167,9 +167,10 @@ def test_plan_and_workspace_are_host_only(kdt):
     b = _args(kdt, kv_row_stride=4096 + 32, max_kv_len=4096 + 32, T=32, H=64, B=1, num_splits=8, vis=0x90000,
               parent=None)
     p = kdt.plan(b)
-    assert p["num_splits"] == 8 and p["num_launches"] == 2        # attention + merge
+    # 33 blocks of 128 keys asked in 8 splits: 5 blocks a split, so 7 splits
+    assert p["num_splits"] == 7 and p["num_launches"] == 2        # attention + merge
     rows = 1 * 32 * 64
-    assert p["workspace_bytes"] >= 8 * rows * 512 * 4 + 8 * rows * 4
+    assert p["workspace_bytes"] >= 7 * rows * 512 * 4 + 7 * rows * 4
     assert kdt.workspace_size(_args(kdt, D_c=3)) == 0
     # bf16 inputs plan onto the tensor-core kernel: one 4-CTA cluster per resident slot (at
     # most 48), sharing all units' key blocks; units cut by the split leave piece states in
