@@ -126,11 +126,15 @@ typedef struct {
     float *lse;             /* device fp32 [B,T,H], or NULL */
     int32_t *err;           /* device int32 error word for the parent path, or NULL */
     int impl;               /* kdt_impl */
-    int num_splits;         /* 0 = choose automatically. SIMT kernel: KV splits per 64-row tile
-                               (at most 32). Tensor-core kernel: the number of persistent
-                               4-CTA clusters its (256-row unit, 128-key block) work is cut
-                               into equal shares for (at most those resident at once); the
-                               units a share boundary cuts are merged by log-sum-exp. */
+    int num_splits;         /* 0 = choose automatically. SIMT_SMALL: KV splits per 16-row
+                               tile (at most 32), merged by log-sum-exp. SIMT (64-row tiles):
+                               the number of CTAs its (64-row tile, 128-key block) pairs are
+                               cut into equal contiguous shares for (at most one per pair;
+                               automatic: one per SM). Tensor-core kernel: the number of
+                               persistent 4-CTA clusters its (256-row unit, 128-key block)
+                               work is cut into equal shares for (at most those resident at
+                               once). With either share split, the tiles or units a share
+                               boundary cuts are merged by log-sum-exp. */
     int64_t q_nope_row_stride; /* elements between consecutive (b,i,h) rows of q_nope; 0 = 512
                                   (contiguous). Lets the kernels read a combined [.., 512 + 64]
                                   query buffer where it lies (stride 576, q_pe = q_nope + 512)
@@ -167,8 +171,8 @@ size_t kdt_verify_attn_workspace_size(const kdt_verify_args *a);
 
 /* What kdt_verify_attn will launch for these arguments. */
 typedef struct {
-    int impl;               /* KDT_IMPL_SIMT or KDT_IMPL_TCGEN05 */
-    int num_splits;         /* KV splits actually used */
+    int impl;               /* the kdt_impl chosen (never KDT_IMPL_AUTO) */
+    int num_splits;         /* splits, CTAs or clusters actually used (see kdt_verify_args) */
     int num_launches;       /* kernels launched per call */
     int ctas;               /* CTAs of the main attention kernel */
     size_t workspace_bytes;
@@ -280,9 +284,10 @@ kdt_status kdt_vc_up_proj(const float *o, const void *w_vc, kdt_dtype w_dtype, i
  * device array of KDT_NOALLOC_SCRATCH_BYTES inside libkdt.so, present on every GPU
  * that loads the library until the process exits. Nothing is allocated: no
  * cudaMalloc, no cudaFree, no allocating library routine.
- *  - Size limit: 64 MiB, enough for the bf16 tensor-core path's partial states on
- *    any GPU it supports. If the call needs more scratch, an SIMT call's automatic
- *    split count (num_splits == 0) is lowered until the partials fit;
+ *  - Size limit: 64 MiB, enough for the partial states of the tensor-core path and of
+ *    the 64-row SIMT path on any GPU they support. If the call needs more scratch, a
+ *    SIMT_SMALL call's automatic split count (num_splits == 0) is lowered until the
+ *    partials fit;
  *    if the call still does not fit, or an explicit num_splits does not fit, it
  *    returns KDT_ERR_WORKSPACE and launches nothing.
  *  - Set-up: the first call made on a device (with that device current) looks up

@@ -67,6 +67,7 @@ struct Plan {
     int impl = KDT_IMPL_SIMT;
     int splits = 1;
     int tc_clusters = 1;                   // tensor path: resident clusters the work is split across
+    int simt_ctas = 0;                     // SIMT 64-row tile: CTAs the work is split across
     int blocks_per_split = 1;
     int ctas = 0;
     int launches = 0;
@@ -143,22 +144,25 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         p.splits = p.tc_clusters;
         p.blocks_per_split = nblk;
         p.ctas = 4 * p.tc_clusters;
+    } else if (!simt_small) {
+        // SIMT 64-row tile: one CTA per SM, each taking an equal contiguous share of all
+        // (row tile, key block) pairs (the split adapts on the device to the actual prefix
+        // lengths), or the caller's num_splits CTAs; never more CTAs than pairs
+        const int64_t pairs = base * nblk;
+        int64_t C = a->num_splits > 0 ? a->num_splits : sm_count();
+        if (C > pairs) C = pairs;
+        if (C < 1) C = 1;
+        p.simt_ctas = (int)C;
+        p.splits = p.simt_ctas;
+        p.blocks_per_split = nblk;
+        p.ctas = p.simt_ctas;
     } else {
-        // SIMT: one CTA per SM at a time; fill about two waves, with at least 256 keys per
-        // split (4 blocks of the 16-row tile, 2 of the 64-row tile), unless the caller fixed
-        // the splits
-        const int64_t slots = sm_count();
+        // SIMT 16-row tile: one 64-key block per split unless the caller fixed the splits
         int splits;
         if (a->num_splits > 0) {
             splits = a->num_splits;
-        } else if (simt_small) {
-            splits = nblk;                  // one 64-key block per split: short chains, many CTAs
         } else {
-            const int64_t want = (2LL * slots + base - 1) / base;
-            splits = (int)(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
-            const int min_blocks = 256 / unit_keys;
-            const int cap = nblk / min_blocks > 1 ? nblk / min_blocks : 1;
-            if (splits > cap) splits = cap;
+            splits = nblk;                  // one 64-key block per split: short chains, many CTAs
         }
         if (splits > kMaxSplits) splits = kMaxSplits;
         if (splits > nblk) splits = nblk;
@@ -174,7 +178,17 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         off = align_up(off + p.vis_bytes);
     }
     const bool tc_pieces = tc && p.tc_clusters > 1;
-    if (p.splits > 1 || tc_pieces) {
+    const bool simt_pieces = impl == KDT_IMPL_SIMT && p.simt_ctas > 1;
+    if (simt_pieces) {
+        // [2 * CTAs][64] piece states
+        const int64_t prow = (int64_t)2 * p.simt_ctas * unit_rows;
+        p.po_off = off;
+        p.po_bytes = (size_t)prow * kDc * sizeof(float);
+        off = align_up(off + p.po_bytes);
+        p.pl_off = off;
+        p.pl_bytes = (size_t)prow * sizeof(float);
+        off = align_up(off + p.pl_bytes);
+    } else if (p.splits > 1 || tc_pieces) {
         // SIMT: [splits][rows_total]; tensor path: [2 * clusters][256] piece states
         const int64_t prow = tc_pieces ? (int64_t)2 * p.tc_clusters * unit_rows : rows_total;
         const int ns = tc_pieces ? 1 : p.splits;
@@ -190,7 +204,7 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         }
     }
     p.ws_bytes = off;
-    p.launches = (a->parent ? 1 : 0) + 1 + ((p.splits > 1 || tc_pieces) ? 1 : 0);
+    p.launches = (a->parent ? 1 : 0) + 1 + ((p.splits > 1 || tc_pieces) ? 1 : 0);   // SIMT pieces: splits > 1 too
     *pl = p;
     return KDT_OK;
 }
@@ -364,11 +378,13 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
     vp.num_splits = p.splits;
     vp.blocks_per_split = p.blocks_per_split;
     vp.rows_total = (int64_t)a->B * a->T * a->H;
-    const bool partials = p.splits > 1 || (p.impl == KDT_IMPL_TCGEN05 && p.tc_clusters > 1);
+    const bool partials = p.splits > 1 || (p.impl == KDT_IMPL_TCGEN05 && p.tc_clusters > 1);   // SIMT: splits = CTAs
     vp.part_o = partials ? reinterpret_cast<float *>(ws + p.po_off) : nullptr;
     vp.part_lse = partials ? reinterpret_cast<float *>(ws + p.pl_off) : nullptr;
     vp.err = a->err;
     vp.tc_clusters = p.tc_clusters;
+    vp.simt_ctas = p.simt_ctas;
+    if (p.impl == KDT_IMPL_SIMT) vp.num_splits = 1;   // pieces, not uniform splits
     vp.tc_sched = (p.impl == KDT_IMPL_TCGEN05 && p.tc_clusters > 1) ? reinterpret_cast<int64_t *>(ws + p.sched_off)
                                                                     : nullptr;
     if (hooks) {
@@ -388,10 +404,13 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
     const cudaError_t e = p.impl == KDT_IMPL_TCGEN05 ? launch_verify_tc(vp, stream)
                                                      : launch_verify_simt(vp, a->dtype, unit_rows_of(p), stream);
     if (e != cudaSuccess) return KDT_ERR_CUDA;
-    if (p.impl != KDT_IMPL_TCGEN05 && p.splits > 1) {
+    if (p.impl == KDT_IMPL_SIMT_SMALL && p.splits > 1) {
         if (launch_merge_splits(vp.part_o, vp.part_lse, p.splits, vp.rows_total, a->out, a->lse, stream) !=
             cudaSuccess)
             return KDT_ERR_CUDA;
+    }
+    if (p.impl == KDT_IMPL_SIMT && p.simt_ctas > 1) {
+        if (launch_merge_simt_pieces(vp, stream) != cudaSuccess) return KDT_ERR_CUDA;
     }
     return KDT_OK;
 }

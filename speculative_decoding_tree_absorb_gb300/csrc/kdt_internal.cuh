@@ -46,6 +46,9 @@ struct VerifyParams {
     // Tensor-core path: the resident clusters the work is split across; part_o/part_lse
     // then hold [2 * tc_clusters][256] partial states (unused when tc_clusters == 1).
     int tc_clusters;
+    // SIMT 64-row tile: the CTAs the (row tile, key block) work is split across; with more
+    // than one, part_o/part_lse hold [2 * simt_ctas][64] piece states.
+    int simt_ctas = 0;
     // Tensor path: the kernel may start while the visibility kernel this call launched just
     // before it still runs (programmatic dependent launch); it waits for that kernel only
     // before its first read of the bits. Set only when the previous kernel of the stream is
@@ -70,6 +73,8 @@ constexpr int kSimtSmallRows = 16;
 constexpr int kSimtKeys = 64;          // keys per block of the 16-row tile
 constexpr int kSimtKeysTm = 128;       // keys per block of the 64-row tile
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s);
+// Merges the piece states the 64-row SIMT tile left (when simt_ctas > 1).
+cudaError_t launch_merge_simt_pieces(const VerifyParams &p, cudaStream_t s);
 
 // K1: tcgen05 verify (bf16 inputs): one 4-CTA cluster (two CTA pairs) per resident slot,
 // each taking an equal share of the (256-row unit, 128-key block) work; launch_verify_tc

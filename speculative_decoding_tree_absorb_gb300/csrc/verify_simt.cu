@@ -337,7 +337,8 @@ template <typename T> struct LayoutTm {
     static constexpr int kOffRed = kOffPt + kKB * kPtRow * 4;     // [2 key halves][64 rows]
     static constexpr int kOffAlpha = kOffRed + 2 * kRows * 4;     // [64]
     static constexpr int kOffTmem = kOffAlpha + kRows * 4;        // tensor-memory base address
-    static constexpr int kSmem = kOffTmem + 16;
+    static constexpr int kOffWork = kOffTmem + 16;                // this CTA's work range (5 x int64)
+    static constexpr int kSmem = kOffWork + 5 * 8;
     static constexpr uint32_t kTmemCols = 256;
 };
 
@@ -347,6 +348,54 @@ template <> __device__ __forceinline__ float2 get2<float>(const float *p) { retu
 template <> __device__ __forceinline__ float2 get2<__nv_bfloat16>(const __nv_bfloat16 *p) {
     const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
+// Key blocks of sequence b for blocks of kb keys.
+__device__ __forceinline__ int seq_blocks_of(const VerifyParams &p, int b, int kb) {
+    return (p.prefix_len[b] + p.T + kb - 1) / kb;
+}
+
+// The work of the 64-row tile is the list of (row tile, key block) pairs, sequence-major,
+// then tile-major, then in key order: W = tiles_seq * sum_b blocks(b) of them. CTA c of C
+// takes positions [W c / C, W (c + 1) / C). One warp computes W, the range and the
+// (sequence, tile, block) of its first position; lane 0 writes {s0, s1, b, tile, block}.
+__device__ __forceinline__ void locate_work(const VerifyParams &p, int tiles_seq, int kb, int64_t C, int64_t c,
+                                            int lane, int64_t *out) {
+    int64_t W = 0;
+    for (int b = lane; b < p.B; b += 32) W += (int64_t)tiles_seq * seq_blocks_of(p, b, kb);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    const int64_t s0 = W * c / C, s1 = W * (c + 1) / C;
+    int fb = -1, fnb = 1;
+    int64_t fbefore = 0, acc = 0;
+    for (int base = 0; base < p.B && fb < 0; base += 32) {
+        const int b = base + lane;
+        const int nbk = b < p.B ? seq_blocks_of(p, b, kb) : 1;
+        const int64_t w = b < p.B ? (int64_t)tiles_seq * nbk : 0;
+        int64_t incl = w;                            // inclusive scan over the lanes
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const int64_t before = acc + incl - w;
+        const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && s0 >= before && s0 < before + w);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            fb = base + src;
+            fbefore = __shfl_sync(0xffffffffu, before, src);
+            fnb = __shfl_sync(0xffffffffu, nbk, src);
+        }
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+        const int64_t off = fb >= 0 ? s0 - fbefore : 0;
+        out[0] = s0;
+        out[1] = s1;
+        out[2] = fb >= 0 ? fb : 0;
+        out[3] = off / fnb;
+        out[4] = off % fnb;
+    }
 }
 
 template <typename Tin>
@@ -360,6 +409,7 @@ __global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyPara
     float *red = reinterpret_cast<float *>(smem_raw + L::kOffRed);     // [2][64]
     float *alpha_s = reinterpret_cast<float *>(smem_raw + L::kOffAlpha);
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + L::kOffTmem);
+    int64_t *work_s = reinterpret_cast<int64_t *>(smem_raw + L::kOffWork);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // score tile
@@ -371,25 +421,12 @@ __global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyPara
     const int orow = 32 * (warp >> 3) + 8 * (lane >> 3);
     const int ocol = 64 * (warp & 7) + 4 * (lane & 7);
 
-    const int b = blockIdx.z;
-    const int split = blockIdx.y;
     const int rows_seq = p.T * p.H;
-    const int r0 = blockIdx.x * kR;
+    const int tiles_seq = (rows_seq + kR - 1) / kR;      // row tiles of a sequence
     const Tin *q_nope = static_cast<const Tin *>(p.q_nope);
     const Tin *q_pe = static_cast<const Tin *>(p.q_pe);
     const Tin *c_kv = static_cast<const Tin *>(p.c_kv);
     const Tin *k_pe = static_cast<const Tin *>(p.k_pe);
-
-    const int P = p.prefix_len[b];
-    const int kv_len = P + p.T;
-    const int nblk = (kv_len + kKB - 1) / kKB;
-    const int kb0 = split * p.blocks_per_split;
-    const int kb1 = min(nblk, kb0 + p.blocks_per_split);
-    const int key_end = min(kv_len, kb1 * kKB);
-    const int64_t q_row0 = (int64_t)b * rows_seq + r0;
-    const int64_t kv_row0 = (int64_t)b * p.L;
-    const int nb = kb1 > kb0 ? kb1 - kb0 : 0;
-    const int total = nb * kSteps;
 
     // tensor memory for the output tile between blocks: warp w uses lanes 32 (w % 4) ..
     // and columns 64 (w / 4) .. + 64
@@ -401,6 +438,30 @@ __global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyPara
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem_o = *tmem_base_s + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(64 * (warp >> 2));
+
+    // ---- this CTA's share of the work: (row tile, key block) pairs in sequence-major,
+    // tile-major, key-block order, W of them, cut into gridDim.x equal contiguous ranges;
+    // a range is processed as segments of one tile each
+    const int C = gridDim.x, c = blockIdx.x;
+    if (warp == 0) locate_work(p, tiles_seq, kKB, (int64_t)C, (int64_t)c, lane, work_s);
+    __syncthreads();
+    const int64_t s_begin = work_s[0], s_end = work_s[1];
+    int b = (int)work_s[2], rt = (int)work_s[3], kb_at = (int)work_s[4];
+    bool vis_ready = false;
+    bool first_seg = true;
+    for (int64_t pos = s_begin; pos < s_end;) {
+    const int r0 = rt * kR;
+    const int P = p.prefix_len[b];
+    const int kv_len = P + p.T;
+    const int nblk = (kv_len + kKB - 1) / kKB;
+    const int kb0 = kb_at;
+    const int kb1 = (int)min((int64_t)nblk, (int64_t)kb0 + (s_end - pos));
+    const int key_end = min(kv_len, kb1 * kKB);
+    const int64_t q_row0 = (int64_t)b * rows_seq + r0;
+    const int64_t kv_row0 = (int64_t)b * p.L;
+    const int nb = kb1 - kb0;
+    const int total = nb * kSteps;
+    const bool whole = kb0 == 0 && kb1 == nblk;
 
     // Queue load g (block kb0 + g / kSteps, step g % kSteps) into its ring slot: Q rows and
     // the block's 128 key rows of one 64-dim chunk, or 16 value rows; one commit group a
@@ -453,7 +514,6 @@ __global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyPara
     for (int i = 0; i < 2; ++i) qidx[i] = min(r0 + mrow + i, rows_seq - 1) / p.H;
     float m2[2] = {-INFINITY, -INFINITY}, lpart[2] = {0.f, 0.f};
     float o[8][8];
-    bool vis_ready = false;
     int g = 0;                                        // loads consumed so far
 
 #pragma unroll
@@ -617,10 +677,9 @@ __global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyPara
         }
     }
     cp_async_wait<0>();
-    tc::griddep_launch_dependents();   // the split merge may launch; it waits for this kernel's end
 
-    // ---------------- epilogue: o = O / l, lse = ln2 * (m2 + log2 l) -------------------------
-    __syncthreads();           // every read of the maxima buffer is done
+    // ---------------- segment epilogue: o = O / l, lse = ln2 * (m2 + log2 l) ---------------
+    __syncthreads();           // every read of the maxima buffer and of the ring is done
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         float l = lpart[i];
@@ -629,39 +688,46 @@ __global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyPara
         if (kt == 0) red[kh * kR + mrow + i] = l;
     }
     __syncthreads();
-    const bool partial = p.num_splits > 1;
-    float *obase = partial ? p.part_o + (int64_t)split * p.rows_total * kDc : p.out;
-    float *lbase = partial ? p.part_lse + (int64_t)split * p.rows_total : p.lse;
+    // a whole tile writes its final rows; a piece of one its normalised state, in slot 2c
+    // when it is the first segment of this CTA's range, else (its last) in slot 2c + 1
+    float *obase = p.out, *lbase = p.lse;
+    int64_t rowbase = (int64_t)b * rows_seq + r0;
+    if (!whole) {
+        obase = p.part_o;
+        lbase = p.part_lse;
+        rowbase = (int64_t)(first_seg ? 2 * c : 2 * c + 1) * kR;
+    }
     if (kh == 0 && kt == 0 && lbase) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const int r = r0 + mrow + i;
             const float l = red[mrow + i] + red[kR + mrow + i];
-            if (r < rows_seq) lbase[(int64_t)b * rows_seq + r] = (l > 0.f) ? 0.6931471805599453f * (m2[i] + log2f(l)) : -INFINITY;
+            if (r0 + mrow + i < rows_seq)
+                lbase[rowbase + mrow + i] = (l > 0.f) ? 0.6931471805599453f * (m2[i] + log2f(l)) : -INFINITY;
         }
     }
-    if (nb > 0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = r0 + orow + i;
-            if (r >= rows_seq) continue;
-            const float l = red[orow + i] + red[kR + orow + i];
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            float *orow_p = obase + ((int64_t)b * rows_seq + r) * kDc + ocol;
-            *reinterpret_cast<float4 *>(orow_p) = make_float4(o[i][0] * inv, o[i][1] * inv, o[i][2] * inv, o[i][3] * inv);
-            *reinterpret_cast<float4 *>(orow_p + 32) = make_float4(o[i][4] * inv, o[i][5] * inv, o[i][6] * inv, o[i][7] * inv);
-        }
-    } else {
-        // no key block in this split (can only happen with caller-chosen splits): zero state
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = r0 + orow + i;
-            if (r >= rows_seq) continue;
-            float *orow_p = obase + ((int64_t)b * rows_seq + r) * kDc + ocol;
-            *reinterpret_cast<float4 *>(orow_p) = make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4 *>(orow_p + 32) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 8; ++i) {
+        if (r0 + orow + i >= rows_seq) continue;
+        const float l = red[orow + i] + red[kR + orow + i];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float *orow_p = obase + (rowbase + orow + i) * kDc + ocol;
+        *reinterpret_cast<float4 *>(orow_p) = make_float4(o[i][0] * inv, o[i][1] * inv, o[i][2] * inv, o[i][3] * inv);
+        *reinterpret_cast<float4 *>(orow_p + 32) = make_float4(o[i][4] * inv, o[i][5] * inv, o[i][6] * inv, o[i][7] * inv);
+    }
+    // the next segment: the rest of this tile cannot follow (a segment ends at the tile's
+    // last block or at the end of the range), so the next tile
+    pos += nb;
+    first_seg = false;
+    kb_at = kb1;
+    if (kb_at == nblk) {
+        kb_at = 0;
+        if (++rt == tiles_seq) {
+            rt = 0;
+            ++b;
         }
     }
+    }   // segments
+    tc::griddep_launch_dependents();   // the piece merge may launch; it waits for this kernel's end
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(*tmem_base_s, L::kTmemCols);
@@ -678,7 +744,7 @@ cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((rows_seq + L::kRows - 1) / L::kRows, p.num_splits, p.B);
+    cfg.gridDim = dim3(p.simt_ctas > 0 ? p.simt_ctas : 1);
     cfg.blockDim = dim3(L::kThreads);
     cfg.dynamicSmemBytes = L::kSmem;
     cfg.stream = s;
@@ -709,12 +775,107 @@ cudaError_t launch_typed(const VerifyParams &p, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, verify_simt_kernel<Tin, kRows>, p);
 }
 
+// Combines the pieces of every row tile that the work split of the 64-row tile cut: CTA
+// (tile, y) merges rows 8 y .. 8 y + 7 of the tile, one warp a row. The tile spans work
+// positions [T0, T1); the CTAs whose ranges meet it are c_a = cta_of(T0) .. c_b =
+// cta_of(T1 - 1) (one CTA: the tile was written whole), each with a normalised state
+// (o, lse) in slot 2c (its range starts inside the tile) or 2c + 1 (its range starts
+// before). Merge by log-sum-exp: lse = log sum_k e^lse_k, o = sum_k e^(lse_k - lse) o_k.
+__global__ void __launch_bounds__(256) merge_simt_pieces_kernel(const VerifyParams p) {
+    tc::griddep_wait();                       // the pieces are written by the kernel before
+    constexpr int kR = kSimtRows, kKB = kSimtKeysTm;
+    const int rows_seq = p.T * p.H;
+    const int tiles_seq = (rows_seq + kR - 1) / kR;
+    const int tile = blockIdx.x, b = tile / tiles_seq, rt = tile % tiles_seq;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t C = p.simt_ctas;
+    // W and the positions before sequence b, over all threads
+    int64_t tot = 0, bef = 0;
+    for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
+        const int64_t w = (int64_t)tiles_seq * seq_blocks_of(p, bb, kKB);
+        tot += w;
+        if (bb < b) bef += w;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        bef += __shfl_xor_sync(0xffffffffu, bef, off);
+    }
+    __shared__ int64_t part[2][8];
+    if (lane == 0) {
+        part[0][warp] = tot;
+        part[1][warp] = bef;
+    }
+    __syncthreads();
+    int64_t W = 0, before = 0;
+    for (int k = 0; k < (int)(blockDim.x >> 5); ++k) {
+        W += part[0][k];
+        before += part[1][k];
+    }
+    const int nblk = seq_blocks_of(p, b, kKB);
+    const int64_t T0 = before + (int64_t)rt * nblk, T1 = T0 + nblk;
+    auto cta_of = [&](int64_t x) { return ((x + 1) * C - 1) / W; };   // largest c with W c / C <= x
+    auto start_of = [&](int64_t cc) { return W * cc / C; };
+    const int64_t ca = cta_of(T0), cb = cta_of(T1 - 1);
+    if (ca == cb) return;
+    const int row = blockIdx.y * 8 + warp;
+    const int r = rt * kR + row;
+    if (row >= kR || r >= rows_seq) return;
+    float M = -INFINITY;
+    for (int64_t cc = ca; cc <= cb; ++cc) {
+        if (start_of(cc) == start_of(cc + 1)) continue;              // an empty range
+        const int64_t slot = start_of(cc) >= T0 ? 2 * cc : 2 * cc + 1;
+        M = fmaxf(M, p.part_lse[slot * kR + row]);
+    }
+    float4 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float S = 0.f;
+    if (M > -INFINITY) {
+        for (int64_t cc = ca; cc <= cb; ++cc) {
+            if (start_of(cc) == start_of(cc + 1)) continue;
+            const int64_t slot = start_of(cc) >= T0 ? 2 * cc : 2 * cc + 1;
+            const float w = __expf(p.part_lse[slot * kR + row] - M);
+            S += w;
+            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (slot * kR + row) * kDc) + lane;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = src[32 * q];
+                acc[q].x = fmaf(w, v.x, acc[q].x);
+                acc[q].y = fmaf(w, v.y, acc[q].y);
+                acc[q].z = fmaf(w, v.z, acc[q].z);
+                acc[q].w = fmaf(w, v.w, acc[q].w);
+            }
+        }
+    }
+    const float inv = S > 0.f ? 1.f / S : 0.f;
+    float4 *dst = reinterpret_cast<float4 *>(p.out + ((int64_t)b * rows_seq + r) * kDc) + lane;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[32 * q] = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+    if (lane == 0 && p.lse) p.lse[(int64_t)b * rows_seq + r] = S > 0.f ? M + __logf(S) : -INFINITY;
+}
+
 }  // namespace
 
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s) {
     if (rows_per_cta == kSimtSmallRows)
         return dt == KDT_F32 ? launch_typed<float, kSimtSmallRows>(p, s) : launch_typed<__nv_bfloat16, kSimtSmallRows>(p, s);
     return dt == KDT_F32 ? launch_typed_tm<float>(p, s) : launch_typed_tm<__nv_bfloat16>(p, s);
+}
+
+cudaError_t launch_merge_simt_pieces(const VerifyParams &p, cudaStream_t s) {
+    const int rows_seq = p.T * p.H;
+    const int tiles_seq = (rows_seq + kSimtRows - 1) / kSimtRows;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)p.B * tiles_seq), kSimtRows / 8);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_simt_pieces_kernel, p);
 }
 
 }  // namespace kdt

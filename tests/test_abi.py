@@ -161,16 +161,22 @@ def test_host_entry_checks(kdt):
 def test_plan_and_workspace_are_host_only(kdt):
     a = _args(kdt, num_splits=3)
     p = kdt.plan(a)
-    assert p["impl"] == "simt" and p["num_splits"] == 1            # 46 keys = one 64-key block
-    assert p["num_launches"] == 2                                  # visibility + attention
-    assert kdt.workspace_size(a) == p["workspace_bytes"] >= 2 * 9 * 4
+    # the 64-row SIMT tile: 3 CTAs share the 4 (row tile, key block) pairs (2 sequences of
+    # 72 rows, one 128-key block each) and leave piece states for a merge
+    assert p["impl"] == "simt" and p["num_splits"] == 3
+    assert p["num_launches"] == 3                                  # visibility + attention + merge
+    assert kdt.workspace_size(a) == p["workspace_bytes"] >= 2 * 9 * 4 + 2 * 3 * 64 * 513 * 4
+    assert kdt.plan(_args(kdt, num_splits=9))["num_splits"] == 4   # never more CTAs than pairs
+    # the 16-row tile splits uniformly: 46 keys are one 64-key block
+    s = kdt.plan(_args(kdt, impl=3, num_splits=3))
+    assert s["impl"] == "simt_small" and s["num_splits"] == 1 and s["num_launches"] == 2
     b = _args(kdt, kv_row_stride=4096 + 32, max_kv_len=4096 + 32, T=32, H=64, B=1, num_splits=8, vis=0x90000,
               parent=None)
     p = kdt.plan(b)
-    # 33 blocks of 128 keys asked in 8 splits: 5 blocks a split, so 7 splits
-    assert p["num_splits"] == 7 and p["num_launches"] == 2        # attention + merge
-    rows = 1 * 32 * 64
-    assert p["workspace_bytes"] >= 7 * rows * 512 * 4 + 7 * rows * 4
+    # the 64-row SIMT tile shares its (row tile, key block) pairs over the asked 8 CTAs,
+    # each leaving at most two piece states of 64 rows for the merge
+    assert p["num_splits"] == 8 and p["num_launches"] == 2        # attention + merge
+    assert p["workspace_bytes"] >= 2 * 8 * 64 * 512 * 4 + 2 * 8 * 64 * 4
     assert kdt.workspace_size(_args(kdt, D_c=3)) == 0
     # bf16 inputs plan onto the tensor-core kernel: one 4-CTA cluster per resident slot (at
     # most 48), sharing all units' key blocks; units cut by the split leave piece states in

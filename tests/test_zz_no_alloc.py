@@ -73,16 +73,16 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(kdt, oracle
 
 
 def _auto_simt_plan_over_limit(kdt):
-    """A fp32 shape whose automatic SIMT split count needs more than the fixed scratch: with
-    about two waves of CTAs wanted, B sequences of 59 row tiles (T=59, H=64) and a prefix of
-    a few key blocks per split; B is searched because the split count depends on the SM count."""
+    """A fp32 shape whose automatic split count on the 16-row SIMT tile (one split per 64-key
+    block, each with a partial state of every row) needs more than the fixed scratch. (The
+    64-row tile's pieces, two of 64 rows per CTA, always fit.)"""
     import torch
     for B in range(3, 12):
         c = wl.make_case("noalloc_simt", B=B, T=59, H=64, prefix=640, dtype="f32", tree="uniform", seed=44)
         d = G.to_device(c)
         out = torch.empty((c.B, c.T, c.H, 512), device="cuda")
         a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
-                          max_kv_len=c.max_kv_len, scale=c.scale, out=out, impl="simt")
+                          max_kv_len=c.max_kv_len, scale=c.scale, out=out, impl="simt_small")
         if kdt.workspace_size(a) > (64 << 20):
             return c, kdt.plan(a)
     return None, None
@@ -94,8 +94,8 @@ def test_noalloc_fits_automatic_splits_and_rejects_oversize(kdt, oracle_mod):
     # split count until they fit, and the result still matches
     c, pl = _auto_simt_plan_over_limit(kdt)
     assert c is not None, "no fp32 shape with an automatic split plan above 64 MiB"
-    assert pl["impl"] == "simt" and pl["num_splits"] > 1
-    got, ref = _both(kdt, c, impl="simt")
+    assert pl["impl"] == "simt_small" and pl["num_splits"] > 1
+    got, ref = _both(kdt, c, impl="simt_small")
     _check(c, got, ref, oracle_mod)
     # the bf16 tensor path's automatic plan fits as it is
     t = wl.make_case("noalloc_c", B=2, T=64, H=64, prefix=2000, dtype="bf16", tree="geometric", seed=43)
@@ -106,7 +106,7 @@ def test_noalloc_fits_automatic_splits_and_rejects_oversize(kdt, oracle_mod):
     d = G.to_device(c)
     out = torch.empty((c.B, c.T, c.H, 512), device="cuda")
     a = kdt.make_args(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"], d["prefix_len"], parent=d["parent"],
-                      max_kv_len=c.max_kv_len, scale=c.scale, out=out, impl="simt", num_splits=16)
+                      max_kv_len=c.max_kv_len, scale=c.scale, out=out, impl="simt_small", num_splits=16)
     assert kdt.workspace_size(a) > (64 << 20)
     st = kdt.lib().kdt_verify_attn_noalloc(ctypes.byref(a), None)
     assert st == kdt.kdt.KDT_ERR_WORKSPACE
