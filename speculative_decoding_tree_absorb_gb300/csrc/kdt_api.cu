@@ -68,6 +68,7 @@ struct Plan {
     int splits = 1;
     int tc_clusters = 1;                   // tensor path: resident clusters the work is split across
     int simt_ctas = 0;                     // SIMT 64-row tile: CTAs the work is split across
+    bool one_pass = false;                 // SIMT_SMALL with every sequence in one 64-key block
     int blocks_per_split = 1;
     int ctas = 0;
     int launches = 0;
@@ -156,6 +157,11 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         p.splits = p.simt_ctas;
         p.blocks_per_split = nblk;
         p.ctas = p.simt_ctas;
+    } else if (a->max_kv_len <= kSimtOneKeys) {
+        // every sequence is one block: the one-pass kernel, 4 rows a CTA, visibility built
+        // in the kernel (no visibility launch, no workspace)
+        p.one_pass = true;
+        p.ctas = (int)(((rows_seq + 3) / 4) * a->B);
     } else {
         // SIMT 16-row tile: one 64-key block per split unless the caller fixed the splits
         int splits;
@@ -171,7 +177,7 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         p.ctas = (int)(base * p.splits);
     }
     size_t off = 0;
-    if (a->parent) {
+    if (a->parent && !p.one_pass) {
         const int W = (a->T + 31) / 32;
         p.vis_off = off;
         p.vis_bytes = (size_t)a->B * a->T * W * sizeof(uint32_t);
@@ -204,7 +210,7 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         }
     }
     p.ws_bytes = off;
-    p.launches = (a->parent ? 1 : 0) + 1 + ((p.splits > 1 || tc_pieces) ? 1 : 0);   // SIMT pieces: splits > 1 too
+    p.launches = ((a->parent && !p.one_pass) ? 1 : 0) + 1 + ((p.splits > 1 || tc_pieces) ? 1 : 0);   // SIMT pieces: splits > 1 too
     *pl = p;
     return KDT_OK;
 }
@@ -392,6 +398,11 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
         vp.fault = hooks->fault;
     }
 
+    if (p.one_pass) {
+        vp.vis = a->vis;
+        if (a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t), stream) != cudaSuccess) return KDT_ERR_CUDA;
+        return launch_verify_simt_one(vp, a->dtype, a->parent, stream) == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
+    }
     if (a->parent) {
         uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);
         if (launch_build_visibility(a->parent, a->B, a->T, vis, a->err, stream) != cudaSuccess) return KDT_ERR_CUDA;

@@ -73,6 +73,10 @@ constexpr int kSimtSmallRows = 16;
 constexpr int kSimtKeys = 64;          // keys per block of the 16-row tile
 constexpr int kSimtKeysTm = 128;       // keys per block of the 64-row tile
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s);
+// Shapes with max_kv_len <= kSimtOneKeys: one pass a CTA of 4 rows, the visibility built in
+// the kernel from `parent` (or read from p.vis when parent is NULL); no workspace.
+constexpr int kSimtOneKeys = 64;
+cudaError_t launch_verify_simt_one(const VerifyParams &p, kdt_dtype dt, const int32_t *parent, cudaStream_t s);
 // Merges the piece states the 64-row SIMT tile left (when simt_ctas > 1).
 cudaError_t launch_merge_simt_pieces(const VerifyParams &p, cudaStream_t s);
 

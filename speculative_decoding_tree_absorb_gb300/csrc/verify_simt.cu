@@ -753,6 +753,218 @@ cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, verify_simt_tm_kernel<Tin>, p);
 }
 
+// Shapes whose every sequence fits one block of at most 64 keys (prefix + tree): one pass,
+// no key loop. A CTA takes 4 rows of one sequence; it loads their queries and ALL the
+// sequence's cache rows with one cp.async group, builds the rows' visibility from the
+// parent array itself while they land (no separate visibility launch), and computes the
+// scores, the softmax and P.V from shared memory, the value rows being the staged latent
+// rows. With 4 rows a CTA the work spreads over many SMs: a shape this small is bound by
+// latency, not by any pipe.
+//  * scores: 16 dim groups (warp w, half-warp h: dim pairs 2 (2 w + h) + 32 u) each
+//    compute the 4 x 64 partial scores as 2 rows x 8 keys a lane (8 key lanes x 2 row
+//    pairs, so a key read is 8 consecutive rows and a query read a broadcast); the
+//    partials meet through one shuffle and shared memory.
+//  * softmax: warp r < 4 takes row r (keys lane, lane + 32).
+//  * output: thread t the columns 2 t, 2 t + 1 of the 4 rows.
+constexpr int kOneRows = 4;
+constexpr int kOneKeys = 64;
+constexpr int kOneThreads = 256;
+
+template <typename T> struct LayoutOne {
+    static constexpr int kRow = kDqk + (sizeof(T) == 4 ? 4 : 8);     // staged row: 576 + pad elements
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kOneRows * kRow * (int)sizeof(T);
+    static constexpr int kOffRed = (kOffK + kOneKeys * kRow * (int)sizeof(T) + 15) / 16 * 16;   // [8][4][64] partials
+    static constexpr int kOffS = kOffRed + 8 * kOneRows * kOneKeys * 4;                         // [4][64] scores
+    static constexpr int kOffPt = kOffS + kOneRows * kOneKeys * 4;                              // [64][4] P^T
+    static constexpr int kOffRow = kOffPt + kOneKeys * kOneRows * 4;                            // [4] masks, [4] l
+    static constexpr int kSmem = kOffRow + kOneRows * 8 + kOneRows * 4;
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const VerifyParams p, const int32_t *parent) {
+    using L = LayoutOne<Tin>;
+    constexpr int kEl16 = 16 / (int)sizeof(Tin);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Tin *qs = reinterpret_cast<Tin *>(smem_raw + L::kOffQ);
+    Tin *ks = reinterpret_cast<Tin *>(smem_raw + L::kOffK);
+    float *red = reinterpret_cast<float *>(smem_raw + L::kOffRed);
+    float *ss = reinterpret_cast<float *>(smem_raw + L::kOffS);
+    float *pt = reinterpret_cast<float *>(smem_raw + L::kOffPt);
+    uint64_t *mask_s = reinterpret_cast<uint64_t *>(smem_raw + L::kOffRow);
+    float *l_s = reinterpret_cast<float *>(smem_raw + L::kOffRow + kOneRows * 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.y;
+    const int rows_seq = p.T * p.H;
+    const int r0 = blockIdx.x * kOneRows;
+    const int P = p.prefix_len[b];
+    const int kv = P + p.T;                          // <= 64 (checked on the host)
+    const int nk = (kv + 7) & ~7;                    // keys computed: kv rounded up to 8
+    const Tin *q_nope = static_cast<const Tin *>(p.q_nope);
+    const Tin *q_pe = static_cast<const Tin *>(p.q_pe);
+    const Tin *c_kv = static_cast<const Tin *>(p.c_kv);
+    const Tin *k_pe = static_cast<const Tin *>(p.k_pe);
+
+    // ---- every operand in one cp.async group: 4 query rows, the sequence's nk cache rows
+    constexpr int kNopePieces = kDc / kEl16, kPePieces = kDr / kEl16, kRowPieces = kNopePieces + kPePieces;
+    for (int i = tid; i < (kOneRows + nk) * kRowPieces; i += kOneThreads) {
+        const int rr = i / kRowPieces, pc = i % kRowPieces;
+        const bool nope = pc < kNopePieces;
+        const int e0 = (nope ? pc : pc - kNopePieces) * kEl16;       // element offset in its array row
+        const int col = (nope ? 0 : kDc) + e0;
+        if (rr < kOneRows) {
+            const int r = r0 + rr;
+            const bool ok = r < rows_seq;
+            const int64_t grow = (int64_t)b * rows_seq + (ok ? r : 0);
+            const Tin *src = nope ? q_nope + grow * p.q_nope_stride + e0 : q_pe + grow * p.q_pe_stride + e0;
+            cp_async16(qs + rr * L::kRow + col, src, ok ? 16u : 0u);
+        } else {
+            const int key = rr - kOneRows;
+            const bool ok = key < kv;
+            const int64_t krow = (int64_t)b * p.L + (ok ? key : 0);
+            const Tin *src = nope ? c_kv + krow * kDc + e0 : k_pe + krow * kDr + e0;
+            cp_async16(ks + key * L::kRow + col, src, ok ? 16u : 0u);
+        }
+    }
+    cp_async_commit();
+    // ---- meanwhile: the rows' visible keys (prefix, ancestors, self) as 64-bit masks
+    if (warp == 0) {
+        if (lane < kOneRows) {
+            const int r = min(r0 + lane, rows_seq - 1);
+            const int qi = r / p.H;
+            uint64_t m = P > 0 ? (~0ull >> (64 - P)) : 0ull;          // P <= 63 here (kv <= 64, T >= 1)
+            if (parent) {
+                const int32_t *par = parent + (int64_t)b * p.T;
+                int j = qi;
+                while (true) {                        // parents strictly decrease: <= T steps
+                    m |= 1ull << (P + j);
+                    const int pj = par[j];
+                    if (pj < -1 || pj >= j || pj < 0) break;   // malformed entries are recorded below
+                    j = pj;
+                }
+            } else {
+                const uint32_t *vrow = p.vis + ((int64_t)b * p.T + qi) * p.W;
+                const uint64_t bits = (uint64_t)vrow[0] | (p.W > 1 ? (uint64_t)vrow[1] << 32 : 0ull);
+                m |= (p.T >= 64 ? bits : (bits & ((1ull << p.T) - 1))) << P;
+            }
+            mask_s[lane] = m;
+        }
+        // the first CTA of a sequence checks every parent entry (the error word gets the
+        // first malformed entry over all sequences, as the visibility kernel reports it)
+        if (parent && blockIdx.x == 0) {
+            const int32_t *par = parent + (int64_t)b * p.T;
+            for (int j = lane; j < p.T; j += 32) {
+                const int pj = par[j];
+                if (pj < -1 || pj >= j) record_error(p.err, (int32_t)((int64_t)b * p.T + j + 1));
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- partial scores of this lane's dim group
+    const int grp = 2 * warp + (lane >> 4);          // 0..15
+    const int rp = (lane >> 3) & 1, kg = lane & 7;
+    float acc[2][8];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    {
+        const Tin *qa = qs + (2 * rp) * L::kRow + 2 * grp;
+        const Tin *kb = ks + kg * L::kRow + 2 * grp;
+        for (int u = 0; u < kDqk / 32; ++u) {
+            const float2 a0 = get2(qa + 32 * u), a1 = get2(qa + L::kRow + 32 * u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (8 * j < nk) {
+                    const float2 k = get2(kb + 8 * j * L::kRow + 32 * u);
+                    acc[0][j] = fmaf(a0.x, k.x, fmaf(a0.y, k.y, acc[0][j]));
+                    acc[1][j] = fmaf(a1.x, k.x, fmaf(a1.y, k.y, acc[1][j]));
+                }
+            }
+        }
+    }
+    // the two half-warps' groups, then the 8 warps through shared memory
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], 16);
+    if (lane < 16) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) red[(warp * kOneRows + 2 * rp + i) * kOneKeys + kg + 8 * j] = acc[i][j];
+    }
+    __syncthreads();
+    {
+        const int r = tid >> 6, key = tid & 63;      // 256 threads = 4 rows x 64 keys
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += red[(w * kOneRows + r) * kOneKeys + key];
+        const bool visible = key < kv && ((mask_s[r] >> key) & 1ull);
+        ss[r * kOneKeys + key] = visible ? s * p.scale_log2 : -INFINITY;
+    }
+    __syncthreads();
+    // ---- softmax, one warp a row
+    if (warp < kOneRows) {
+        const int r = warp;
+        const float x0 = ss[r * kOneKeys + lane], x1 = ss[r * kOneKeys + lane + 32];
+        float m = fmaxf(x0, x1);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const float p0 = m == -INFINITY ? 0.f : exp2f(x0 - m), p1 = m == -INFINITY ? 0.f : exp2f(x1 - m);
+        pt[lane * kOneRows + r] = p0;
+        pt[(lane + 32) * kOneRows + r] = p1;
+        float l = p0 + p1;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if (lane == 0) {
+            l_s[r] = l;
+            const int gr = r0 + r;
+            if (gr < rows_seq && p.lse)
+                p.lse[(int64_t)b * rows_seq + gr] = l > 0.f ? 0.6931471805599453f * (m + log2f(l)) : -INFINITY;
+        }
+    }
+    __syncthreads();
+    // ---- O = P V over the visible block, columns 2 tid, 2 tid + 1 of the 4 rows
+    float o[kOneRows][2];
+#pragma unroll
+    for (int i = 0; i < kOneRows; ++i) o[i][0] = o[i][1] = 0.f;
+    for (int key = 0; key < kv; ++key) {
+        const float4 pr = *reinterpret_cast<const float4 *>(pt + key * kOneRows);
+        const float2 v = get2(ks + key * L::kRow + 2 * tid);
+        o[0][0] = fmaf(pr.x, v.x, o[0][0]);
+        o[0][1] = fmaf(pr.x, v.y, o[0][1]);
+        o[1][0] = fmaf(pr.y, v.x, o[1][0]);
+        o[1][1] = fmaf(pr.y, v.y, o[1][1]);
+        o[2][0] = fmaf(pr.z, v.x, o[2][0]);
+        o[2][1] = fmaf(pr.z, v.y, o[2][1]);
+        o[3][0] = fmaf(pr.w, v.x, o[3][0]);
+        o[3][1] = fmaf(pr.w, v.y, o[3][1]);
+    }
+#pragma unroll
+    for (int i = 0; i < kOneRows; ++i) {
+        const int gr = r0 + i;
+        if (gr >= rows_seq) continue;
+        const float inv = l_s[i] > 0.f ? 1.f / l_s[i] : 0.f;
+        *reinterpret_cast<float2 *>(p.out + ((int64_t)b * rows_seq + gr) * kDc + 2 * tid) =
+            make_float2(o[i][0] * inv, o[i][1] * inv);
+    }
+}
+
+template <typename Tin>
+cudaError_t launch_typed_one(const VerifyParams &p, const int32_t *parent, cudaStream_t s) {
+    using L = LayoutOne<Tin>;
+    cudaError_t e = cudaFuncSetAttribute(verify_simt_one_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    if (e != cudaSuccess) return e;
+    const int rows_seq = p.T * p.H;
+    dim3 grid((rows_seq + kOneRows - 1) / kOneRows, p.B);
+    verify_simt_one_kernel<Tin><<<grid, kOneThreads, L::kSmem, s>>>(p, parent);
+    return cudaGetLastError();
+}
+
 template <typename Tin, int kRows>
 cudaError_t launch_typed(const VerifyParams &p, cudaStream_t s) {
     using L = Layout<Tin, kRows>;
@@ -861,6 +1073,10 @@ cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per
     if (rows_per_cta == kSimtSmallRows)
         return dt == KDT_F32 ? launch_typed<float, kSimtSmallRows>(p, s) : launch_typed<__nv_bfloat16, kSimtSmallRows>(p, s);
     return dt == KDT_F32 ? launch_typed_tm<float>(p, s) : launch_typed_tm<__nv_bfloat16>(p, s);
+}
+
+cudaError_t launch_verify_simt_one(const VerifyParams &p, kdt_dtype dt, const int32_t *parent, cudaStream_t s) {
+    return dt == KDT_F32 ? launch_typed_one<float>(p, parent, s) : launch_typed_one<__nv_bfloat16>(p, parent, s);
 }
 
 cudaError_t launch_merge_simt_pieces(const VerifyParams &p, cudaStream_t s) {

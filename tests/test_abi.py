@@ -167,9 +167,14 @@ def test_plan_and_workspace_are_host_only(kdt):
     assert p["num_launches"] == 3                                  # visibility + attention + merge
     assert kdt.workspace_size(a) == p["workspace_bytes"] >= 2 * 9 * 4 + 2 * 3 * 64 * 513 * 4
     assert kdt.plan(_args(kdt, num_splits=9))["num_splits"] == 4   # never more CTAs than pairs
-    # the 16-row tile splits uniformly: 46 keys are one 64-key block
+    # the small-shape path: 46 keys fit one 64-key block, so one pass a CTA with the
+    # visibility built in the kernel: one launch, no workspace
     s = kdt.plan(_args(kdt, impl=3, num_splits=3))
-    assert s["impl"] == "simt_small" and s["num_splits"] == 1 and s["num_launches"] == 2
+    assert s["impl"] == "simt_small" and s["num_splits"] == 1 and s["num_launches"] == 1
+    assert s["workspace_bytes"] == 0 and s["ctas"] == 2 * 18
+    # longer caches take the 16-row tile, one 64-key block per split
+    s = kdt.plan(_args(kdt, impl=3, kv_row_stride=200, max_kv_len=200, num_splits=0))
+    assert s["impl"] == "simt_small" and s["num_splits"] == 4 and s["num_launches"] == 3
     b = _args(kdt, kv_row_stride=4096 + 32, max_kv_len=4096 + 32, T=32, H=64, B=1, num_splits=8, vis=0x90000,
               parent=None)
     p = kdt.plan(b)
