@@ -400,8 +400,11 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
 
     if (p.one_pass) {
         vp.vis = a->vis;
-        if (a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t), stream) != cudaSuccess) return KDT_ERR_CUDA;
-        return launch_verify_simt_one(vp, a->dtype, a->parent, stream) == cudaSuccess ? KDT_OK : KDT_ERR_CUDA;
+        const bool check_all = (int64_t)a->B * a->T <= kSimtOneCheckAll;
+        if (a->err && !check_all && cudaMemsetAsync(a->err, 0, sizeof(int32_t), stream) != cudaSuccess)
+            return KDT_ERR_CUDA;
+        return launch_verify_simt_one(vp, a->dtype, a->parent, check_all, stream) == cudaSuccess ? KDT_OK
+                                                                                               : KDT_ERR_CUDA;
     }
     if (a->parent) {
         uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);

@@ -76,7 +76,11 @@ cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per
 // Shapes with max_kv_len <= kSimtOneKeys: one pass a CTA of 4 rows, the visibility built in
 // the kernel from `parent` (or read from p.vis when parent is NULL); no workspace.
 constexpr int kSimtOneKeys = 64;
-cudaError_t launch_verify_simt_one(const VerifyParams &p, kdt_dtype dt, const int32_t *parent, cudaStream_t s);
+// check_all: one CTA validates every parent entry and writes the error word (no clearing
+// needed); else the caller clears the word first. kSimtOneCheckAll bounds B * T for it.
+constexpr int kSimtOneCheckAll = 1024;
+cudaError_t launch_verify_simt_one(const VerifyParams &p, kdt_dtype dt, const int32_t *parent, bool check_all,
+                                   cudaStream_t s);
 // Merges the piece states the 64-row SIMT tile left (when simt_ctas > 1).
 cudaError_t launch_merge_simt_pieces(const VerifyParams &p, cudaStream_t s);
 

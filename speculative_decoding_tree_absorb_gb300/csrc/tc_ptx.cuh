@@ -51,6 +51,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Raise the transaction count of the current phase by `bytes` without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
 // Arrive on the barrier at the same offset in CTA `rank` of the cluster, with
 // release semantics at cluster scope (orders this thread's prior DSMEM stores).
 __device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank) {
@@ -156,6 +161,15 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 // Warm L2 with `bytes` (a multiple of 16) of global memory from a 16-byte aligned address.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to this
+// CTA's shared memory, completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
 

@@ -778,13 +778,17 @@ template <typename T> struct LayoutOne {
     static constexpr int kOffS = kOffRed + 8 * kOneRows * kOneKeys * 4;                         // [4][64] scores
     static constexpr int kOffPt = kOffS + kOneRows * kOneKeys * 4;                              // [64][4] P^T
     static constexpr int kOffRow = kOffPt + kOneKeys * kOneRows * 4;                            // [4] masks, [4] l
-    static constexpr int kSmem = kOffRow + kOneRows * 8 + kOneRows * 4;
+    static constexpr int kOffBar = kOffRow + kOneRows * 8 + kOneRows * 4;                       // copy barrier
+    static constexpr int kSmem = kOffBar + 8;
 };
 
+// check_all: this grid is small enough that CTA (0, 0) checks every parent entry of the
+// batch and writes the error word (0 if none; no clearing before the launch); otherwise
+// the word was cleared and each sequence's first CTA records its malformed entries.
 template <typename Tin>
-__global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const VerifyParams p, const int32_t *parent) {
+__global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const VerifyParams p, const int32_t *parent,
+                                                                      bool check_all) {
     using L = LayoutOne<Tin>;
-    constexpr int kEl16 = 16 / (int)sizeof(Tin);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Tin *qs = reinterpret_cast<Tin *>(smem_raw + L::kOffQ);
     Tin *ks = reinterpret_cast<Tin *>(smem_raw + L::kOffK);
@@ -793,41 +797,53 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
     float *pt = reinterpret_cast<float *>(smem_raw + L::kOffPt);
     uint64_t *mask_s = reinterpret_cast<uint64_t *>(smem_raw + L::kOffRow);
     float *l_s = reinterpret_cast<float *>(smem_raw + L::kOffRow + kOneRows * 8);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + L::kOffBar);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.y;
     const int rows_seq = p.T * p.H;
     const int r0 = blockIdx.x * kOneRows;
-    const int P = p.prefix_len[b];
-    const int kv = P + p.T;                          // <= 64 (checked on the host)
-    const int nk = (kv + 7) & ~7;                    // keys computed: kv rounded up to 8
+    const int nq = min(kOneRows, rows_seq - r0);
+    constexpr uint32_t kNopeBytes = kDc * sizeof(Tin), kPeBytes = kDr * sizeof(Tin);
+    if (tid == 0) {
+        tc::mbar_init(bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    // ---- every operand by bulk copies (one per row part, issued by warp 0's lanes) on one
+    // barrier: first the rows of the 4 queries that exist (while the prefix length is read),
+    // then the sequence's kv cache rows. Rows past them are never read as operands (their
+    // scores are masked, their outputs unused).
     const Tin *q_nope = static_cast<const Tin *>(p.q_nope);
     const Tin *q_pe = static_cast<const Tin *>(p.q_pe);
     const Tin *c_kv = static_cast<const Tin *>(p.c_kv);
     const Tin *k_pe = static_cast<const Tin *>(p.k_pe);
-
-    // ---- every operand in one cp.async group: 4 query rows, the sequence's nk cache rows
-    constexpr int kNopePieces = kDc / kEl16, kPePieces = kDr / kEl16, kRowPieces = kNopePieces + kPePieces;
-    for (int i = tid; i < (kOneRows + nk) * kRowPieces; i += kOneThreads) {
-        const int rr = i / kRowPieces, pc = i % kRowPieces;
-        const bool nope = pc < kNopePieces;
-        const int e0 = (nope ? pc : pc - kNopePieces) * kEl16;       // element offset in its array row
-        const int col = (nope ? 0 : kDc) + e0;
-        if (rr < kOneRows) {
-            const int r = r0 + rr;
-            const bool ok = r < rows_seq;
-            const int64_t grow = (int64_t)b * rows_seq + (ok ? r : 0);
-            const Tin *src = nope ? q_nope + grow * p.q_nope_stride + e0 : q_pe + grow * p.q_pe_stride + e0;
-            cp_async16(qs + rr * L::kRow + col, src, ok ? 16u : 0u);
-        } else {
-            const int key = rr - kOneRows;
-            const bool ok = key < kv;
-            const int64_t krow = (int64_t)b * p.L + (ok ? key : 0);
-            const Tin *src = nope ? c_kv + krow * kDc + e0 : k_pe + krow * kDr + e0;
-            cp_async16(ks + key * L::kRow + col, src, ok ? 16u : 0u);
+    if (warp == 0) {
+        if (lane == 0) tc::mbar_expect_tx(bar, (uint32_t)nq * (kNopeBytes + kPeBytes));
+        __syncwarp();
+        if (lane < 2 * nq) {
+            const int rr = lane >> 1;
+            const bool nope = (lane & 1) == 0;
+            const int64_t grow = (int64_t)b * rows_seq + r0 + rr;
+            tc::bulk_load_1d(qs + rr * L::kRow + (nope ? 0 : kDc),
+                             nope ? q_nope + grow * p.q_nope_stride : q_pe + grow * p.q_pe_stride,
+                             nope ? kNopeBytes : kPeBytes, bar);
         }
     }
-    cp_async_commit();
+    const int P = p.prefix_len[b];
+    const int kv = P + p.T;                          // <= 64 (checked on the host)
+    const int nk = (kv + 7) & ~7;                    // keys computed: kv rounded up to 8
+    if (warp == 0) {
+        if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)kv * (kNopeBytes + kPeBytes));
+        __syncwarp();
+        for (int i = lane; i < 2 * kv; i += 32) {
+            const int key = i >> 1;
+            const bool nope = (i & 1) == 0;
+            const int64_t krow = (int64_t)b * p.L + key;
+            tc::bulk_load_1d(ks + key * L::kRow + (nope ? 0 : kDc), nope ? c_kv + krow * kDc : k_pe + krow * kDr,
+                             nope ? kNopeBytes : kPeBytes, bar);
+        }
+    }
     // ---- meanwhile: the rows' visible keys (prefix, ancestors, self) as 64-bit masks
     if (warp == 0) {
         if (lane < kOneRows) {
@@ -850,9 +866,22 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
             }
             mask_s[lane] = m;
         }
-        // the first CTA of a sequence checks every parent entry (the error word gets the
-        // first malformed entry over all sequences, as the visibility kernel reports it)
-        if (parent && blockIdx.x == 0) {
+        // the error word gets the first malformed parent entry over all sequences, as the
+        // visibility kernel reports it
+        if (check_all) {
+            if (blockIdx.x == 0 && blockIdx.y == 0 && p.err) {
+                int first = 0x7fffffff;
+                if (parent)
+#pragma unroll 8
+                    for (int j = lane; j < p.B * p.T; j += 32) {
+                        const int pj = parent[j], jj = j % p.T;
+                        if ((pj < -1 || pj >= jj) && j + 1 < first) first = j + 1;
+                    }
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, off));
+                if (lane == 0) *p.err = first == 0x7fffffff ? 0 : first;
+            }
+        } else if (parent && blockIdx.x == 0) {
             const int32_t *par = parent + (int64_t)b * p.T;
             for (int j = lane; j < p.T; j += 32) {
                 const int pj = par[j];
@@ -860,8 +889,14 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
             }
         }
     }
-    cp_async_wait<0>();
-    __syncthreads();
+    // every thread sees the copies land (bounded: a lost completion ends the call with an
+    // error, after a second wait for copies still in flight)
+    const bool landed = tc::mbar_wait(bar, 0, 200000000ull);
+    if (__syncthreads_or(!landed)) {
+        if (tid == 0 && p.err) atomicCAS(p.err, 0, -40);
+        tc::mbar_wait(bar, 0, 200000000ull);
+        return;
+    }
 
     // ---- partial scores of this lane's dim group
     const int grp = 2 * warp + (lane >> 4);          // 0..15
@@ -932,6 +967,8 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
     float o[kOneRows][2];
 #pragma unroll
     for (int i = 0; i < kOneRows; ++i) o[i][0] = o[i][1] = 0.f;
+#pragma unroll 4
+#pragma unroll 4
     for (int key = 0; key < kv; ++key) {
         const float4 pr = *reinterpret_cast<const float4 *>(pt + key * kOneRows);
         const float2 v = get2(ks + key * L::kRow + 2 * tid);
@@ -955,13 +992,13 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
 }
 
 template <typename Tin>
-cudaError_t launch_typed_one(const VerifyParams &p, const int32_t *parent, cudaStream_t s) {
+cudaError_t launch_typed_one(const VerifyParams &p, const int32_t *parent, bool check_all, cudaStream_t s) {
     using L = LayoutOne<Tin>;
     cudaError_t e = cudaFuncSetAttribute(verify_simt_one_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
     const int rows_seq = p.T * p.H;
     dim3 grid((rows_seq + kOneRows - 1) / kOneRows, p.B);
-    verify_simt_one_kernel<Tin><<<grid, kOneThreads, L::kSmem, s>>>(p, parent);
+    verify_simt_one_kernel<Tin><<<grid, kOneThreads, L::kSmem, s>>>(p, parent, check_all);
     return cudaGetLastError();
 }
 
@@ -1075,8 +1112,10 @@ cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per
     return dt == KDT_F32 ? launch_typed_tm<float>(p, s) : launch_typed_tm<__nv_bfloat16>(p, s);
 }
 
-cudaError_t launch_verify_simt_one(const VerifyParams &p, kdt_dtype dt, const int32_t *parent, cudaStream_t s) {
-    return dt == KDT_F32 ? launch_typed_one<float>(p, parent, s) : launch_typed_one<__nv_bfloat16>(p, parent, s);
+cudaError_t launch_verify_simt_one(const VerifyParams &p, kdt_dtype dt, const int32_t *parent, bool check_all,
+                                   cudaStream_t s) {
+    return dt == KDT_F32 ? launch_typed_one<float>(p, parent, check_all, s)
+                         : launch_typed_one<__nv_bfloat16>(p, parent, check_all, s);
 }
 
 cudaError_t launch_merge_simt_pieces(const VerifyParams &p, cudaStream_t s) {
