@@ -371,6 +371,7 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
     vp.H = a->H;
     vp.W = (a->T + 31) / 32;
     vp.L = a->kv_row_stride;
+    vp.max_kv = a->max_kv_len;
     vp.q_nope = a->q_nope;
     vp.q_pe = a->q_pe;
     vp.q_nope_stride = a->q_nope_row_stride ? a->q_nope_row_stride : kDc;

@@ -32,6 +32,7 @@ constexpr int kMaxT = 4096;
 struct VerifyParams {
     int B, T, H, W;            // W = ceil(T/32) visibility words per query
     int64_t L;                 // cache rows per sequence
+    int max_kv = 0;            // the caller's bound on prefix_len[b] + T
     const void *q_nope, *q_pe, *c_kv, *k_pe;
     int64_t q_nope_stride, q_pe_stride;   // elements between consecutive (b,i,h) query rows
     const int32_t *prefix_len;

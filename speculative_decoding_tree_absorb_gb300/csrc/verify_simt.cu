@@ -736,7 +736,6 @@ __global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyPara
 template <typename Tin>
 cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
     using L = LayoutTm<Tin>;
-    const int rows_seq = p.T * p.H;
     cudaError_t e = cudaFuncSetAttribute(verify_simt_tm_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
     // programmatic dependent launch after the visibility kernel of the same call
@@ -770,11 +769,15 @@ constexpr int kOneRows = 4;
 constexpr int kOneKeys = 64;
 constexpr int kOneThreads = 256;
 
+// Operands land unpadded, as the few large bulk copies of whole row ranges (a copy's cost
+// is per request); lane (group, key lane) walks the dim pairs in an order rotated by its
+// key lane, so the 8 key rows a half-warp reads sit in different banks all the same.
 template <typename T> struct LayoutOne {
-    static constexpr int kRow = kDqk + (sizeof(T) == 4 ? 4 : 8);     // staged row: 576 + pad elements
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kOneRows * kRow * (int)sizeof(T);
-    static constexpr int kOffRed = (kOffK + kOneKeys * kRow * (int)sizeof(T) + 15) / 16 * 16;   // [8][4][64] partials
+    static constexpr int kOffQn = 0;                                                 // [4][512]
+    static constexpr int kOffQp = kOffQn + kOneRows * kDc * (int)sizeof(T);          // [4][64]
+    static constexpr int kOffKn = kOffQp + kOneRows * kDr * (int)sizeof(T);          // [64][512]
+    static constexpr int kOffKp = kOffKn + kOneKeys * kDc * (int)sizeof(T);          // [64][64]
+    static constexpr int kOffRed = kOffKp + kOneKeys * kDr * (int)sizeof(T);         // [8][4][64] partials
     static constexpr int kOffS = kOffRed + 8 * kOneRows * kOneKeys * 4;                         // [4][64] scores
     static constexpr int kOffPt = kOffS + kOneRows * kOneKeys * 4;                              // [64][4] P^T
     static constexpr int kOffRow = kOffPt + kOneKeys * kOneRows * 4;                            // [4] masks, [4] l
@@ -790,8 +793,10 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
                                                                       bool check_all) {
     using L = LayoutOne<Tin>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    Tin *qs = reinterpret_cast<Tin *>(smem_raw + L::kOffQ);
-    Tin *ks = reinterpret_cast<Tin *>(smem_raw + L::kOffK);
+    Tin *qn_s = reinterpret_cast<Tin *>(smem_raw + L::kOffQn);
+    Tin *qp_s = reinterpret_cast<Tin *>(smem_raw + L::kOffQp);
+    Tin *kn_s = reinterpret_cast<Tin *>(smem_raw + L::kOffKn);
+    Tin *kp_s = reinterpret_cast<Tin *>(smem_raw + L::kOffKp);
     float *red = reinterpret_cast<float *>(smem_raw + L::kOffRed);
     float *ss = reinterpret_cast<float *>(smem_raw + L::kOffS);
     float *pt = reinterpret_cast<float *>(smem_raw + L::kOffPt);
@@ -810,40 +815,34 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
         tc::fence_mbar_init();
     }
     __syncthreads();
-    // ---- every operand by bulk copies (one per row part, issued by warp 0's lanes) on one
-    // barrier: first the rows of the 4 queries that exist (while the prefix length is read),
-    // then the sequence's kv cache rows. Rows past them are never read as operands (their
-    // scores are masked, their outputs unused).
+    // ---- every operand by bulk copies on one barrier: the rows of the 4 queries that exist
+    // (one copy per part when the rows are contiguous) and the sequence's first max_kv
+    // (<= 64) cache rows, whatever its own length (one copy per part). Rows past them are
+    // never read as operands (their scores are masked, their outputs unused).
     const Tin *q_nope = static_cast<const Tin *>(p.q_nope);
     const Tin *q_pe = static_cast<const Tin *>(p.q_pe);
     const Tin *c_kv = static_cast<const Tin *>(p.c_kv);
     const Tin *k_pe = static_cast<const Tin *>(p.k_pe);
-    if (warp == 0) {
-        if (lane == 0) tc::mbar_expect_tx(bar, (uint32_t)nq * (kNopeBytes + kPeBytes));
-        __syncwarp();
-        if (lane < 2 * nq) {
-            const int rr = lane >> 1;
-            const bool nope = (lane & 1) == 0;
-            const int64_t grow = (int64_t)b * rows_seq + r0 + rr;
-            tc::bulk_load_1d(qs + rr * L::kRow + (nope ? 0 : kDc),
-                             nope ? q_nope + grow * p.q_nope_stride : q_pe + grow * p.q_pe_stride,
-                             nope ? kNopeBytes : kPeBytes, bar);
+    const int nkv = p.max_kv;
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(bar, (uint32_t)(nq + nkv) * (kNopeBytes + kPeBytes));
+        const int64_t g0 = (int64_t)b * rows_seq + r0;
+        if (p.q_nope_stride == kDc) {
+            tc::bulk_load_1d(qn_s, q_nope + g0 * kDc, (uint32_t)nq * kNopeBytes, bar);
+        } else {
+            for (int rr = 0; rr < nq; ++rr) tc::bulk_load_1d(qn_s + rr * kDc, q_nope + (g0 + rr) * p.q_nope_stride, kNopeBytes, bar);
         }
+        if (p.q_pe_stride == kDr) {
+            tc::bulk_load_1d(qp_s, q_pe + g0 * kDr, (uint32_t)nq * kPeBytes, bar);
+        } else {
+            for (int rr = 0; rr < nq; ++rr) tc::bulk_load_1d(qp_s + rr * kDr, q_pe + (g0 + rr) * p.q_pe_stride, kPeBytes, bar);
+        }
+        tc::bulk_load_1d(kn_s, c_kv + (int64_t)b * p.L * kDc, (uint32_t)nkv * kNopeBytes, bar);
+        tc::bulk_load_1d(kp_s, k_pe + (int64_t)b * p.L * kDr, (uint32_t)nkv * kPeBytes, bar);
     }
     const int P = p.prefix_len[b];
-    const int kv = P + p.T;                          // <= 64 (checked on the host)
+    const int kv = min(P + p.T, nkv);                // <= max_kv <= 64 (the caller's bound; clamped for safety)
     const int nk = (kv + 7) & ~7;                    // keys computed: kv rounded up to 8
-    if (warp == 0) {
-        if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)kv * (kNopeBytes + kPeBytes));
-        __syncwarp();
-        for (int i = lane; i < 2 * kv; i += 32) {
-            const int key = i >> 1;
-            const bool nope = (i & 1) == 0;
-            const int64_t krow = (int64_t)b * p.L + key;
-            tc::bulk_load_1d(ks + key * L::kRow + (nope ? 0 : kDc), nope ? c_kv + krow * kDc : k_pe + krow * kDr,
-                             nope ? kNopeBytes : kPeBytes, bar);
-        }
-    }
     // ---- meanwhile: the rows' visible keys (prefix, ancestors, self) as 64-bit masks
     if (warp == 0) {
         if (lane < kOneRows) {
@@ -906,21 +905,25 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
     for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-    {
-        const Tin *qa = qs + (2 * rp) * L::kRow + 2 * grp;
-        const Tin *kb = ks + kg * L::kRow + 2 * grp;
-        for (int u = 0; u < kDqk / 32; ++u) {
-            const float2 a0 = get2(qa + 32 * u), a1 = get2(qa + L::kRow + 32 * u);
+    // dim pairs 2 dp + 32 u of the latent (u < 16) and of the rope dims (u < 2)
+    const int dp = (grp + kg) & 15;
+    auto scores = [&](const Tin *q, const Tin *k, int width, int npairs) {
+        const Tin *qa = q + (2 * rp) * width + 2 * dp;
+        const Tin *kb = k + kg * width + 2 * dp;
+        for (int u = 0; u < npairs; ++u) {
+            const float2 a0 = get2(qa + 32 * u), a1 = get2(qa + width + 32 * u);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (8 * j < nk) {
-                    const float2 k = get2(kb + 8 * j * L::kRow + 32 * u);
-                    acc[0][j] = fmaf(a0.x, k.x, fmaf(a0.y, k.y, acc[0][j]));
-                    acc[1][j] = fmaf(a1.x, k.x, fmaf(a1.y, k.y, acc[1][j]));
+                    const float2 kk = get2(kb + 8 * j * width + 32 * u);
+                    acc[0][j] = fmaf(a0.x, kk.x, fmaf(a0.y, kk.y, acc[0][j]));
+                    acc[1][j] = fmaf(a1.x, kk.x, fmaf(a1.y, kk.y, acc[1][j]));
                 }
             }
         }
-    }
+    };
+    scores(qn_s, kn_s, kDc, kDc / 32);
+    scores(qp_s, kp_s, kDr, kDr / 32);
     // the two half-warps' groups, then the 8 warps through shared memory
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -971,7 +974,7 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
 #pragma unroll 4
     for (int key = 0; key < kv; ++key) {
         const float4 pr = *reinterpret_cast<const float4 *>(pt + key * kOneRows);
-        const float2 v = get2(ks + key * L::kRow + 2 * tid);
+        const float2 v = get2(kn_s + key * kDc + 2 * tid);
         o[0][0] = fmaf(pr.x, v.x, o[0][0]);
         o[0][1] = fmaf(pr.x, v.y, o[0][1]);
         o[1][0] = fmaf(pr.y, v.x, o[1][0]);
