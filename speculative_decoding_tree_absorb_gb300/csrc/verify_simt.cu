@@ -763,8 +763,18 @@ cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
 //    compute the 4 x 64 partial scores as 2 rows x 8 keys a lane (8 key lanes x 2 row
 //    pairs, so a key read is 8 consecutive rows and a query read a broadcast); the
 //    partials meet through one shuffle and shared memory.
-//  * softmax: warp r < 4 takes row r (keys lane, lane + 32).
+//  * softmax: warp r < 4 sums row r's partials and takes its softmax (keys lane, lane + 32).
 //  * output: thread t the columns 2 t, 2 t + 1 of the 4 rows.
+__device__ __forceinline__ float fast_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fast_lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 constexpr int kOneRows = 4;
 constexpr int kOneKeys = 64;
 constexpr int kOneThreads = 256;
@@ -778,8 +788,7 @@ template <typename T> struct LayoutOne {
     static constexpr int kOffKn = kOffQp + kOneRows * kDr * (int)sizeof(T);          // [64][512]
     static constexpr int kOffKp = kOffKn + kOneKeys * kDc * (int)sizeof(T);          // [64][64]
     static constexpr int kOffRed = kOffKp + kOneKeys * kDr * (int)sizeof(T);         // [8][4][64] partials
-    static constexpr int kOffS = kOffRed + 8 * kOneRows * kOneKeys * 4;                         // [4][64] scores
-    static constexpr int kOffPt = kOffS + kOneRows * kOneKeys * 4;                              // [64][4] P^T
+    static constexpr int kOffPt = kOffRed + 8 * kOneRows * kOneKeys * 4;                        // [64][4] P^T
     static constexpr int kOffRow = kOffPt + kOneKeys * kOneRows * 4;                            // [4] masks, [4] l
     static constexpr int kOffBar = kOffRow + kOneRows * 8 + kOneRows * 4;                       // copy barrier
     static constexpr int kSmem = kOffBar + 8;
@@ -798,7 +807,6 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
     Tin *kn_s = reinterpret_cast<Tin *>(smem_raw + L::kOffKn);
     Tin *kp_s = reinterpret_cast<Tin *>(smem_raw + L::kOffKp);
     float *red = reinterpret_cast<float *>(smem_raw + L::kOffRed);
-    float *ss = reinterpret_cast<float *>(smem_raw + L::kOffS);
     float *pt = reinterpret_cast<float *>(smem_raw + L::kOffPt);
     uint64_t *mask_s = reinterpret_cast<uint64_t *>(smem_raw + L::kOffRow);
     float *l_s = reinterpret_cast<float *>(smem_raw + L::kOffRow + kOneRows * 8);
@@ -936,23 +944,24 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
             for (int j = 0; j < 8; ++j) red[(warp * kOneRows + 2 * rp + i) * kOneKeys + kg + 8 * j] = acc[i][j];
     }
     __syncthreads();
-    {
-        const int r = tid >> 6, key = tid & 63;      // 256 threads = 4 rows x 64 keys
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) s += red[(w * kOneRows + r) * kOneKeys + key];
-        const bool visible = key < kv && ((mask_s[r] >> key) & 1ull);
-        ss[r * kOneKeys + key] = visible ? s * p.scale_log2 : -INFINITY;
-    }
-    __syncthreads();
-    // ---- softmax, one warp a row
+    // ---- scores summed over the 8 warps, masked, and the softmax: one warp a row
     if (warp < kOneRows) {
         const int r = warp;
-        const float x0 = ss[r * kOneKeys + lane], x1 = ss[r * kOneKeys + lane + 32];
-        float m = fmaxf(x0, x1);
+        float x[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int key = lane + 32 * h;
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) sum += red[(w * kOneRows + r) * kOneKeys + key];
+            const bool visible = key < kv && ((mask_s[r] >> key) & 1ull);
+            x[h] = visible ? sum * p.scale_log2 : -INFINITY;
+        }
+        float m = fmaxf(x[0], x[1]);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        const float p0 = m == -INFINITY ? 0.f : exp2f(x0 - m), p1 = m == -INFINITY ? 0.f : exp2f(x1 - m);
+        // the hardware base-2 exponential and logarithm (relative error about 2^-22)
+        const float p0 = m == -INFINITY ? 0.f : fast_ex2(x[0] - m), p1 = m == -INFINITY ? 0.f : fast_ex2(x[1] - m);
         pt[lane * kOneRows + r] = p0;
         pt[(lane + 32) * kOneRows + r] = p1;
         float l = p0 + p1;
@@ -962,7 +971,7 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
             l_s[r] = l;
             const int gr = r0 + r;
             if (gr < rows_seq && p.lse)
-                p.lse[(int64_t)b * rows_seq + gr] = l > 0.f ? 0.6931471805599453f * (m + log2f(l)) : -INFINITY;
+                p.lse[(int64_t)b * rows_seq + gr] = l > 0.f ? 0.6931471805599453f * (m + fast_lg2(l)) : -INFINITY;
         }
     }
     __syncthreads();
@@ -970,7 +979,6 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
     float o[kOneRows][2];
 #pragma unroll
     for (int i = 0; i < kOneRows; ++i) o[i][0] = o[i][1] = 0.f;
-#pragma unroll 4
 #pragma unroll 4
     for (int key = 0; key < kv; ++key) {
         const float4 pr = *reinterpret_cast<const float4 *>(pt + key * kOneRows);
