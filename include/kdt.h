@@ -124,7 +124,9 @@ typedef struct {
     float scale;            /* score scale, e.g. 1/sqrt(192) */
     float *out;             /* device fp32 [B,T,H,512] */
     float *lse;             /* device fp32 [B,T,H], or NULL */
-    int32_t *err;           /* device int32 error word for the parent path, or NULL */
+    int32_t *err;           /* device int32 error word, or NULL: 0, or with `parent` 1 + the
+                               index b*T + i of the first malformed entry, or a negative
+                               code if an internal wait for a copy or pipeline stage gave up */
     int impl;               /* kdt_impl */
     int num_splits;         /* 0 = choose automatically. SIMT_SMALL: KV splits per 16-row
                                tile (at most 32), merged by log-sum-exp. SIMT (64-row tiles):
@@ -150,8 +152,10 @@ typedef struct {
  * malformed tree). With `vis`, the caller's bits are used as given: they need not
  * come from a tree, and a row whose visible set is empty (no prefix, no bit set)
  * gets out = 0 and lse = -inf.
- * Rows of c_kv/k_pe at or beyond prefix_len[b] + T are never read, whatever they
- * hold. Inputs are all fp32 or all bf16; out and lse are fp32.
+ * Rows of c_kv/k_pe at or beyond prefix_len[b] + T never affect the result, whatever
+ * they hold (NaN included); rows below max_kv_len may be read (the one-pass small-shape
+ * kernel copies a sequence's first max_kv_len rows before it knows prefix_len[b]).
+ * Inputs are all fp32 or all bf16; out and lse are fp32.
  * `workspace` must hold kdt_verify_attn_workspace_size(a) bytes (256-byte aligned;
  * may be NULL when that size is 0). Its contents need no initialisation.
  * Errors: KDT_ERR_NULL_ARG, KDT_ERR_BAD_SHAPE (including prefix bound violations
