@@ -114,9 +114,10 @@ def test_tiny_config_full(kdt, oracle_mod, dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_result_independent_of_split_count(kdt, oracle_mod, dtype):
-    # SIMT: num_splits KV ranges per row tile, merged by the split-merge kernel. Tensor
-    # path: num_splits persistent clusters sharing the (unit, key block) work, so every
-    # count moves the share boundaries that cut units into pieces (1 = no pieces at all).
+    # SIMT 64-row tile: num_splits CTAs sharing the (row tile, key block) pairs; 16-row
+    # tile: num_splits KV ranges per row tile, merged by the split-merge kernel. Tensor
+    # path: num_splits persistent clusters sharing the (unit, key block) work. Every count
+    # moves the boundaries that cut tiles or units into pieces (1 = no pieces at all).
     import torch
     case = wl.make_case("splits", B=3, T=16, H=8, prefix=(700, 33, 1000), dtype=dtype, tree="geometric", seed=5)
     ref_out, ref_lse = oracle_mod.verify_attn(case)
