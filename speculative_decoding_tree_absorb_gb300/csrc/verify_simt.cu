@@ -34,6 +34,17 @@
 
 namespace kdt {
 namespace {
+// (o0, o1) += p * (v0, v1) as one packed fp32x2 FMA (each lane an IEEE fma, as fmaf).
+__device__ __forceinline__ void fma2_bcast(float &o0, float &o1, float p, float v0, float v1) {
+    asm("{\n\t.reg .b64 acc, pp, vv;\n\t"
+        "mov.b64 acc, {%0, %1};\n\t"
+        "mov.b64 pp, {%2, %2};\n\t"
+        "mov.b64 vv, {%3, %4};\n\t"
+        "fma.rn.f32x2 acc, pp, vv, acc;\n\t"
+        "mov.b64 {%0, %1}, acc;\n\t}"
+        : "+f"(o0), "+f"(o1)
+        : "f"(p), "f"(v0), "f"(v1));
+}
 
 constexpr int kKeys = kSimtKeys;       // 64 keys per block
 constexpr int kDChunk = 64;            // dims per score chunk (fewer, larger steps: each step ends at a barrier)
@@ -657,7 +668,7 @@ __global__ void __launch_bounds__(512, 1) verify_simt_tm_kernel(const VerifyPara
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) o[i][c] = fmaf(pr[i], vv[c], o[i][c]);
+                    for (int c = 0; c < 8; c += 2) fma2_bcast(o[i][c], o[i][c + 1], pr[i], vv[c], vv[c + 1]);
             }
             ++g;
         }
