@@ -630,6 +630,26 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t o_rank = 2u + (uint32_t)kpair;  // the O-CTA an S-CTA feeds
     constexpr uint16_t kMaskS = 0x3, kMaskO = 0xC, kMaskAll = 0xF;
 
+    // Before the set-up: warm L2 with this CTA's rows of Q for unit c, the cluster's first
+    // item whenever a round of whole units goes out first (every unit costs the same, or
+    // the first round fits the fair share); otherwise the request is merely unused. The
+    // first Q load then reads L2 instead of DRAM.
+    if (s_role && warp == 4 && lane == 0) {
+        const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
+        if (p.B * p.pairs_per_seq >= C) {
+            const int b = c / p.pairs_per_seq;
+            const int r0 = (2 * (c % p.pairs_per_seq) + kpair) * kRows;
+            if (r0 < p.rows_seq) {
+                const int nrows = min(kRows, p.rows_seq - r0);
+                const unsigned char *qsrc =
+                    reinterpret_cast<const unsigned char *>(p.q_nope + ((int64_t)b * p.rows_seq + r0) * p.q_stride);
+                const uint32_t bytes = (uint32_t)((nrows - 1) * p.q_stride + kDc) * 2;
+                for (uint32_t o = 0; o < bytes; o += kQPrefetchChunk)
+                    prefetch_l2_bulk(qsrc + o, min(kQPrefetchChunk, bytes - o));
+            }
+        }
+    }
+
     // ---- set-up: this cluster's work, barriers, TMEM ---------------------------------
     if (warp == 0) {
         const int c = (int)(blockIdx.x >> 2), C = (int)(gridDim.x >> 2);
