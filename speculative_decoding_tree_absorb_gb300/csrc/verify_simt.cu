@@ -1092,32 +1092,47 @@ __global__ void __launch_bounds__(256) merge_simt_pieces_kernel(const VerifyPara
     const int row = blockIdx.y * 8 + warp;
     const int r = rt * kR + row;
     if (row >= kR || r >= rows_seq) return;
+    // the pieces' lse, 32 at a time (lane k: CTA base + k), in one round trip each
+    auto slot_of = [&](int64_t cc) -> int64_t {                      // -1: an empty range
+        if (cc > cb || start_of(cc) == start_of(cc + 1)) return -1;
+        return start_of(cc) >= T0 ? 2 * cc : 2 * cc + 1;
+    };
     float M = -INFINITY;
-    for (int64_t cc = ca; cc <= cb; ++cc) {
-        if (start_of(cc) == start_of(cc + 1)) continue;              // an empty range
-        const int64_t slot = start_of(cc) >= T0 ? 2 * cc : 2 * cc + 1;
-        M = fmaxf(M, p.part_lse[slot * kR + row]);
+    for (int64_t base = ca; base <= cb; base += 32) {
+        const int64_t sl = slot_of(base + lane);
+        if (sl >= 0) M = fmaxf(M, p.part_lse[sl * kR + row]);
     }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float4 acc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     float S = 0.f;
     if (M > -INFINITY) {
-        for (int64_t cc = ca; cc <= cb; ++cc) {
-            if (start_of(cc) == start_of(cc + 1)) continue;
-            const int64_t slot = start_of(cc) >= T0 ? 2 * cc : 2 * cc + 1;
-            const float w = __expf(p.part_lse[slot * kR + row] - M);
+        for (int64_t base = ca; base <= cb; base += 32) {
+            const int64_t sl = slot_of(base + lane);
+            const float w = sl >= 0 ? __expf(p.part_lse[sl * kR + row] - M) : 0.f;
             S += w;
-            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (slot * kR + row) * kDc) + lane;
+            const int cnt = (int)(cb - base + 1 < 32 ? cb - base + 1 : 32);
+            // the pieces' rows as independent loads, the weights broadcast from their lanes
+#pragma unroll 4
+            for (int k = 0; k < cnt; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, w, k);
+                const int64_t slk = __shfl_sync(0xffffffffu, sl, k);
+                if (slk < 0) continue;                                // the same for the whole warp
+                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (slk * kR + row) * kDc) + lane;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = src[32 * q];
-                acc[q].x = fmaf(w, v.x, acc[q].x);
-                acc[q].y = fmaf(w, v.y, acc[q].y);
-                acc[q].z = fmaf(w, v.z, acc[q].z);
-                acc[q].w = fmaf(w, v.w, acc[q].w);
+                for (int q = 0; q < 4; ++q) {
+                    const float4 v = src[32 * q];
+                    acc[q].x = fmaf(wk, v.x, acc[q].x);
+                    acc[q].y = fmaf(wk, v.y, acc[q].y);
+                    acc[q].z = fmaf(wk, v.z, acc[q].z);
+                    acc[q].w = fmaf(wk, v.w, acc[q].w);
+                }
             }
         }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
     }
     const float inv = S > 0.f ? 1.f / S : 0.f;
     float4 *dst = reinterpret_cast<float4 *>(p.out + ((int64_t)b * rows_seq + r) * kDc) + lane;
