@@ -19,14 +19,18 @@
 //  * Work: tiles of 128 rows of one head (M = 128, cta_group::1), persistent CTAs (one
 //    per SM) taking tiles in head-major order, so the CTAs running at once share a few
 //    heads' weights in L2. Per 64-wide latent chunk the fp32 rows arrive by TMA (two
-//    128B-swizzled [128 x 32] boxes) into a 5-slot staging ring, so about 160 KB per SM
-//    are in flight; eight converter warps (one row per thread, half a chunk per warp)
-//    write hi and lo into tensor memory with tcgen05.st, where the MMA reads its A
-//    operand, so shared memory holds only the staging, the weights and the epilogue
-//    transpose. The weights arrive by TMA as MN-major tiles; one thread issues the MMAs.
+//    128B-swizzled [128 x 32] boxes) into a 4-slot staging ring and the weights into a
+//    4-slot ring, so 128 KB of rows and 64 KB of weights per SM are in flight; eight
+//    converter warps (one row per thread, half a chunk per warp) write hi and lo into
+//    tensor memory with tcgen05.st, where the MMA reads its A operand, so shared memory
+//    holds only the staging, the weights and the epilogue transpose. The weights arrive by TMA as MN-major tiles; one thread issues the MMAs.
 //    The accumulator is double-buffered in tensor memory (2 x 128 columns, next to two
 //    64-column A slots) so one tile's epilogue (four warps, rows transposed through
 //    shared memory into whole 128-byte line stores) overlaps the next tile's loads.
+//  * Measured and not kept: equal shares of 8-row groups per CTA instead of whole tiles
+//    (a share then spans up to three partial tiles, each streaming the head's full
+//    weights: slower on both shapes timed although it evens out the last wave), and an
+//    L2 bulk prefetch of a tile's whole 2 KB rows ahead of its chunk loads (slower).
 #include "kdt_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -41,9 +45,9 @@ constexpr int kVRows = 128;                  // rows of a tile (MMA M)
 constexpr int kVChunk = 64;                  // latent dims per chunk (one 128-byte bf16 row)
 constexpr int kVChunks = kDc / kVChunk;      // 8
 constexpr int kVThreads = 512;               // 16 warps
-constexpr int kNF = 5;                       // fp32 staging slots
+constexpr int kNF = 4;                       // fp32 staging slots
 constexpr int kNA = 2;                       // tensor-memory A slots (hi + lo of one chunk)
-constexpr int kNW = 3;                       // weight slots
+constexpr int kNW = 4;                       // weight slots
 constexpr int kConvWarps = 8;                // converter warps 4..11
 constexpr int kF32Box = kVRows * 32 * 4;            // [128 rows x 32 fp32], 128B-swizzled: 16 KB
 constexpr int kF32Bytes = 2 * kF32Box;              // one chunk: 32 KB
