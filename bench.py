@@ -57,6 +57,7 @@ TRAFFIC = {
     ("tcgen05", "dsv3"): {"src_hash": "2b8913615f321a79", "bytes": 594.74e6},
     ("simt", "kimi"): {"src_hash": "397b11efd808cae9", "bytes": 14.31e6},
     ("simt_small", "tiny"): {"src_hash": "397b11efd808cae9", "bytes": 0.58e6},
+    ("vc_proj", "target"): {"src_hash": "6d2fd9c107be75b7", "bytes": 77.55e6},
 }
 
 
@@ -78,7 +79,8 @@ def fp32_fma_peak_tflops(sms, sm_mhz):
 def kernel_src_hash(impl):
     import hashlib
     csrc = os.path.join(ROOT, "speculative_decoding_tree_absorb_gb300", "csrc")
-    files = ["verify_tc.cu", "tc_ptx.cuh"] if impl == "tcgen05" else ["verify_simt.cu"]
+    files = {"tcgen05": ["verify_tc.cu", "tc_ptx.cuh"], "vc_proj": ["vc_proj.cu", "tc_ptx.cuh"]}.get(
+        impl, ["verify_simt.cu"])
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
@@ -335,7 +337,7 @@ def run_vc_proj(args, case, dev):
                        "l2": "flushed before each call"},
             "us_median": statistics.median(times), "tflops": flops / (us * 1e-6) / 1e12,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": measured_traffic("vc_proj", args.config),
                          "peak_basis": f"copy bandwidth ({peaks['source']})", "kernel": "vc_proj_kernel"},
             "algorithmic": {"bytes": nbytes, "flops": flops,
                             "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6},
