@@ -219,7 +219,7 @@ kdt_status kdt_verify_attn_plan(const kdt_verify_args *a, kdt_plan *plan);
  *               legacy default stream with blocking streams, or the copies and the
  *               compute serialise (the results are the same).
  * The library creates two events per chunk plus two per call and releases them
- * before it returns (the driver frees them once they complete).
+ * before it returns (CUDA frees an event destroyed while pending once it completes).
  * Errors: those of kdt_verify_attn; KDT_ERR_BAD_SHAPE also for an n_chunks that
  * does not divide B, a nonzero row stride, or two equal streams; KDT_ERR_WORKSPACE
  * for a missing, short or misaligned dev_buf; KDT_ERR_NOT_DEVICE when dev_buf or
