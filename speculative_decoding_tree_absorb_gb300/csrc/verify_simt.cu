@@ -770,10 +770,14 @@ cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
 // scores, the softmax and P.V from shared memory, the value rows being the staged latent
 // rows. With 4 rows a CTA the work spreads over many SMs: a shape this small is bound by
 // latency, not by any pipe.
-//  * scores: 16 dim groups (warp w, half-warp h: dim pairs 2 (2 w + h) + 32 u) each
-//    compute the 4 x 64 partial scores as 2 rows x 8 keys a lane (8 key lanes x 2 row
-//    pairs, so a key read is 8 consecutive rows and a query read a broadcast); the
-//    partials meet through one shuffle and shared memory.
+//  * scores: lane (key lane kg, dim slot 4 w + sl) computes all 4 rows x 8 keys (kg + 8 j)
+//    over the dim pairs pr + 32 s, pr = (4 w + sl + 2 kg) mod 32: the 16 lanes of a
+//    half-warp then read 16 different pair columns, so every 8-byte key or query read is
+//    one conflict-free shared-memory wavefront of distinct bytes. The number of 8-key
+//    groups (2, 4, 6 or 8, covering the block's keys) is a compile-time count picked once:
+//    a runtime bound around each group kept its loads and FMAs from overlapping and cost
+//    a third of the phase. The 32 slots' partials meet through two shuffle steps and
+//    shared memory.
 //  * softmax: warp r < 4 sums row r's partials and takes its softmax (keys lane, lane + 32).
 //  * output: thread t the columns 2 t, 2 t + 1 of the 4 rows.
 __device__ __forceinline__ float fast_ex2(float x) {
@@ -805,12 +809,37 @@ template <typename T> struct LayoutOne {
     static constexpr int kSmem = kOffBar + 8;
 };
 
+// Partial scores of one lane: rows 0..3 x keys kg + 8 j (j < KJ) over the latent pairs
+// pr + 32 s (s < 8) and the rope pair pr, accumulated into acc.
+template <int KJ, typename Tin>
+__device__ __forceinline__ void one_scores(float (&acc)[kOneRows][8], const Tin *qn, const Tin *qp, const Tin *kn,
+                                           const Tin *kp, int pr, int kg) {
+    auto part = [&](const Tin *q, const Tin *k, int width, int nsteps) {
+        const Tin *qa = q + 2 * pr;
+        const Tin *kb = k + kg * width + 2 * pr;
+#pragma unroll 2
+        for (int u = 0; u < nsteps; ++u) {
+            float2 a[kOneRows];
+#pragma unroll
+            for (int i = 0; i < kOneRows; ++i) a[i] = get2(qa + i * width + 64 * u);
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) {
+                const float2 kk = get2(kb + 8 * j * width + 64 * u);
+#pragma unroll
+                for (int i = 0; i < kOneRows; ++i) acc[i][j] = fmaf(a[i].x, kk.x, fmaf(a[i].y, kk.y, acc[i][j]));
+            }
+        }
+    };
+    part(qn, kn, kDc, kDc / 64);
+    part(qp, kp, kDr, kDr / 64);
+}
+
 // check_all: this grid is small enough that CTA (0, 0) checks every parent entry of the
 // batch and writes the error word (0 if none; no clearing before the launch); otherwise
 // the word was cleared and each sequence's first CTA records its malformed entries.
 template <typename Tin>
-__global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const VerifyParams p, const int32_t *parent,
-                                                                      bool check_all) {
+__global__ void __launch_bounds__(kOneThreads, 1) verify_simt_one_kernel(const VerifyParams p,
+                                                                         const int32_t *parent, bool check_all) {
     using L = LayoutOne<Tin>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Tin *qn_s = reinterpret_cast<Tin *>(smem_raw + L::kOffQn);
@@ -916,43 +945,48 @@ __global__ void __launch_bounds__(kOneThreads) verify_simt_one_kernel(const Veri
         return;
     }
 
-    // ---- partial scores of this lane's dim group
-    const int grp = 2 * warp + (lane >> 4);          // 0..15
-    const int rp = (lane >> 3) & 1, kg = lane & 7;
-    float acc[2][8];
+    // ---- partial scores of this lane's dim slot: all 4 rows x 8 keys
+    const int kg = lane & 7, sl = lane >> 3;         // key lane (keys kg + 8 j), slot in the warp
+    const int pr = (4 * warp + sl + 2 * kg) & 31;    // dim pairs pr + 32 s of the latent, pr of the rope
+    float acc[kOneRows][8];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kOneRows; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-    // dim pairs 2 dp + 32 u of the latent (u < 16) and of the rope dims (u < 2)
-    const int dp = (grp + kg) & 15;
-    auto scores = [&](const Tin *q, const Tin *k, int width, int npairs) {
-        const Tin *qa = q + (2 * rp) * width + 2 * dp;
-        const Tin *kb = k + kg * width + 2 * dp;
-        for (int u = 0; u < npairs; ++u) {
-            const float2 a0 = get2(qa + 32 * u), a1 = get2(qa + width + 32 * u);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (8 * j < nk) {
-                    const float2 kk = get2(kb + 8 * j * width + 32 * u);
-                    acc[0][j] = fmaf(a0.x, kk.x, fmaf(a0.y, kk.y, acc[0][j]));
-                    acc[1][j] = fmaf(a1.x, kk.x, fmaf(a1.y, kk.y, acc[1][j]));
-                }
-            }
-        }
-    };
-    scores(qn_s, kn_s, kDc, kDc / 32);
-    scores(qp_s, kp_s, kDr, kDr / 32);
-    // the two half-warps' groups, then the 8 warps through shared memory
+    // the key groups computed (a multiple of 2 covering nk) are fixed at compile time:
+    // a runtime bound around each group's loads and FMAs serialises them
+    switch ((nk + 15) >> 4) {
+        case 1:
+            one_scores<2>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
+            break;
+        case 2:
+            one_scores<4>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
+            break;
+        case 3:
+            one_scores<6>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
+            break;
+        default:
+            one_scores<8>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
+            break;
+    }
+    // the warp's 4 slots in two transposing shuffle steps (lane ^ 16 trades rows 0-1 against
+    // 2-3, lane ^ 8 row 2 a + 0 against 2 a + 1): lane (kg, sl) ends with row sl, then the
+    // 8 warps through shared memory
+    const bool up2 = (sl & 2) != 0, up1 = (sl & 1) != 0;
+    float s2[2][8];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], 16);
-    if (lane < 16) {
+        for (int j = 0; j < 8; ++j) {
+            const float give = up2 ? acc[i][j] : acc[2 + i][j];
+            const float keep = up2 ? acc[2 + i][j] : acc[i][j];
+            s2[i][j] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+        }
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) red[(warp * kOneRows + 2 * rp + i) * kOneKeys + kg + 8 * j] = acc[i][j];
+    for (int j = 0; j < 8; ++j) {
+        const float give = up1 ? s2[0][j] : s2[1][j];
+        const float keep = up1 ? s2[1][j] : s2[0][j];
+        red[(warp * kOneRows + sl) * kOneKeys + kg + 8 * j] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
     }
     __syncthreads();
     // ---- scores summed over the 8 warps, masked, and the softmax: one warp a row
