@@ -43,6 +43,9 @@ ONE_PASS_CASES = [
     ("op_full_block_chain", 2, 64, 1, 0, "chain"),
     ("op_kv64", 2, 9, 5, 55, "geometric"),
     ("op_one_query", 4, 1, 7, (0, 1, 30, 63), "uniform"),
+    # 17, 33, 48 and 49 keys: the kernel computes 32, 48, 48 and 64 keys (4, 6, 6 and 8
+    # groups of 8, a compile-time count per sequence), the extra ones masked
+    ("op_key_groups", 4, 7, 3, (10, 26, 41, 42), "geometric"),
 ]
 
 
