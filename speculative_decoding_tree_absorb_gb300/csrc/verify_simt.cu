@@ -765,11 +765,11 @@ cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
 
 // Shapes whose every sequence fits one block of at most 64 keys (prefix + tree): one pass,
 // no key loop. A CTA takes 4 rows of one sequence; it loads their queries and ALL the
-// sequence's cache rows with one cp.async group, builds the rows' visibility from the
-// parent array itself while they land (no separate visibility launch), and computes the
-// scores, the softmax and P.V from shared memory, the value rows being the staged latent
-// rows. With 4 rows a CTA the work spreads over many SMs: a shape this small is bound by
-// latency, not by any pipe.
+// sequence's cache rows as a few bulk copies on one mbarrier, builds the rows' visibility
+// from the parent array itself while they land (no separate visibility launch), and
+// computes the scores, the softmax and P.V from shared memory, the value rows being the
+// staged latent rows. With 4 rows a CTA the work spreads over many SMs: a shape this small
+// is bound by latency, not by any pipe.
 //  * scores: lane (key lane kg, dim slot 4 w + sl) computes all 4 rows x 8 keys (kg + 8 j)
 //    over the dim pairs pr + 32 s, pr = (4 w + sl + 2 kg) mod 32: the 16 lanes of a
 //    half-warp then read 16 different pair columns, so every 8-byte key or query read is
