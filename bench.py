@@ -55,8 +55,8 @@ TRAFFIC = {
     ("tcgen05", "ragged"): {"src_hash": "2b8913615f321a79", "bytes": 155.58e6},
     ("tcgen05", "long"): {"src_hash": "2b8913615f321a79", "bytes": 338.96e6},
     ("tcgen05", "dsv3"): {"src_hash": "2b8913615f321a79", "bytes": 594.74e6},
-    ("simt", "kimi"): {"src_hash": "91817341bc6a5db1", "bytes": 14.31e6},
-    ("simt_small", "tiny"): {"src_hash": "91817341bc6a5db1", "bytes": 0.59e6},
+    ("simt", "kimi"): {"src_hash": "31869aea57861729", "bytes": 14.31e6},
+    ("simt_small", "tiny"): {"src_hash": "31869aea57861729", "bytes": 0.57e6},
     ("vc_proj", "target"): {"src_hash": "6d2fd9c107be75b7", "bytes": 77.55e6},
 }
 

@@ -69,6 +69,7 @@ struct Plan {
     int tc_clusters = 1;                   // tensor path: resident clusters the work is split across
     int simt_ctas = 0;                     // SIMT 64-row tile: CTAs the work is split across
     bool one_pass = false;                 // SIMT_SMALL with every sequence in one 64-key block
+    int one_rows = 4;                      // one-pass kernel: query rows a CTA
     int blocks_per_split = 1;
     int ctas = 0;
     int launches = 0;
@@ -158,10 +159,11 @@ kdt_status make_plan(const kdt_verify_args *a, Plan *pl) {
         p.blocks_per_split = nblk;
         p.ctas = p.simt_ctas;
     } else if (a->max_kv_len <= kSimtOneKeys) {
-        // every sequence is one block: the one-pass kernel, 4 rows a CTA, visibility built
-        // in the kernel (no visibility launch, no workspace)
+        // every sequence is one block: the one-pass kernel, 1, 2 or 4 rows a CTA, visibility
+        // built in the kernel (no visibility launch, no workspace)
         p.one_pass = true;
-        p.ctas = (int)(((rows_seq + 3) / 4) * a->B);
+        p.one_rows = simt_one_rows(a->dtype, a->B, rows_seq);
+        p.ctas = (int)(((rows_seq + p.one_rows - 1) / p.one_rows) * a->B);
     } else {
         // SIMT 16-row tile: one 64-key block per split unless the caller fixed the splits
         int splits;
@@ -404,8 +406,9 @@ kdt_status verify_attn_checked(const kdt_verify_args *a, void *workspace, size_t
         const bool check_all = (int64_t)a->B * a->T <= kSimtOneCheckAll;
         if (a->err && !check_all && cudaMemsetAsync(a->err, 0, sizeof(int32_t), stream) != cudaSuccess)
             return KDT_ERR_CUDA;
-        return launch_verify_simt_one(vp, a->dtype, a->parent, check_all, stream) == cudaSuccess ? KDT_OK
-                                                                                               : KDT_ERR_CUDA;
+        return launch_verify_simt_one(vp, a->dtype, a->parent, check_all, p.one_rows, stream) == cudaSuccess
+                   ? KDT_OK
+                   : KDT_ERR_CUDA;
     }
     if (a->parent) {
         uint32_t *vis = reinterpret_cast<uint32_t *>(ws + p.vis_off);

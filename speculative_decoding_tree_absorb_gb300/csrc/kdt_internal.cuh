@@ -74,14 +74,18 @@ constexpr int kSimtSmallRows = 16;
 constexpr int kSimtKeys = 64;          // keys per block of the 16-row tile
 constexpr int kSimtKeysTm = 128;       // keys per block of the 64-row tile
 cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per_cta, cudaStream_t s);
-// Shapes with max_kv_len <= kSimtOneKeys: one pass a CTA of 4 rows, the visibility built in
-// the kernel from `parent` (or read from p.vis when parent is NULL); no workspace.
+// Shapes with max_kv_len <= kSimtOneKeys: one pass a CTA of 1, 2 or 4 rows, the visibility
+// built in the kernel from `parent` (or read from p.vis when parent is NULL); no workspace.
 constexpr int kSimtOneKeys = 64;
+// Rows a CTA of the one-pass kernel takes: the fewest of 1, 2 or 4 whose grid the device
+// holds at once (every CTA loads its sequence's whole key block, so more and shorter CTAs
+// pay only within one wave); 4 when none fits.
+int simt_one_rows(kdt_dtype dt, int64_t B, int64_t rows_seq);
 // check_all: one CTA validates every parent entry and writes the error word (no clearing
 // needed); else the caller clears the word first. kSimtOneCheckAll bounds B * T for it.
 constexpr int kSimtOneCheckAll = 1024;
 cudaError_t launch_verify_simt_one(const VerifyParams &p, kdt_dtype dt, const int32_t *parent, bool check_all,
-                                   cudaStream_t s);
+                                   int rows_per_cta, cudaStream_t s);
 // Merges the piece states the 64-row SIMT tile left (when simt_ctas > 1).
 cudaError_t launch_merge_simt_pieces(const VerifyParams &p, cudaStream_t s);
 

@@ -764,13 +764,16 @@ cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
 }
 
 // Shapes whose every sequence fits one block of at most 64 keys (prefix + tree): one pass,
-// no key loop. A CTA takes 4 rows of one sequence; it loads their queries and ALL the
-// sequence's cache rows as a few bulk copies on one mbarrier, builds the rows' visibility
-// from the parent array itself while they land (no separate visibility launch), and
-// computes the scores, the softmax and P.V from shared memory, the value rows being the
-// staged latent rows. With 4 rows a CTA the work spreads over many SMs: a shape this small
-// is bound by latency, not by any pipe.
-//  * scores: lane (key lane kg, dim slot 4 w + sl) computes all 4 rows x 8 keys (kg + 8 j)
+// no key loop. A CTA takes R = 1, 2 or 4 rows of one sequence; it loads their queries and
+// ALL the sequence's cache rows as a few bulk copies on one mbarrier, builds the rows'
+// visibility from the parent array itself while they land (no separate visibility
+// launch), and computes the scores, the softmax and P.V from shared memory, the value rows
+// being the staged latent rows. A shape this small is bound by latency, not by any pipe:
+// the launch takes the fewest rows a CTA whose grid the device holds at once, so each CTA
+// is as short as the one-wave budget allows (on Tiny 2 rows a CTA instead of 4 cut the CTA
+// from 5.4 to 4.5 us; fewer rows only pay within one wave, as every CTA loads the whole
+// key block).
+//  * scores: lane (key lane kg, dim slot 4 w + sl) computes all R rows x 8 keys (kg + 8 j)
 //    over the dim pairs pr + 32 s, pr = (4 w + sl + 2 kg) mod 32: the 16 lanes of a
 //    half-warp then read 16 different pair columns, so every 8-byte key or query read is
 //    one conflict-free shared-memory wavefront of distinct bytes. The number of 8-key
@@ -778,8 +781,8 @@ cudaError_t launch_typed_tm(const VerifyParams &p, cudaStream_t s) {
 //    a runtime bound around each group kept its loads and FMAs from overlapping and cost
 //    a third of the phase. The 32 slots' partials meet through two shuffle steps and
 //    shared memory.
-//  * softmax: warp r < 4 sums row r's partials and takes its softmax (keys lane, lane + 32).
-//  * output: thread t the columns 2 t, 2 t + 1 of the 4 rows.
+//  * softmax: warp r < R sums row r's partials and takes its softmax (keys lane, lane + 32).
+//  * output: thread t the columns 2 t, 2 t + 1 of the R rows.
 __device__ __forceinline__ float fast_ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -790,43 +793,42 @@ __device__ __forceinline__ float fast_lg2(float x) {
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-constexpr int kOneRows = 4;
 constexpr int kOneKeys = 64;
 constexpr int kOneThreads = 256;
 
 // Operands land unpadded, as the few large bulk copies of whole row ranges (a copy's cost
 // is per request); lane (group, key lane) walks the dim pairs in an order rotated by its
 // key lane, so the 8 key rows a half-warp reads sit in different banks all the same.
-template <typename T> struct LayoutOne {
-    static constexpr int kOffQn = 0;                                                 // [4][512]
-    static constexpr int kOffQp = kOffQn + kOneRows * kDc * (int)sizeof(T);          // [4][64]
-    static constexpr int kOffKn = kOffQp + kOneRows * kDr * (int)sizeof(T);          // [64][512]
+template <typename T, int R> struct LayoutOne {
+    static constexpr int kOffQn = 0;                                                 // [R][512]
+    static constexpr int kOffQp = kOffQn + R * kDc * (int)sizeof(T);                 // [R][64]
+    static constexpr int kOffKn = kOffQp + R * kDr * (int)sizeof(T);                 // [64][512]
     static constexpr int kOffKp = kOffKn + kOneKeys * kDc * (int)sizeof(T);          // [64][64]
-    static constexpr int kOffRed = kOffKp + kOneKeys * kDr * (int)sizeof(T);         // [8][4][64] partials
-    static constexpr int kOffPt = kOffRed + 8 * kOneRows * kOneKeys * 4;                        // [64][4] P^T
-    static constexpr int kOffRow = kOffPt + kOneKeys * kOneRows * 4;                            // [4] masks, [4] l
-    static constexpr int kOffBar = kOffRow + kOneRows * 8 + kOneRows * 4;                       // copy barrier
+    static constexpr int kOffRed = kOffKp + kOneKeys * kDr * (int)sizeof(T);         // [8][R][64] partials
+    static constexpr int kOffPt = kOffRed + 8 * R * kOneKeys * 4;                    // [64][R] P^T
+    static constexpr int kOffRow = kOffPt + kOneKeys * R * 4;                        // [R] masks, [R] l
+    static constexpr int kOffBar = (kOffRow + R * 12 + 7) & ~7;                      // copy barrier
     static constexpr int kSmem = kOffBar + 8;
 };
 
-// Partial scores of one lane: rows 0..3 x keys kg + 8 j (j < KJ) over the latent pairs
+// Partial scores of one lane: rows 0..R-1 x keys kg + 8 j (j < KJ) over the latent pairs
 // pr + 32 s (s < 8) and the rope pair pr, accumulated into acc.
-template <int KJ, typename Tin>
-__device__ __forceinline__ void one_scores(float (&acc)[kOneRows][8], const Tin *qn, const Tin *qp, const Tin *kn,
+template <int KJ, int R, typename Tin>
+__device__ __forceinline__ void one_scores(float (&acc)[R][8], const Tin *qn, const Tin *qp, const Tin *kn,
                                            const Tin *kp, int pr, int kg) {
     auto part = [&](const Tin *q, const Tin *k, int width, int nsteps) {
         const Tin *qa = q + 2 * pr;
         const Tin *kb = k + kg * width + 2 * pr;
 #pragma unroll 2
         for (int u = 0; u < nsteps; ++u) {
-            float2 a[kOneRows];
+            float2 a[R];
 #pragma unroll
-            for (int i = 0; i < kOneRows; ++i) a[i] = get2(qa + i * width + 64 * u);
+            for (int i = 0; i < R; ++i) a[i] = get2(qa + i * width + 64 * u);
 #pragma unroll
             for (int j = 0; j < KJ; ++j) {
                 const float2 kk = get2(kb + 8 * j * width + 64 * u);
 #pragma unroll
-                for (int i = 0; i < kOneRows; ++i) acc[i][j] = fmaf(a[i].x, kk.x, fmaf(a[i].y, kk.y, acc[i][j]));
+                for (int i = 0; i < R; ++i) acc[i][j] = fmaf(a[i].x, kk.x, fmaf(a[i].y, kk.y, acc[i][j]));
             }
         }
     };
@@ -837,10 +839,11 @@ __device__ __forceinline__ void one_scores(float (&acc)[kOneRows][8], const Tin 
 // check_all: this grid is small enough that CTA (0, 0) checks every parent entry of the
 // batch and writes the error word (0 if none; no clearing before the launch); otherwise
 // the word was cleared and each sequence's first CTA records its malformed entries.
-template <typename Tin>
+template <typename Tin, int R>
 __global__ void __launch_bounds__(kOneThreads, 1) verify_simt_one_kernel(const VerifyParams p,
                                                                          const int32_t *parent, bool check_all) {
-    using L = LayoutOne<Tin>;
+    constexpr int kOneRows = R;
+    using L = LayoutOne<Tin, R>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Tin *qn_s = reinterpret_cast<Tin *>(smem_raw + L::kOffQn);
     Tin *qp_s = reinterpret_cast<Tin *>(smem_raw + L::kOffQp);
@@ -945,7 +948,7 @@ __global__ void __launch_bounds__(kOneThreads, 1) verify_simt_one_kernel(const V
         return;
     }
 
-    // ---- partial scores of this lane's dim slot: all 4 rows x 8 keys
+    // ---- partial scores of this lane's dim slot: all R rows x 8 keys
     const int kg = lane & 7, sl = lane >> 3;         // key lane (keys kg + 8 j), slot in the warp
     const int pr = (4 * warp + sl + 2 * kg) & 31;    // dim pairs pr + 32 s of the latent, pr of the rope
     float acc[kOneRows][8];
@@ -957,36 +960,71 @@ __global__ void __launch_bounds__(kOneThreads, 1) verify_simt_one_kernel(const V
     // a runtime bound around each group's loads and FMAs serialises them
     switch ((nk + 15) >> 4) {
         case 1:
-            one_scores<2>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
+            one_scores<2, R>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
             break;
         case 2:
-            one_scores<4>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
+            one_scores<4, R>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
             break;
         case 3:
-            one_scores<6>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
+            one_scores<6, R>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
             break;
         default:
-            one_scores<8>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
+            one_scores<8, R>(acc, qn_s, qp_s, kn_s, kp_s, pr, kg);
             break;
     }
-    // the warp's 4 slots in two transposing shuffle steps (lane ^ 16 trades rows 0-1 against
-    // 2-3, lane ^ 8 row 2 a + 0 against 2 a + 1): lane (kg, sl) ends with row sl, then the
-    // 8 warps through shared memory
+    // the warp's 4 slots in two transposing shuffle steps (partner lane ^ 16, then lane ^ 8),
+    // each trading half of what a lane holds, then the 8 warps through shared memory:
+    //  R = 4: rows 0-1 against 2-3, then row 2 a against 2 a + 1: lane (kg, sl) keeps row sl;
+    //  R = 2: row 0 against row 1, then keys j < 4 against j >= 4;
+    //  R = 1: keys j < 4 against j >= 4, then j < 2 against j >= 2 of those.
     const bool up2 = (sl & 2) != 0, up1 = (sl & 1) != 0;
-    float s2[2][8];
+    if constexpr (R == 4) {
+        float s2[2][8];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float give = up2 ? acc[i][j] : acc[2 + i][j];
+                const float keep = up2 ? acc[2 + i][j] : acc[i][j];
+                s2[i][j] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+            }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float give = up2 ? acc[i][j] : acc[2 + i][j];
-            const float keep = up2 ? acc[2 + i][j] : acc[i][j];
-            s2[i][j] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+            const float give = up1 ? s2[0][j] : s2[1][j];
+            const float keep = up1 ? s2[1][j] : s2[0][j];
+            red[(warp * R + sl) * kOneKeys + kg + 8 * j] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+        }
+    } else if constexpr (R == 2) {
+        float s1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float give = up2 ? acc[0][j] : acc[1][j];
+            const float keep = up2 ? acc[1][j] : acc[0][j];
+            s1[j] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
         }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float give = up1 ? s2[0][j] : s2[1][j];
-        const float keep = up1 ? s2[1][j] : s2[0][j];
-        red[(warp * kOneRows + sl) * kOneKeys + kg + 8 * j] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+        for (int t = 0; t < 4; ++t) {
+            const float give = up1 ? s1[t] : s1[4 + t];
+            const float keep = up1 ? s1[4 + t] : s1[t];
+            red[(warp * R + (up2 ? 1 : 0)) * kOneKeys + kg + 8 * (4 * (up1 ? 1 : 0) + t)] =
+                keep + __shfl_xor_sync(0xffffffffu, give, 8);
+        }
+    } else {
+        static_assert(R == 1, "rows a CTA: 1, 2 or 4");
+        float s1[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float give = up2 ? acc[0][t] : acc[0][4 + t];
+            const float keep = up2 ? acc[0][4 + t] : acc[0][t];
+            s1[t] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const float give = up1 ? s1[t] : s1[2 + t];
+            const float keep = up1 ? s1[2 + t] : s1[t];
+            red[warp * kOneKeys + kg + 8 * (4 * (up2 ? 1 : 0) + 2 * (up1 ? 1 : 0) + t)] =
+                keep + __shfl_xor_sync(0xffffffffu, give, 8);
+        }
     }
     __syncthreads();
     // ---- scores summed over the 8 warps, masked, and the softmax: one warp a row
@@ -1020,22 +1058,32 @@ __global__ void __launch_bounds__(kOneThreads, 1) verify_simt_one_kernel(const V
         }
     }
     __syncthreads();
-    // ---- O = P V over the visible block, columns 2 tid, 2 tid + 1 of the 4 rows
+    // ---- O = P V over the visible block, columns 2 tid, 2 tid + 1 of the R rows
     float o[kOneRows][2];
 #pragma unroll
     for (int i = 0; i < kOneRows; ++i) o[i][0] = o[i][1] = 0.f;
 #pragma unroll 4
     for (int key = 0; key < kv; ++key) {
-        const float4 pr = *reinterpret_cast<const float4 *>(pt + key * kOneRows);
+        float pr[R];
+        if constexpr (R == 4) {
+            const float4 q4 = *reinterpret_cast<const float4 *>(pt + key * R);
+            pr[0] = q4.x;
+            pr[1] = q4.y;
+            pr[2] = q4.z;
+            pr[3] = q4.w;
+        } else if constexpr (R == 2) {
+            const float2 q2 = *reinterpret_cast<const float2 *>(pt + key * R);
+            pr[0] = q2.x;
+            pr[1] = q2.y;
+        } else {
+            pr[0] = pt[key];
+        }
         const float2 v = get2(kn_s + key * kDc + 2 * tid);
-        o[0][0] = fmaf(pr.x, v.x, o[0][0]);
-        o[0][1] = fmaf(pr.x, v.y, o[0][1]);
-        o[1][0] = fmaf(pr.y, v.x, o[1][0]);
-        o[1][1] = fmaf(pr.y, v.y, o[1][1]);
-        o[2][0] = fmaf(pr.z, v.x, o[2][0]);
-        o[2][1] = fmaf(pr.z, v.y, o[2][1]);
-        o[3][0] = fmaf(pr.w, v.x, o[3][0]);
-        o[3][1] = fmaf(pr.w, v.y, o[3][1]);
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            o[i][0] = fmaf(pr[i], v.x, o[i][0]);
+            o[i][1] = fmaf(pr[i], v.y, o[i][1]);
+        }
     }
 #pragma unroll
     for (int i = 0; i < kOneRows; ++i) {
@@ -1047,15 +1095,35 @@ __global__ void __launch_bounds__(kOneThreads, 1) verify_simt_one_kernel(const V
     }
 }
 
-template <typename Tin>
-cudaError_t launch_typed_one(const VerifyParams &p, const int32_t *parent, bool check_all, cudaStream_t s) {
-    using L = LayoutOne<Tin>;
-    cudaError_t e = cudaFuncSetAttribute(verify_simt_one_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+template <typename Tin, int R>
+cudaError_t launch_one_rows(const VerifyParams &p, const int32_t *parent, bool check_all, cudaStream_t s) {
+    using L = LayoutOne<Tin, R>;
+    cudaError_t e =
+        cudaFuncSetAttribute(verify_simt_one_kernel<Tin, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
     const int rows_seq = p.T * p.H;
-    dim3 grid((rows_seq + kOneRows - 1) / kOneRows, p.B);
-    verify_simt_one_kernel<Tin><<<grid, kOneThreads, L::kSmem, s>>>(p, parent, check_all);
+    dim3 grid((rows_seq + R - 1) / R, p.B);
+    verify_simt_one_kernel<Tin, R><<<grid, kOneThreads, L::kSmem, s>>>(p, parent, check_all);
     return cudaGetLastError();
+}
+
+// CTAs of R rows the device holds at once: by shared memory (the key block dominates),
+// at most 3 an SM (the register file, 256 threads of at most 80 registers).
+template <typename Tin, int R> int64_t one_wave_ctas() {
+    int dev = 0, smem_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        smem_sm <= 0)
+        smem_sm = 228 * 1024;
+    int per_sm = smem_sm / (LayoutOne<Tin, R>::kSmem + 1024);   // 1 KB reserved a CTA
+    per_sm = per_sm < 1 ? 1 : (per_sm > 3 ? 3 : per_sm);
+    return (int64_t)sm_count() * per_sm;
+}
+
+template <typename Tin> int one_rows_typed(int64_t B, int64_t rows_seq) {
+    if (B * rows_seq <= one_wave_ctas<Tin, 1>()) return 1;
+    if (B * ((rows_seq + 1) / 2) <= one_wave_ctas<Tin, 2>()) return 2;
+    return 4;
 }
 
 template <typename Tin, int kRows>
@@ -1183,10 +1251,20 @@ cudaError_t launch_verify_simt(const VerifyParams &p, kdt_dtype dt, int rows_per
     return dt == KDT_F32 ? launch_typed_tm<float>(p, s) : launch_typed_tm<__nv_bfloat16>(p, s);
 }
 
+int simt_one_rows(kdt_dtype dt, int64_t B, int64_t rows_seq) {
+    return dt == KDT_F32 ? one_rows_typed<float>(B, rows_seq) : one_rows_typed<__nv_bfloat16>(B, rows_seq);
+}
+
 cudaError_t launch_verify_simt_one(const VerifyParams &p, kdt_dtype dt, const int32_t *parent, bool check_all,
-                                   cudaStream_t s) {
-    return dt == KDT_F32 ? launch_typed_one<float>(p, parent, check_all, s)
-                         : launch_typed_one<__nv_bfloat16>(p, parent, check_all, s);
+                                   int rows_per_cta, cudaStream_t s) {
+    if (dt == KDT_F32) {
+        return rows_per_cta == 1   ? launch_one_rows<float, 1>(p, parent, check_all, s)
+               : rows_per_cta == 2 ? launch_one_rows<float, 2>(p, parent, check_all, s)
+                                   : launch_one_rows<float, 4>(p, parent, check_all, s);
+    }
+    return rows_per_cta == 1   ? launch_one_rows<__nv_bfloat16, 1>(p, parent, check_all, s)
+           : rows_per_cta == 2 ? launch_one_rows<__nv_bfloat16, 2>(p, parent, check_all, s)
+                               : launch_one_rows<__nv_bfloat16, 4>(p, parent, check_all, s);
 }
 
 cudaError_t launch_merge_simt_pieces(const VerifyParams &p, cudaStream_t s) {

@@ -168,10 +168,14 @@ def test_plan_and_workspace_are_host_only(kdt):
     assert kdt.workspace_size(a) == p["workspace_bytes"] >= 2 * 9 * 4 + 2 * 3 * 64 * 513 * 4
     assert kdt.plan(_args(kdt, num_splits=9))["num_splits"] == 4   # never more CTAs than pairs
     # the small-shape path: 46 keys fit one 64-key block, so one pass a CTA with the
-    # visibility built in the kernel: one launch, no workspace
+    # visibility built in the kernel: one launch, no workspace; its 2 x 72 rows fit one
+    # wave at one row a CTA (one fp32 CTA an SM, at least 148 SMs)
     s = kdt.plan(_args(kdt, impl=3, num_splits=3))
     assert s["impl"] == "simt_small" and s["num_splits"] == 1 and s["num_launches"] == 1
-    assert s["workspace_bytes"] == 0 and s["ctas"] == 2 * 18
+    assert s["workspace_bytes"] == 0 and s["ctas"] == 2 * 72
+    # more rows than SMs: 2, then 4 rows a CTA (the grid of the fewest rows that fits one wave)
+    assert kdt.plan(_args(kdt, impl=3, H=16))["ctas"] == 2 * 72
+    assert kdt.plan(_args(kdt, impl=3, H=64))["ctas"] == 2 * 144
     # longer caches take the 16-row tile, one 64-key block per split
     s = kdt.plan(_args(kdt, impl=3, kv_row_stride=200, max_kv_len=200, num_splits=0))
     assert s["impl"] == "simt_small" and s["num_splits"] == 4 and s["num_launches"] == 3

@@ -46,6 +46,12 @@ ONE_PASS_CASES = [
     # 17, 33, 48 and 49 keys: the kernel computes 32, 48, 48 and 64 keys (4, 6, 6 and 8
     # groups of 8, a compile-time count per sequence), the extra ones masked
     ("op_key_groups", 4, 7, 3, (10, 26, 41, 42), "geometric"),
+    # more rows than one-row CTAs fit at once (one fp32 CTA an SM, two bf16): rows a CTA
+    # fp32 / bf16 = 2 / 1, 4 / 2, 4 / 4 and 4 / 4 with a last CTA of fewer rows
+    ("op_rows2", 2, 9, 16, 37, "uniform"),
+    ("op_rows_mid", 4, 9, 16, 12, "chain"),
+    ("op_rows4", 8, 9, 16, 50, "uniform"),
+    ("op_rows4_ragged", 4, 9, 17, (20, 0, 55, 33), "geometric"),
 ]
 
 
